@@ -1,0 +1,474 @@
+"""Benchmark of the sparse MoE layer on one GB300 (or N replicas under torchrun).
+
+Headline: Qwen-shaped decode layer (H=2048, E=256 routed experts, top-8,
+SwiGLU intermediate 512, one shared expert, bf16 experts, fp32 router), T=1:
+microseconds per layer call, over 64 different seeded tokens per step, with
+the L2 cache flushed (a 256 MiB write) before every call, outside the timed
+events. The same line also reports the verify window (T=4), the MXFP4 Ling
+layer (T=1, T=4) and the prefill chunk (T=4096) as secondary workloads.
+
+  python bench.py [--steps K] [--warmup W] [--impl ours|reference] [--quick]
+
+Prints ONE JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE layer µs at T=1/4 (HBM GB/s, % peak); prefill tokens/s at T=4096 (TC % peak)"
+HEADLINE = "qwen_decode"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+class Bench:
+    def __init__(self, device):
+        import torch
+        self.torch = torch
+        self.dev = device
+        self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+        self.layers = {}
+
+    def layer(self, spec: mi.LayerSpec, max_tokens: int):
+        from sparse_mixture_experts_gemv_gb300 import MoeLayer, weights_from_raw
+        key = (spec, max_tokens)
+        if key not in self.layers:
+            for k in list(self.layers):
+                if k[0] != spec:
+                    self.layers.pop(k).close()
+            S = mi.SynthLayer(spec)
+            w = weights_from_raw(S.router(), S.router_bias(), S.stacked(), S.shared_raw())
+            self.layers[key] = MoeLayer(spec.H, spec.E, spec.k, spec.I, spec.Is, w, fmt=spec.fmt,
+                                        max_tokens=max_tokens, device=self.dev)
+        return self.layers[key]
+
+    def inputs(self, w: mi.Workload, calls: int):
+        torch = self.torch
+        xs = [torch.from_numpy(mi.workload_tokens(w, c).view(np.int16)).to(self.dev) for c in range(calls)]
+        lbs = [None] * calls
+        if w.logit_bias_sigma:
+            lbs = [torch.from_numpy(mi.workload_logit_bias(w, c)).to(self.dev) for c in range(calls)]
+        return xs, lbs
+
+    def time_calls(self, L, xs, lbs, outs, flush=True, profile=False):
+        """Per-call device time (ms) of each forward, L2 flushed before each call."""
+        torch = self.torch
+        from sparse_mixture_experts_gemv_gb300 import _native as N
+        n = len(xs)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        stages = []
+        if profile:
+            N.moe_layer_profile_enable(L.handle, True)
+        torch.cuda._sleep(20_000_000)  # let the host queue the whole loop ahead of the GPU
+        for i in range(n):
+            if flush:
+                self.flush.zero_()
+            ev[i][0].record()
+            L.forward(xs[i], outs[i], lbs[i])
+            ev[i][1].record()
+            if profile:
+                stages.append(N.moe_layer_profile_read(L.handle))
+        torch.cuda.synchronize()
+        if profile:
+            N.moe_layer_profile_enable(L.handle, False)
+        return [a.elapsed_time(b) for a, b in ev], stages
+
+    def warm_back_to_back(self, L, xs, lbs, outs, reps=4):
+        torch = self.torch
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(50_000_000)
+        s.record()
+        for _ in range(reps):
+            for i in range(len(xs)):
+                L.forward(xs[i], outs[i], lbs[i])
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / (reps * len(xs))
+
+    def e2e(self, L, w: mi.Workload, calls: int):
+        """Host-buffer calls through moe_layer_forward_host: H2D + layer + D2H + sync, wall clock."""
+        torch = self.torch
+        xh = [torch.from_numpy(mi.workload_tokens(w, c).view(np.int16)).pin_memory() for c in range(calls)]
+        oh = [torch.empty_like(x).pin_memory() for x in xh]
+        lb = [None] * calls
+        if w.logit_bias_sigma:
+            lb = [torch.from_numpy(mi.workload_logit_bias(w, c)).pin_memory() for c in range(calls)]
+        for i in range(min(3, calls)):
+            L.forward_host(xh[i], oh[i], lb[i])
+        tot = 0.0
+        for i in range(calls):
+            self.flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            L.forward_host(xh[i], oh[i], lb[i])
+            tot += time.perf_counter() - t0
+        h2d = xh[0].numel() * 2 + (lb[0].numel() * 4 if lb[0] is not None else 0)
+        d2h = oh[0].numel() * 2
+        return tot / calls * 1e6, h2d, d2h
+
+
+def decode_workload(B: Bench, wname: str, steps: int, warmup: int, peaks, profile=True):
+    """Returns a result dict for one small-T workload (per-call us, GB/s, per-kernel roofline)."""
+    torch = B.torch
+    w = mi.WORKLOADS[wname]
+    L = B.layer(w.layer, max_tokens=4096 if w.layer.fmt == "bf16" else 8)
+    calls = w.calls
+    xs, lbs = B.inputs(w, calls)
+    outs = [torch.empty_like(x) for x in xs]
+    # routed-expert bytes per call from the realised routing
+    stats = []
+    for i in range(calls):
+        L.forward(xs[i], outs[i], lbs[i])
+        stats.append(L.stats())
+    for _ in range(warmup):
+        B.time_calls(L, xs, lbs, outs)
+    times = []
+    for _ in range(steps):
+        t, _ = B.time_calls(L, xs, lbs, outs)
+        times += t
+    us = float(np.mean(times) * 1e3)
+    alg_bytes = float(np.mean([s.algorithmic_bytes for s in stats]))
+    distinct = float(np.mean([s.distinct_experts for s in stats]))
+    warm_us = B.warm_back_to_back(L, xs, lbs, outs) * 1e3
+    res = {"workload": wname, "T": w.T, "us_per_call": us, "us_p50": float(np.median(times) * 1e3),
+           "us_p90": float(np.percentile(times, 90) * 1e3), "warm_us_per_call": warm_us,
+           "distinct_experts_mean": distinct, "algorithmic_bytes": alg_bytes,
+           "layer_gbs": alg_bytes / (us * 1e-6) / 1e9,
+           "layer_frac_of_hbm": alg_bytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+           "calls_timed": len(times), "launches_per_call": 3}
+    if profile:
+        st_all = []
+        for _ in range(max(1, steps // 2)):
+            _, st = B.time_calls(L, xs, lbs, outs, profile=True)
+            st_all += st
+        st_mean = np.mean(np.array(st_all), axis=0)
+        spec = w.layer
+        rb_gu = 2 * spec.H if spec.fmt == "bf16" else spec.H // 2 + ((spec.H // 32 + 15) // 16) * 16
+        gu_bytes = distinct * spec.I * 2 * rb_gu
+        res["stage_us"] = {"router_shared": float(st_mean[0] * 1e3), "routed_gateup": float(st_mean[1] * 1e3),
+                           "down_combine": float(st_mean[2] * 1e3)}
+        k3_s = st_mean[1] * 1e-3
+        res["routed_gateup_gbs"] = gu_bytes / k3_s / 1e9
+        res["routed_gateup_bytes"] = gu_bytes
+    return res
+
+
+def run_ours(args):
+    import torch
+    peaks = _peaks()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B = Bench(dev)
+
+    # ---- headline: Qwen decode T=1, flushed L2, per-call CUDA events
+    w = mi.WORKLOADS[HEADLINE]
+    L = B.layer(w.layer, max_tokens=4096)
+    xs, lbs = B.inputs(w, w.calls)
+    outs = [torch.empty_like(x) for x in xs]
+    stats = []
+    for i in range(w.calls):
+        L.forward(xs[i], outs[i], lbs[i])
+        stats.append(L.stats())
+    for _ in range(args.warmup):
+        B.time_calls(L, xs, lbs, outs)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        times = []
+        for _ in range(args.steps):
+            t, _ = B.time_calls(L, xs, lbs, outs)
+            times += t
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    us = float(np.mean(times) * 1e3)
+    step_ms = float(np.sum(times) / args.steps)
+    if world > 1:
+        t = torch.tensor([us, step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        us, step_ms = float(t[0]), float(t[1])
+    alg_bytes = float(np.mean([s.algorithmic_bytes for s in stats]))
+    distinct = float(np.mean([s.distinct_experts for s in stats]))
+
+    # dominant kernel (routed gate/up GEMV) timed per stage with CUDA events
+    stage_all = []
+    for _ in range(max(1, args.steps // 2)):
+        _, st = B.time_calls(L, xs, lbs, outs, profile=True)
+        stage_all += st
+    st_mean = np.mean(np.array(stage_all), axis=0)
+    spec = w.layer
+    gu_bytes = distinct * spec.I * 2 * (2 * spec.H)
+    k3_us = float(st_mean[1] * 1e3)
+    achieved = gu_bytes / (k3_us * 1e-6) / 1e9
+    warm_us = B.warm_back_to_back(L, xs, lbs, outs) * 1e3
+    e2e_us, h2d, d2h = B.e2e(L, w, min(w.calls, 32))
+
+    result = {
+        "metric": METRIC, "value": round(us, 3), "unit": "us", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "qwen_decode: H=2048 E=256 top-8 I=512 + shared expert I=512, bf16 experts, "
+                               "fp32 router, T=1, 64 seeded tokens per step",
+                   "tokens_per_call": 1, "calls_per_step": w.calls, "l2": "flushed (256 MiB write) before every call",
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu"},
+        "layer": {"algorithmic_bytes_per_call": alg_bytes, "gbs": alg_bytes / (us * 1e-6) / 1e9,
+                  "frac_of_measured_hbm": alg_bytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+                  "warm_us_per_call": warm_us, "us_p50": float(np.median(times) * 1e3),
+                  "us_p90": float(np.percentile(times, 90) * 1e3),
+                  "stage_us": {"router_shared": float(st_mean[0] * 1e3), "routed_gateup": k3_us,
+                               "down_combine": float(st_mean[2] * 1e3)}},
+        "roofline": {"kernel": "routed_gateup_kernel<1,bf16>", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": None, "peak_source": peaks["source"],
+                     "bytes_per_launch": gu_bytes, "launch_us": k3_us},
+        "e2e": {"value": round(e2e_us, 3), "unit": "us", "h2d_bytes_per_step": h2d * w.calls,
+                "d2h_bytes_per_step": d2h * w.calls},
+        "gpu_launches": 3 * w.calls * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed": round(wall, 3),
+    }
+    traffic = _profile_traffic("routed_gateup")
+    if traffic is not None:
+        result["roofline"]["traffic"] = traffic
+
+    # ---- secondary workloads
+    extra = {}
+    if not args.quick:
+        for wname in ("qwen_verify", "ling_mxfp4_t1", "ling_mxfp4_t4"):
+            try:
+                extra[wname] = decode_workload(B, wname, max(2, args.steps // 2), 2, peaks)
+            except Exception as ex:  # report, never hide
+                extra[wname] = {"error": repr(ex)}
+        try:
+            extra["qwen_prefill"] = prefill_workload(B, max(2, args.steps // 2), 2, peaks)
+        except Exception as ex:
+            extra["qwen_prefill"] = {"error": repr(ex)}
+    result["workloads"] = extra
+
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def prefill_workload(B: Bench, steps: int, warmup: int, peaks):
+    torch = B.torch
+    w = mi.WORKLOADS["qwen_prefill"]
+    L = B.layer(w.layer, max_tokens=4096)
+    x = torch.from_numpy(mi.workload_tokens(w, 0).view(np.int16)).to(B.dev)
+    out = torch.empty_like(x)
+    L.forward(x, out)
+    st = L.stats()
+    for _ in range(warmup):
+        L.forward(x, out)
+    times = []
+    for _ in range(steps):
+        t, _ = B.time_calls(L, [x], [None], [out])
+        times += t
+    ms = float(np.mean(times))
+    tok_s = w.T / (ms * 1e-3)
+    tflops = st.flops / (ms * 1e-3) / 1e12
+    return {"workload": "qwen_prefill", "T": w.T, "ms_per_call": ms, "tokens_per_s": tok_s,
+            "useful_tflops": tflops, "frac_of_measured_bf16": tflops / peaks["bf16_tflops"],
+            "touched_experts": st.distinct_experts, "max_expert_rows": st.max_expert_rows,
+            "algorithmic_bytes": st.algorithmic_bytes,
+            "hbm_frac": st.algorithmic_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+
+
+def _profile_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary for `kernel`, if present and current."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    v = d.get(kernel)
+    return None if v is None or v.get("stale") else v.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+class StackedLayer:
+    """Oracle accessor over pre-drawn stacked arrays (so timing excludes random draws)."""
+
+    def __init__(self, S: mi.SynthLayer):
+        self.spec = S.spec
+        self._r = S.router()
+        self._b = S.router_bias()
+        self._st = S.stacked()
+        self._sh = S.shared_raw()
+
+    def router(self):
+        return self._r
+
+    def router_bias(self):
+        return self._b
+
+    def expert_raw(self, e):
+        return {k: v[e] for k, v in self._st.items()}
+
+    def shared_raw(self):
+        return self._sh
+
+
+def cpu_baseline(seconds: float, wname: str = HEADLINE):
+    from oracle import moe_oracle as o
+    w = mi.WORKLOADS[wname]
+    SL = StackedLayer(mi.SynthLayer(w.layer))
+    xs = [mi.workload_tokens(w, c) for c in range(w.calls)]
+    o.moe_forward(SL, xs[0])
+    n, t0 = 0, time.perf_counter()
+    while True:
+        o.moe_forward(SL, xs[n % len(xs)])
+        n += 1
+        if time.perf_counter() - t0 >= seconds and n >= 2:
+            break
+    el = time.perf_counter() - t0
+    return {"value": round(el / n * 1e6, 1), "unit": "us", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} T=1 calls of the {wname} layer (fp64 numpy oracle, {el:.1f} s)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import moe_oracle as o
+    w = mi.WORKLOADS[HEADLINE]
+    SL = StackedLayer(mi.SynthLayer(w.layer))
+    xs = [mi.workload_tokens(w, c) for c in range(w.calls)]
+    per_step = max(1, args.ref_calls_per_step)
+    for i in range(args.warmup):
+        o.moe_forward(SL, xs[i % len(xs)])
+    t0 = time.perf_counter()
+    n = 0
+    for s in range(args.steps):
+        for c in range(per_step):
+            o.moe_forward(SL, xs[n % len(xs)])
+            n += 1
+    el = time.perf_counter() - t0
+    us = el / n * 1e6
+    cb = {"value": round(us, 1), "unit": "us", "cores": os.cpu_count(), "kind": "oracle",
+          "sample": f"{per_step} T=1 calls per step of the {HEADLINE} layer, {args.steps} steps"}
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "qwen_decode: H=2048 E=256 top-8 I=512 + shared, T=1 "
+                                                    "(fp64 CPU oracle, the layer's plain definition)"},
+        "cpu_baseline": cb, "e2e": {"value": round(us, 1), "unit": "us", "h2d_bytes_per_step": 0,
+                                    "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-calls-per-step", type=int, default=8)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,238 @@
+/*
+ * moe_layer.h -- C ABI of a single-GPU (GB300, sm_103a) sparse mixture-of-experts layer.
+ *
+ * The layer (forward pass only):
+ *   logits[t,e] = sum_h x[t,h] * W_r[h,e] + router_bias[e] + logit_bias[t,e]     (fp32)
+ *   idx[t,:]    = the k largest logits, descending; exact ties go to the lower index
+ *   w[t,j]      = softmax(logits[t,:])[idx[t,j]] renormalised over the k selected
+ *   y_e(x)      = W_down[e] * ( silu(W_gate[e] x) .* (W_up[e] x) ),  silu(z) = z/(1+e^-z)
+ *   out[t,:]    = sum_j w[t,j] * y_{idx[t,j]}(x_t) + y_shared(x_t)                (bf16)
+ *
+ * Sources: "Optimizing on-device inference for Apple Silicon" -- section "Qwen
+ * creates three different workload shapes" (a router scores 256 experts and
+ * picks 8 per token), section "Keep expert routing on the GPU" (histogram,
+ * prefix scan, scatter and block map stay on the GPU; the CPU never waits
+ * inside the layer), section "Reduce intermediate and state traffic" (fused
+ * gated gate/up projection; down projection fused with the routing score and
+ * the shared-expert result). "Three ways to speed up MoE inference on DGX
+ * Spark" -- section "Why decoding was slow in the first place" (512 routed
+ * experts, 8 selected, one shared expert; MXFP4 expert weights) and its closing
+ * advice to verify at startup which optimisation is actually active
+ * (moe_layer_describe). The pages give no API; this interface is this
+ * library's own.
+ *
+ * Conventions for every call:
+ *  - Pointers named *_dev are device pointers (cudaMalloc'ed, or any memory the
+ *    device can address); *_host are host pointers. Row-major, densest
+ *    dimension last, no padding between rows.
+ *  - bf16 is IEEE binary16 "brain float" (the top 16 bits of an fp32), passed
+ *    as raw 16-bit words.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *  - Every function returns a moe_status_t; nothing throws or aborts. A
+ *    failing CUDA runtime call returns MOE_ERR_CUDA and its text is kept for
+ *    moe_last_cuda_error(). No function writes to stdout or stderr.
+ *  - One moe_layer_t may be used by one host thread at a time.
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, size out of range, bad enum       */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid but not implemented shape (see moe_layer_create)     */
+  MOE_ERR_OOM = 3,           /* device allocation failed; nothing is left allocated        */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed; see moe_last_cuda_error()      */
+  MOE_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out; outputs are undefined  */
+  MOE_ERR_DEVICE_CHECK = 6   /* a device-side index check failed; outputs are undefined    */
+} moe_status_t;
+
+typedef enum {
+  MOE_WEIGHTS_BF16 = 0,      /* routed experts in bf16                                     */
+  MOE_WEIGHTS_MXFP4 = 1      /* routed experts in MXFP4: e2m1 codes, two per byte with the
+                                even element in the low nibble, plus one e8m0 scale byte per
+                                32 consecutive elements along the contraction dimension;
+                                value = e2m1(code) * 2^(scale-127). The shared expert stays
+                                bf16 and the router fp32.                                  */
+} moe_weight_format_t;
+
+/* Create-time flags (moe_layer_config_t.flags). */
+#define MOE_FLAG_FORCE_GROUPED 0x1u        /* run every T through the grouped (prefill)
+                                              path, also T <= MOE_DECODE_MAX_T; for tests */
+#define MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT 0x100u  /* test only: the router kernel waits on a
+                                              device flag that nothing sets; the bounded wait
+                                              runs out (~2 ms) and the next status check
+                                              reports MOE_ERR_TIMEOUT                       */
+
+/* Largest T served by the weight-streaming (GEMV) path; larger T use the grouped
+   tensor-core path. Verify windows of 2-5 rows and 2-token-per-draft batches fit. */
+#define MOE_DECODE_MAX_T 8
+
+typedef struct {
+  int32_t hidden;              /* H: multiple of 256, <= 8192                               */
+  int32_t num_experts;         /* E: routed experts, k <= E <= 512                          */
+  int32_t top_k;               /* k: 1..8                                                   */
+  int32_t intermediate;        /* I: routed expert intermediate size, multiple of 128       */
+  int32_t shared_intermediate; /* Is: shared expert intermediate size, multiple of 128      */
+  int32_t max_tokens;          /* largest T a forward call may pass, >= 1                   */
+  int32_t weight_format;       /* moe_weight_format_t                                       */
+  uint32_t flags;              /* MOE_FLAG_*                                                */
+} moe_layer_config_t;
+
+/*
+ * Weights, all device pointers, read only during moe_layer_create. The layer
+ * copies and repacks them into memory it owns; the caller may free them as soon
+ * as create returns.
+ *   router_dev       fp32 [H, E]
+ *   router_bias_dev  fp32 [E] per-expert logit bias, or NULL for none
+ *   BF16 format:
+ *     gate_dev, up_dev   bf16 [E, I, H]   (row = intermediate feature, H contiguous)
+ *     down_dev           bf16 [E, H, I]   (row = output feature, I contiguous)
+ *     *_scales_dev       unused (NULL)
+ *   MXFP4 format:
+ *     gate_dev, up_dev   uint8 codes [E, I, H/2];  gate_scales_dev, up_scales_dev uint8 [E, I, H/32]
+ *     down_dev           uint8 codes [E, H, I/2];  down_scales_dev uint8 [E, H, I/32]
+ *   shared_gate_dev, shared_up_dev  bf16 [Is, H];  shared_down_dev bf16 [H, Is]
+ */
+typedef struct {
+  const float* router_dev;
+  const float* router_bias_dev;
+  const void* gate_dev;
+  const void* up_dev;
+  const void* down_dev;
+  const uint8_t* gate_scales_dev;
+  const uint8_t* up_scales_dev;
+  const uint8_t* down_scales_dev;
+  const void* shared_gate_dev;
+  const void* shared_up_dev;
+  const void* shared_down_dev;
+} moe_layer_weights_t;
+
+typedef struct moe_layer moe_layer_t;
+
+/* Path ids reported by moe_layer_get_stats. */
+#define MOE_PATH_NONE 0
+#define MOE_PATH_DECODE_GEMV 1     /* T <= MOE_DECODE_MAX_T: router -> gate/up GEMV -> down+combine */
+#define MOE_PATH_GROUPED 2         /* router -> dispatch -> grouped tcgen05 GEMMs -> combine       */
+
+typedef struct {
+  int32_t path;                /* MOE_PATH_* of the last forward                           */
+  int32_t tokens;              /* T of the last forward                                     */
+  int32_t distinct_experts;    /* routed experts touched by the last forward                */
+  int32_t max_expert_rows;     /* largest number of tokens routed to one expert             */
+  int64_t weight_bytes;        /* bytes of weights the path must read once (router, touched
+                                  routed experts, shared expert)                            */
+  int64_t algorithmic_bytes;   /* weight_bytes + activations in/out                         */
+  double flops;                /* 2*(router) + 2*3*I*H per (token, expert) + shared, useful  */
+} moe_stats_t;
+
+/*
+ * Create a layer: validates the config (MOE_ERR_INVALID_ARG for out-of-range
+ * values, MOE_ERR_UNSUPPORTED for shapes outside the limits above), allocates
+ * device memory for the repacked weights and a workspace sized for max_tokens,
+ * and repacks on the current device. Synchronous: returns after the repack has
+ * finished. On failure *out is NULL and nothing stays allocated.
+ */
+moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_weights_t* w,
+                              moe_layer_t** out);
+
+/* Free everything the layer owns (synchronises the device first). NULL is accepted. */
+void moe_layer_destroy(moe_layer_t* layer);
+
+/*
+ * out = layer(x) for T tokens. x_dev: bf16 [T, H]; out_dev: bf16 [T, H]; both
+ * 16-byte aligned and not overlapping. 0 <= T <= max_tokens (T == 0 is a no-op).
+ * Enqueued on `stream`; no allocation, no host synchronisation, no host readback
+ * of routing decisions. The workspace is owned by the layer, so calls on one layer
+ * must be ordered (same stream, or ordered by events). A device-side error from
+ * an earlier call (MOE_ERR_TIMEOUT / MOE_ERR_DEVICE_CHECK) is returned by
+ * moe_layer_sync_status.
+ */
+moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x_dev, void* out_dev, int32_t T,
+                               void* stream);
+
+/*
+ * As moe_layer_forward, plus an optional per-(token, expert) fp32 logit bias
+ * logit_bias_dev [T, E] added to the router logits before top-k (NULL = none).
+ */
+moe_status_t moe_layer_forward_ex(moe_layer_t* layer, const void* x_dev, void* out_dev, int32_t T,
+                                  const float* logit_bias_dev, void* stream);
+
+/*
+ * Host-buffer forward: copies x_host (bf16 [T, H]) to the device, runs the layer
+ * on `stream`, copies the result to out_host (bf16 [T, H]) and synchronises the
+ * stream before returning. Pinned (page-locked) host buffers give asynchronous
+ * copies; pageable buffers work but are slower. logit_bias_host may be NULL.
+ */
+moe_status_t moe_layer_forward_host(moe_layer_t* layer, const void* x_host, void* out_host,
+                                    int32_t T, const float* logit_bias_host, void* stream);
+
+/*
+ * Statistics of the last forward. Synchronises `stream` and reads the routing
+ * back (diagnostic call, not for the hot loop).
+ */
+moe_status_t moe_layer_get_stats(moe_layer_t* layer, void* stream, moe_stats_t* stats);
+
+/*
+ * Copy the routing of the last forward: idx_dev int32 [T, k], weights_dev fp32
+ * [T, k] (device pointers; either may be NULL). Enqueued on `stream`.
+ */
+moe_status_t moe_layer_get_routing(moe_layer_t* layer, int32_t* idx_dev, float* weights_dev,
+                                   void* stream);
+
+/*
+ * Copy the dispatch of the last grouped-path forward (MOE_ERR_INVALID_ARG after a
+ * decode-path forward). All int32 device pointers, any may be NULL:
+ *   hist_dev [E]        assignments per routed expert
+ *   offsets_dev [E+1]   exclusive prefix sum of hist
+ *   perm_dev [T*k]      assignment t*k+j at each grouped row, token order within an expert
+ *   pos_dev [T*k]       grouped row of assignment t*k+j
+ * Enqueued on `stream`.
+ */
+moe_status_t moe_layer_get_dispatch(moe_layer_t* layer, int32_t* hist_dev, int32_t* offsets_dev,
+                                    int32_t* perm_dev, int32_t* pos_dev, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word: MOE_OK,
+ * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK (or MOE_ERR_CUDA if the stream itself
+ * failed).
+ */
+moe_status_t moe_layer_sync_status(moe_layer_t* layer, void* stream);
+
+/*
+ * A static string naming the kernels instantiated for this layer and the path
+ * each T range takes, e.g. to verify at startup which path is active.
+ */
+const char* moe_layer_describe(const moe_layer_t* layer);
+
+/*
+ * Per-stage timing (diagnostic). With profiling enabled, moe_layer_forward
+ * records a CUDA event before the first kernel and after each stage's kernel
+ * on the call's stream; the stages run without programmatic overlap while
+ * enabled. moe_layer_profile_read synchronises on the last event and writes the
+ * elapsed milliseconds of each stage of the last forward into stage_ms
+ * (up to max_stages values) and their number into *n_stages. Stage names, in
+ * order: decode path "router_shared", "routed_gateup", "down_combine"; grouped
+ * path "router", "dispatch", "grouped_gateup", "grouped_down", "combine".
+ */
+moe_status_t moe_layer_profile_enable(moe_layer_t* layer, int32_t enable);
+moe_status_t moe_layer_profile_read(moe_layer_t* layer, float* stage_ms, int32_t max_stages,
+                                    int32_t* n_stages);
+
+/* Name of a status code (static string). */
+const char* moe_status_string(moe_status_t status);
+
+/* Text of the last failing CUDA runtime call in this thread ("" if none). */
+const char* moe_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LAYER_H */

@@ -1,0 +1,704 @@
+// Weight-streaming (GEMV) path of the MoE layer for small token windows
+// (T <= MOE_DECODE_MAX_T: batch-1 decode and speculative verify windows).
+//
+// "Optimizing on-device inference for Apple Silicon", section "Decode: reduce
+// bytes moved per token": at batch 1 the layer is bound by how many weight bytes
+// it reads, so every kernel here streams each needed weight byte exactly once
+// with 16-byte coalesced loads and keeps the arithmetic in registers. Section
+// "Overlap independent work": the shared expert does not depend on routing, so
+// its gate/up projection runs in the same kernel as the router. Section "Reduce
+// intermediate and state traffic": the gated gate/up projection is one kernel
+// and the down projection is fused with the routing weight and the shared
+// expert. "Three ways to speed up MoE inference on DGX Spark", section
+// "Optimization 3": a 4-token verify window touches up to 32 experts, so the
+// window's distinct experts are read once each, for all tokens that chose them.
+//
+// Three kernels, chained with programmatic dependent launch:
+//   K1 router_shared  fp32 router logits + shared-expert gate/up (SwiGLU);
+//                     the last CTA to finish does top-k, the renormalised
+//                     softmax weights and the window's distinct-expert list.
+//   K3 routed_gateup  one pass over the gate/up rows of each distinct expert;
+//                     also prefetches the down rows K4 will need into L2.
+//   K4 down_combine   down rows of every distinct expert and of the shared
+//                     expert, weighted by the routing weights, summed, bf16 out.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+struct FmtBF16 {};
+struct FmtMXFP4 {};
+
+constexpr int kRouterThreads = 256;
+constexpr int kGemvThreads = 512;
+
+// e2m1 code values (OCP MX FP4 element): sign, 2 exponent bits (bias 1), 1 mantissa bit.
+__device__ __forceinline__ void fill_e2m1_lut(float* lut) {
+  if (threadIdx.x < 16) {
+    const int c = threadIdx.x;
+    const int e = (c >> 1) & 3, m = c & 1;
+    float mag = (e == 0) ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, e - 1);
+    lut[c] = (c & 8) ? -mag : mag;
+  }
+}
+
+__device__ __forceinline__ float e8m0_scale(uint32_t s) { return ldexpf(1.0f, (int)s - 127); }
+
+// Sum of 8 bf16 weights (one 16-byte chunk) times 8 bf16 activations.
+__device__ __forceinline__ float dot8_bf16(const uint4 w, const uint4 x) {
+  float a = bf16_lo(w.x) * bf16_lo(x.x);
+  a = fmaf(bf16_hi(w.x), bf16_hi(x.x), a);
+  a = fmaf(bf16_lo(w.y), bf16_lo(x.y), a);
+  a = fmaf(bf16_hi(w.y), bf16_hi(x.y), a);
+  a = fmaf(bf16_lo(w.z), bf16_lo(x.z), a);
+  a = fmaf(bf16_hi(w.z), bf16_hi(x.z), a);
+  a = fmaf(bf16_lo(w.w), bf16_lo(x.w), a);
+  a = fmaf(bf16_hi(w.w), bf16_hi(x.w), a);
+  return a;
+}
+
+// Sum of 8 bf16 weights times 8 fp32 activations (two float4).
+__device__ __forceinline__ float dot8_bf16_f32(const uint4 w, const float4 a, const float4 b) {
+  float s = bf16_lo(w.x) * a.x;
+  s = fmaf(bf16_hi(w.x), a.y, s);
+  s = fmaf(bf16_lo(w.y), a.z, s);
+  s = fmaf(bf16_hi(w.y), a.w, s);
+  s = fmaf(bf16_lo(w.z), b.x, s);
+  s = fmaf(bf16_hi(w.z), b.y, s);
+  s = fmaf(bf16_lo(w.w), b.z, s);
+  s = fmaf(bf16_hi(w.w), b.w, s);
+  return s;
+}
+
+// Sum of 32 e2m1 codes (16 bytes, even element in the low nibble) times 32 bf16
+// activations starting at xs (shared memory, 16-byte aligned); unscaled.
+__device__ __forceinline__ float dot32_e2m1_bf16(const uint4 c, const uint16_t* xs, const float* lut) {
+  const uint4* xv = reinterpret_cast<const uint4*>(xs);
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+  float s = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {       // 8 codes per 32-bit word, 8 activations per uint4
+    const uint4 x = xv[q];
+    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {     // one byte = elements 2b (low nibble), 2b+1 (high nibble)
+      const uint32_t byte = (cw[q] >> (8 * b)) & 0xFFu;
+      s = fmaf(lut[byte & 15u], bf16_lo(xw[b]), s);
+      s = fmaf(lut[byte >> 4], bf16_hi(xw[b]), s);
+    }
+  }
+  return s;
+}
+
+__device__ __forceinline__ float dot32_e2m1_f32(const uint4 c, const float* hs, const float* lut) {
+  const float4* hv = reinterpret_cast<const float4*>(hs);
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+  float s = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 a = hv[2 * q], b = hv[2 * q + 1];
+    const float h8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int bb = 0; bb < 4; ++bb) {
+      const uint32_t byte = (cw[q] >> (8 * bb)) & 0xFFu;
+      s = fmaf(lut[byte & 15u], h8[2 * bb], s);
+      s = fmaf(lut[byte >> 4], h8[2 * bb + 1], s);
+    }
+  }
+  return s;
+}
+
+// ===========================================================================
+// K1: router logits + shared expert gate/up; last CTA: top-k + window list.
+// ===========================================================================
+struct RouterArgs {
+  const uint16_t* x;           // bf16 [T][H]
+  int T, H, E, k, Is;
+  const float* router_t;       // fp32 [E][H]
+  const float* router_bias;    // fp32 [E]
+  const float* logit_bias;     // fp32 [T][E] or nullptr
+  const uint16_t* ws_gu;       // bf16 [Is][2][H]
+  float* logits;               // [T][E]
+  float* h_shared;             // [T][Is]
+  int* idx;                    // [T][k]
+  float* weights;              // [T][k]
+  DecodeMeta* meta;
+  unsigned int* counter;
+  int* err;
+  const int* never_set;
+  int force_timeout;
+};
+
+template <int TMAX>
+__global__ void __launch_bounds__(kRouterThreads)
+router_shared_kernel(const RouterArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [T][H] bf16
+  __shared__ int s_idx[kMaxDecodeT * kMaxTopK];
+  __shared__ int s_slot_of[kMaxDecodeT * kMaxTopK];
+  __shared__ unsigned int s_ticket;
+
+  // Everything below reads the layer input and overwrites the workspace of the
+  // previous call: wait for the preceding kernels of the stream first.
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int T = a.T, H = a.H;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  if (a.force_timeout && blockIdx.x == 0 && threadIdx.x == 0) {
+    if (!bounded_wait_flag(a.never_set, 2000000LL)) set_error(a.err, kDevTimeout);
+  }
+
+  {  // x -> shared memory
+    const uint4* src = reinterpret_cast<const uint4*>(a.x);
+    uint4* dst = reinterpret_cast<uint4*>(xs);
+    const int n16 = T * H / 8;
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src[i];
+  }
+  __syncthreads();
+
+  const int nwarps = gridDim.x * (kRouterThreads / 32);
+  const int gw = blockIdx.x * (kRouterThreads / 32) + warp;
+  const int units = a.E + a.Is;
+  for (int u = gw; u < units; u += nwarps) {
+    if (u < a.E) {
+      // Router row: logits[t][u] = sum_h x[t][h] * W_r[h][u]   (fp32 row of H)
+      const float* row = a.router_t + (size_t)u * H;
+      const int nch = H / 4;  // 16-byte chunks of 4 floats
+      float acc[TMAX];
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
+      for (int m0 = 0; m0 < nch; m0 += 32 * 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = m0 + lane + 32 * q;
+          if (c < nch) v[q] = ldg_stream(row + 4 * c);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = m0 + lane + 32 * q;
+          if (c < nch) {
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+              if (t < T) {
+                const uint2 xx = *reinterpret_cast<const uint2*>(xs + t * H + 4 * c);
+                float s = acc[t];
+                s = fmaf(__uint_as_float(v[q].x), bf16_lo(xx.x), s);
+                s = fmaf(__uint_as_float(v[q].y), bf16_hi(xx.x), s);
+                s = fmaf(__uint_as_float(v[q].z), bf16_lo(xx.y), s);
+                s = fmaf(__uint_as_float(v[q].w), bf16_hi(xx.y), s);
+                acc[t] = s;
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (t < T) {
+          float s = warp_sum(acc[t]);
+          if (lane == 0) {
+            s += a.router_bias[u];
+            if (a.logit_bias) s += a.logit_bias[(size_t)t * a.E + u];
+            a.logits[(size_t)t * a.E + u] = s;
+          }
+        }
+      }
+    } else {
+      // Shared expert, intermediate feature i: gate row and up row (bf16, H each).
+      const int i = u - a.E;
+      const uint16_t* grow = a.ws_gu + (size_t)i * 2 * H;
+      const uint16_t* urow = grow + H;
+      const int nch = H / 8;
+      float ag[TMAX], au[TMAX];
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) ag[t] = au[t] = 0.f;
+      for (int m0 = 0; m0 < nch; m0 += 32 * 8) {
+        uint4 g[8], uu[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = m0 + lane + 32 * q;
+          if (c < nch) { g[q] = ldg_stream(grow + 8 * c); uu[q] = ldg_stream(urow + 8 * c); }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = m0 + lane + 32 * q;
+          if (c < nch) {
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+              if (t < T) {
+                const uint4 xx = *reinterpret_cast<const uint4*>(xs + t * H + 8 * c);
+                ag[t] += dot8_bf16(g[q], xx);
+                au[t] += dot8_bf16(uu[q], xx);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (t < T) {
+          const float gs = warp_sum(ag[t]);
+          const float us = warp_sum(au[t]);
+          if (lane == 0) a.h_shared[(size_t)t * a.Is + i] = swiglu(gs, us);
+        }
+      }
+    }
+  }
+
+  // ---- last CTA: top-k over the complete logits --------------------------
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = atomicAdd(a.counter, 1u);
+  __syncthreads();
+  if (s_ticket != gridDim.x - 1) return;
+  __threadfence();
+
+  const int E = a.E, k = a.k;
+  if (warp < T) {
+    const int t = warp;
+    constexpr int kPer = kMaxExperts / 32;
+    uint32_t key[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int e = lane + 32 * j;
+      key[j] = (e < E) ? f32_order_key(ldg_cg_f32(a.logits + (size_t)t * E + e)) : 0u;
+    }
+    float sel_v[kMaxTopK];
+    int sel_e[kMaxTopK];
+#pragma unroll
+    for (int r = 0; r < kMaxTopK; ++r) {
+      if (r < k) {
+        uint32_t lk = 0u;
+        int lj = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+          if (key[j] > lk) { lk = key[j]; lj = j; }
+        const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, lk);
+        const uint32_t cand = (lk == gmax) ? (uint32_t)(lane + 32 * lj) : 0xFFFFFFFFu;
+        const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
+        if (lane == (int)(gidx & 31u)) {
+#pragma unroll
+          for (int j = 0; j < kPer; ++j)
+            if (j == (int)(gidx >> 5)) key[j] = 0u;
+        }
+        sel_v[r] = f32_from_order_key(gmax);
+        sel_e[r] = (int)gidx;
+      }
+    }
+    // Renormalised softmax over the k selected logits.
+    float ex[kMaxTopK], sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxTopK; ++r) {
+      if (r < k) { ex[r] = expf(sel_v[r] - sel_v[0]); sum += ex[r]; }
+    }
+#pragma unroll
+    for (int r = 0; r < kMaxTopK; ++r) {
+      if (r < k && lane == r) {
+        a.idx[t * k + r] = sel_e[r];
+        a.weights[t * k + r] = ex[r] / sum;
+        s_idx[t * k + r] = sel_e[r];
+      }
+    }
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // Distinct experts of the window, in order of first appearance over (t, j).
+    const int n = T * k;
+    bool first[2] = {false, false};
+    int firstpos[2] = {0, 0};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int aidx = lane + 32 * h;
+      if (aidx < n) {
+        const int e = s_idx[aidx];
+        int b = 0;
+        while (s_idx[b] != e) ++b;  // terminates at b == aidx at the latest
+        first[h] = (b == aidx);
+        firstpos[h] = b;
+      }
+    }
+    const unsigned m0 = __ballot_sync(0xFFFFFFFFu, first[0]);
+    const unsigned m1 = __ballot_sync(0xFFFFFFFFu, first[1]);
+    const unsigned lt = (1u << lane) - 1u;
+    if (first[0]) s_slot_of[lane] = __popc(m0 & lt);
+    if (first[1]) s_slot_of[lane + 32] = __popc(m0) + __popc(m1 & lt);
+    __syncwarp();
+    const int D = __popc(m0) + __popc(m1);
+    // Clear slot_j for the window's slots, then fill it.
+    for (int q = lane; q < D * kMaxDecodeT; q += 32)
+      a.meta->slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = -1;
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int aidx = lane + 32 * h;
+      if (aidx < n) {
+        const int slot = s_slot_of[firstpos[h]];
+        if (first[h]) a.meta->slot_expert[slot] = s_idx[aidx];
+        a.meta->slot_j[slot][aidx / k] = (signed char)(aidx % k);
+      }
+    }
+    if (lane == 0) {
+      a.meta->num_slots = D;
+      *a.counter = 0u;  // ready for the next call
+    }
+  }
+}
+
+// ===========================================================================
+// K3: routed gate/up GEMV over the window's distinct experts.
+// ===========================================================================
+struct GateUpArgs {
+  const uint16_t* x;       // bf16 [T][H]
+  int T, H, I, k;
+  const uint8_t* w_gu;     // [E][I][2][rb_gu]
+  int64_t rb_gu;
+  const DecodeMeta* meta;
+  float* h;                // [T*k][I]
+  // L2 prefetch of what K4 reads (same CTA partition of the H output rows).
+  const uint8_t* w_down;   // [E][H][rb_down]
+  int64_t rb_down;
+  const uint16_t* ws_down; // [H][Is]
+  int Is;
+};
+
+template <int TMAX, class Fmt>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+routed_gateup_kernel(const GateUpArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [T][H]
+  __shared__ float lut[16];
+  __shared__ int s_slot_expert[kMaxSlots];
+  __shared__ signed char s_slot_j[kMaxSlots][kMaxDecodeT];
+
+  const int T = a.T, H = a.H, I = a.I;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if constexpr (std::is_same<Fmt, FmtMXFP4>::value) fill_e2m1_lut(lut);
+  {  // x -> shared memory (the layer input: complete before the router started)
+    const uint4* src = reinterpret_cast<const uint4*>(a.x);
+    uint4* dst = reinterpret_cast<uint4*>(xs);
+    for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) dst[i] = src[i];
+  }
+
+  pdl_wait();  // routing of this window is complete
+  pdl_launch_dependents();
+
+  const int D = ldg_cg_s32(&a.meta->num_slots);
+  for (int q = threadIdx.x; q < D; q += blockDim.x) s_slot_expert[q] = ldg_cg_s32(&a.meta->slot_expert[q]);
+  for (int q = threadIdx.x; q < D * kMaxDecodeT; q += blockDim.x) {
+    const signed char* src = &a.meta->slot_j[0][0];
+    s_slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = *((volatile const signed char*)(src + q));
+  }
+  __syncthreads();
+
+  // Down rows this CTA's twin in K4 will read: start their HBM -> L2 transfer now.
+  if (threadIdx.x == 0) {
+    const int n0 = (int)((int64_t)blockIdx.x * H / gridDim.x);
+    const int n1 = (int)((int64_t)(blockIdx.x + 1) * H / gridDim.x);
+    if (n1 > n0) {
+      for (int d = 0; d < D; ++d) {
+        const uint8_t* p = a.w_down + ((int64_t)s_slot_expert[d] * H + n0) * a.rb_down;
+        prefetch_l2_bulk(p, (uint32_t)((n1 - n0) * a.rb_down));
+      }
+      if (a.Is > 0) prefetch_l2_bulk(a.ws_down + (int64_t)n0 * a.Is, (uint32_t)((n1 - n0) * a.Is * 2));
+    }
+  }
+
+  const int64_t U = (int64_t)D * I;
+  const int64_t u0 = (int64_t)blockIdx.x * U / gridDim.x;
+  const int64_t u1 = (int64_t)(blockIdx.x + 1) * U / gridDim.x;
+  const int nw = kGemvThreads / 32;
+
+  for (int64_t u = u0 + warp; u < u1; u += nw) {
+    const int d = (int)(u / I), i = (int)(u % I);
+    const int e = s_slot_expert[d];
+    const uint8_t* grec = a.w_gu + ((int64_t)e * I + i) * 2 * a.rb_gu;
+    const uint8_t* urec = grec + a.rb_gu;
+    float ag[TMAX], au[TMAX];
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) ag[t] = au[t] = 0.f;
+
+    if constexpr (std::is_same<Fmt, FmtBF16>::value) {
+      const int nch = H / 8;  // 16-byte chunks per row
+      for (int m0 = 0; m0 < nch; m0 += 32 * 8) {
+        uint4 g[8], uu[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = m0 + lane + 32 * q;
+          if (c < nch) { g[q] = ldg_stream(grec + 16 * c); uu[q] = ldg_stream(urec + 16 * c); }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = m0 + lane + 32 * q;
+          if (c < nch) {
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+              if (t < T) {
+                const uint4 xx = *reinterpret_cast<const uint4*>(xs + t * H + 8 * c);
+                ag[t] += dot8_bf16(g[q], xx);
+                au[t] += dot8_bf16(uu[q], xx);
+              }
+            }
+          }
+        }
+      }
+    } else {
+      const int nch = H / 32;  // 16-byte chunks of 32 codes = one scale block each
+      const uint8_t* gsc = grec + H / 2;
+      const uint8_t* usc = urec + H / 2;
+      for (int m0 = 0; m0 < nch; m0 += 32 * 4) {
+        uint4 g[4], uu[4];
+        uint32_t gs[4], us[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c = m0 + lane + 32 * q;
+          if (c < nch) {
+            g[q] = ldg_stream(grec + 16 * c);
+            uu[q] = ldg_stream(urec + 16 * c);
+            gs[q] = gsc[c];
+            us[q] = usc[c];
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c = m0 + lane + 32 * q;
+          if (c < nch) {
+            const float sg = e8m0_scale(gs[q]), su = e8m0_scale(us[q]);
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+              if (t < T) {
+                const uint16_t* xp = xs + t * H + 32 * c;
+                ag[t] = fmaf(dot32_e2m1_bf16(g[q], xp, lut), sg, ag[t]);
+                au[t] = fmaf(dot32_e2m1_bf16(uu[q], xp, lut), su, au[t]);
+              }
+            }
+          }
+        }
+      }
+    }
+
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      if (t < T) {
+        const float gsum = warp_sum(ag[t]);
+        const float usum = warp_sum(au[t]);
+        const int j = s_slot_j[d][t];
+        if (lane == t && j >= 0) a.h[((int64_t)t * a.k + j) * I + i] = swiglu(gsum, usum);
+      }
+    }
+  }
+}
+
+// ===========================================================================
+// K4: down projection of every distinct expert + shared expert, weighted sum.
+// ===========================================================================
+struct DownArgs {
+  int T, H, I, Is, k;
+  const uint8_t* w_down;   // [E][H][rb_down]
+  int64_t rb_down;
+  const uint16_t* ws_down; // bf16 [H][Is]
+  const DecodeMeta* meta;
+  const float* h;          // [T*k][I]
+  const float* h_shared;   // [T][Is]
+  const float* weights;    // [T][k]
+  uint16_t* out;           // bf16 [T][H]
+};
+
+template <int TMAX, class Fmt>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+down_combine_kernel(const DownArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int T = a.T, H = a.H, I = a.I, Is = a.Is, k = a.k;
+  float* hs = reinterpret_cast<float*>(smem);        // [T*k][I]
+  float* hss = hs + (size_t)T * k * I;               // [T][Is]
+  __shared__ float lut[16];
+  __shared__ float s_w[kMaxDecodeT * kMaxTopK];
+  __shared__ int s_slot_expert[kMaxSlots];
+  __shared__ signed char s_slot_j[kMaxSlots][kMaxDecodeT];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if constexpr (std::is_same<Fmt, FmtMXFP4>::value) fill_e2m1_lut(lut);
+
+  pdl_wait();  // SwiGLU outputs of this window are complete
+  pdl_launch_dependents();
+
+  const int D = ldg_cg_s32(&a.meta->num_slots);
+  for (int q = threadIdx.x; q < D; q += blockDim.x) s_slot_expert[q] = ldg_cg_s32(&a.meta->slot_expert[q]);
+  for (int q = threadIdx.x; q < D * kMaxDecodeT; q += blockDim.x) {
+    const signed char* src = &a.meta->slot_j[0][0];
+    s_slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = *((volatile const signed char*)(src + q));
+  }
+  for (int q = threadIdx.x; q < T * k; q += blockDim.x) s_w[q] = ldg_cg_f32(a.weights + q);
+  {
+    const int n16 = T * k * I / 4;
+    for (int q = threadIdx.x; q < n16; q += blockDim.x)
+      reinterpret_cast<uint4*>(hs)[q] = ldg_cg(reinterpret_cast<const uint4*>(a.h) + q);
+    const int s16 = T * Is / 4;
+    for (int q = threadIdx.x; q < s16; q += blockDim.x)
+      reinterpret_cast<uint4*>(hss)[q] = ldg_cg(reinterpret_cast<const uint4*>(a.h_shared) + q);
+  }
+  __syncthreads();
+
+  const int n0 = (int)((int64_t)blockIdx.x * H / gridDim.x);
+  const int n1 = (int)((int64_t)(blockIdx.x + 1) * H / gridDim.x);
+  const int nw = kGemvThreads / 32;
+
+  for (int n = n0 + warp; n < n1; n += nw) {
+    float acc[TMAX];
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
+
+    for (int d = 0; d < D; ++d) {
+      const uint8_t* rec = a.w_down + ((int64_t)s_slot_expert[d] * H + n) * a.rb_down;
+      if constexpr (std::is_same<Fmt, FmtBF16>::value) {
+        const int nch = I / 8;
+        for (int c = lane; c < nch; c += 32) {
+          const uint4 wv = ldg_stream(rec + 16 * c);
+#pragma unroll
+          for (int t = 0; t < TMAX; ++t) {
+            if (t < T) {
+              const int j = s_slot_j[d][t];
+              if (j >= 0) {
+                const float* hp = hs + ((size_t)t * k + j) * I + 8 * c;
+                const float4 h0 = *reinterpret_cast<const float4*>(hp);
+                const float4 h1 = *reinterpret_cast<const float4*>(hp + 4);
+                acc[t] = fmaf(s_w[t * k + j], dot8_bf16_f32(wv, h0, h1), acc[t]);
+              }
+            }
+          }
+        }
+      } else {
+        const int nch = I / 32;
+        const uint8_t* sc = rec + I / 2;
+        for (int c = lane; c < nch; c += 32) {
+          const uint4 wv = ldg_stream(rec + 16 * c);
+          const float s = e8m0_scale(sc[c]);
+#pragma unroll
+          for (int t = 0; t < TMAX; ++t) {
+            if (t < T) {
+              const int j = s_slot_j[d][t];
+              if (j >= 0) {
+                const float* hp = hs + ((size_t)t * k + j) * I + 32 * c;
+                acc[t] = fmaf(s_w[t * k + j] * s, dot32_e2m1_f32(wv, hp, lut), acc[t]);
+              }
+            }
+          }
+        }
+      }
+    }
+    if (Is > 0) {  // shared expert, weight 1
+      const uint16_t* srow = a.ws_down + (size_t)n * Is;
+      const int nch = Is / 8;
+      for (int c = lane; c < nch; c += 32) {
+        const uint4 wv = ldg_stream(srow + 8 * c);
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+          if (t < T) {
+            const float* hp = hss + (size_t)t * Is + 8 * c;
+            const float4 h0 = *reinterpret_cast<const float4*>(hp);
+            const float4 h1 = *reinterpret_cast<const float4*>(hp + 4);
+            acc[t] += dot8_bf16_f32(wv, h0, h1);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      if (t < T) {
+        const float s = warp_sum(acc[t]);
+        if (lane == t) a.out[(size_t)t * H + n] = f32_to_bf16_rne(s);
+      }
+    }
+  }
+}
+
+// ===========================================================================
+// Host launchers
+// ===========================================================================
+size_t decode_smem_bytes_down(const moe_layer* L, int T) {
+  const auto& c = L->cfg;
+  return (size_t)T * ((size_t)c.top_k * c.intermediate + c.shared_intermediate) * sizeof(float);
+}
+
+template <class K, class A>
+static cudaError_t launch_pdl(K kernel, int grid, int block, size_t smem, cudaStream_t s, const A& args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args);
+}
+
+template <int TMAX, class Fmt>
+static cudaError_t launch_decode_t(moe_layer* L, const uint16_t* x, uint16_t* out, int T,
+                                   const float* logit_bias, cudaStream_t s) {
+  const auto& c = L->cfg;
+  const int H = c.hidden;
+  const size_t xs_bytes = (size_t)T * H * sizeof(uint16_t);
+  static bool attr_set = false;  // per instantiation; max smem is a per-function attribute
+  if (!attr_set) {
+    cudaFuncSetAttribute(router_shared_kernel<TMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaFuncSetAttribute(routed_gateup_kernel<TMAX, Fmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaFuncSetAttribute(down_combine_kernel<TMAX, Fmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    attr_set = true;
+  }
+
+  RouterArgs ra;
+  ra.x = x; ra.T = T; ra.H = H; ra.E = c.num_experts; ra.k = c.top_k; ra.Is = c.shared_intermediate;
+  ra.router_t = L->router_t; ra.router_bias = L->router_bias; ra.logit_bias = logit_bias;
+  ra.ws_gu = L->ws_gu; ra.logits = L->dec.logits; ra.h_shared = L->dec.h_shared;
+  ra.idx = L->dec.idx; ra.weights = L->dec.weights; ra.meta = L->dec.meta;
+  ra.counter = L->dec.counter; ra.err = L->err; ra.never_set = L->never_set;
+  ra.force_timeout = (c.flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? 1 : 0;
+  prof_mark(L, s);
+  cudaError_t e = launch_pdl(router_shared_kernel<TMAX>, L->num_sms, kRouterThreads, xs_bytes, s, ra);
+  if (e != cudaSuccess) return e;
+  prof_mark(L, s);
+
+  GateUpArgs ga;
+  ga.x = x; ga.T = T; ga.H = H; ga.I = c.intermediate; ga.k = c.top_k;
+  ga.w_gu = L->w_gu; ga.rb_gu = L->row_bytes.gu; ga.meta = L->dec.meta; ga.h = L->dec.h;
+  ga.w_down = L->w_down; ga.rb_down = L->row_bytes.down; ga.ws_down = L->ws_down;
+  ga.Is = c.shared_intermediate;
+  e = launch_pdl(routed_gateup_kernel<TMAX, Fmt>, L->num_sms, kGemvThreads, xs_bytes, s, ga);
+  if (e != cudaSuccess) return e;
+  prof_mark(L, s);
+
+  DownArgs da;
+  da.T = T; da.H = H; da.I = c.intermediate; da.Is = c.shared_intermediate; da.k = c.top_k;
+  da.w_down = L->w_down; da.rb_down = L->row_bytes.down; da.ws_down = L->ws_down;
+  da.meta = L->dec.meta; da.h = L->dec.h; da.h_shared = L->dec.h_shared;
+  da.weights = L->dec.weights; da.out = out;
+  e = launch_pdl(down_combine_kernel<TMAX, Fmt>, L->num_sms, kGemvThreads,
+                 decode_smem_bytes_down(L, T), s, da);
+  prof_mark(L, s);
+  return e;
+}
+
+template <class Fmt>
+static cudaError_t launch_decode_fmt(moe_layer* L, const uint16_t* x, uint16_t* out, int T,
+                                     const float* lb, cudaStream_t s) {
+  if (T <= 1) return launch_decode_t<1, Fmt>(L, x, out, T, lb, s);
+  if (T <= 2) return launch_decode_t<2, Fmt>(L, x, out, T, lb, s);
+  if (T <= 4) return launch_decode_t<4, Fmt>(L, x, out, T, lb, s);
+  return launch_decode_t<8, Fmt>(L, x, out, T, lb, s);
+}
+
+cudaError_t launch_decode(moe_layer* L, const uint16_t* x, uint16_t* out, int T,
+                          const float* logit_bias, cudaStream_t s) {
+  if (L->cfg.weight_format == MOE_WEIGHTS_MXFP4) return launch_decode_fmt<FmtMXFP4>(L, x, out, T, logit_bias, s);
+  return launch_decode_fmt<FmtBF16>(L, x, out, T, logit_bias, s);
+}
+
+}  // namespace moe

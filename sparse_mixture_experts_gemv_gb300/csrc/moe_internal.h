@@ -1,0 +1,107 @@
+// Host-side layer state shared by the API and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_layer.h"
+
+namespace moe {
+
+constexpr int kMaxDecodeT = MOE_DECODE_MAX_T;  // weight-streaming path limit
+constexpr int kMaxTopK = 8;
+constexpr int kMaxExperts = 512;
+constexpr int kMaxSlots = kMaxDecodeT * kMaxTopK;  // distinct experts in one window
+
+// Routing metadata of one decode window, written by the router kernel.
+struct DecodeMeta {
+  int num_slots;                              // D: distinct routed experts in the window
+  int slot_expert[kMaxSlots];                 // expert of slot d, first-appearance order
+  signed char slot_j[kMaxSlots][kMaxDecodeT];  // j with idx[t][j] == slot_expert[d], or -1
+};
+
+// Byte sizes of one repacked row ("record") of each weight matrix.
+struct RowBytes {
+  int64_t gu;    // one gate or up row of a routed expert (codes + padded scales for MXFP4)
+  int64_t down;  // one down row of a routed expert
+};
+
+struct DecodeWorkspace {
+  float* logits;         // [kMaxDecodeT][E]
+  int* idx;              // [kMaxDecodeT][k]
+  float* weights;        // [kMaxDecodeT][k]
+  DecodeMeta* meta;      // one
+  float* h;              // [kMaxDecodeT * k][I]   SwiGLU outputs of routed assignments (t*k+j)
+  float* h_shared;       // [kMaxDecodeT][Is]
+  unsigned int* counter; // router last-block ticket
+};
+
+struct GroupedWorkspace {
+  int max_tokens;
+  float* logits;         // [T][E]
+  int* idx;              // [T][k]
+  float* weights;        // [T][k]
+  int* hist;             // [E + 1] (slot E = shared expert)
+  int* offsets;          // [E + 2]
+  int* chunk_counts;     // [num_chunks][E]
+  int* perm;             // [T*k]  assignment at each grouped row
+  int* pos;              // [T*k]  grouped row of each assignment
+  int* tiles;            // [max_tiles] packed (expert << 20 | row0 >> 7)... see grouped path
+  int* num_tiles;        // [2]: gate/up tiles, down tiles
+  uint16_t* h;           // bf16 [T*k + T][I or Is]  SwiGLU outputs in grouped order (+ shared rows)
+  uint16_t* y;           // bf16 [T*k + T][H]        weighted down outputs in grouped order
+  int max_tiles;
+};
+
+}  // namespace moe
+
+struct moe_layer {
+  moe_layer_config_t cfg;
+  int device;
+  int num_sms;
+  int decode_max_t;      // largest T the weight-streaming path serves for this shape
+
+  // Repacked weights (owned).
+  float* router_t;       // fp32 [E][H]   (W_r transposed: one row per expert)
+  float* router_bias;    // fp32 [E]      (zeros when none was given)
+  uint16_t* router_split;  // bf16 [3][E][H]  W_r^T = hi + mid + lo exactly (grouped path)
+  uint8_t* w_gu;         // routed gate/up, [E][I][2][row_bytes.gu]  (gate row, up row per i)
+  uint8_t* w_down;       // routed down,    [E][H][row_bytes.down]
+  uint16_t* ws_gu;       // shared gate/up bf16 [Is][2][H]
+  uint16_t* ws_down;     // shared down bf16 [H][Is]
+  moe::RowBytes row_bytes;
+
+  moe::DecodeWorkspace dec;
+  moe::GroupedWorkspace grp;
+  int* err;              // device error word
+  int* never_set;        // device flag nothing sets (timeout test)
+  uint16_t* x_stage;     // bf16 [max_tokens][H]  forward_host staging
+  uint16_t* out_stage;   // bf16 [max_tokens][H]
+  float* bias_stage;     // fp32 [max_tokens][E]
+
+  // Last forward.
+  int last_path;
+  int last_T;
+  const float* last_logit_bias;
+  void* tmaps;           // grouped-path tensor maps (host copy), see moe_grouped.cu
+  // Per-stage profiling (moe_layer_profile_enable).
+  int profile;
+  cudaEvent_t prof_ev[8];
+  int prof_n;            // events recorded by the last forward
+  char describe[1024];
+};
+
+namespace moe {
+// Records the next profiling event on s (no-op unless profiling is enabled).
+inline void prof_mark(moe_layer* L, cudaStream_t s) {
+  if (L->profile && L->prof_n < 8) cudaEventRecord(L->prof_ev[L->prof_n++], s);
+}
+// Launchers (moe_decode.cu / moe_grouped.cu). Return cudaSuccess or the launch error.
+cudaError_t launch_decode(moe_layer* L, const uint16_t* x, uint16_t* out, int T,
+                          const float* logit_bias, cudaStream_t s);
+cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T,
+                           const float* logit_bias, cudaStream_t s);
+cudaError_t grouped_prepare(moe_layer* L);   // tensor maps etc. at create
+void grouped_release(moe_layer* L);
+size_t decode_smem_bytes_down(const moe_layer* L, int T);
+}  // namespace moe

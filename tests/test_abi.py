@@ -1,0 +1,40 @@
+"""The C-ABI library builds, loads and exports every function include/moe_layer.h declares (CPU only)."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe_layer.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_function():
+    from sparse_mixture_experts_gemv_gb300 import build as b
+    lib_path = b.build()
+    lib = ctypes.CDLL(lib_path)
+    names = _declared()
+    assert "moe_layer_forward" in names and "moe_layer_create" in names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    from sparse_mixture_experts_gemv_gb300 import _native as N
+    assert sorted(N.exported_names()) == names  # the binding covers the whole header
+
+
+def test_status_strings_without_gpu():
+    from sparse_mixture_experts_gemv_gb300 import _native as N
+    assert N.moe_status_string(N.MOE_ERR_TIMEOUT) == "MOE_ERR_TIMEOUT"
+    assert N.moe_status_string(99) == "MOE_ERR_UNKNOWN"
+
+
+def test_create_rejects_bad_config_before_touching_the_device():
+    from sparse_mixture_experts_gemv_gb300 import _native as N
+    cfg = N.moe_layer_config_t(256, 16, 17, 128, 128, 8, 0, 0)  # k > E
+    st, h = N.moe_layer_create_status(cfg, N.moe_layer_weights_t())
+    assert st == N.MOE_ERR_INVALID_ARG and h is None
+    cfg = N.moe_layer_config_t(256, 16, 2, 128, 128, 8, 7, 0)  # unknown format
+    st, h = N.moe_layer_create_status(cfg, N.moe_layer_weights_t())
+    assert st == N.MOE_ERR_INVALID_ARG
