@@ -71,7 +71,10 @@ typedef enum {
                                               reports MOE_ERR_TIMEOUT                       */
 
 /* Largest T served by the weight-streaming (GEMV) path; larger T use the grouped
-   tensor-core path. Verify windows of 2-5 rows and 2-token-per-draft batches fit. */
+   tensor-core path. Verify windows of 2-5 rows and 2-token-per-draft batches fit.
+   (The limit is lower when T*(k*I + Is)*4 bytes of SwiGLU outputs would exceed
+   200 KB, see moe_layer_describe.) The grouped path needs bf16 routed experts and
+   E a multiple of 16; other layers return MOE_ERR_UNSUPPORTED for larger T. */
 #define MOE_DECODE_MAX_T 8
 
 typedef struct {

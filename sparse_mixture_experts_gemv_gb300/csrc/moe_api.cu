@@ -289,7 +289,9 @@ moe_status_t moe_layer_forward_ex(moe_layer_t* L, const void* x, void* out, int3
   if (logit_bias && ((uintptr_t)logit_bias & 3)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   const bool grouped = (L->cfg.flags & MOE_FLAG_FORCE_GROUPED) || T > L->decode_max_t;
-  if (grouped && L->cfg.weight_format == MOE_WEIGHTS_MXFP4) return MOE_ERR_UNSUPPORTED;
+  // The grouped path serves bf16 routed experts with E a multiple of 16.
+  if (grouped && (L->cfg.weight_format == MOE_WEIGHTS_MXFP4 || L->cfg.num_experts % 16 != 0))
+    return MOE_ERR_UNSUPPORTED;
   L->prof_n = 0;
   cudaError_t e = grouped ? moe::launch_grouped(L, (const uint16_t*)x, (uint16_t*)out, T, logit_bias, s)
                           : moe::launch_decode(L, (const uint16_t*)x, (uint16_t*)out, T, logit_bias, s);

@@ -69,9 +69,15 @@ MOE_DEV int ldg_cg_s32(const int* p) {
 }
 
 // Fire-and-forget prefetch of `bytes` (multiple of 16) starting at a 16-byte
-// aligned global address into L2.
+// aligned global address into L2, issued in pieces of at most 32 KB.
 MOE_DEV void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+  const char* c = static_cast<const char*>(p);
+  while (bytes > 0) {
+    const uint32_t n = bytes < 32768u ? bytes : 32768u;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(c), "r"(n) : "memory");
+    c += n;
+    bytes -= n;
+  }
 }
 
 // ---------------------------------------------------------------------------

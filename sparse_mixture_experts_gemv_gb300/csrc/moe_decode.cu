@@ -19,6 +19,13 @@
 //                     softmax weights and the window's distinct-expert list.
 //   K3 routed_gateup  one pass over the gate/up rows of each distinct expert;
 //                     also prefetches the down rows K4 will need into L2.
+//
+// Latency, not arithmetic, sets the time of a batch-1 layer: each kernel issues
+// its weight loads in batches of 16 x 16 bytes per lane before using any of
+// them, reads its routing metadata in one round trip, and the router's last
+// CTA starts the first routed weights on their way from HBM to L2 (bulk L2
+// prefetch) the moment the routing is known, so HBM keeps streaming across the
+// kernel boundaries.
 //   K4 down_combine   down rows of every distinct expert and of the shared
 //                     expert, weighted by the routing weights, summed, bf16 out.
 #include <cuda_runtime.h>
@@ -112,15 +119,100 @@ __device__ __forceinline__ float dot32_e2m1_f32(const uint4 c, const float* hs, 
 }
 
 // ===========================================================================
-// K1: router logits + shared expert gate/up; last CTA: top-k + window list.
+// Shared pieces
+// ===========================================================================
+// Copy the window's routing metadata into shared memory in one round trip.
+__device__ __forceinline__ void load_meta(const DecodeMeta* m, DecodeMeta* s_meta) {
+  const int* src = reinterpret_cast<const int*>(m);
+  int* dst = reinterpret_cast<int*>(s_meta);
+  constexpr int kWords = (int)(sizeof(DecodeMeta) / 4);
+  for (int q = threadIdx.x; q < kWords; q += blockDim.x) dst[q] = ldg_cg_s32(src + q);
+}
+
+// One batch of a gate/up row pair: 8 chunks of 16 bytes per row per lane.
+__device__ __forceinline__ void gu_load_bf16(const uint8_t* grec, const uint8_t* urec, int b0, int nch,
+                                             uint4 (&v)[16], int lane) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int c = b0 + lane + 32 * q;
+    if (c < nch) {
+      v[q] = ldg_stream(grec + 16 * c);
+      v[8 + q] = ldg_stream(urec + 16 * c);
+    }
+  }
+}
+
+template <int TMAX>
+__device__ __forceinline__ void gu_fma_bf16(const uint4 (&v)[16], int b0, int nch, const uint16_t* xs, int T,
+                                            int H, float (&ag)[TMAX], float (&au)[TMAX], int lane) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int c = b0 + lane + 32 * q;
+    if (c < nch) {
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (t < T) {
+          const uint4 xx = *reinterpret_cast<const uint4*>(xs + t * H + 8 * c);
+          ag[t] += dot8_bf16(v[q], xx);
+          au[t] += dot8_bf16(v[8 + q], xx);
+        }
+      }
+    }
+  }
+}
+
+// MXFP4 row pair: each 16-byte chunk holds 32 codes = one scale block; the
+// scale bytes follow the codes in the row record.
+__device__ __forceinline__ void gu_load_mx(const uint8_t* grec, const uint8_t* urec, int H, int b0, int nch,
+                                           uint4 (&v)[16], uint32_t (&sc)[16], int lane) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int c = b0 + lane + 32 * q;
+    if (c < nch) {
+      v[q] = ldg_stream(grec + 16 * c);
+      v[8 + q] = ldg_stream(urec + 16 * c);
+      sc[q] = __ldg(grec + H / 2 + c);
+      sc[8 + q] = __ldg(urec + H / 2 + c);
+    }
+  }
+}
+
+template <int TMAX>
+__device__ __forceinline__ void gu_fma_mx(const uint4 (&v)[16], const uint32_t (&sc)[16], int b0, int nch,
+                                          const uint16_t* xs, int T, int H, float (&ag)[TMAX], float (&au)[TMAX],
+                                          const float* lut, int lane) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int c = b0 + lane + 32 * q;
+    if (c < nch) {
+      const float sg = e8m0_scale(sc[q]), su = e8m0_scale(sc[8 + q]);
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (t < T) {
+          const uint16_t* xp = xs + t * H + 32 * c;
+          ag[t] = fmaf(dot32_e2m1_bf16(v[q], xp, lut), sg, ag[t]);
+          au[t] = fmaf(dot32_e2m1_bf16(v[8 + q], xp, lut), su, au[t]);
+        }
+      }
+    }
+  }
+}
+
+// ===========================================================================
+// K1: router logits + shared expert gate/up; last CTA: top-k, window list and
+// the L2 prefetch of the first routed weights K3 will read.
 // ===========================================================================
 struct RouterArgs {
   const uint16_t* x;           // bf16 [T][H]
-  int T, H, E, k, Is;
+  int T, H, E, k, I, Is;
   const float* router_t;       // fp32 [E][H]
   const float* router_bias;    // fp32 [E]
   const float* logit_bias;     // fp32 [T][E] or nullptr
   const uint16_t* ws_gu;       // bf16 [Is][2][H]
+  const uint16_t* ws_down;     // bf16 [H][Is]
+  const uint8_t* w_gu;         // routed gate/up records [E][I][2][rb_gu]
+  int64_t rb_gu;
+  int grid_next;               // grid of K3 and K4 (same partitions)
   float* logits;               // [T][E]
   float* h_shared;             // [T][Is]
   int* idx;                    // [T][k]
@@ -132,6 +224,8 @@ struct RouterArgs {
   int force_timeout;
 };
 
+constexpr int kFirstUnits = 16;     // gate/up units per K3 CTA prefetched by the router's last CTA
+
 template <int TMAX>
 __global__ void __launch_bounds__(kRouterThreads)
 router_shared_kernel(const RouterArgs a) {
@@ -139,6 +233,8 @@ router_shared_kernel(const RouterArgs a) {
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [T][H] bf16
   __shared__ int s_idx[kMaxDecodeT * kMaxTopK];
   __shared__ int s_slot_of[kMaxDecodeT * kMaxTopK];
+  __shared__ int s_slot_expert[kMaxSlots];
+  __shared__ int s_D;
   __shared__ unsigned int s_ticket;
 
   // Everything below reads the layer input and overwrites the workspace of the
@@ -146,13 +242,39 @@ router_shared_kernel(const RouterArgs a) {
   pdl_wait();
   pdl_launch_dependents();
 
-  const int T = a.T, H = a.H;
+  const int T = a.T, H = a.H, E = a.E;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   if (a.force_timeout && blockIdx.x == 0 && threadIdx.x == 0) {
     if (!bounded_wait_flag(a.never_set, 2000000LL)) set_error(a.err, kDevTimeout);
   }
+  // Shared-expert down rows of this CTA's twin in K4: start HBM -> L2 now.
+  if (threadIdx.x == 0 && a.Is > 0) {
+    for (int b = blockIdx.x; b < a.grid_next; b += gridDim.x) {
+      const int n0 = (int)((int64_t)b * H / a.grid_next), n1 = (int)((int64_t)(b + 1) * H / a.grid_next);
+      if (n1 > n0) prefetch_l2_bulk(a.ws_down + (int64_t)n0 * a.Is, (uint32_t)((n1 - n0) * a.Is * 2));
+    }
+  }
 
+  const int nwarps = gridDim.x * (kRouterThreads / 32);
+  const int gw = blockIdx.x * (kRouterThreads / 32) + warp;
+  const int units = E + a.Is;
+
+  // First unit of this warp: issue its first batch of loads before x arrives.
+  uint4 v[16];
+  const int u_first = gw;
+  if (u_first < E) {
+    const float* row = a.router_t + (size_t)u_first * H;
+    const int nch = H / 4;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int c = lane + 32 * q;
+      if (c < nch) v[q] = ldg_stream(row + 4 * c);
+    }
+  } else if (u_first < units) {
+    const uint8_t* grec = reinterpret_cast<const uint8_t*>(a.ws_gu + (size_t)(u_first - E) * 2 * H);
+    gu_load_bf16(grec, grec + 2 * H, 0, H / 8, v, lane);
+  }
   {  // x -> shared memory
     const uint4* src = reinterpret_cast<const uint4*>(a.x);
     uint4* dst = reinterpret_cast<uint4*>(xs);
@@ -161,27 +283,26 @@ router_shared_kernel(const RouterArgs a) {
   }
   __syncthreads();
 
-  const int nwarps = gridDim.x * (kRouterThreads / 32);
-  const int gw = blockIdx.x * (kRouterThreads / 32) + warp;
-  const int units = a.E + a.Is;
-  for (int u = gw; u < units; u += nwarps) {
-    if (u < a.E) {
+  for (int u = u_first; u < units; u += nwarps) {
+    const bool preloaded = (u == u_first);
+    if (u < E) {
       // Router row: logits[t][u] = sum_h x[t][h] * W_r[h][u]   (fp32 row of H)
       const float* row = a.router_t + (size_t)u * H;
       const int nch = H / 4;  // 16-byte chunks of 4 floats
       float acc[TMAX];
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-      for (int m0 = 0; m0 < nch; m0 += 32 * 8) {
-        uint4 v[8];
+      for (int b0 = 0; b0 < nch; b0 += 32 * 16) {
+        if (!(preloaded && b0 == 0)) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = m0 + lane + 32 * q;
-          if (c < nch) v[q] = ldg_stream(row + 4 * c);
+          for (int q = 0; q < 16; ++q) {
+            const int c = b0 + lane + 32 * q;
+            if (c < nch) v[q] = ldg_stream(row + 4 * c);
+          }
         }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = m0 + lane + 32 * q;
+        for (int q = 0; q < 16; ++q) {
+          const int c = b0 + lane + 32 * q;
           if (c < nch) {
 #pragma unroll
             for (int t = 0; t < TMAX; ++t) {
@@ -204,48 +325,30 @@ router_shared_kernel(const RouterArgs a) {
           float s = warp_sum(acc[t]);
           if (lane == 0) {
             s += a.router_bias[u];
-            if (a.logit_bias) s += a.logit_bias[(size_t)t * a.E + u];
-            a.logits[(size_t)t * a.E + u] = s;
+            if (a.logit_bias) s += a.logit_bias[(size_t)t * E + u];
+            a.logits[(size_t)t * E + u] = s;
           }
         }
       }
     } else {
       // Shared expert, intermediate feature i: gate row and up row (bf16, H each).
-      const int i = u - a.E;
-      const uint16_t* grow = a.ws_gu + (size_t)i * 2 * H;
-      const uint16_t* urow = grow + H;
+      const int i = u - E;
+      const uint8_t* grec = reinterpret_cast<const uint8_t*>(a.ws_gu + (size_t)i * 2 * H);
+      const uint8_t* urec = grec + 2 * H;
       const int nch = H / 8;
       float ag[TMAX], au[TMAX];
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) ag[t] = au[t] = 0.f;
-      for (int m0 = 0; m0 < nch; m0 += 32 * 8) {
-        uint4 g[8], uu[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = m0 + lane + 32 * q;
-          if (c < nch) { g[q] = ldg_stream(grow + 8 * c); uu[q] = ldg_stream(urow + 8 * c); }
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = m0 + lane + 32 * q;
-          if (c < nch) {
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              if (t < T) {
-                const uint4 xx = *reinterpret_cast<const uint4*>(xs + t * H + 8 * c);
-                ag[t] += dot8_bf16(g[q], xx);
-                au[t] += dot8_bf16(uu[q], xx);
-              }
-            }
-          }
-        }
+      for (int b0 = 0; b0 < nch; b0 += 32 * 8) {
+        if (!(preloaded && b0 == 0)) gu_load_bf16(grec, urec, b0, nch, v, lane);
+        gu_fma_bf16<TMAX>(v, b0, nch, xs, T, H, ag, au, lane);
       }
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) {
         if (t < T) {
           const float gs = warp_sum(ag[t]);
           const float us = warp_sum(au[t]);
-          if (lane == 0) a.h_shared[(size_t)t * a.Is + i] = swiglu(gs, us);
+          if (lane == t) a.h_shared[(size_t)t * a.Is + i] = swiglu(gs, us);
         }
       }
     }
@@ -259,7 +362,7 @@ router_shared_kernel(const RouterArgs a) {
   if (s_ticket != gridDim.x - 1) return;
   __threadfence();
 
-  const int E = a.E, k = a.k;
+  const int k = a.k;
   if (warp < T) {
     const int t = warp;
     constexpr int kPer = kMaxExperts / 32;
@@ -331,7 +434,6 @@ router_shared_kernel(const RouterArgs a) {
     if (first[1]) s_slot_of[lane + 32] = __popc(m0) + __popc(m1 & lt);
     __syncwarp();
     const int D = __popc(m0) + __popc(m1);
-    // Clear slot_j for the window's slots, then fill it.
     for (int q = lane; q < D * kMaxDecodeT; q += 32)
       a.meta->slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = -1;
     __syncwarp();
@@ -340,13 +442,39 @@ router_shared_kernel(const RouterArgs a) {
       const int aidx = lane + 32 * h;
       if (aidx < n) {
         const int slot = s_slot_of[firstpos[h]];
-        if (first[h]) a.meta->slot_expert[slot] = s_idx[aidx];
+        if (first[h]) {
+          a.meta->slot_expert[slot] = s_idx[aidx];
+          s_slot_expert[slot] = s_idx[aidx];
+        }
         a.meta->slot_j[slot][aidx / k] = (signed char)(aidx % k);
       }
     }
     if (lane == 0) {
       a.meta->num_slots = D;
+      s_D = D;
       *a.counter = 0u;  // ready for the next call
+    }
+  }
+  __syncthreads();
+
+  // Routing is known: start the first gate/up units of every K3 CTA on their way
+  // from HBM to L2 while this grid drains and K3 starts.
+  {
+    const int D = s_D, I = a.I;
+    const int64_t U = (int64_t)D * I;
+    const int64_t unit_bytes = 2 * a.rb_gu;
+    for (int b = threadIdx.x; b < a.grid_next; b += blockDim.x) {
+      int64_t u0 = U * b / a.grid_next;
+      const int64_t u1 = U * (b + 1) / a.grid_next;
+      int64_t left = (u1 - u0 < kFirstUnits) ? u1 - u0 : kFirstUnits;
+      while (left > 0) {
+        const int d = (int)(u0 / I), i = (int)(u0 % I);
+        const int64_t run = (I - i < left) ? I - i : left;
+        const uint8_t* p = a.w_gu + ((int64_t)s_slot_expert[d] * I + i) * unit_bytes;
+        prefetch_l2_bulk(p, (uint32_t)(run * unit_bytes));
+        u0 += run;
+        left -= run;
+      }
     }
   }
 }
@@ -361,12 +489,13 @@ struct GateUpArgs {
   int64_t rb_gu;
   const DecodeMeta* meta;
   float* h;                // [T*k][I]
-  // L2 prefetch of what K4 reads (same CTA partition of the H output rows).
+  // L2 prefetch of the down rows K4 reads (same CTA partition of the H output rows)
   const uint8_t* w_down;   // [E][H][rb_down]
   int64_t rb_down;
-  const uint16_t* ws_down; // [H][Is]
-  int Is;
+  int64_t down_prefetch_limit;  // prefetch K4's rows here only if D*H*rb_down <= this
 };
+
+constexpr int kLookahead = 2;  // extra rounds of units each warp keeps on their way to L2
 
 template <int TMAX, class Fmt>
 __global__ void __launch_bounds__(kGemvThreads, 1)
@@ -374,8 +503,7 @@ routed_gateup_kernel(const GateUpArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [T][H]
   __shared__ float lut[16];
-  __shared__ int s_slot_expert[kMaxSlots];
-  __shared__ signed char s_slot_j[kMaxSlots][kMaxDecodeT];
+  __shared__ DecodeMeta s_meta;
 
   const int T = a.T, H = a.H, I = a.I;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -388,107 +516,66 @@ routed_gateup_kernel(const GateUpArgs a) {
 
   pdl_wait();  // routing of this window is complete
   pdl_launch_dependents();
-
-  const int D = ldg_cg_s32(&a.meta->num_slots);
-  for (int q = threadIdx.x; q < D; q += blockDim.x) s_slot_expert[q] = ldg_cg_s32(&a.meta->slot_expert[q]);
-  for (int q = threadIdx.x; q < D * kMaxDecodeT; q += blockDim.x) {
-    const signed char* src = &a.meta->slot_j[0][0];
-    s_slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = *((volatile const signed char*)(src + q));
-  }
+  load_meta(a.meta, &s_meta);
   __syncthreads();
-
-  // Down rows this CTA's twin in K4 will read: start their HBM -> L2 transfer now.
-  if (threadIdx.x == 0) {
-    const int n0 = (int)((int64_t)blockIdx.x * H / gridDim.x);
-    const int n1 = (int)((int64_t)(blockIdx.x + 1) * H / gridDim.x);
-    if (n1 > n0) {
-      for (int d = 0; d < D; ++d) {
-        const uint8_t* p = a.w_down + ((int64_t)s_slot_expert[d] * H + n0) * a.rb_down;
-        prefetch_l2_bulk(p, (uint32_t)((n1 - n0) * a.rb_down));
-      }
-      if (a.Is > 0) prefetch_l2_bulk(a.ws_down + (int64_t)n0 * a.Is, (uint32_t)((n1 - n0) * a.Is * 2));
-    }
-  }
+  const int D = s_meta.num_slots;
 
   const int64_t U = (int64_t)D * I;
-  const int64_t u0 = (int64_t)blockIdx.x * U / gridDim.x;
-  const int64_t u1 = (int64_t)(blockIdx.x + 1) * U / gridDim.x;
-  const int nw = kGemvThreads / 32;
+  const int64_t u0 = U * blockIdx.x / gridDim.x;
+  const int64_t u1 = U * (blockIdx.x + 1) / gridDim.x;
+  constexpr int nw = kGemvThreads / 32;
+  const int64_t unit_bytes = 2 * a.rb_gu;
+  auto unit_ptr = [&](int64_t u) {
+    const int d = (int)(u / I), i = (int)(u % I);
+    return a.w_gu + ((int64_t)s_meta.slot_expert[d] * I + i) * unit_bytes;
+  };
+  // Keep this warp's next rounds of units on their way to L2 (round 0 was
+  // started by the router's last CTA).
+  if (lane == 0) {
+    for (int r = 1; r <= kLookahead; ++r) {
+      const int64_t u = u0 + warp + (int64_t)nw * r;
+      if (u < u1) prefetch_l2_bulk(unit_ptr(u), (uint32_t)unit_bytes);
+    }
+  }
+  // The down rows K4's twin CTA reads, when they fit comfortably in L2.
+  if (threadIdx.x == 32 && (int64_t)D * H * a.rb_down <= a.down_prefetch_limit) {
+    const int n0 = (int)((int64_t)blockIdx.x * H / gridDim.x), n1 = (int)((int64_t)(blockIdx.x + 1) * H / gridDim.x);
+    if (n1 > n0)
+      for (int d = 0; d < D; ++d)
+        prefetch_l2_bulk(a.w_down + ((int64_t)s_meta.slot_expert[d] * H + n0) * a.rb_down,
+                         (uint32_t)((n1 - n0) * a.rb_down));
+  }
 
   for (int64_t u = u0 + warp; u < u1; u += nw) {
+    if (lane == 0 && u + (int64_t)nw * (kLookahead + 1) < u1)
+      prefetch_l2_bulk(unit_ptr(u + (int64_t)nw * (kLookahead + 1)), (uint32_t)unit_bytes);
     const int d = (int)(u / I), i = (int)(u % I);
-    const int e = s_slot_expert[d];
-    const uint8_t* grec = a.w_gu + ((int64_t)e * I + i) * 2 * a.rb_gu;
+    const uint8_t* grec = unit_ptr(u);
     const uint8_t* urec = grec + a.rb_gu;
     float ag[TMAX], au[TMAX];
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) ag[t] = au[t] = 0.f;
-
+    uint4 v[16];
     if constexpr (std::is_same<Fmt, FmtBF16>::value) {
       const int nch = H / 8;  // 16-byte chunks per row
-      for (int m0 = 0; m0 < nch; m0 += 32 * 8) {
-        uint4 g[8], uu[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = m0 + lane + 32 * q;
-          if (c < nch) { g[q] = ldg_stream(grec + 16 * c); uu[q] = ldg_stream(urec + 16 * c); }
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = m0 + lane + 32 * q;
-          if (c < nch) {
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              if (t < T) {
-                const uint4 xx = *reinterpret_cast<const uint4*>(xs + t * H + 8 * c);
-                ag[t] += dot8_bf16(g[q], xx);
-                au[t] += dot8_bf16(uu[q], xx);
-              }
-            }
-          }
-        }
+      for (int b0 = 0; b0 < nch; b0 += 32 * 8) {
+        gu_load_bf16(grec, urec, b0, nch, v, lane);
+        gu_fma_bf16<TMAX>(v, b0, nch, xs, T, H, ag, au, lane);
       }
     } else {
       const int nch = H / 32;  // 16-byte chunks of 32 codes = one scale block each
-      const uint8_t* gsc = grec + H / 2;
-      const uint8_t* usc = urec + H / 2;
-      for (int m0 = 0; m0 < nch; m0 += 32 * 4) {
-        uint4 g[4], uu[4];
-        uint32_t gs[4], us[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c = m0 + lane + 32 * q;
-          if (c < nch) {
-            g[q] = ldg_stream(grec + 16 * c);
-            uu[q] = ldg_stream(urec + 16 * c);
-            gs[q] = gsc[c];
-            us[q] = usc[c];
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c = m0 + lane + 32 * q;
-          if (c < nch) {
-            const float sg = e8m0_scale(gs[q]), su = e8m0_scale(us[q]);
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              if (t < T) {
-                const uint16_t* xp = xs + t * H + 32 * c;
-                ag[t] = fmaf(dot32_e2m1_bf16(g[q], xp, lut), sg, ag[t]);
-                au[t] = fmaf(dot32_e2m1_bf16(uu[q], xp, lut), su, au[t]);
-              }
-            }
-          }
-        }
+      uint32_t sc[16];
+      for (int b0 = 0; b0 < nch; b0 += 32 * 8) {
+        gu_load_mx(grec, urec, H, b0, nch, v, sc, lane);
+        gu_fma_mx<TMAX>(v, sc, b0, nch, xs, T, H, ag, au, lut, lane);
       }
     }
-
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) {
       if (t < T) {
         const float gsum = warp_sum(ag[t]);
         const float usum = warp_sum(au[t]);
-        const int j = s_slot_j[d][t];
+        const int j = s_meta.slot_j[d][t];
         if (lane == t && j >= 0) a.h[((int64_t)t * a.k + j) * I + i] = swiglu(gsum, usum);
       }
     }
@@ -519,20 +606,14 @@ down_combine_kernel(const DownArgs a) {
   float* hss = hs + (size_t)T * k * I;               // [T][Is]
   __shared__ float lut[16];
   __shared__ float s_w[kMaxDecodeT * kMaxTopK];
-  __shared__ int s_slot_expert[kMaxSlots];
-  __shared__ signed char s_slot_j[kMaxSlots][kMaxDecodeT];
+  __shared__ DecodeMeta s_meta;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if constexpr (std::is_same<Fmt, FmtMXFP4>::value) fill_e2m1_lut(lut);
 
   pdl_wait();  // SwiGLU outputs of this window are complete
   pdl_launch_dependents();
 
-  const int D = ldg_cg_s32(&a.meta->num_slots);
-  for (int q = threadIdx.x; q < D; q += blockDim.x) s_slot_expert[q] = ldg_cg_s32(&a.meta->slot_expert[q]);
-  for (int q = threadIdx.x; q < D * kMaxDecodeT; q += blockDim.x) {
-    const signed char* src = &a.meta->slot_j[0][0];
-    s_slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = *((volatile const signed char*)(src + q));
-  }
+  load_meta(a.meta, &s_meta);
   for (int q = threadIdx.x; q < T * k; q += blockDim.x) s_w[q] = ldg_cg_f32(a.weights + q);
   {
     const int n16 = T * k * I / 4;
@@ -543,67 +624,91 @@ down_combine_kernel(const DownArgs a) {
       reinterpret_cast<uint4*>(hss)[q] = ldg_cg(reinterpret_cast<const uint4*>(a.h_shared) + q);
   }
   __syncthreads();
+  const int D = s_meta.num_slots;
 
   const int n0 = (int)((int64_t)blockIdx.x * H / gridDim.x);
   const int n1 = (int)((int64_t)(blockIdx.x + 1) * H / gridDim.x);
-  const int nw = kGemvThreads / 32;
+  constexpr int nw = kGemvThreads / 32;
+  const bool bf = std::is_same<Fmt, FmtBF16>::value;
+  const int nch = bf ? I / 8 : I / 32;   // 16-byte chunks per routed down row
+  const int F = D * nch;
 
   for (int n = n0 + warp; n < n1; n += nw) {
     float acc[TMAX];
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
 
-    for (int d = 0; d < D; ++d) {
-      const uint8_t* rec = a.w_down + ((int64_t)s_slot_expert[d] * H + n) * a.rb_down;
-      if constexpr (std::is_same<Fmt, FmtBF16>::value) {
-        const int nch = I / 8;
-        for (int c = lane; c < nch; c += 32) {
-          const uint4 wv = ldg_stream(rec + 16 * c);
+    // shared expert row (weight 1): loads issued first, consumed last
+    const uint16_t* srow = a.ws_down + (size_t)n * Is;
+    const int snch = Is / 8;
+    uint4 sv[4];
 #pragma unroll
-          for (int t = 0; t < TMAX; ++t) {
-            if (t < T) {
-              const int j = s_slot_j[d][t];
-              if (j >= 0) {
-                const float* hp = hs + ((size_t)t * k + j) * I + 8 * c;
-                const float4 h0 = *reinterpret_cast<const float4*>(hp);
-                const float4 h1 = *reinterpret_cast<const float4*>(hp + 4);
-                acc[t] = fmaf(s_w[t * k + j], dot8_bf16_f32(wv, h0, h1), acc[t]);
-              }
-            }
-          }
+    for (int q = 0; q < 4; ++q) {
+      const int c = lane + 32 * q;
+      if (c < snch) sv[q] = ldg_stream(srow + 8 * c);
+    }
+
+    // routed rows of the window's distinct experts, flattened over (slot, chunk)
+    for (int f0 = 0; f0 < F; f0 += 32 * 16) {
+      uint4 v[16];
+      uint32_t sc[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int f = f0 + lane + 32 * q;
+        if (f < F) {
+          const int d = f / nch, c = f - d * nch;
+          const uint8_t* rec = a.w_down + ((int64_t)s_meta.slot_expert[d] * H + n) * a.rb_down;
+          v[q] = ldg_stream(rec + 16 * c);
+          if (!bf) sc[q] = __ldg(rec + I / 2 + c);
         }
-      } else {
-        const int nch = I / 32;
-        const uint8_t* sc = rec + I / 2;
-        for (int c = lane; c < nch; c += 32) {
-          const uint4 wv = ldg_stream(rec + 16 * c);
-          const float s = e8m0_scale(sc[c]);
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int f = f0 + lane + 32 * q;
+        if (f < F) {
+          const int d = f / nch, c = f - d * nch;
 #pragma unroll
           for (int t = 0; t < TMAX; ++t) {
             if (t < T) {
-              const int j = s_slot_j[d][t];
+              const int j = s_meta.slot_j[d][t];
               if (j >= 0) {
-                const float* hp = hs + ((size_t)t * k + j) * I + 32 * c;
-                acc[t] = fmaf(s_w[t * k + j] * s, dot32_e2m1_f32(wv, hp, lut), acc[t]);
+                if (bf) {
+                  const float* hp = hs + ((size_t)t * k + j) * I + 8 * c;
+                  const float4 h0 = *reinterpret_cast<const float4*>(hp);
+                  const float4 h1 = *reinterpret_cast<const float4*>(hp + 4);
+                  acc[t] = fmaf(s_w[t * k + j], dot8_bf16_f32(v[q], h0, h1), acc[t]);
+                } else {
+                  const float* hp = hs + ((size_t)t * k + j) * I + 32 * c;
+                  acc[t] = fmaf(s_w[t * k + j] * e8m0_scale(sc[q]), dot32_e2m1_f32(v[q], hp, lut), acc[t]);
+                }
               }
             }
           }
         }
       }
     }
-    if (Is > 0) {  // shared expert, weight 1
-      const uint16_t* srow = a.ws_down + (size_t)n * Is;
-      const int nch = Is / 8;
-      for (int c = lane; c < nch; c += 32) {
-        const uint4 wv = ldg_stream(srow + 8 * c);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = lane + 32 * q;
+      if (c < snch) {
 #pragma unroll
         for (int t = 0; t < TMAX; ++t) {
           if (t < T) {
             const float* hp = hss + (size_t)t * Is + 8 * c;
             const float4 h0 = *reinterpret_cast<const float4*>(hp);
             const float4 h1 = *reinterpret_cast<const float4*>(hp + 4);
-            acc[t] += dot8_bf16_f32(wv, h0, h1);
+            acc[t] += dot8_bf16_f32(sv[q], h0, h1);
           }
+        }
+      }
+    }
+    for (int c = lane + 128; c < snch; c += 32) {  // shared rows longer than 128 chunks
+      const uint4 wv = ldg_stream(srow + 8 * c);
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (t < T) {
+          const float* hp = hss + (size_t)t * Is + 8 * c;
+          acc[t] += dot8_bf16_f32(wv, *reinterpret_cast<const float4*>(hp), *reinterpret_cast<const float4*>(hp + 4));
         }
       }
     }
@@ -656,8 +761,11 @@ static cudaError_t launch_decode_t(moe_layer* L, const uint16_t* x, uint16_t* ou
 
   RouterArgs ra;
   ra.x = x; ra.T = T; ra.H = H; ra.E = c.num_experts; ra.k = c.top_k; ra.Is = c.shared_intermediate;
+  ra.I = c.intermediate;
   ra.router_t = L->router_t; ra.router_bias = L->router_bias; ra.logit_bias = logit_bias;
-  ra.ws_gu = L->ws_gu; ra.logits = L->dec.logits; ra.h_shared = L->dec.h_shared;
+  ra.ws_gu = L->ws_gu; ra.ws_down = L->ws_down; ra.w_gu = L->w_gu; ra.rb_gu = L->row_bytes.gu;
+  ra.grid_next = L->num_sms;
+  ra.logits = L->dec.logits; ra.h_shared = L->dec.h_shared;
   ra.idx = L->dec.idx; ra.weights = L->dec.weights; ra.meta = L->dec.meta;
   ra.counter = L->dec.counter; ra.err = L->err; ra.never_set = L->never_set;
   ra.force_timeout = (c.flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? 1 : 0;
@@ -669,8 +777,8 @@ static cudaError_t launch_decode_t(moe_layer* L, const uint16_t* x, uint16_t* ou
   GateUpArgs ga;
   ga.x = x; ga.T = T; ga.H = H; ga.I = c.intermediate; ga.k = c.top_k;
   ga.w_gu = L->w_gu; ga.rb_gu = L->row_bytes.gu; ga.meta = L->dec.meta; ga.h = L->dec.h;
-  ga.w_down = L->w_down; ga.rb_down = L->row_bytes.down; ga.ws_down = L->ws_down;
-  ga.Is = c.shared_intermediate;
+  ga.w_down = L->w_down; ga.rb_down = L->row_bytes.down;
+  ga.down_prefetch_limit = 40ll << 20;
   e = launch_pdl(routed_gateup_kernel<TMAX, Fmt>, L->num_sms, kGemvThreads, xs_bytes, s, ga);
   if (e != cudaSuccess) return e;
   prof_mark(L, s);

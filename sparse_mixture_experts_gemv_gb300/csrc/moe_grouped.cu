@@ -1,10 +1,740 @@
-// Grouped (prefill) path of the MoE layer -- placeholder until the tensor-core kernels land.
+// Grouped (prefill) path of the MoE layer: many tokens per call.
+//
+// "Optimizing on-device inference for Apple Silicon", sections "Prefill: reuse
+// weights, keep routing on the GPU" and "Keep expert routing on the GPU": the
+// grouped GEMM needs each expert's activation rows together, so after top-k a
+// histogram counts the assignments per expert, a prefix scan turns the counts
+// into offsets, a scatter writes the token rows into per-expert groups and a
+// block map lists the fixed-size row blocks the grouped GEMM processes -- all
+// on the GPU, with no host round trip inside the layer. Section "Match tile
+// size to expert load": expert loads are uneven, so tiles follow the actual
+// per-expert row counts (128-row blocks here, any count per expert).
+//
+// Kernels, chained with programmatic dependent launch:
+//   grouped_gemm<ROUTER>  fp32-exact router logits on the tensor cores: W_r is
+//                         split exactly into three bf16 terms (hi + mid + lo), x is
+//                         bf16, so every product is exact and the accumulation is
+//                         fp32 (three passes over K into one TMEM accumulator).
+//   topk_hist             per-token top-k + renormalised softmax weights; per
+//                         32-token chunk expert histogram.
+//   dispatch_scan         per-expert totals, chunk bases, offsets, block map.
+//   dispatch_scatter      grouped row of every (token, slot), token order kept.
+//   grouped_gemm<SWIGLU>  gate/up for every expert group (+ the shared expert
+//                         over all tokens), A rows gathered from x by cp.async,
+//                         SwiGLU in the epilogue, bf16 h in grouped order.
+//   grouped_gemm<STORE>   down projection of every group (TMA A = h), bf16 y.
+//   combine               out[t] = sum_j w[t,j] y[pos[t,j]] + y_shared[t].
+//
+// The grouped GEMM is a persistent, warp-specialised tcgen05 kernel: warp 0
+// issues TMA loads, warp 1 owns tensor memory and issues the MMAs, warps 2-5
+// drain the double-buffered TMEM accumulators; for gathered A, warps 6-9 copy
+// the token rows with cp.async into the 128-byte-swizzled layout.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "moe_common.cuh"
 #include "moe_internal.h"
+#include "moe_sm100.cuh"
 
 namespace moe {
-cudaError_t grouped_prepare(moe_layer*) { return cudaSuccess; }
-void grouped_release(moe_layer*) {}
-cudaError_t launch_grouped(moe_layer*, const uint16_t*, uint16_t*, int, const float*, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128;                  // rows (tokens) per tile = TMEM lanes
+constexpr int BK = 64;                   // bf16 per 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kStageA = BM * BK * 2;     // 16 KB
+constexpr int kStageB = 256 * BK * 2;    // 32 KB (N up to 256)
+constexpr int kTmemCols = 512;           // two 256-column fp32 accumulators
+constexpr int kChunk = 32;               // tokens per dispatch chunk
+constexpr size_t kGemmSmem = (size_t)kStages * (kStageA + kStageB) + 1024 /*align*/ + 256 /*barriers*/;
+
+enum Epi { EPI_ROUTER = 0, EPI_SWIGLU = 1, EPI_STORE = 2 };
+
+struct GemmParams {
+  // Tiles: routed M-blocks come from the block map (count in device memory),
+  // shared-expert M-blocks cover the tokens directly.
+  const int2* mtiles;       // [R] (expert, first grouped row); nullptr for the router
+  const int* num_routed;    // device count R (nullptr: R = n_routed_static)
+  int n_routed_static;
+  int n_shared_mtiles;      // S
+  int nt_routed, nt_shared; // N tiles per M-block
+  int ks_routed, ks_shared; // 64-wide K steps per tile
+  int ks_part;              // router: K steps per bf16 term
+  int BN;
+  int max_mtiles;           // capacity of the block map
+  int E;
+  int T;
+  int k;
+  const int* offsets;       // [E + 1] grouped-row offsets
+  // gathered A (gate/up)
+  const uint16_t* x;        // bf16 [T][H]
+  int H;
+  const int* perm;          // [T*k] assignment t*k+j at each grouped row
+  // B rows of expert e start at e * b_rows_per_expert (routed map)
+  int b_rows_per_expert;
+  // epilogue outputs
+  uint16_t* out_routed; int ld_routed;
+  uint16_t* out_shared; int ld_shared;
+  float* logits; const float* router_bias; const float* logit_bias;
+  int* err;
+};
+
+struct TileInfo {
+  bool shared;
+  int e, row0, row_end, nt, ks;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int R, int tile) {
+  TileInfo ti;
+  const int routed_tiles = R * p.nt_routed;
+  if (tile < routed_tiles) {
+    const int m = tile / p.nt_routed;
+    ti.shared = false;
+    ti.nt = tile % p.nt_routed;
+    ti.ks = p.ks_routed;
+    if (p.mtiles) {
+      const int2 mt = p.mtiles[m];
+      const int TK = p.T * p.k;
+      if (mt.x < 0 || mt.x >= p.E || mt.y < 0 || mt.y >= TK) {  // inconsistent block map
+        set_error(p.err, kDevCheck);
+        ti.e = 0; ti.row0 = 0; ti.row_end = 0;
+      } else {
+        ti.e = mt.x;
+        ti.row0 = mt.y;
+        ti.row_end = min(p.offsets[mt.x + 1], TK);
+      }
+    } else {  // router: plain token blocks
+      ti.e = 0;
+      ti.row0 = m * BM;
+      ti.row_end = p.T;
+    }
+  } else {
+    const int t2 = tile - routed_tiles;
+    ti.shared = true;
+    ti.e = p.E;
+    ti.nt = t2 % p.nt_shared;
+    ti.row0 = (t2 / p.nt_shared) * BM;
+    ti.row_end = p.T;
+    ti.ks = p.ks_shared;
+  }
+  return ti;
 }
+
+template <int EPI, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_constant__ CUtensorMap mapA_s,
+                    const __grid_constant__ CUtensorMap mapB_r, const __grid_constant__ CUtensorMap mapB_s,
+                    const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kStageA;
+  uint64_t* full = (uint64_t*)(sB + kStages * kStageB);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = (uint32_t*)(drain + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1 + (GATHER ? 128 : 0));
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&mapB_r);
+    prefetch_tmap(&mapB_s);
+    if (!GATHER) { prefetch_tmap(&mapA_r); prefetch_tmap(&mapA_s); }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_wait();  // routing / dispatch / SwiGLU outputs of this call are complete
+  pdl_launch_dependents();
+
+  int R = p.num_routed ? ldg_cg_s32(p.num_routed) : p.n_routed_static;
+  if (R < 0 || R > p.max_mtiles) {
+    if (threadIdx.x == 0) set_error(p.err, kDevCheck);
+    R = 0;
+  }
+  const int total = R * p.nt_routed + p.n_shared_mtiles * p.nt_shared;
+  const uint32_t idesc = idesc_bf16_f32(BM, p.BN);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      const uint32_t bytes = (uint32_t)p.BN * BK * 2 + (GATHER ? 0u : (uint32_t)kStageA);
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(p, R, tile);
+        for (int kb = 0; kb < ti.ks; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, abort_flag)) break;
+          mbar_arrive_expect_tx(&full[s], bytes);
+          int kcol = kb * BK, brow;
+          if (EPI == EPI_ROUTER) {
+            const int part = kb / p.ks_part;       // 0: hi, 1: mid, 2: lo
+            kcol = (kb % p.ks_part) * BK;
+            brow = part * p.E + ti.nt * p.BN;
+          } else {
+            brow = (ti.shared ? 0 : ti.e * p.b_rows_per_expert) + ti.nt * p.BN;
+          }
+          tma_load_2d(sB + s * kStageB, ti.shared ? &mapB_s : &mapB_r, kcol, brow, &full[s]);
+          if (!GATHER) tma_load_2d(sA + s * kStageA, ti.shared ? &mapA_s : &mapA_r, kcol, ti.row0, &full[s]);
+        }
+      }
+      if (*abort_flag) {  // let copies already issued land before the CTA exits
+        for (uint32_t q = (it > (uint32_t)kStages ? it - kStages : 0); q < it; ++q)
+          mbar_wait(&full[q % kStages], (q / kStages) & 1, p.err, abort_flag, 20000000LL, false);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, tc = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++tc) {
+        const TileInfo ti = decode_tile(p, R, tile);
+        const int ab = tc & 1;
+        if (!mbar_wait(&acc_empty[ab], ((tc >> 1) & 1) ^ 1, p.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + ab * 256;
+        bool ok = true;
+        for (int kb = 0; kb < ti.ks; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&full[s], (it / kStages) & 1, p.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * kStageA), b0 = smem_u32(sB + s * kStageB);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
+                     (kb | kk) != 0 ? 1u : 0u);
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[ab]);
+      }
+      // all issued MMAs complete before tensor memory is released
+      mma_commit(drain);
+      mbar_wait(drain, 0, p.err, abort_flag, 2000000000LL, false);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;           // TMEM lane quadrant this warp may access
+    const int r = q * 32 + lane;      // tile row = TMEM lane
+    uint32_t tc = 0;
+    for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++tc) {
+      const TileInfo ti = decode_tile(p, R, tile);
+      const int ab = tc & 1;
+      if (!mbar_wait(&acc_full[ab], (tc >> 1) & 1, p.err, abort_flag)) break;
+      tc_fence_after();
+      const int gr = ti.row0 + r;
+      const bool valid = gr < ti.row_end;
+      const uint32_t taddr = tmem + ab * 256 + ((uint32_t)(q * 32) << 16);
+      for (int c0 = 0; c0 < p.BN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + c0, v);
+        if (!valid) continue;
+        if (EPI == EPI_SWIGLU) {
+          // columns alternate gate / up of intermediate features i0 + c0/2 + (0..15)
+          uint32_t packed[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float h0 = swiglu(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]));
+            const float h1 = swiglu(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            packed[i] = (uint32_t)f32_to_bf16_rne(h0) | ((uint32_t)f32_to_bf16_rne(h1) << 16);
+          }
+          uint16_t* dst = ti.shared ? p.out_shared + (size_t)gr * p.ld_shared
+                                    : p.out_routed + (size_t)gr * p.ld_routed;
+          dst += ti.nt * (p.BN / 2) + c0 / 2;
+          reinterpret_cast<uint4*>(dst)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          reinterpret_cast<uint4*>(dst)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        } else if (EPI == EPI_STORE) {
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[i] = (uint32_t)f32_to_bf16_rne(__uint_as_float(v[2 * i])) |
+                        ((uint32_t)f32_to_bf16_rne(__uint_as_float(v[2 * i + 1])) << 16);
+          uint16_t* dst = ti.shared ? p.out_shared + (size_t)gr * p.ld_shared
+                                    : p.out_routed + (size_t)gr * p.ld_routed;
+          dst += ti.nt * p.BN + c0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            reinterpret_cast<uint4*>(dst)[i] =
+                make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        } else {  // EPI_ROUTER: fp32 logits + biases
+          const int e0 = ti.nt * p.BN + c0;
+          const int ncol = min(32, p.BN - c0);
+          float* dst = p.logits + (size_t)gr * p.E + e0;
+          const float* lb = p.logit_bias ? p.logit_bias + (size_t)gr * p.E + e0 : nullptr;
+          for (int i = 0; i < ncol; i += 4) {
+            float4 o;
+            o.x = __uint_as_float(v[i + 0]) + p.router_bias[e0 + i + 0];
+            o.y = __uint_as_float(v[i + 1]) + p.router_bias[e0 + i + 1];
+            o.z = __uint_as_float(v[i + 2]) + p.router_bias[e0 + i + 2];
+            o.w = __uint_as_float(v[i + 3]) + p.router_bias[e0 + i + 3];
+            if (lb) { o.x += lb[i]; o.y += lb[i + 1]; o.z += lb[i + 2]; o.w += lb[i + 3]; }
+            *reinterpret_cast<float4*>(dst + i) = o;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[ab]);
+    }
+  } else {
+    // ------------------------------------------------------------ A gather (gate/up)
+    if (GATHER) {
+      const int r = threadIdx.x - 192;   // tile row this thread copies
+      uint32_t it = 0;
+      int pending = -1;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(p, R, tile);
+        const int gr = ti.row0 + r;
+        int token = -1;
+        if (gr < ti.row_end) {
+          if (ti.shared) {
+            token = gr;
+          } else {
+            const int a = p.perm[gr];
+            if (a >= 0 && a < p.T * p.k) token = a / p.k;
+            else set_error(p.err, kDevCheck);
+          }
+        }
+        const uint16_t* src = p.x + (size_t)(token < 0 ? 0 : token) * p.H;
+        const uint32_t nbytes = token < 0 ? 0u : 16u;
+        bool ok = true;
+        for (int kb = 0; kb < ti.ks; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
+          uint8_t* dst = sA + s * kStageA + r * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) cp_async_16(dst + ((j ^ (r & 7)) << 4), src + kb * BK + j * 8, nbytes);
+          cp_async_commit();
+          if (pending >= 0) {
+            cp_async_wait<1>();
+            fence_proxy_async_smem();
+            mbar_arrive(&full[pending]);
+          }
+          pending = s;
+        }
+        if (!ok) break;
+      }
+      cp_async_wait<0>();
+      if (pending >= 0) {
+        fence_proxy_async_smem();
+        mbar_arrive(&full[pending]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ===========================================================================
+// Routing: top-k per token, per-chunk histogram
+// ===========================================================================
+__global__ void __launch_bounds__(256)
+topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k, int* __restrict__ idx,
+                 float* __restrict__ weights, int* __restrict__ chunk_counts) {
+  __shared__ int s_count[kMaxExperts];
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_count[e] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kPer = kMaxExperts / 32;
+  for (int tl = warp; tl < kChunk; tl += 8) {
+    const int t = blockIdx.x * kChunk + tl;
+    if (t >= T) break;
+    uint32_t key[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int e = lane + 32 * j;
+      key[j] = (e < E) ? f32_order_key(logits[(size_t)t * E + e]) : 0u;
+    }
+    float sel_v[kMaxTopK];
+    int sel_e[kMaxTopK];
+#pragma unroll
+    for (int r = 0; r < kMaxTopK; ++r) {
+      if (r < k) {
+        uint32_t lk = 0u;
+        int lj = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+          if (key[j] > lk) { lk = key[j]; lj = j; }
+        const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, lk);
+        const uint32_t cand = (lk == gmax) ? (uint32_t)(lane + 32 * lj) : 0xFFFFFFFFu;
+        const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
+        if (lane == (int)(gidx & 31u)) {
+#pragma unroll
+          for (int j = 0; j < kPer; ++j)
+            if (j == (int)(gidx >> 5)) key[j] = 0u;
+        }
+        sel_v[r] = f32_from_order_key(gmax);
+        sel_e[r] = (int)gidx;
+      }
+    }
+    float ex[kMaxTopK], sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxTopK; ++r)
+      if (r < k) { ex[r] = expf(sel_v[r] - sel_v[0]); sum += ex[r]; }
+#pragma unroll
+    for (int r = 0; r < kMaxTopK; ++r) {
+      if (r < k && lane == r) {
+        idx[(size_t)t * k + r] = sel_e[r];
+        weights[(size_t)t * k + r] = ex[r] / sum;
+        atomicAdd(&s_count[sel_e[r]], 1);
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + e] = s_count[e];
+}
+
+// One CTA, one thread per expert: chunk bases, totals, offsets, block map.
+__global__ void __launch_bounds__(512)
+dispatch_scan_kernel(int* __restrict__ chunk_counts /* in: counts, out: bases */, int num_chunks, int E, int T,
+                     int k, int* __restrict__ hist, int* __restrict__ offsets, int2* __restrict__ mtiles,
+                     int* __restrict__ num_routed, int max_mtiles, int* __restrict__ err) {
+  __shared__ int s_tot[kMaxExperts];
+  __shared__ int s_tiles[kMaxExperts];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int c = 0; c < num_chunks; ++c) {
+      int* p = chunk_counts + (size_t)c * E + e;
+      const int v = *p;
+      *p = run;
+      run += v;
+    }
+    hist[e] = run;
+  }
+  s_tot[e] = (e < E) ? run : 0;
+  s_tiles[e] = (e < E) ? (run + BM - 1) / BM : 0;
+  __syncthreads();
+  // exclusive scans over experts (E <= 512, simple two-array Hillis-Steele)
+  for (int d = 1; d < blockDim.x; d <<= 1) {
+    int a = 0, b = 0;
+    if (e >= d) { a = s_tot[e - d]; b = s_tiles[e - d]; }
+    __syncthreads();
+    s_tot[e] += a;
+    s_tiles[e] += b;
+    __syncthreads();
+  }
+  if (e < E) {
+    const int off = s_tot[e] - run;  // exclusive
+    const int ntile = (run + BM - 1) / BM;
+    const int tile0 = s_tiles[e] - ntile;
+    offsets[e] = off;
+    for (int m = 0; m < ntile; ++m) {
+      if (tile0 + m < max_mtiles) mtiles[tile0 + m] = make_int2(e, off + m * BM);
+      else set_error(err, kDevCheck);
+    }
+    if (e == E - 1) {
+      offsets[E] = off + run;  // == T * k
+      *num_routed = tile0 + ntile;
+    }
+  }
+}
+
+// Grouped row of every assignment: offsets[e] + chunk base + rank within the chunk.
+__global__ void __launch_bounds__(256)
+dispatch_scatter_kernel(const int* __restrict__ idx, const int* __restrict__ chunk_bases,
+                        const int* __restrict__ offsets, int T, int E, int k, int* __restrict__ perm,
+                        int* __restrict__ pos, int* __restrict__ err) {
+  __shared__ int s_idx[kChunk * kMaxTopK];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t0 = blockIdx.x * kChunk;
+  const int n = min(kChunk, T - t0) * k;
+  for (int a = threadIdx.x; a < n; a += blockDim.x) s_idx[a] = idx[(size_t)t0 * k + a];
+  __syncthreads();
+  for (int a = threadIdx.x; a < n; a += blockDim.x) {
+    const int e = s_idx[a];
+    if (e < 0 || e >= E) { set_error(err, kDevCheck); continue; }
+    const int tl = a / k;
+    int rank = 0;
+    for (int b = 0; b < tl * k; ++b) rank += (s_idx[b] == e);
+    const int g = offsets[e] + chunk_bases[(size_t)blockIdx.x * E + e] + rank;
+    if (g < 0 || g >= T * k) { set_error(err, kDevCheck); continue; }
+    perm[g] = t0 * k + a;
+    pos[(size_t)t0 * k + a] = g;
+  }
+}
+
+// out[t, :] = sum_j w[t, j] * y[pos[t, j], :] + y_shared[t, :], fp32 sum, bf16 out.
+__global__ void __launch_bounds__(256)
+combine_kernel(const uint16_t* __restrict__ y, const uint16_t* __restrict__ ys, const int* __restrict__ pos,
+               const float* __restrict__ w, int T, int H, int k, int has_shared, uint16_t* __restrict__ out,
+               int* __restrict__ err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int chunks = H / 8;
+  const size_t n = (size_t)T * chunks;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n; q += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(q / chunks), c = (int)(q % chunks);
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int r = pos[(size_t)t * k + j];
+      if (r < 0 || r >= T * k) { set_error(err, kDevCheck); continue; }
+      const float wt = w[(size_t)t * k + j];
+      const uint4 v = *reinterpret_cast<const uint4*>(y + (size_t)r * H + 8 * c);
+      acc[0] = fmaf(wt, bf16_lo(v.x), acc[0]); acc[1] = fmaf(wt, bf16_hi(v.x), acc[1]);
+      acc[2] = fmaf(wt, bf16_lo(v.y), acc[2]); acc[3] = fmaf(wt, bf16_hi(v.y), acc[3]);
+      acc[4] = fmaf(wt, bf16_lo(v.z), acc[4]); acc[5] = fmaf(wt, bf16_hi(v.z), acc[5]);
+      acc[6] = fmaf(wt, bf16_lo(v.w), acc[6]); acc[7] = fmaf(wt, bf16_hi(v.w), acc[7]);
+    }
+    if (has_shared) {
+      const uint4 v = *reinterpret_cast<const uint4*>(ys + (size_t)t * H + 8 * c);
+      acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x); acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+      acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z); acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
+    }
+    uint4 o;
+    o.x = (uint32_t)f32_to_bf16_rne(acc[0]) | ((uint32_t)f32_to_bf16_rne(acc[1]) << 16);
+    o.y = (uint32_t)f32_to_bf16_rne(acc[2]) | ((uint32_t)f32_to_bf16_rne(acc[3]) << 16);
+    o.z = (uint32_t)f32_to_bf16_rne(acc[4]) | ((uint32_t)f32_to_bf16_rne(acc[5]) << 16);
+    o.w = (uint32_t)f32_to_bf16_rne(acc[6]) | ((uint32_t)f32_to_bf16_rne(acc[7]) << 16);
+    *reinterpret_cast<uint4*>(out + (size_t)t * H + 8 * c) = o;
+  }
+}
+
+// ===========================================================================
+// Host side
+// ===========================================================================
+struct GroupedMaps {
+  CUtensorMap router_split;  // B router: [3E][H] bf16, box {64, BNr}
+  CUtensorMap w_gu;          // B gate/up routed: [E*2I][H], box {64, 256}
+  CUtensorMap ws_gu;         // B gate/up shared: [2Is][H], box {64, 256}
+  CUtensorMap h;             // A down routed: [Tmax*k][I], box {64, 128}
+  CUtensorMap hs;            // A down shared: [Tmax][Is], box {64, 128}
+  CUtensorMap w_down;        // B down routed: [E*H][I], box {64, 256}
+  CUtensorMap ws_down;       // B down shared: [H][Is], box {64, 256}
+  int router_bn;
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t get_encoder() {
+  if (g_encode) return cudaSuccess;
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+  g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  return cudaSuccess;
+}
+
+// 2-D bf16 map over a row-major [rows][cols] matrix, box {64 cols, box_rows rows},
+// 128-byte swizzle, zero fill outside the matrix.
+cudaError_t encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <class K, class... A>
+cudaError_t launch_pdl(K kernel, int grid, int block, size_t smem, cudaStream_t s, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace
+
+cudaError_t grouped_prepare(moe_layer* L) {
+  const auto& c = L->cfg;
+  auto& g = L->grp;
+  const int Tm = c.max_tokens, k = c.top_k, E = c.num_experts, H = c.hidden, I = c.intermediate,
+            Is = c.shared_intermediate;
+  memset(&g, 0, sizeof(g));
+  g.max_tokens = Tm;
+  const int chunks = (Tm + kChunk - 1) / kChunk;
+  g.max_tiles = (Tm * k + BM - 1) / BM + E + 1;
+  const size_t TK = (size_t)Tm * k;
+  cudaError_t e;
+#define GALLOC(ptr, bytes)                                                    \
+  do {                                                                        \
+    e = cudaMalloc((void**)&(ptr), (bytes) ? (bytes) : 16);                   \
+    if (e != cudaSuccess) return e;                                           \
+  } while (0)
+  GALLOC(g.logits, sizeof(float) * (size_t)Tm * E);
+  GALLOC(g.idx, sizeof(int) * TK);
+  GALLOC(g.weights, sizeof(float) * TK);
+  GALLOC(g.hist, sizeof(int) * (E + 1));
+  GALLOC(g.offsets, sizeof(int) * (E + 2));
+  GALLOC(g.chunk_counts, sizeof(int) * (size_t)chunks * E);
+  GALLOC(g.perm, sizeof(int) * TK);
+  GALLOC(g.pos, sizeof(int) * TK);
+  GALLOC(g.tiles, sizeof(int2) * g.max_tiles);
+  GALLOC(g.num_tiles, sizeof(int) * 4);
+  GALLOC(g.h, sizeof(uint16_t) * TK * I);
+  GALLOC(g.hs, sizeof(uint16_t) * (size_t)Tm * (Is > 0 ? Is : 1));
+  GALLOC(g.y, sizeof(uint16_t) * TK * H);
+  GALLOC(g.ys, sizeof(uint16_t) * (size_t)Tm * H);
+#undef GALLOC
+
+  if ((e = get_encoder()) != cudaSuccess) return e;
+  GroupedMaps* m = new GroupedMaps();
+  L->tmaps = m;
+  m->router_bn = (E % 64 == 0) ? 64 : (E % 32 == 0 ? 32 : 16);  // N tile dividing E (E % 16 == 0)
+  if ((e = encode_2d(&m->router_split, L->router_split, 3ull * E, H, m->router_bn)) != cudaSuccess) return e;
+  if ((e = encode_2d(&m->h, g.h, TK, I, BM)) != cudaSuccess) return e;
+  if (c.weight_format == MOE_WEIGHTS_BF16) {  // the grouped path serves bf16 routed experts
+    if ((e = encode_2d(&m->w_gu, L->w_gu, (uint64_t)E * 2 * I, H, 256)) != cudaSuccess) return e;
+    if ((e = encode_2d(&m->w_down, L->w_down, (uint64_t)E * H, I, 256)) != cudaSuccess) return e;
+  } else {
+    m->w_gu = m->h;
+    m->w_down = m->h;
+  }
+  if (Is > 0) {
+    if ((e = encode_2d(&m->ws_gu, L->ws_gu, 2ull * Is, H, 256)) != cudaSuccess) return e;
+    if ((e = encode_2d(&m->hs, g.hs, (uint64_t)Tm, Is, BM)) != cudaSuccess) return e;
+    if ((e = encode_2d(&m->ws_down, L->ws_down, (uint64_t)H, Is, 256)) != cudaSuccess) return e;
+  } else {
+    m->ws_gu = m->w_gu;
+    m->hs = m->h;
+    m->ws_down = m->w_down;
+  }
+  e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_ROUTER, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_SWIGLU, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_STORE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+  return e;
+}
+
+void grouped_release(moe_layer* L) {
+  auto& g = L->grp;
+  void* ptrs[] = {g.logits, g.idx, g.weights, g.hist, g.offsets, g.chunk_counts, g.perm, g.pos,
+                  g.tiles, g.num_tiles, g.h, g.hs, g.y, g.ys};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  memset(&g, 0, sizeof(g));
+  delete reinterpret_cast<GroupedMaps*>(L->tmaps);
+  L->tmaps = nullptr;
+}
+
+cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
+                           cudaStream_t s) {
+  const auto& c = L->cfg;
+  auto& g = L->grp;
+  GroupedMaps* m = reinterpret_cast<GroupedMaps*>(L->tmaps);
+  const int E = c.num_experts, k = c.top_k, H = c.hidden, I = c.intermediate, Is = c.shared_intermediate;
+  const int mt_tokens = (T + BM - 1) / BM;
+  const int chunks = (T + kChunk - 1) / kChunk;
+  cudaError_t e;
+
+  CUtensorMap map_x;
+  if ((e = encode_2d(&map_x, x, (uint64_t)T, H, BM)) != cudaSuccess) return e;
+
+  GemmParams base;
+  memset(&base, 0, sizeof(base));
+  base.E = E; base.T = T; base.k = k; base.H = H; base.err = L->err; base.max_mtiles = g.max_tiles;
+
+  // 1. router logits (tensor cores, exact 3-term split of W_r)
+  prof_mark(L, s);
+  {
+    GemmParams p = base;
+    p.mtiles = nullptr; p.num_routed = nullptr;
+    p.BN = m->router_bn;
+    p.n_routed_static = mt_tokens; p.nt_routed = E / p.BN; p.ks_part = H / BK; p.ks_routed = 3 * (H / BK);
+    p.n_shared_mtiles = 0; p.nt_shared = 1; p.ks_shared = 0;
+    p.logits = g.logits; p.router_bias = L->router_bias; p.logit_bias = logit_bias;
+    const int tiles = mt_tokens * p.nt_routed;
+    e = launch_pdl(grouped_gemm_kernel<EPI_ROUTER, false>, tiles < L->num_sms ? tiles : L->num_sms, 192,
+                   kGemmSmem, s, map_x, map_x, m->router_split, m->router_split, p);
+    if (e != cudaSuccess) return e;
+  }
+  prof_mark(L, s);
+  // 2-4. top-k, histogram, scan, block map, scatter
+  e = launch_pdl(topk_hist_kernel, chunks, 256, 0, s, (const float*)g.logits, T, E, k, g.idx, g.weights,
+                 g.chunk_counts);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(dispatch_scan_kernel, 1, 512, 0, s, g.chunk_counts, chunks, E, T, k, g.hist, g.offsets,
+                 (int2*)g.tiles, g.num_tiles, g.max_tiles, L->err);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(dispatch_scatter_kernel, chunks, 256, 0, s, (const int*)g.idx, (const int*)g.chunk_counts,
+                 (const int*)g.offsets, T, E, k, g.perm, g.pos, L->err);
+  if (e != cudaSuccess) return e;
+  prof_mark(L, s);
+  // 5. gate/up + SwiGLU (routed groups, then the shared expert over all tokens)
+  {
+    GemmParams p = base;
+    p.mtiles = (const int2*)g.tiles; p.num_routed = g.num_tiles; p.offsets = g.offsets;
+    p.BN = 256;
+    p.nt_routed = 2 * I / 256; p.ks_routed = H / BK;
+    p.n_shared_mtiles = Is > 0 ? mt_tokens : 0; p.nt_shared = Is > 0 ? 2 * Is / 256 : 1; p.ks_shared = H / BK;
+    p.x = x; p.perm = g.perm; p.b_rows_per_expert = 2 * I;
+    p.out_routed = g.h; p.ld_routed = I; p.out_shared = g.hs; p.ld_shared = Is;
+    e = launch_pdl(grouped_gemm_kernel<EPI_SWIGLU, true>, L->num_sms, 320, kGemmSmem, s, map_x, map_x, m->w_gu,
+                   m->ws_gu, p);
+    if (e != cudaSuccess) return e;
+  }
+  prof_mark(L, s);
+  // 6. down projection (routed groups + shared)
+  {
+    GemmParams p = base;
+    p.mtiles = (const int2*)g.tiles; p.num_routed = g.num_tiles; p.offsets = g.offsets;
+    p.BN = 256;
+    p.nt_routed = H / 256; p.ks_routed = I / BK;
+    p.n_shared_mtiles = Is > 0 ? mt_tokens : 0; p.nt_shared = H / 256; p.ks_shared = Is > 0 ? Is / BK : 1;
+    p.b_rows_per_expert = H;
+    p.out_routed = g.y; p.ld_routed = H; p.out_shared = g.ys; p.ld_shared = H;
+    e = launch_pdl(grouped_gemm_kernel<EPI_STORE, false>, L->num_sms, 192, kGemmSmem, s, m->h, m->hs, m->w_down,
+                   m->ws_down, p);
+    if (e != cudaSuccess) return e;
+  }
+  prof_mark(L, s);
+  // 7. weighted combine
+  {
+    const size_t n = (size_t)T * (H / 8);
+    int grid = (int)((n + 255) / 256);
+    if (grid > 8 * L->num_sms) grid = 8 * L->num_sms;
+    e = launch_pdl(combine_kernel, grid, 256, 0, s, (const uint16_t*)g.y, (const uint16_t*)g.ys,
+                   (const int*)g.pos, (const float*)g.weights, T, H, k, Is > 0 ? 1 : 0, out, L->err);
+    if (e != cudaSuccess) return e;
+  }
+  prof_mark(L, s);
+  return cudaSuccess;
+}
+
 }  // namespace moe

@@ -38,19 +38,21 @@ struct DecodeWorkspace {
 
 struct GroupedWorkspace {
   int max_tokens;
+  int max_tiles;
   float* logits;         // [T][E]
   int* idx;              // [T][k]
   float* weights;        // [T][k]
-  int* hist;             // [E + 1] (slot E = shared expert)
-  int* offsets;          // [E + 2]
-  int* chunk_counts;     // [num_chunks][E]
-  int* perm;             // [T*k]  assignment at each grouped row
+  int* hist;             // [E]
+  int* offsets;          // [E + 1] grouped-row offsets (offsets[E] = T*k)
+  int* chunk_counts;     // [chunks][E] per 32-token chunk counts, then chunk bases
+  int* perm;             // [T*k]  assignment t*k+j at each grouped row
   int* pos;              // [T*k]  grouped row of each assignment
-  int* tiles;            // [max_tiles] packed (expert << 20 | row0 >> 7)... see grouped path
-  int* num_tiles;        // [2]: gate/up tiles, down tiles
-  uint16_t* h;           // bf16 [T*k + T][I or Is]  SwiGLU outputs in grouped order (+ shared rows)
-  uint16_t* y;           // bf16 [T*k + T][H]        weighted down outputs in grouped order
-  int max_tiles;
+  int* tiles;            // int2 [max_tiles] (expert, first grouped row) of each 128-row block
+  int* num_tiles;        // [1] number of routed 128-row blocks
+  uint16_t* h;           // bf16 [T*k][I]  SwiGLU outputs in grouped order
+  uint16_t* hs;          // bf16 [T][Is]   shared-expert SwiGLU outputs
+  uint16_t* y;           // bf16 [T*k][H]  down outputs in grouped order
+  uint16_t* ys;          // bf16 [T][H]    shared-expert down outputs
 };
 
 }  // namespace moe
