@@ -122,14 +122,16 @@ moe_status_t alloc_workspace(LayerOwner* o) {
   GET(L.dec.meta, sizeof(moe::DecodeMeta));
   GET(L.dec.h, sizeof(float) * (size_t)T8 * c.top_k * c.intermediate);
   GET(L.dec.h_shared, sizeof(float) * (size_t)T8 * std::max(c.shared_intermediate, 1));
-  GET(L.dec.counter, sizeof(unsigned int));
+  GET(L.dec.sync_ctr, sizeof(unsigned long long) * 2);
+  GET(L.dec.sync_flag, sizeof(unsigned long long) * 2);
   GET(L.err, sizeof(int) * 4);
   GET(L.never_set, sizeof(int));
   GET(L.x_stage, sizeof(uint16_t) * (size_t)c.max_tokens * c.hidden);
   GET(L.out_stage, sizeof(uint16_t) * (size_t)c.max_tokens * c.hidden);
   GET(L.bias_stage, sizeof(float) * (size_t)c.max_tokens * c.num_experts);
 #undef GET
-  cudaMemset(L.dec.counter, 0, sizeof(unsigned int));
+  cudaMemset(L.dec.sync_ctr, 0, sizeof(unsigned long long) * 2);
+  cudaMemset(L.dec.sync_flag, 0, sizeof(unsigned long long) * 2);
   cudaMemset(L.err, 0, sizeof(int) * 4);
   cudaMemset(L.never_set, 0, sizeof(int));
   cudaMemset(L.dec.meta, 0, sizeof(moe::DecodeMeta));
@@ -255,7 +257,8 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
     destroy_owner(o);
     return st;
   }
-  e = moe::grouped_prepare(&L);
+  e = moe::decode_prepare(&L);
+  if (e == cudaSuccess) e = moe::grouped_prepare(&L);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     st = (e == cudaErrorMemoryAllocation) ? MOE_ERR_OOM : cuda_fail(e, "moe_layer_create");
@@ -264,13 +267,12 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
   }
   snprintf(L.describe, sizeof(L.describe),
            "moe_layer H=%d E=%d k=%d I=%d Is=%d format=%s max_tokens=%d | "
-           "T<=%d: decode GEMV path [router_shared_kernel, routed_gateup_kernel<%s>, down_combine_kernel<%s>] | "
+           "T<=%d: decode GEMV path [moe_decode_fused_kernel<%s> (cooperative: router+shared, routed gate/up, down+combine)%s] | "
            "T>%d: grouped path [grouped_router_tc, dispatch, grouped_gateup_tc (tcgen05), grouped_down_tc (tcgen05), combine]%s",
            cfg->hidden, cfg->num_experts, cfg->top_k, cfg->intermediate, cfg->shared_intermediate,
            cfg->weight_format == MOE_WEIGHTS_MXFP4 ? "mxfp4" : "bf16", cfg->max_tokens,
            (cfg->flags & MOE_FLAG_FORCE_GROUPED) ? 0 : L.decode_max_t,
-           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? "mxfp4" : "bf16",
-           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? "mxfp4" : "bf16",
+           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? "mxfp4" : "bf16", "",
            (cfg->flags & MOE_FLAG_FORCE_GROUPED) ? 0 : L.decode_max_t,
            (cfg->flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? " [test: forced wait timeout]" : "");
   *out = &o->L;
@@ -393,6 +395,10 @@ moe_status_t moe_layer_sync_status(moe_layer_t* L, void* stream) {
   int code = 0;
   MOE_CUDA(cudaMemcpy(&code, L->err, sizeof(int), cudaMemcpyDeviceToHost));
   MOE_CUDA(cudaMemset(L->err, 0, sizeof(int)));
+  if (code != 0) {  // an aborted call can leave the grid-sync counters mid-generation
+    MOE_CUDA(cudaMemset(L->dec.sync_ctr, 0, sizeof(unsigned long long) * 2));
+    MOE_CUDA(cudaMemset(L->dec.sync_flag, 0, sizeof(unsigned long long) * 2));
+  }
   if (code == moe::kDevTimeout) return MOE_ERR_TIMEOUT;
   if (code != 0) return MOE_ERR_DEVICE_CHECK;
   return MOE_OK;

@@ -13,21 +13,22 @@
 // "Optimization 3": a 4-token verify window touches up to 32 experts, so the
 // window's distinct experts are read once each, for all tokens that chose them.
 //
-// Three kernels, chained with programmatic dependent launch:
-//   K1 router_shared  fp32 router logits + shared-expert gate/up (SwiGLU);
-//                     the last CTA to finish does top-k, the renormalised
-//                     softmax weights and the window's distinct-expert list.
-//   K3 routed_gateup  one pass over the gate/up rows of each distinct expert;
-//                     also prefetches the down rows K4 will need into L2.
-//
-// Latency, not arithmetic, sets the time of a batch-1 layer: each kernel issues
-// its weight loads in batches of 16 x 16 bytes per lane before using any of
-// them, reads its routing metadata in one round trip, and the router's last
-// CTA starts the first routed weights on their way from HBM to L2 (bulk L2
-// prefetch) the moment the routing is known, so HBM keeps streaming across the
-// kernel boundaries.
-//   K4 down_combine   down rows of every distinct expert and of the shared
-//                     expert, weighted by the routing weights, summed, bf16 out.
+// One cooperative kernel, one CTA per SM, three phases separated by two
+// bounded grid-wide synchronisations (monotonic arrival counters; the last CTA
+// to arrive releases the next generation, so the kernel is also safe to replay
+// from a CUDA graph):
+//   phase 1  fp32 router logits + shared-expert gate/up (SwiGLU); the last CTA
+//            to arrive does top-k, the renormalised softmax weights and the
+//            window's distinct-expert list.
+//   phase 2  one pass over the gate/up rows of each distinct expert for all
+//            tokens that chose it; each warp keeps its next units on their way
+//            from HBM to L2, and each CTA prefetches the down rows it needs in
+//            phase 3.
+//   phase 3  down rows of every distinct expert and of the shared expert,
+//            weighted by the routing weights, summed in a fixed order, bf16 out.
+// Latency, not arithmetic, sets the time of a batch-1 layer: warps issue their
+// weight loads in batches of 16 x 16 bytes per lane before using any of them,
+// and kernel boundaries are replaced by the two in-kernel synchronisations.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -39,8 +40,8 @@ namespace moe {
 struct FmtBF16 {};
 struct FmtMXFP4 {};
 
-constexpr int kRouterThreads = 256;
 constexpr int kGemvThreads = 512;
+constexpr int kLookahead = 2;  // extra rounds of gate/up units each warp keeps on their way to L2
 
 // e2m1 code values (OCP MX FP4 element): sign, 2 exponent bits (bias 1), 1 mantissa bit.
 __device__ __forceinline__ void fill_e2m1_lut(float* lut) {
@@ -199,10 +200,9 @@ __device__ __forceinline__ void gu_fma_mx(const uint4 (&v)[16], const uint32_t (
 }
 
 // ===========================================================================
-// K1: router logits + shared expert gate/up; last CTA: top-k, window list and
-// the L2 prefetch of the first routed weights K3 will read.
+// The fused decode kernel: one cooperative launch, one CTA per SM.
 // ===========================================================================
-struct RouterArgs {
+struct FusedArgs {
   const uint16_t* x;           // bf16 [T][H]
   int T, H, E, k, I, Is;
   const float* router_t;       // fp32 [E][H]
@@ -212,83 +212,114 @@ struct RouterArgs {
   const uint16_t* ws_down;     // bf16 [H][Is]
   const uint8_t* w_gu;         // routed gate/up records [E][I][2][rb_gu]
   int64_t rb_gu;
-  int grid_next;               // grid of K3 and K4 (same partitions)
+  const uint8_t* w_down;       // routed down records [E][H][rb_down]
+  int64_t rb_down;
+  int64_t down_prefetch_limit; // prefetch the routed down rows during phase 2 if they total <= this
   float* logits;               // [T][E]
+  float* h;                    // [T*k][I]
   float* h_shared;             // [T][Is]
   int* idx;                    // [T][k]
   float* weights;              // [T][k]
   DecodeMeta* meta;
-  unsigned int* counter;
+  unsigned long long* sync_ctr;   // [2] monotonic arrival counters
+  unsigned long long* sync_flag;  // [2] generation released by the last arrival
+  uint16_t* out;               // bf16 [T][H]
   int* err;
   const int* never_set;
   int force_timeout;
 };
 
-constexpr int kFirstUnits = 16;     // gate/up units per K3 CTA prefetched by the router's last CTA
+MOE_DEV unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+MOE_DEV void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
 
-template <int TMAX>
-__global__ void __launch_bounds__(kRouterThreads)
-router_shared_kernel(const RouterArgs a) {
+// Grid-wide arrival of this CTA (thread 0 only). Returns the generation of this
+// call and whether this CTA is the last to arrive.
+MOE_DEV unsigned long long grid_arrive(unsigned long long* ctr, bool* last) {
+  __threadfence();
+  const unsigned long long t = atomicAdd(ctr, 1ull);
+  *last = (t % gridDim.x) == gridDim.x - 1;
+  return t / gridDim.x;
+}
+// Wait (thread 0 only, bounded) until generation `gen` has been released.
+MOE_DEV bool grid_wait(const unsigned long long* flag, unsigned long long gen, int* err) {
+  const long long t0 = clock64();
+  while ((long long)(ld_acquire_u64(flag) - (gen + 1)) < 0) {
+    if (clock64() - t0 > 4000000000LL) {  // ~2 s: something is wrong, do not hang the GPU
+      set_error(err, kDevTimeout);
+      return false;
+    }
+    __nanosleep(32);
+  }
+  return true;
+}
+
+template <int TMAX, class Fmt>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+moe_decode_fused_kernel(const FusedArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [T][H] bf16
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // phases 1-2: x [T][H] bf16
+  float* hs = reinterpret_cast<float*>(smem);        // phase 3:   h [T*k][I] fp32, then h_shared [T][Is]
+  __shared__ float lut[16];
+  __shared__ DecodeMeta s_meta;
+  __shared__ float s_w[kMaxDecodeT * kMaxTopK];
   __shared__ int s_idx[kMaxDecodeT * kMaxTopK];
   __shared__ int s_slot_of[kMaxDecodeT * kMaxTopK];
-  __shared__ int s_slot_expert[kMaxSlots];
-  __shared__ int s_D;
-  __shared__ unsigned int s_ticket;
+  __shared__ int s_last;                 // this CTA arrived last at sync A
+  __shared__ int s_abort;                // a grid-wide wait ran out: leave
+  __shared__ unsigned long long s_gen;   // generation of sync A in this call
 
-  // Everything below reads the layer input and overwrites the workspace of the
-  // previous call: wait for the preceding kernels of the stream first.
-  pdl_wait();
-  pdl_launch_dependents();
-
-  const int T = a.T, H = a.H, E = a.E;
+  const int T = a.T, H = a.H, E = a.E, I = a.I, Is = a.Is, k = a.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int nw = kGemvThreads / 32;
+  const int G = gridDim.x, b = blockIdx.x;
+  const int n0 = (int)((int64_t)b * H / G), n1 = (int)((int64_t)(b + 1) * H / G);  // phase-3 rows
+  if constexpr (std::is_same<Fmt, FmtMXFP4>::value) fill_e2m1_lut(lut);
 
-  if (a.force_timeout && blockIdx.x == 0 && threadIdx.x == 0) {
-    if (!bounded_wait_flag(a.never_set, 2000000LL)) set_error(a.err, kDevTimeout);
+  if (threadIdx.x == 0) {
+    if (a.force_timeout && b == 0 && !bounded_wait_flag(a.never_set, 2000000LL)) set_error(a.err, kDevTimeout);
+    // shared-expert down rows of phase 3: start HBM -> L2 now
+    if (Is > 0 && n1 > n0) prefetch_l2_bulk(a.ws_down + (int64_t)n0 * Is, (uint32_t)((n1 - n0) * Is * 2));
   }
-  // Shared-expert down rows of this CTA's twin in K4: start HBM -> L2 now.
-  if (threadIdx.x == 0 && a.Is > 0) {
-    for (int b = blockIdx.x; b < a.grid_next; b += gridDim.x) {
-      const int n0 = (int)((int64_t)b * H / a.grid_next), n1 = (int)((int64_t)(b + 1) * H / a.grid_next);
-      if (n1 > n0) prefetch_l2_bulk(a.ws_down + (int64_t)n0 * a.Is, (uint32_t)((n1 - n0) * a.Is * 2));
-    }
-  }
 
-  const int nwarps = gridDim.x * (kRouterThreads / 32);
-  const int gw = blockIdx.x * (kRouterThreads / 32) + warp;
-  const int units = E + a.Is;
-
-  // First unit of this warp: issue its first batch of loads before x arrives.
+  // ------------------------------------------------ phase 1: router + shared gate/up
+  // CTA b: router rows r = b, b + G, ... (one per warp from warp 0 up) and the
+  // shared-expert units [sh0, sh1) on the following warps.
+  const int nr = (E - b + G - 1) / G;
+  const int sh0 = (int)((int64_t)b * Is / G), sh1 = (int)((int64_t)(b + 1) * Is / G);
   uint4 v[16];
-  const int u_first = gw;
-  if (u_first < E) {
-    const float* row = a.router_t + (size_t)u_first * H;
-    const int nch = H / 4;
+  {
+    const int slot = warp;   // first assignment of this warp (loads issued before x arrives)
+    if (slot < nr) {
+      const float* row = a.router_t + (size_t)(b + slot * G) * H;
+      const int nch = H / 4;
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int c = lane + 32 * q;
-      if (c < nch) v[q] = ldg_stream(row + 4 * c);
+      for (int q = 0; q < 16; ++q) {
+        const int c = lane + 32 * q;
+        if (c < nch) v[q] = ldg_stream(row + 4 * c);
+      }
+    } else if (slot - nr < sh1 - sh0) {
+      const uint8_t* grec = reinterpret_cast<const uint8_t*>(a.ws_gu + (size_t)(sh0 + slot - nr) * 2 * H);
+      gu_load_bf16(grec, grec + 2 * H, 0, H / 8, v, lane);
     }
-  } else if (u_first < units) {
-    const uint8_t* grec = reinterpret_cast<const uint8_t*>(a.ws_gu + (size_t)(u_first - E) * 2 * H);
-    gu_load_bf16(grec, grec + 2 * H, 0, H / 8, v, lane);
   }
-  {  // x -> shared memory
+  {
     const uint4* src = reinterpret_cast<const uint4*>(a.x);
     uint4* dst = reinterpret_cast<uint4*>(xs);
-    const int n16 = T * H / 8;
-    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src[i];
+    for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) dst[i] = src[i];
   }
   __syncthreads();
-
-  for (int u = u_first; u < units; u += nwarps) {
-    const bool preloaded = (u == u_first);
-    if (u < E) {
-      // Router row: logits[t][u] = sum_h x[t][h] * W_r[h][u]   (fp32 row of H)
+  for (int slot = warp; slot < nr + (sh1 - sh0); slot += nw) {
+    const bool preloaded = slot == warp;
+    if (slot < nr) {
+      const int u = b + slot * G;
       const float* row = a.router_t + (size_t)u * H;
-      const int nch = H / 4;  // 16-byte chunks of 4 floats
+      const int nch = H / 4;
       float acc[TMAX];
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
@@ -323,7 +354,7 @@ router_shared_kernel(const RouterArgs a) {
       for (int t = 0; t < TMAX; ++t) {
         if (t < T) {
           float s = warp_sum(acc[t]);
-          if (lane == 0) {
+          if (lane == t) {
             s += a.router_bias[u];
             if (a.logit_bias) s += a.logit_bias[(size_t)t * E + u];
             a.logits[(size_t)t * E + u] = s;
@@ -331,8 +362,7 @@ router_shared_kernel(const RouterArgs a) {
         }
       }
     } else {
-      // Shared expert, intermediate feature i: gate row and up row (bf16, H each).
-      const int i = u - E;
+      const int i = sh0 + slot - nr;
       const uint8_t* grec = reinterpret_cast<const uint8_t*>(a.ws_gu + (size_t)i * 2 * H);
       const uint8_t* urec = grec + 2 * H;
       const int nch = H / 8;
@@ -348,204 +378,137 @@ router_shared_kernel(const RouterArgs a) {
         if (t < T) {
           const float gs = warp_sum(ag[t]);
           const float us = warp_sum(au[t]);
-          if (lane == t) a.h_shared[(size_t)t * a.Is + i] = swiglu(gs, us);
+          if (lane == t) a.h_shared[(size_t)t * Is + i] = swiglu(gs, us);
         }
       }
     }
   }
 
-  // ---- last CTA: top-k over the complete logits --------------------------
-  __threadfence();
+  // ------------------------------------------------ sync A: routing
   __syncthreads();
-  if (threadIdx.x == 0) s_ticket = atomicAdd(a.counter, 1u);
+  if (threadIdx.x == 0) {
+    bool last;
+    s_gen = grid_arrive(&a.sync_ctr[0], &last);
+    s_last = last ? 1 : 0;
+    s_abort = 0;
+  }
   __syncthreads();
-  if (s_ticket != gridDim.x - 1) return;
-  __threadfence();
-
-  const int k = a.k;
-  if (warp < T) {
-    const int t = warp;
-    constexpr int kPer = kMaxExperts / 32;
-    uint32_t key[kPer];
+  const unsigned long long genA = s_gen;
+  if (s_last) {
+    // Last CTA: top-k over the complete logits, weights, distinct-expert list.
+    __threadfence();
+    if (warp < T) {
+      const int t = warp;
+      constexpr int kPer = kMaxExperts / 32;
+      uint32_t key[kPer];
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int e = lane + 32 * j;
-      key[j] = (e < E) ? f32_order_key(ldg_cg_f32(a.logits + (size_t)t * E + e)) : 0u;
-    }
-    float sel_v[kMaxTopK];
-    int sel_e[kMaxTopK];
+      for (int j = 0; j < kPer; ++j) {
+        const int e = lane + 32 * j;
+        key[j] = (e < E) ? f32_order_key(ldg_cg_f32(a.logits + (size_t)t * E + e)) : 0u;
+      }
+      float sel_v[kMaxTopK];
+      int sel_e[kMaxTopK];
 #pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r) {
-      if (r < k) {
-        uint32_t lk = 0u;
-        int lj = 0;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j)
-          if (key[j] > lk) { lk = key[j]; lj = j; }
-        const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, lk);
-        const uint32_t cand = (lk == gmax) ? (uint32_t)(lane + 32 * lj) : 0xFFFFFFFFu;
-        const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
-        if (lane == (int)(gidx & 31u)) {
+      for (int r = 0; r < kMaxTopK; ++r) {
+        if (r < k) {
+          uint32_t lk = 0u;
+          int lj = 0;
 #pragma unroll
           for (int j = 0; j < kPer; ++j)
-            if (j == (int)(gidx >> 5)) key[j] = 0u;
+            if (key[j] > lk) { lk = key[j]; lj = j; }
+          const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, lk);
+          const uint32_t cand = (lk == gmax) ? (uint32_t)(lane + 32 * lj) : 0xFFFFFFFFu;
+          const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
+          if (lane == (int)(gidx & 31u)) {
+#pragma unroll
+            for (int j = 0; j < kPer; ++j)
+              if (j == (int)(gidx >> 5)) key[j] = 0u;
+          }
+          sel_v[r] = f32_from_order_key(gmax);
+          sel_e[r] = (int)gidx;
         }
-        sel_v[r] = f32_from_order_key(gmax);
-        sel_e[r] = (int)gidx;
       }
-    }
-    // Renormalised softmax over the k selected logits.
-    float ex[kMaxTopK], sum = 0.f;
+      float ex[kMaxTopK], sum = 0.f;
 #pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r) {
-      if (r < k) { ex[r] = expf(sel_v[r] - sel_v[0]); sum += ex[r]; }
-    }
+      for (int r = 0; r < kMaxTopK; ++r)
+        if (r < k) { ex[r] = expf(sel_v[r] - sel_v[0]); sum += ex[r]; }
 #pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r) {
-      if (r < k && lane == r) {
-        a.idx[t * k + r] = sel_e[r];
-        a.weights[t * k + r] = ex[r] / sum;
-        s_idx[t * k + r] = sel_e[r];
-      }
-    }
-  }
-  __syncthreads();
-
-  if (warp == 0) {
-    // Distinct experts of the window, in order of first appearance over (t, j).
-    const int n = T * k;
-    bool first[2] = {false, false};
-    int firstpos[2] = {0, 0};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int aidx = lane + 32 * h;
-      if (aidx < n) {
-        const int e = s_idx[aidx];
-        int b = 0;
-        while (s_idx[b] != e) ++b;  // terminates at b == aidx at the latest
-        first[h] = (b == aidx);
-        firstpos[h] = b;
-      }
-    }
-    const unsigned m0 = __ballot_sync(0xFFFFFFFFu, first[0]);
-    const unsigned m1 = __ballot_sync(0xFFFFFFFFu, first[1]);
-    const unsigned lt = (1u << lane) - 1u;
-    if (first[0]) s_slot_of[lane] = __popc(m0 & lt);
-    if (first[1]) s_slot_of[lane + 32] = __popc(m0) + __popc(m1 & lt);
-    __syncwarp();
-    const int D = __popc(m0) + __popc(m1);
-    for (int q = lane; q < D * kMaxDecodeT; q += 32)
-      a.meta->slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = -1;
-    __syncwarp();
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int aidx = lane + 32 * h;
-      if (aidx < n) {
-        const int slot = s_slot_of[firstpos[h]];
-        if (first[h]) {
-          a.meta->slot_expert[slot] = s_idx[aidx];
-          s_slot_expert[slot] = s_idx[aidx];
+      for (int r = 0; r < kMaxTopK; ++r) {
+        if (r < k && lane == r) {
+          a.idx[t * k + r] = sel_e[r];
+          a.weights[t * k + r] = ex[r] / sum;
+          s_idx[t * k + r] = sel_e[r];
         }
-        a.meta->slot_j[slot][aidx / k] = (signed char)(aidx % k);
       }
     }
-    if (lane == 0) {
-      a.meta->num_slots = D;
-      s_D = D;
-      *a.counter = 0u;  // ready for the next call
+    __syncthreads();
+    if (warp == 0) {
+      const int n = T * k;
+      bool first[2] = {false, false};
+      int firstpos[2] = {0, 0};
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int aidx = lane + 32 * h2;
+        if (aidx < n) {
+          const int e = s_idx[aidx];
+          int q = 0;
+          while (s_idx[q] != e) ++q;
+          first[h2] = (q == aidx);
+          firstpos[h2] = q;
+        }
+      }
+      const unsigned m0 = __ballot_sync(0xFFFFFFFFu, first[0]);
+      const unsigned m1 = __ballot_sync(0xFFFFFFFFu, first[1]);
+      const unsigned lt = (1u << lane) - 1u;
+      if (first[0]) s_slot_of[lane] = __popc(m0 & lt);
+      if (first[1]) s_slot_of[lane + 32] = __popc(m0) + __popc(m1 & lt);
+      __syncwarp();
+      const int D = __popc(m0) + __popc(m1);
+      for (int q = lane; q < D * kMaxDecodeT; q += 32) a.meta->slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = -1;
+      __syncwarp();
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int aidx = lane + 32 * h2;
+        if (aidx < n) {
+          const int slot = s_slot_of[firstpos[h2]];
+          if (first[h2]) a.meta->slot_expert[slot] = s_idx[aidx];
+          a.meta->slot_j[slot][aidx / k] = (signed char)(aidx % k);
+        }
+      }
+      if (lane == 0) a.meta->num_slots = D;
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        st_release_u64(&a.sync_flag[0], genA + 1);
+      }
     }
   }
+  if (threadIdx.x == 0 && !grid_wait(&a.sync_flag[0], genA, a.err)) s_abort = 1;
   __syncthreads();
+  if (s_abort) return;
 
-  // Routing is known: start the first gate/up units of every K3 CTA on their way
-  // from HBM to L2 while this grid drains and K3 starts.
-  {
-    const int D = s_D, I = a.I;
-    const int64_t U = (int64_t)D * I;
-    const int64_t unit_bytes = 2 * a.rb_gu;
-    for (int b = threadIdx.x; b < a.grid_next; b += blockDim.x) {
-      int64_t u0 = U * b / a.grid_next;
-      const int64_t u1 = U * (b + 1) / a.grid_next;
-      int64_t left = (u1 - u0 < kFirstUnits) ? u1 - u0 : kFirstUnits;
-      while (left > 0) {
-        const int d = (int)(u0 / I), i = (int)(u0 % I);
-        const int64_t run = (I - i < left) ? I - i : left;
-        const uint8_t* p = a.w_gu + ((int64_t)s_slot_expert[d] * I + i) * unit_bytes;
-        prefetch_l2_bulk(p, (uint32_t)(run * unit_bytes));
-        u0 += run;
-        left -= run;
-      }
-    }
-  }
-}
-
-// ===========================================================================
-// K3: routed gate/up GEMV over the window's distinct experts.
-// ===========================================================================
-struct GateUpArgs {
-  const uint16_t* x;       // bf16 [T][H]
-  int T, H, I, k;
-  const uint8_t* w_gu;     // [E][I][2][rb_gu]
-  int64_t rb_gu;
-  const DecodeMeta* meta;
-  float* h;                // [T*k][I]
-  // L2 prefetch of the down rows K4 reads (same CTA partition of the H output rows)
-  const uint8_t* w_down;   // [E][H][rb_down]
-  int64_t rb_down;
-  int64_t down_prefetch_limit;  // prefetch K4's rows here only if D*H*rb_down <= this
-};
-
-constexpr int kLookahead = 2;  // extra rounds of units each warp keeps on their way to L2
-
-template <int TMAX, class Fmt>
-__global__ void __launch_bounds__(kGemvThreads, 1)
-routed_gateup_kernel(const GateUpArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [T][H]
-  __shared__ float lut[16];
-  __shared__ DecodeMeta s_meta;
-
-  const int T = a.T, H = a.H, I = a.I;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if constexpr (std::is_same<Fmt, FmtMXFP4>::value) fill_e2m1_lut(lut);
-  {  // x -> shared memory (the layer input: complete before the router started)
-    const uint4* src = reinterpret_cast<const uint4*>(a.x);
-    uint4* dst = reinterpret_cast<uint4*>(xs);
-    for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) dst[i] = src[i];
-  }
-
-  pdl_wait();  // routing of this window is complete
-  pdl_launch_dependents();
+  // ------------------------------------------------ phase 2: routed gate/up
   load_meta(a.meta, &s_meta);
   __syncthreads();
   const int D = s_meta.num_slots;
-
   const int64_t U = (int64_t)D * I;
-  const int64_t u0 = U * blockIdx.x / gridDim.x;
-  const int64_t u1 = U * (blockIdx.x + 1) / gridDim.x;
-  constexpr int nw = kGemvThreads / 32;
+  const int64_t u0 = U * b / G, u1 = U * (b + 1) / G;
   const int64_t unit_bytes = 2 * a.rb_gu;
   auto unit_ptr = [&](int64_t u) {
     const int d = (int)(u / I), i = (int)(u % I);
     return a.w_gu + ((int64_t)s_meta.slot_expert[d] * I + i) * unit_bytes;
   };
-  // Keep this warp's next rounds of units on their way to L2 (round 0 was
-  // started by the router's last CTA).
-  if (lane == 0) {
-    for (int r = 1; r <= kLookahead; ++r) {
+  if (lane == 0) {  // this warp's next rounds of units: HBM -> L2
+    for (int r = 0; r <= kLookahead; ++r) {
       const int64_t u = u0 + warp + (int64_t)nw * r;
       if (u < u1) prefetch_l2_bulk(unit_ptr(u), (uint32_t)unit_bytes);
     }
   }
-  // The down rows K4's twin CTA reads, when they fit comfortably in L2.
-  if (threadIdx.x == 32 && (int64_t)D * H * a.rb_down <= a.down_prefetch_limit) {
-    const int n0 = (int)((int64_t)blockIdx.x * H / gridDim.x), n1 = (int)((int64_t)(blockIdx.x + 1) * H / gridDim.x);
-    if (n1 > n0)
-      for (int d = 0; d < D; ++d)
-        prefetch_l2_bulk(a.w_down + ((int64_t)s_meta.slot_expert[d] * H + n0) * a.rb_down,
-                         (uint32_t)((n1 - n0) * a.rb_down));
+  if (threadIdx.x == 32 && (int64_t)D * H * a.rb_down <= a.down_prefetch_limit && n1 > n0) {
+    for (int d = 0; d < D; ++d)  // phase-3 down rows of this CTA
+      prefetch_l2_bulk(a.w_down + ((int64_t)s_meta.slot_expert[d] * H + n0) * a.rb_down,
+                       (uint32_t)((n1 - n0) * a.rb_down));
   }
-
   for (int64_t u = u0 + warp; u < u1; u += nw) {
     if (lane == 0 && u + (int64_t)nw * (kLookahead + 1) < u1)
       prefetch_l2_bulk(unit_ptr(u + (int64_t)nw * (kLookahead + 1)), (uint32_t)unit_bytes);
@@ -555,15 +518,14 @@ routed_gateup_kernel(const GateUpArgs a) {
     float ag[TMAX], au[TMAX];
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) ag[t] = au[t] = 0.f;
-    uint4 v[16];
     if constexpr (std::is_same<Fmt, FmtBF16>::value) {
-      const int nch = H / 8;  // 16-byte chunks per row
+      const int nch = H / 8;
       for (int b0 = 0; b0 < nch; b0 += 32 * 8) {
         gu_load_bf16(grec, urec, b0, nch, v, lane);
         gu_fma_bf16<TMAX>(v, b0, nch, xs, T, H, ag, au, lane);
       }
     } else {
-      const int nch = H / 32;  // 16-byte chunks of 32 codes = one scale block each
+      const int nch = H / 32;
       uint32_t sc[16];
       for (int b0 = 0; b0 < nch; b0 += 32 * 8) {
         gu_load_mx(grec, urec, H, b0, nch, v, sc, lane);
@@ -576,44 +538,24 @@ routed_gateup_kernel(const GateUpArgs a) {
         const float gsum = warp_sum(ag[t]);
         const float usum = warp_sum(au[t]);
         const int j = s_meta.slot_j[d][t];
-        if (lane == t && j >= 0) a.h[((int64_t)t * a.k + j) * I + i] = swiglu(gsum, usum);
+        if (lane == t && j >= 0) a.h[((int64_t)t * k + j) * I + i] = swiglu(gsum, usum);
       }
     }
   }
-}
 
-// ===========================================================================
-// K4: down projection of every distinct expert + shared expert, weighted sum.
-// ===========================================================================
-struct DownArgs {
-  int T, H, I, Is, k;
-  const uint8_t* w_down;   // [E][H][rb_down]
-  int64_t rb_down;
-  const uint16_t* ws_down; // bf16 [H][Is]
-  const DecodeMeta* meta;
-  const float* h;          // [T*k][I]
-  const float* h_shared;   // [T][Is]
-  const float* weights;    // [T][k]
-  uint16_t* out;           // bf16 [T][H]
-};
+  // ------------------------------------------------ sync B: all SwiGLU outputs written
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool last;
+    const unsigned long long gen = grid_arrive(&a.sync_ctr[1], &last);
+    if (last) st_release_u64(&a.sync_flag[1], gen + 1);
+    if (!grid_wait(&a.sync_flag[1], gen, a.err)) s_abort = 1;
+  }
+  __syncthreads();
+  if (s_abort) return;
 
-template <int TMAX, class Fmt>
-__global__ void __launch_bounds__(kGemvThreads, 1)
-down_combine_kernel(const DownArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int T = a.T, H = a.H, I = a.I, Is = a.Is, k = a.k;
-  float* hs = reinterpret_cast<float*>(smem);        // [T*k][I]
-  float* hss = hs + (size_t)T * k * I;               // [T][Is]
-  __shared__ float lut[16];
-  __shared__ float s_w[kMaxDecodeT * kMaxTopK];
-  __shared__ DecodeMeta s_meta;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if constexpr (std::is_same<Fmt, FmtMXFP4>::value) fill_e2m1_lut(lut);
-
-  pdl_wait();  // SwiGLU outputs of this window are complete
-  pdl_launch_dependents();
-
-  load_meta(a.meta, &s_meta);
+  // ------------------------------------------------ phase 3: down + combine
+  float* hss = hs + (size_t)T * k * I;
   for (int q = threadIdx.x; q < T * k; q += blockDim.x) s_w[q] = ldg_cg_f32(a.weights + q);
   {
     const int n16 = T * k * I / 4;
@@ -624,21 +566,13 @@ down_combine_kernel(const DownArgs a) {
       reinterpret_cast<uint4*>(hss)[q] = ldg_cg(reinterpret_cast<const uint4*>(a.h_shared) + q);
   }
   __syncthreads();
-  const int D = s_meta.num_slots;
-
-  const int n0 = (int)((int64_t)blockIdx.x * H / gridDim.x);
-  const int n1 = (int)((int64_t)(blockIdx.x + 1) * H / gridDim.x);
-  constexpr int nw = kGemvThreads / 32;
   const bool bf = std::is_same<Fmt, FmtBF16>::value;
-  const int nch = bf ? I / 8 : I / 32;   // 16-byte chunks per routed down row
+  const int nch = bf ? I / 8 : I / 32;
   const int F = D * nch;
-
   for (int n = n0 + warp; n < n1; n += nw) {
     float acc[TMAX];
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-
-    // shared expert row (weight 1): loads issued first, consumed last
     const uint16_t* srow = a.ws_down + (size_t)n * Is;
     const int snch = Is / 8;
     uint4 sv[4];
@@ -647,10 +581,7 @@ down_combine_kernel(const DownArgs a) {
       const int c = lane + 32 * q;
       if (c < snch) sv[q] = ldg_stream(srow + 8 * c);
     }
-
-    // routed rows of the window's distinct experts, flattened over (slot, chunk)
     for (int f0 = 0; f0 < F; f0 += 32 * 16) {
-      uint4 v[16];
       uint32_t sc[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
@@ -674,9 +605,10 @@ down_combine_kernel(const DownArgs a) {
               if (j >= 0) {
                 if (bf) {
                   const float* hp = hs + ((size_t)t * k + j) * I + 8 * c;
-                  const float4 h0 = *reinterpret_cast<const float4*>(hp);
-                  const float4 h1 = *reinterpret_cast<const float4*>(hp + 4);
-                  acc[t] = fmaf(s_w[t * k + j], dot8_bf16_f32(v[q], h0, h1), acc[t]);
+                  acc[t] = fmaf(s_w[t * k + j],
+                                dot8_bf16_f32(v[q], *reinterpret_cast<const float4*>(hp),
+                                              *reinterpret_cast<const float4*>(hp + 4)),
+                                acc[t]);
                 } else {
                   const float* hp = hs + ((size_t)t * k + j) * I + 32 * c;
                   acc[t] = fmaf(s_w[t * k + j] * e8m0_scale(sc[q]), dot32_e2m1_f32(v[q], hp, lut), acc[t]);
@@ -695,9 +627,8 @@ down_combine_kernel(const DownArgs a) {
         for (int t = 0; t < TMAX; ++t) {
           if (t < T) {
             const float* hp = hss + (size_t)t * Is + 8 * c;
-            const float4 h0 = *reinterpret_cast<const float4*>(hp);
-            const float4 h1 = *reinterpret_cast<const float4*>(hp + 4);
-            acc[t] += dot8_bf16_f32(sv[q], h0, h1);
+            acc[t] += dot8_bf16_f32(sv[q], *reinterpret_cast<const float4*>(hp),
+                                    *reinterpret_cast<const float4*>(hp + 4));
           }
         }
       }
@@ -723,88 +654,82 @@ down_combine_kernel(const DownArgs a) {
 }
 
 // ===========================================================================
-// Host launchers
+// Host launcher
 // ===========================================================================
 size_t decode_smem_bytes_down(const moe_layer* L, int T) {
   const auto& c = L->cfg;
   return (size_t)T * ((size_t)c.top_k * c.intermediate + c.shared_intermediate) * sizeof(float);
 }
 
-template <class K, class A>
-static cudaError_t launch_pdl(K kernel, int grid, int block, size_t smem, cudaStream_t s, const A& args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args);
+static size_t fused_smem_bytes(const moe_layer* L, int T) {
+  const size_t xb = (size_t)T * L->cfg.hidden * sizeof(uint16_t);
+  const size_t hb = decode_smem_bytes_down(L, T);
+  return xb > hb ? xb : hb;
 }
 
 template <int TMAX, class Fmt>
-static cudaError_t launch_decode_t(moe_layer* L, const uint16_t* x, uint16_t* out, int T,
-                                   const float* logit_bias, cudaStream_t s) {
+static cudaError_t launch_fused_t(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
+                                  cudaStream_t s) {
   const auto& c = L->cfg;
-  const int H = c.hidden;
-  const size_t xs_bytes = (size_t)T * H * sizeof(uint16_t);
-  static bool attr_set = false;  // per instantiation; max smem is a per-function attribute
-  if (!attr_set) {
-    cudaFuncSetAttribute(router_shared_kernel<TMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    cudaFuncSetAttribute(routed_gateup_kernel<TMAX, Fmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    cudaFuncSetAttribute(down_combine_kernel<TMAX, Fmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-    attr_set = true;
-  }
+  FusedArgs a;
+  a.x = x; a.T = T; a.H = c.hidden; a.E = c.num_experts; a.k = c.top_k; a.I = c.intermediate;
+  a.Is = c.shared_intermediate;
+  a.router_t = L->router_t; a.router_bias = L->router_bias; a.logit_bias = logit_bias;
+  a.ws_gu = L->ws_gu; a.ws_down = L->ws_down;
+  a.w_gu = L->w_gu; a.rb_gu = L->row_bytes.gu; a.w_down = L->w_down; a.rb_down = L->row_bytes.down;
+  a.down_prefetch_limit = 40ll << 20;
+  a.logits = L->dec.logits; a.h = L->dec.h; a.h_shared = L->dec.h_shared;
+  a.idx = L->dec.idx; a.weights = L->dec.weights; a.meta = L->dec.meta;
+  a.sync_ctr = L->dec.sync_ctr; a.sync_flag = L->dec.sync_flag;
+  a.out = out; a.err = L->err; a.never_set = L->never_set;
+  a.force_timeout = (c.flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? 1 : 0;
 
-  RouterArgs ra;
-  ra.x = x; ra.T = T; ra.H = H; ra.E = c.num_experts; ra.k = c.top_k; ra.Is = c.shared_intermediate;
-  ra.I = c.intermediate;
-  ra.router_t = L->router_t; ra.router_bias = L->router_bias; ra.logit_bias = logit_bias;
-  ra.ws_gu = L->ws_gu; ra.ws_down = L->ws_down; ra.w_gu = L->w_gu; ra.rb_gu = L->row_bytes.gu;
-  ra.grid_next = L->num_sms;
-  ra.logits = L->dec.logits; ra.h_shared = L->dec.h_shared;
-  ra.idx = L->dec.idx; ra.weights = L->dec.weights; ra.meta = L->dec.meta;
-  ra.counter = L->dec.counter; ra.err = L->err; ra.never_set = L->never_set;
-  ra.force_timeout = (c.flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L->num_sms);
+  cfg.blockDim = dim3(kGemvThreads);
+  cfg.dynamicSmemBytes = fused_smem_bytes(L, T);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs co-resident: they wait on one another
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_mark(L, s);
-  cudaError_t e = launch_pdl(router_shared_kernel<TMAX>, L->num_sms, kRouterThreads, xs_bytes, s, ra);
-  if (e != cudaSuccess) return e;
-  prof_mark(L, s);
-
-  GateUpArgs ga;
-  ga.x = x; ga.T = T; ga.H = H; ga.I = c.intermediate; ga.k = c.top_k;
-  ga.w_gu = L->w_gu; ga.rb_gu = L->row_bytes.gu; ga.meta = L->dec.meta; ga.h = L->dec.h;
-  ga.w_down = L->w_down; ga.rb_down = L->row_bytes.down;
-  ga.down_prefetch_limit = 40ll << 20;
-  e = launch_pdl(routed_gateup_kernel<TMAX, Fmt>, L->num_sms, kGemvThreads, xs_bytes, s, ga);
-  if (e != cudaSuccess) return e;
-  prof_mark(L, s);
-
-  DownArgs da;
-  da.T = T; da.H = H; da.I = c.intermediate; da.Is = c.shared_intermediate; da.k = c.top_k;
-  da.w_down = L->w_down; da.rb_down = L->row_bytes.down; da.ws_down = L->ws_down;
-  da.meta = L->dec.meta; da.h = L->dec.h; da.h_shared = L->dec.h_shared;
-  da.weights = L->dec.weights; da.out = out;
-  e = launch_pdl(down_combine_kernel<TMAX, Fmt>, L->num_sms, kGemvThreads,
-                 decode_smem_bytes_down(L, T), s, da);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_decode_fused_kernel<TMAX, Fmt>, a);
   prof_mark(L, s);
   return e;
 }
 
 template <class Fmt>
-static cudaError_t launch_decode_fmt(moe_layer* L, const uint16_t* x, uint16_t* out, int T,
-                                     const float* lb, cudaStream_t s) {
-  if (T <= 1) return launch_decode_t<1, Fmt>(L, x, out, T, lb, s);
-  if (T <= 2) return launch_decode_t<2, Fmt>(L, x, out, T, lb, s);
-  if (T <= 4) return launch_decode_t<4, Fmt>(L, x, out, T, lb, s);
-  return launch_decode_t<8, Fmt>(L, x, out, T, lb, s);
+static cudaError_t set_attrs_fmt() {
+  cudaError_t e = cudaSuccess;
+  auto set = [&](const void* f) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
+  };
+  set((const void*)moe_decode_fused_kernel<1, Fmt>);
+  set((const void*)moe_decode_fused_kernel<2, Fmt>);
+  set((const void*)moe_decode_fused_kernel<4, Fmt>);
+  set((const void*)moe_decode_fused_kernel<8, Fmt>);
+  return e;
 }
 
-cudaError_t launch_decode(moe_layer* L, const uint16_t* x, uint16_t* out, int T,
-                          const float* logit_bias, cudaStream_t s) {
+cudaError_t decode_prepare(moe_layer* L) {
+  cudaError_t e = set_attrs_fmt<FmtBF16>();
+  if (e == cudaSuccess) e = set_attrs_fmt<FmtMXFP4>();
+  return e;
+}
+
+template <class Fmt>
+static cudaError_t launch_decode_fmt(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* lb,
+                                     cudaStream_t s) {
+  if (T <= 1) return launch_fused_t<1, Fmt>(L, x, out, T, lb, s);
+  if (T <= 2) return launch_fused_t<2, Fmt>(L, x, out, T, lb, s);
+  if (T <= 4) return launch_fused_t<4, Fmt>(L, x, out, T, lb, s);
+  return launch_fused_t<8, Fmt>(L, x, out, T, lb, s);
+}
+
+cudaError_t launch_decode(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
+                          cudaStream_t s) {
   if (L->cfg.weight_format == MOE_WEIGHTS_MXFP4) return launch_decode_fmt<FmtMXFP4>(L, x, out, T, logit_bias, s);
   return launch_decode_fmt<FmtBF16>(L, x, out, T, logit_bias, s);
 }

@@ -33,7 +33,8 @@ struct DecodeWorkspace {
   DecodeMeta* meta;      // one
   float* h;              // [kMaxDecodeT * k][I]   SwiGLU outputs of routed assignments (t*k+j)
   float* h_shared;       // [kMaxDecodeT][Is]
-  unsigned int* counter; // router last-block ticket
+  unsigned long long* sync_ctr;   // [2] grid-sync arrival counters (monotonic)
+  unsigned long long* sync_flag;  // [2] grid-sync released generations
 };
 
 struct GroupedWorkspace {
@@ -106,4 +107,5 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
 cudaError_t grouped_prepare(moe_layer* L);   // tensor maps etc. at create
 void grouped_release(moe_layer* L);
 size_t decode_smem_bytes_down(const moe_layer* L, int T);
+cudaError_t decode_prepare(moe_layer* L);
 }  // namespace moe
