@@ -123,7 +123,6 @@ moe_status_t alloc_workspace(LayerOwner* o) {
   GET(L.dec.h, sizeof(float) * (size_t)T8 * c.top_k * c.intermediate);
   GET(L.dec.h_shared, sizeof(float) * (size_t)T8 * std::max(c.shared_intermediate, 1));
   GET(L.dec.sync_ctr, sizeof(unsigned long long) * 2);
-  GET(L.dec.sync_flag, sizeof(unsigned long long) * 2);
   GET(L.err, sizeof(int) * 4);
   GET(L.never_set, sizeof(int));
   GET(L.x_stage, sizeof(uint16_t) * (size_t)c.max_tokens * c.hidden);
@@ -131,7 +130,6 @@ moe_status_t alloc_workspace(LayerOwner* o) {
   GET(L.bias_stage, sizeof(float) * (size_t)c.max_tokens * c.num_experts);
 #undef GET
   cudaMemset(L.dec.sync_ctr, 0, sizeof(unsigned long long) * 2);
-  cudaMemset(L.dec.sync_flag, 0, sizeof(unsigned long long) * 2);
   cudaMemset(L.err, 0, sizeof(int) * 4);
   cudaMemset(L.never_set, 0, sizeof(int));
   cudaMemset(L.dec.meta, 0, sizeof(moe::DecodeMeta));
@@ -397,7 +395,6 @@ moe_status_t moe_layer_sync_status(moe_layer_t* L, void* stream) {
   MOE_CUDA(cudaMemset(L->err, 0, sizeof(int)));
   if (code != 0) {  // an aborted call can leave the grid-sync counters mid-generation
     MOE_CUDA(cudaMemset(L->dec.sync_ctr, 0, sizeof(unsigned long long) * 2));
-    MOE_CUDA(cudaMemset(L->dec.sync_flag, 0, sizeof(unsigned long long) * 2));
   }
   if (code == moe::kDevTimeout) return MOE_ERR_TIMEOUT;
   if (code != 0) return MOE_ERR_DEVICE_CHECK;

@@ -34,6 +34,7 @@
 
 #include "moe_common.cuh"
 #include "moe_internal.h"
+#include "moe_sm100.cuh"
 
 namespace moe {
 
@@ -214,15 +215,16 @@ struct FusedArgs {
   int64_t rb_gu;
   const uint8_t* w_down;       // routed down records [E][H][rb_down]
   int64_t rb_down;
-  int64_t down_prefetch_limit; // prefetch the routed down rows during phase 2 if they total <= this
+  // shared-memory plan (bytes): region 1 holds x in phases 1-2 and h in phase 3;
+  // then this CTA's shared-expert down rows; then `slots_cap` slots of routed down rows
+  int smem_r1, smem_sh, slot_stride, slots_cap, rows_max;
   float* logits;               // [T][E]
   float* h;                    // [T*k][I]
   float* h_shared;             // [T][Is]
-  int* idx;                    // [T][k]
-  float* weights;              // [T][k]
-  DecodeMeta* meta;
+  int* idx;                    // [T][k]     (written by CTA 0, diagnostics)
+  float* weights;              // [T][k]     (written by CTA 0, diagnostics)
+  DecodeMeta* meta;            //            (written by CTA 0, diagnostics)
   unsigned long long* sync_ctr;   // [2] monotonic arrival counters
-  unsigned long long* sync_flag;  // [2] generation released by the last arrival
   uint16_t* out;               // bf16 [T][H]
   int* err;
   const int* never_set;
@@ -234,27 +236,23 @@ MOE_DEV unsigned long long ld_acquire_u64(const unsigned long long* p) {
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-MOE_DEV void st_release_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
-}
 
-// Grid-wide arrival of this CTA (thread 0 only). Returns the generation of this
-// call and whether this CTA is the last to arrive.
-MOE_DEV unsigned long long grid_arrive(unsigned long long* ctr, bool* last) {
+// Grid-wide arrival (one thread per CTA): the counter only grows, so the call's
+// generation is the old value / gridDim.x and the barrier opens once the
+// counter reaches (generation + 1) * gridDim.x.
+MOE_DEV unsigned long long grid_arrive(unsigned long long* ctr) {
   __threadfence();
-  const unsigned long long t = atomicAdd(ctr, 1ull);
-  *last = (t % gridDim.x) == gridDim.x - 1;
-  return t / gridDim.x;
+  return atomicAdd(ctr, 1ull) / gridDim.x;
 }
-// Wait (thread 0 only, bounded) until generation `gen` has been released.
-MOE_DEV bool grid_wait(const unsigned long long* flag, unsigned long long gen, int* err) {
+// Bounded wait (one thread per CTA) until every CTA of generation `gen` arrived.
+MOE_DEV bool grid_wait(const unsigned long long* ctr, unsigned long long gen, int* err) {
+  const unsigned long long target = (gen + 1) * gridDim.x;
   const long long t0 = clock64();
-  while ((long long)(ld_acquire_u64(flag) - (gen + 1)) < 0) {
+  while (ld_acquire_u64(ctr) < target) {
     if (clock64() - t0 > 4000000000LL) {  // ~2 s: something is wrong, do not hang the GPU
       set_error(err, kDevTimeout);
       return false;
     }
-    __nanosleep(32);
   }
   return true;
 }
@@ -262,39 +260,52 @@ MOE_DEV bool grid_wait(const unsigned long long* flag, unsigned long long gen, i
 template <int TMAX, class Fmt>
 __global__ void __launch_bounds__(kGemvThreads, 1)
 moe_decode_fused_kernel(const FusedArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // phases 1-2: x [T][H] bf16
-  float* hs = reinterpret_cast<float*>(smem);        // phase 3:   h [T*k][I] fp32, then h_shared [T][Is]
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);   // phases 1-2: x [T][H] bf16
+  float* hs = reinterpret_cast<float*>(smem);         // phase 3: h [T*k][I] fp32, then h_shared [T][Is]
+  uint8_t* s_shrows = smem + a.smem_r1;               // shared-expert down rows [n0, n1) x Is bf16
+  uint8_t* s_rows = s_shrows + a.smem_sh;             // routed down rows, slot d at d * slot_stride
   __shared__ float lut[16];
   __shared__ DecodeMeta s_meta;
   __shared__ float s_w[kMaxDecodeT * kMaxTopK];
   __shared__ int s_idx[kMaxDecodeT * kMaxTopK];
   __shared__ int s_slot_of[kMaxDecodeT * kMaxTopK];
-  __shared__ int s_last;                 // this CTA arrived last at sync A
-  __shared__ int s_abort;                // a grid-wide wait ran out: leave
-  __shared__ unsigned long long s_gen;   // generation of sync A in this call
+  __shared__ int s_router_done;
+  __shared__ int s_abort;
+  __shared__ unsigned long long s_gen;
+  __shared__ __align__(8) uint64_t bar_sh, bar_rt;
 
   const int T = a.T, H = a.H, E = a.E, I = a.I, Is = a.Is, k = a.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int nw = kGemvThreads / 32;
   const int G = gridDim.x, b = blockIdx.x;
   const int n0 = (int)((int64_t)b * H / G), n1 = (int)((int64_t)(b + 1) * H / G);  // phase-3 rows
+  const int nrows = n1 - n0;
+  const int nr = (E - b + G - 1) / G;               // router rows b, b + G, ... of this CTA
+  const int sh0 = (int)((int64_t)b * Is / G), sh1 = (int)((int64_t)(b + 1) * Is / G);
   if constexpr (std::is_same<Fmt, FmtMXFP4>::value) fill_e2m1_lut(lut);
 
   if (threadIdx.x == 0) {
+    sm100::mbar_init(&bar_sh, 1);
+    sm100::mbar_init(&bar_rt, 1);
+    sm100::fence_barrier_init();
+    s_router_done = 0;
+    s_abort = 0;
+    if (nr == 0) s_gen = grid_arrive(&a.sync_ctr[0]);  // no router rows: arrive at once
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
     if (a.force_timeout && b == 0 && !bounded_wait_flag(a.never_set, 2000000LL)) set_error(a.err, kDevTimeout);
-    // shared-expert down rows of phase 3: start HBM -> L2 now
-    if (Is > 0 && n1 > n0) prefetch_l2_bulk(a.ws_down + (int64_t)n0 * Is, (uint32_t)((n1 - n0) * Is * 2));
+    // shared-expert down rows of phase 3 do not depend on routing: copy them now
+    const uint32_t bytes = (uint32_t)(nrows * Is * 2);
+    sm100::mbar_arrive_expect_tx(&bar_sh, bytes);
+    if (bytes) sm100::bulk_copy_g2s(s_shrows, a.ws_down + (int64_t)n0 * Is, bytes, &bar_sh);
   }
 
   // ------------------------------------------------ phase 1: router + shared gate/up
-  // CTA b: router rows r = b, b + G, ... (one per warp from warp 0 up) and the
-  // shared-expert units [sh0, sh1) on the following warps.
-  const int nr = (E - b + G - 1) / G;
-  const int sh0 = (int)((int64_t)b * Is / G), sh1 = (int)((int64_t)(b + 1) * Is / G);
   uint4 v[16];
   {
-    const int slot = warp;   // first assignment of this warp (loads issued before x arrives)
+    const int slot = warp;   // first assignment of this warp: loads issued before x arrives
     if (slot < nr) {
       const float* row = a.router_t + (size_t)(b + slot * G) * H;
       const int nch = H / 4;
@@ -361,6 +372,10 @@ moe_decode_fused_kernel(const FusedArgs a) {
           }
         }
       }
+      __threadfence();
+      __syncwarp();
+      // the warp completing this CTA's router rows arrives for the whole CTA
+      if (lane == 0 && atomicAdd(&s_router_done, 1) == nr - 1) s_gen = grid_arrive(&a.sync_ctr[0]);
     } else {
       const int i = sh0 + slot - nr;
       const uint8_t* grec = reinterpret_cast<const uint8_t*>(a.ws_gu + (size_t)i * 2 * H);
@@ -384,113 +399,116 @@ moe_decode_fused_kernel(const FusedArgs a) {
     }
   }
 
-  // ------------------------------------------------ sync A: routing
+  // ------------------------------------------------ sync A: all router logits written
   __syncthreads();
-  if (threadIdx.x == 0) {
-    bool last;
-    s_gen = grid_arrive(&a.sync_ctr[0], &last);
-    s_last = last ? 1 : 0;
-    s_abort = 0;
-  }
-  __syncthreads();
-  const unsigned long long genA = s_gen;
-  if (s_last) {
-    // Last CTA: top-k over the complete logits, weights, distinct-expert list.
-    __threadfence();
-    if (warp < T) {
-      const int t = warp;
-      constexpr int kPer = kMaxExperts / 32;
-      uint32_t key[kPer];
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const int e = lane + 32 * j;
-        key[j] = (e < E) ? f32_order_key(ldg_cg_f32(a.logits + (size_t)t * E + e)) : 0u;
-      }
-      float sel_v[kMaxTopK];
-      int sel_e[kMaxTopK];
-#pragma unroll
-      for (int r = 0; r < kMaxTopK; ++r) {
-        if (r < k) {
-          uint32_t lk = 0u;
-          int lj = 0;
-#pragma unroll
-          for (int j = 0; j < kPer; ++j)
-            if (key[j] > lk) { lk = key[j]; lj = j; }
-          const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, lk);
-          const uint32_t cand = (lk == gmax) ? (uint32_t)(lane + 32 * lj) : 0xFFFFFFFFu;
-          const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
-          if (lane == (int)(gidx & 31u)) {
-#pragma unroll
-            for (int j = 0; j < kPer; ++j)
-              if (j == (int)(gidx >> 5)) key[j] = 0u;
-          }
-          sel_v[r] = f32_from_order_key(gmax);
-          sel_e[r] = (int)gidx;
-        }
-      }
-      float ex[kMaxTopK], sum = 0.f;
-#pragma unroll
-      for (int r = 0; r < kMaxTopK; ++r)
-        if (r < k) { ex[r] = expf(sel_v[r] - sel_v[0]); sum += ex[r]; }
-#pragma unroll
-      for (int r = 0; r < kMaxTopK; ++r) {
-        if (r < k && lane == r) {
-          a.idx[t * k + r] = sel_e[r];
-          a.weights[t * k + r] = ex[r] / sum;
-          s_idx[t * k + r] = sel_e[r];
-        }
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int n = T * k;
-      bool first[2] = {false, false};
-      int firstpos[2] = {0, 0};
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int aidx = lane + 32 * h2;
-        if (aidx < n) {
-          const int e = s_idx[aidx];
-          int q = 0;
-          while (s_idx[q] != e) ++q;
-          first[h2] = (q == aidx);
-          firstpos[h2] = q;
-        }
-      }
-      const unsigned m0 = __ballot_sync(0xFFFFFFFFu, first[0]);
-      const unsigned m1 = __ballot_sync(0xFFFFFFFFu, first[1]);
-      const unsigned lt = (1u << lane) - 1u;
-      if (first[0]) s_slot_of[lane] = __popc(m0 & lt);
-      if (first[1]) s_slot_of[lane + 32] = __popc(m0) + __popc(m1 & lt);
-      __syncwarp();
-      const int D = __popc(m0) + __popc(m1);
-      for (int q = lane; q < D * kMaxDecodeT; q += 32) a.meta->slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = -1;
-      __syncwarp();
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int aidx = lane + 32 * h2;
-        if (aidx < n) {
-          const int slot = s_slot_of[firstpos[h2]];
-          if (first[h2]) a.meta->slot_expert[slot] = s_idx[aidx];
-          a.meta->slot_j[slot][aidx / k] = (signed char)(aidx % k);
-        }
-      }
-      if (lane == 0) a.meta->num_slots = D;
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence();
-        st_release_u64(&a.sync_flag[0], genA + 1);
-      }
-    }
-  }
-  if (threadIdx.x == 0 && !grid_wait(&a.sync_flag[0], genA, a.err)) s_abort = 1;
+  if (threadIdx.x == 0 && !grid_wait(&a.sync_ctr[0], s_gen, a.err)) s_abort = 1;
   __syncthreads();
   if (s_abort) return;
 
-  // ------------------------------------------------ phase 2: routed gate/up
-  load_meta(a.meta, &s_meta);
+  // Every CTA derives the routing itself from the logits (identical inputs,
+  // identical arithmetic): top-k, renormalised weights, distinct experts.
+  if (warp < T) {
+    const int t = warp;
+    constexpr int kPer = kMaxExperts / 32;
+    const int kp = (E + 31) / 32;
+    uint32_t key[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int e = lane + 32 * j;
+      key[j] = (j < kp && e < E) ? f32_order_key(ldg_cg_f32(a.logits + (size_t)t * E + e)) : 0u;
+    }
+    float v0 = 0.f, sum = 0.f, my_v = 0.f;
+    int my_e = 0;
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+      uint32_t lk = 0u;
+      int lj = 0;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        if (j < kp && key[j] > lk) { lk = key[j]; lj = j; }
+      const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, lk);
+      const uint32_t cand = (lk == gmax) ? (uint32_t)(lane + 32 * lj) : 0xFFFFFFFFu;
+      const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
+      if (lane == (int)(gidx & 31u)) {
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+          if (j == (int)(gidx >> 5)) key[j] = 0u;
+      }
+      const float val = f32_from_order_key(gmax);
+      if (r == 0) v0 = val;
+      const float ex = expf(val - v0);   // renormalised softmax over the k selected logits
+      sum += ex;
+      if (lane == r) { my_v = ex; my_e = (int)gidx; }
+    }
+    if (lane < k) {
+      const float wgt = my_v / sum;
+      s_idx[t * k + lane] = my_e;
+      s_w[t * k + lane] = wgt;
+      if (b == 0) {
+        a.idx[t * k + lane] = my_e;
+        a.weights[t * k + lane] = wgt;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int n = T * k;
+    bool first[2] = {false, false};
+    int firstpos[2] = {0, 0};
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int aidx = lane + 32 * h2;
+      if (aidx < n) {
+        const int e = s_idx[aidx];
+        int q = 0;
+        while (s_idx[q] != e) ++q;
+        first[h2] = (q == aidx);
+        firstpos[h2] = q;
+      }
+    }
+    const unsigned m0 = __ballot_sync(0xFFFFFFFFu, first[0]);
+    const unsigned m1 = __ballot_sync(0xFFFFFFFFu, first[1]);
+    const unsigned lt = (1u << lane) - 1u;
+    if (first[0]) s_slot_of[lane] = __popc(m0 & lt);
+    if (first[1]) s_slot_of[lane + 32] = __popc(m0) + __popc(m1 & lt);
+    __syncwarp();
+    const int D = __popc(m0) + __popc(m1);
+    for (int q = lane; q < D * kMaxDecodeT; q += 32) s_meta.slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = -1;
+    __syncwarp();
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int aidx = lane + 32 * h2;
+      if (aidx < n) {
+        const int slot = s_slot_of[firstpos[h2]];
+        if (first[h2]) s_meta.slot_expert[slot] = s_idx[aidx];
+        s_meta.slot_j[slot][aidx / k] = (signed char)(aidx % k);
+      }
+    }
+    if (lane == 0) s_meta.num_slots = D;
+  }
   __syncthreads();
   const int D = s_meta.num_slots;
+  if (b == 0) {  // diagnostics copy of the window's routing metadata
+    const int* src = reinterpret_cast<const int*>(&s_meta);
+    int* dst = reinterpret_cast<int*>(a.meta);
+    for (int q = threadIdx.x; q < (int)(sizeof(DecodeMeta) / 4); q += blockDim.x) dst[q] = src[q];
+  }
+
+  // ------------------------------------------------ phase 2: routed gate/up
+  const int d_smem = D < a.slots_cap ? D : a.slots_cap;  // slots whose down rows go to shared memory
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = (uint32_t)(nrows * a.rb_down);
+    sm100::mbar_arrive_expect_tx(&bar_rt, bytes * d_smem);
+    if (bytes)
+      for (int d = 0; d < d_smem; ++d)
+        sm100::bulk_copy_g2s(s_rows + (size_t)d * a.slot_stride,
+                             a.w_down + ((int64_t)s_meta.slot_expert[d] * H + n0) * a.rb_down, bytes, &bar_rt);
+  }
+  if (threadIdx.x == 32 && nrows > 0) {  // the remaining slots' down rows: HBM -> L2
+    for (int d = d_smem; d < D; ++d)
+      prefetch_l2_bulk(a.w_down + ((int64_t)s_meta.slot_expert[d] * H + n0) * a.rb_down,
+                       (uint32_t)(nrows * a.rb_down));
+  }
   const int64_t U = (int64_t)D * I;
   const int64_t u0 = U * b / G, u1 = U * (b + 1) / G;
   const int64_t unit_bytes = 2 * a.rb_gu;
@@ -503,11 +521,6 @@ moe_decode_fused_kernel(const FusedArgs a) {
       const int64_t u = u0 + warp + (int64_t)nw * r;
       if (u < u1) prefetch_l2_bulk(unit_ptr(u), (uint32_t)unit_bytes);
     }
-  }
-  if (threadIdx.x == 32 && (int64_t)D * H * a.rb_down <= a.down_prefetch_limit && n1 > n0) {
-    for (int d = 0; d < D; ++d)  // phase-3 down rows of this CTA
-      prefetch_l2_bulk(a.w_down + ((int64_t)s_meta.slot_expert[d] * H + n0) * a.rb_down,
-                       (uint32_t)((n1 - n0) * a.rb_down));
   }
   for (int64_t u = u0 + warp; u < u1; u += nw) {
     if (lane == 0 && u + (int64_t)nw * (kLookahead + 1) < u1)
@@ -546,17 +559,26 @@ moe_decode_fused_kernel(const FusedArgs a) {
   // ------------------------------------------------ sync B: all SwiGLU outputs written
   __syncthreads();
   if (threadIdx.x == 0) {
-    bool last;
-    const unsigned long long gen = grid_arrive(&a.sync_ctr[1], &last);
-    if (last) st_release_u64(&a.sync_flag[1], gen + 1);
-    if (!grid_wait(&a.sync_flag[1], gen, a.err)) s_abort = 1;
+    const unsigned long long gen = grid_arrive(&a.sync_ctr[1]);
+    if (!grid_wait(&a.sync_ctr[1], gen, a.err)) s_abort = 1;
+    // down rows copied to shared memory during phase 2
+    if (!s_abort) {
+      volatile int never = 0;
+      if (!sm100::mbar_wait(&bar_sh, 0, a.err, &never, 4000000000LL, false) ||
+          !sm100::mbar_wait(&bar_rt, 0, a.err, &never, 4000000000LL, false))
+        s_abort = 1;
+    }
   }
   __syncthreads();
   if (s_abort) return;
 
   // ------------------------------------------------ phase 3: down + combine
+  // Warp w takes expert slots w, w + 16, ... (slot D is the shared expert, weight
+  // 1) and, for each of this CTA's output rows, dots the slot's down row with the
+  // slot's SwiGLU outputs, which it reads once per 8 rows. Per-warp partial sums
+  // meet in shared memory and are added in warp order (deterministic).
   float* hss = hs + (size_t)T * k * I;
-  for (int q = threadIdx.x; q < T * k; q += blockDim.x) s_w[q] = ldg_cg_f32(a.weights + q);
+  float* s_part = reinterpret_cast<float*>(s_rows + (size_t)a.slots_cap * a.slot_stride);  // [nw][rows_max][T]
   {
     const int n16 = T * k * I / 4;
     for (int q = threadIdx.x; q < n16; q += blockDim.x)
@@ -564,92 +586,110 @@ moe_decode_fused_kernel(const FusedArgs a) {
     const int s16 = T * Is / 4;
     for (int q = threadIdx.x; q < s16; q += blockDim.x)
       reinterpret_cast<uint4*>(hss)[q] = ldg_cg(reinterpret_cast<const uint4*>(a.h_shared) + q);
+    for (int q = threadIdx.x; q < nw * a.rows_max * T; q += blockDim.x) s_part[q] = 0.f;
   }
   __syncthreads();
-  const bool bf = std::is_same<Fmt, FmtBF16>::value;
-  const int nch = bf ? I / 8 : I / 32;
-  const int F = D * nch;
-  for (int n = n0 + warp; n < n1; n += nw) {
-    float acc[TMAX];
+  constexpr int RB = TMAX <= 2 ? 8 : (TMAX <= 4 ? 4 : 2);   // rows per pass
+  for (int sd = warp; sd <= D; sd += nw) {
+    const bool shared = (sd == D);
+    if (shared && Is == 0) break;
+    const bool mx = !shared && !std::is_same<Fmt, FmtBF16>::value;
+    const int K = shared ? Is : I;
+    const int nsub = K / 8;                    // 8-element sub-chunks of a row
+    const bool in_smem = shared || sd < d_smem;
+    const uint8_t* rows_base;
+    int64_t rstride;
+    if (shared) { rows_base = s_shrows; rstride = (int64_t)Is * 2; }
+    else if (in_smem) { rows_base = s_rows + (size_t)sd * a.slot_stride; rstride = a.rb_down; }
+    else { rows_base = a.w_down + ((int64_t)s_meta.slot_expert[sd] * H + n0) * a.rb_down; rstride = a.rb_down; }
+    float wt[TMAX];
+    const float* hrow[TMAX];
 #pragma unroll
-    for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-    const uint16_t* srow = a.ws_down + (size_t)n * Is;
-    const int snch = Is / 8;
-    uint4 sv[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c = lane + 32 * q;
-      if (c < snch) sv[q] = ldg_stream(srow + 8 * c);
-    }
-    for (int f0 = 0; f0 < F; f0 += 32 * 16) {
-      uint32_t sc[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int f = f0 + lane + 32 * q;
-        if (f < F) {
-          const int d = f / nch, c = f - d * nch;
-          const uint8_t* rec = a.w_down + ((int64_t)s_meta.slot_expert[d] * H + n) * a.rb_down;
-          v[q] = ldg_stream(rec + 16 * c);
-          if (!bf) sc[q] = __ldg(rec + I / 2 + c);
+    for (int t = 0; t < TMAX; ++t) {
+      wt[t] = 0.f;
+      hrow[t] = nullptr;
+      if (t < T) {
+        if (shared) { wt[t] = 1.f; hrow[t] = hss + (size_t)t * Is; }
+        else {
+          const int j = s_meta.slot_j[sd][t];
+          if (j >= 0) { wt[t] = s_w[t * k + j]; hrow[t] = hs + ((size_t)t * k + j) * I; }
         }
       }
+    }
+    for (int r0 = 0; r0 < nrows; r0 += RB) {
+      float acc[RB][TMAX];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int f = f0 + lane + 32 * q;
-        if (f < F) {
-          const int d = f / nch, c = f - d * nch;
+      for (int rr = 0; rr < RB; ++rr)
 #pragma unroll
-          for (int t = 0; t < TMAX; ++t) {
-            if (t < T) {
-              const int j = s_meta.slot_j[d][t];
-              if (j >= 0) {
-                if (bf) {
-                  const float* hp = hs + ((size_t)t * k + j) * I + 8 * c;
-                  acc[t] = fmaf(s_w[t * k + j],
-                                dot8_bf16_f32(v[q], *reinterpret_cast<const float4*>(hp),
-                                              *reinterpret_cast<const float4*>(hp + 4)),
-                                acc[t]);
-                } else {
-                  const float* hp = hs + ((size_t)t * k + j) * I + 32 * c;
-                  acc[t] = fmaf(s_w[t * k + j] * e8m0_scale(sc[q]), dot32_e2m1_f32(v[q], hp, lut), acc[t]);
-                }
+        for (int t = 0; t < TMAX; ++t) acc[rr][t] = 0.f;
+      for (int c = lane; c < nsub; c += 32) {
+        float4 h0[TMAX], h1[TMAX];
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+          if (hrow[t]) {
+            h0[t] = *reinterpret_cast<const float4*>(hrow[t] + 8 * c);
+            h1[t] = *reinterpret_cast<const float4*>(hrow[t] + 8 * c + 4);
+          }
+        }
+        uint4 wv[RB];
+        uint32_t sb[RB];
+#pragma unroll
+        for (int rr = 0; rr < RB; ++rr) {  // issue the row loads of this pass together
+          if (r0 + rr < nrows) {
+            const uint8_t* rec = rows_base + (r0 + rr) * rstride;
+            if (!mx) {
+              wv[rr] = in_smem ? *reinterpret_cast<const uint4*>(rec + 16 * c) : ldg_stream(rec + 16 * c);
+            } else {
+              wv[rr].x = in_smem ? *reinterpret_cast<const uint32_t*>(rec + 4 * c)
+                                 : __ldg(reinterpret_cast<const uint32_t*>(rec + 4 * c));
+              sb[rr] = in_smem ? rec[I / 2 + c / 4] : __ldg(rec + I / 2 + c / 4);
+            }
+          }
+        }
+#pragma unroll
+        for (int rr = 0; rr < RB; ++rr) {
+          if (r0 + rr < nrows) {
+            float w8[8];
+            if (!mx) {
+              w8[0] = bf16_lo(wv[rr].x); w8[1] = bf16_hi(wv[rr].x); w8[2] = bf16_lo(wv[rr].y); w8[3] = bf16_hi(wv[rr].y);
+              w8[4] = bf16_lo(wv[rr].z); w8[5] = bf16_hi(wv[rr].z); w8[6] = bf16_lo(wv[rr].w); w8[7] = bf16_hi(wv[rr].w);
+            } else {
+              const float sc = e8m0_scale(sb[rr]);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) w8[q] = lut[(wv[rr].x >> (4 * q)) & 15u] * sc;
+            }
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+              if (hrow[t]) {
+                float s = acc[rr][t];
+                s = fmaf(w8[0], h0[t].x, s); s = fmaf(w8[1], h0[t].y, s);
+                s = fmaf(w8[2], h0[t].z, s); s = fmaf(w8[3], h0[t].w, s);
+                s = fmaf(w8[4], h1[t].x, s); s = fmaf(w8[5], h1[t].y, s);
+                s = fmaf(w8[6], h1[t].z, s); s = fmaf(w8[7], h1[t].w, s);
+                acc[rr][t] = s;
               }
             }
           }
         }
       }
-    }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c = lane + 32 * q;
-      if (c < snch) {
+      for (int rr = 0; rr < RB; ++rr) {
 #pragma unroll
         for (int t = 0; t < TMAX; ++t) {
-          if (t < T) {
-            const float* hp = hss + (size_t)t * Is + 8 * c;
-            acc[t] += dot8_bf16_f32(sv[q], *reinterpret_cast<const float4*>(hp),
-                                    *reinterpret_cast<const float4*>(hp + 4));
+          if (hrow[t] && r0 + rr < nrows) {   // warp-uniform conditions
+            const float sum = warp_sum(acc[rr][t]);
+            if (lane == 0) s_part[((size_t)warp * a.rows_max + r0 + rr) * T + t] += wt[t] * sum;
           }
         }
       }
     }
-    for (int c = lane + 128; c < snch; c += 32) {  // shared rows longer than 128 chunks
-      const uint4 wv = ldg_stream(srow + 8 * c);
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        if (t < T) {
-          const float* hp = hss + (size_t)t * Is + 8 * c;
-          acc[t] += dot8_bf16_f32(wv, *reinterpret_cast<const float4*>(hp), *reinterpret_cast<const float4*>(hp + 4));
-        }
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t) {
-      if (t < T) {
-        const float s = warp_sum(acc[t]);
-        if (lane == t) a.out[(size_t)t * H + n] = f32_to_bf16_rne(s);
-      }
-    }
+  }
+  __syncthreads();
+  for (int q = threadIdx.x; q < nrows * T; q += blockDim.x) {
+    const int r = q / T, t = q - r * T;
+    float sum = 0.f;
+    for (int w = 0; w < nw; ++w) sum += s_part[((size_t)w * a.rows_max + r) * T + t];
+    a.out[(size_t)t * H + n0 + r] = f32_to_bf16_rne(sum);
   }
 }
 
@@ -661,11 +701,9 @@ size_t decode_smem_bytes_down(const moe_layer* L, int T) {
   return (size_t)T * ((size_t)c.top_k * c.intermediate + c.shared_intermediate) * sizeof(float);
 }
 
-static size_t fused_smem_bytes(const moe_layer* L, int T) {
-  const size_t xb = (size_t)T * L->cfg.hidden * sizeof(uint16_t);
-  const size_t hb = decode_smem_bytes_down(L, T);
-  return xb > hb ? xb : hb;
-}
+constexpr int kFusedSmemMax = 216 * 1024;  // dynamic shared memory budget of the fused kernel
+
+static size_t align16(size_t v) { return (v + 15) / 16 * 16; }
 
 template <int TMAX, class Fmt>
 static cudaError_t launch_fused_t(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
@@ -677,17 +715,27 @@ static cudaError_t launch_fused_t(moe_layer* L, const uint16_t* x, uint16_t* out
   a.router_t = L->router_t; a.router_bias = L->router_bias; a.logit_bias = logit_bias;
   a.ws_gu = L->ws_gu; a.ws_down = L->ws_down;
   a.w_gu = L->w_gu; a.rb_gu = L->row_bytes.gu; a.w_down = L->w_down; a.rb_down = L->row_bytes.down;
-  a.down_prefetch_limit = 40ll << 20;
+  const int rows_max = (c.hidden + L->num_sms - 1) / L->num_sms;
+  const size_t xb = (size_t)T * c.hidden * sizeof(uint16_t), hb = decode_smem_bytes_down(L, T);
+  a.smem_r1 = (int)align16(xb > hb ? xb : hb);
+  a.smem_sh = (int)align16((size_t)rows_max * c.shared_intermediate * 2);
+  a.slot_stride = (int)((size_t)rows_max * L->row_bytes.down);
+  a.rows_max = rows_max;
+  const size_t part_bytes = (size_t)(kGemvThreads / 32) * rows_max * T * sizeof(float);
+  long left = (long)kFusedSmemMax - a.smem_r1 - a.smem_sh - (long)part_bytes;
+  int cap = left > 0 ? (int)(left / a.slot_stride) : 0;
+  if (cap > T * c.top_k) cap = T * c.top_k;
+  a.slots_cap = cap;
   a.logits = L->dec.logits; a.h = L->dec.h; a.h_shared = L->dec.h_shared;
   a.idx = L->dec.idx; a.weights = L->dec.weights; a.meta = L->dec.meta;
-  a.sync_ctr = L->dec.sync_ctr; a.sync_flag = L->dec.sync_flag;
+  a.sync_ctr = L->dec.sync_ctr;
   a.out = out; a.err = L->err; a.never_set = L->never_set;
   a.force_timeout = (c.flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L->num_sms);
   cfg.blockDim = dim3(kGemvThreads);
-  cfg.dynamicSmemBytes = fused_smem_bytes(L, T);
+  cfg.dynamicSmemBytes = (size_t)a.smem_r1 + a.smem_sh + (size_t)cap * a.slot_stride + part_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs co-resident: they wait on one another
@@ -704,7 +752,7 @@ template <class Fmt>
 static cudaError_t set_attrs_fmt() {
   cudaError_t e = cudaSuccess;
   auto set = [&](const void* f) {
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemMax);
   };
   set((const void*)moe_decode_fused_kernel<1, Fmt>);
   set((const void*)moe_decode_fused_kernel<2, Fmt>);

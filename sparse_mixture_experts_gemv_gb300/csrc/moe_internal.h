@@ -34,7 +34,6 @@ struct DecodeWorkspace {
   float* h;              // [kMaxDecodeT * k][I]   SwiGLU outputs of routed assignments (t*k+j)
   float* h_shared;       // [kMaxDecodeT][Is]
   unsigned long long* sync_ctr;   // [2] grid-sync arrival counters (monotonic)
-  unsigned long long* sync_flag;  // [2] grid-sync released generations
 };
 
 struct GroupedWorkspace {

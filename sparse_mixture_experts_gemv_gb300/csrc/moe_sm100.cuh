@@ -148,3 +148,15 @@ MOE_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 }  // namespace sm100
 }  // namespace moe
+
+namespace moe {
+namespace sm100 {
+// Bulk (non-tensor) copy of `bytes` (multiple of 16, both addresses 16-byte
+// aligned) from global to this CTA's shared memory; completes as transaction
+// bytes on `bar`.
+MOE_DEV void bulk_copy_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+}  // namespace sm100
+}  // namespace moe
