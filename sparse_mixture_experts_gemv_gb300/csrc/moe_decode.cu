@@ -512,21 +512,19 @@ moe_decode_fused_kernel(const FusedArgs a) {
   const int64_t U = (int64_t)D * I;
   const int64_t u0 = U * b / G, u1 = U * (b + 1) / G;
   const int64_t unit_bytes = 2 * a.rb_gu;
-  auto unit_ptr = [&](int64_t u) {
-    const int d = (int)(u / I), i = (int)(u % I);
-    return a.w_gu + ((int64_t)s_meta.slot_expert[d] * I + i) * unit_bytes;
-  };
   if (lane == 0) {  // this warp's next rounds of units: HBM -> L2
     for (int r = 0; r <= kLookahead; ++r) {
       const int64_t u = u0 + warp + (int64_t)nw * r;
-      if (u < u1) prefetch_l2_bulk(unit_ptr(u), (uint32_t)unit_bytes);
+      if (u < u1)
+        prefetch_l2_bulk(a.w_gu + ((int64_t)s_meta.slot_expert[u / I] * I + u % I) * unit_bytes, (uint32_t)unit_bytes);
     }
   }
   for (int64_t u = u0 + warp; u < u1; u += nw) {
-    if (lane == 0 && u + (int64_t)nw * (kLookahead + 1) < u1)
-      prefetch_l2_bulk(unit_ptr(u + (int64_t)nw * (kLookahead + 1)), (uint32_t)unit_bytes);
+    const int64_t ua = u + (int64_t)nw * (kLookahead + 1);
+    if (lane == 0 && ua < u1)
+      prefetch_l2_bulk(a.w_gu + ((int64_t)s_meta.slot_expert[ua / I] * I + ua % I) * unit_bytes, (uint32_t)unit_bytes);
     const int d = (int)(u / I), i = (int)(u % I);
-    const uint8_t* grec = unit_ptr(u);
+    const uint8_t* grec = a.w_gu + ((int64_t)s_meta.slot_expert[d] * I + i) * unit_bytes;
     const uint8_t* urec = grec + a.rb_gu;
     float ag[TMAX], au[TMAX];
 #pragma unroll
