@@ -228,6 +228,37 @@ moe_status_t moe_layer_profile_enable(moe_layer_t* layer, int32_t enable);
 moe_status_t moe_layer_profile_read(moe_layer_t* layer, float* stage_ms, int32_t max_stages,
                                     int32_t* n_stages);
 
+/*
+ * Routing without any device allocation (no counterpart on the pages; this is
+ * an entry point of this library for callers that cannot call cudaMalloc, for
+ * example code running while a CUDA graph is captured, or a host framework
+ * that owns all device memory through its own pool).
+ *
+ * Computes, for T tokens, the fp32 router logits x . W_r (+ router_bias[e])
+ * (+ logit_bias[t][e]), the top-k experts (descending, exact ties to the lower
+ * index) and their renormalised softmax weights -- the same routing
+ * moe_layer_forward does -- from buffers the caller passes:
+ *   x_dev            bf16 [T, H], 8-byte aligned
+ *   router_t_dev     fp32 [E, H] (W_r transposed: one row of H per expert), 16-byte aligned
+ *   router_bias_dev  fp32 [E] or NULL;  logit_bias_dev fp32 [T, E] or NULL
+ *   idx_dev          int32 [T, k] out;  weights_dev fp32 [T, k] out
+ * Scratch: the T*E router logits live in one fixed device array inside this
+ * library (MOE_NOALLOC_MAX_TOKENS * MOE_NOALLOC_MAX_EXPERTS floats = 16 KB),
+ * held by every GPU that loads the library until the process exits. T above
+ * MOE_NOALLOC_MAX_TOKENS, E above MOE_NOALLOC_MAX_EXPERTS or k above 8 return
+ * MOE_ERR_UNSUPPORTED. Every call overwrites the whole logits region it uses
+ * before reading it, so nothing needs clearing, but all calls share the array:
+ * calls that overlap on the GPU (unordered streams, or several host threads)
+ * race. The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Enqueued on `stream`; no host synchronisation.
+ */
+#define MOE_NOALLOC_MAX_TOKENS 8
+#define MOE_NOALLOC_MAX_EXPERTS 512
+moe_status_t moe_route_topk_noalloc(const void* x_dev, const float* router_t_dev, const float* router_bias_dev,
+                                    const float* logit_bias_dev, int32_t T, int32_t H, int32_t E, int32_t k,
+                                    int32_t* idx_dev, float* weights_dev, void* stream);
+
 /* Name of a status code (static string). */
 const char* moe_status_string(moe_status_t status);
 

@@ -81,6 +81,8 @@ _SIGNATURES = {
     "moe_layer_profile_enable": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     "moe_layer_profile_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.c_int32,
                                               ctypes.POINTER(ctypes.c_int32)]),
+    "moe_route_topk_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int32] * 4 +
+                               [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_cuda_error": (ctypes.c_char_p, []),
 }
@@ -182,6 +184,16 @@ def moe_layer_profile_read(layer: int, max_stages: int = 8):
     if st != MOE_OK:
         raise MoeError(st, "moe_layer_profile_read")
     return [buf[i] for i in range(n.value)]
+
+
+MOE_NOALLOC_MAX_TOKENS = 8
+MOE_NOALLOC_MAX_EXPERTS = 512
+
+
+def moe_route_topk_noalloc(x_dev, router_t_dev, router_bias_dev, logit_bias_dev, T, H, E, k, idx_dev,
+                           weights_dev, stream=0) -> int:
+    return load().moe_route_topk_noalloc(x_dev, router_t_dev, router_bias_dev, logit_bias_dev, T, H, E, k,
+                                         idx_dev, weights_dev, stream)
 
 
 def moe_layer_describe(layer: int) -> str:
