@@ -443,6 +443,25 @@ def run_reference(args):
                                     "d2h_bytes_per_step": 0}}), flush=True)
 
 
+def run_profile_driver(args):
+    """Untimed forward calls of one workload (for ncu captures): builds the layer,
+    then runs --profile-calls calls with the L2 flushed before each."""
+    import torch
+    dev = torch.device("cuda", 0)
+    B = Bench(dev)
+    w = mi.WORKLOADS[args.profile]
+    L = B.layer(w.layer, max_tokens=max(8, w.T) if w.layer.fmt != "bf16" else 4096)
+    xs, lbs = B.inputs(w, min(w.calls, args.profile_calls))
+    for c in range(args.profile_calls):
+        B.flush.zero_()
+        L.forward(xs[c % len(xs)], logit_bias=lbs[c % len(lbs)])
+    torch.cuda.synchronize()
+    st = L.sync_status()
+    print(json.dumps({"profile_driver": args.profile, "calls": args.profile_calls, "status": st}))
+    if st != 0:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -453,7 +472,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-calls-per-step", type=int, default=8)
+    ap.add_argument("--profile", default=None, choices=sorted(mi.WORKLOADS),
+                    help="untimed calls of one workload, for ncu captures")
+    ap.add_argument("--profile-calls", type=int, default=6)
     args = ap.parse_args()
+    if args.profile:
+        run_profile_driver(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
