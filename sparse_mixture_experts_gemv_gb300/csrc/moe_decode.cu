@@ -692,6 +692,430 @@ moe_decode_fused_kernel(const FusedArgs a) {
 }
 
 // ===========================================================================
+// bf16 streaming decode kernel: gate/up and down fused per intermediate feature.
+// ===========================================================================
+// Unit = one (expert slot, intermediate feature i) record [gate row | up row |
+// down column], 3 x H bf16, contiguous. A CTA owns a balanced range of the
+// window's routed units (plus a static share of the shared expert's units),
+// streams them through a ring of shared-memory stages filled by cp.async.bulk,
+// and for each unit computes g = gate.x, u = up.x, h = silu(g) u and adds
+// w * h * down_column to its own output partial. After one grid barrier every
+// CTA adds up its slice of output columns over all CTAs' partials in CTA order.
+constexpr int kStreamUnits = 2;    // units per ring stage
+constexpr int kStreamStages = 6;   // ring depth
+constexpr int kStreamMaxH = 4096;  // two 4-column granules per lane per warp
+
+struct StreamArgs {
+  const uint16_t* x;           // bf16 [T][H]
+  int T, H, E, k, I, Is;
+  const float* router_t;       // fp32 [E][H]
+  const float* router_bias;    // fp32 [E]
+  const float* logit_bias;     // fp32 [T][E] or nullptr
+  const uint16_t* rec;         // routed records [E][I][3][H]
+  const uint16_t* srec;        // shared records [Is][3][H]
+  float* logits;               // [T][E]
+  float* partial;              // [G][T][H]
+  int* idx;                    // [T][k]     (written by CTA 0, diagnostics)
+  float* weights;              // [T][k]     (written by CTA 0, diagnostics)
+  DecodeMeta* meta;            //            (written by CTA 0, diagnostics)
+  unsigned long long* sync_ctr;
+  uint16_t* out;               // bf16 [T][H]
+  int* err;
+  const int* never_set;
+  int force_timeout;
+};
+
+template <int TMAX>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+moe_decode_stream_kernel(const StreamArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int T = a.T, H = a.H, E = a.E, I = a.I, Is = a.Is, k = a.k;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int nw = kGemvThreads / 32;
+  const int G = gridDim.x, b = blockIdx.x;
+  const size_t unit_bytes = (size_t)3 * H * 2;
+  const size_t stage_bytes = kStreamUnits * unit_bytes;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                               // [T][H]
+  uint8_t* ring = smem + ((size_t)T * H * 2 + 127) / 128 * 128;                   // kStreamStages stages
+  float2* s_part = reinterpret_cast<float2*>(ring + kStreamStages * stage_bytes); // [units][8 warps][T] (g, u)
+  __shared__ __align__(8) uint64_t full[kStreamStages];
+  __shared__ DecodeMeta s_meta;
+  __shared__ float s_w[kMaxDecodeT * kMaxTopK];
+  __shared__ int s_idx[kMaxDecodeT * kMaxTopK];
+  __shared__ int s_slot_of[kMaxDecodeT * kMaxTopK];
+  __shared__ int s_router_done, s_abort;
+  __shared__ unsigned long long s_gen;
+
+  // This CTA's units: shared-expert units [sh0, sh1) first, then routed units [u0, u1).
+  const int sh0 = (int)((int64_t)b * Is / G), sh1 = (int)((int64_t)(b + 1) * Is / G);
+  const int nsh = sh1 - sh0;
+  const int st_sh = (nsh + kStreamUnits - 1) / kStreamUnits;  // stages holding shared units
+  const int nr = (E - b + G - 1) / G;                          // router rows b, b + G, ...
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStreamStages; ++s) sm100::mbar_init(&full[s], 1);
+    sm100::fence_barrier_init();
+    s_router_done = 0;
+    s_abort = 0;
+    if (nr == 0) s_gen = grid_arrive(&a.sync_ctr[0]);
+    if (a.force_timeout && b == 0 && !bounded_wait_flag(a.never_set, 2000000LL)) set_error(a.err, kDevTimeout);
+    // shared-expert units do not depend on routing: start their copies now
+    for (int s = 0; s < st_sh && s < kStreamStages; ++s) {
+      const int q0 = s * kStreamUnits, q1 = min(nsh, q0 + kStreamUnits);
+      const uint32_t bytes = (uint32_t)((q1 - q0) * unit_bytes);
+      sm100::mbar_arrive_expect_tx(&full[s], bytes);
+      sm100::bulk_copy_g2s(ring + (size_t)s * stage_bytes, a.srec + (size_t)(sh0 + q0) * 3 * H, bytes, &full[s]);
+    }
+  }
+
+  // ------------------------------------------------ phase 1: router logits
+  uint4 v[16];
+  if (warp < nr) {
+    const float* row = a.router_t + (size_t)(b + warp * G) * H;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int c = lane + 32 * q;
+      if (c < H / 4) v[q] = ldg_stream(row + 4 * c);
+    }
+  }
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(a.x);
+    uint4* dst = reinterpret_cast<uint4*>(xs);
+    for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) dst[i] = src[i];
+  }
+  __syncthreads();
+  for (int slot = warp; slot < nr; slot += nw) {
+    const int u = b + slot * G;
+    const float* row = a.router_t + (size_t)u * H;
+    const int nch = H / 4;
+    float acc[TMAX];
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
+    for (int b0 = 0; b0 < nch; b0 += 32 * 16) {
+      if (!(slot == warp && b0 == 0)) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int c = b0 + lane + 32 * q;
+          if (c < nch) v[q] = ldg_stream(row + 4 * c);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int c = b0 + lane + 32 * q;
+        if (c < nch) {
+#pragma unroll
+          for (int t = 0; t < TMAX; ++t) {
+            if (t < T) {
+              const uint2 xx = *reinterpret_cast<const uint2*>(xs + t * H + 4 * c);
+              float s = acc[t];
+              s = fmaf(__uint_as_float(v[q].x), bf16_lo(xx.x), s);
+              s = fmaf(__uint_as_float(v[q].y), bf16_hi(xx.x), s);
+              s = fmaf(__uint_as_float(v[q].z), bf16_lo(xx.y), s);
+              s = fmaf(__uint_as_float(v[q].w), bf16_hi(xx.y), s);
+              acc[t] = s;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      if (t < T) {
+        float s = warp_sum(acc[t]);
+        if (lane == t) {
+          s += a.router_bias[u];
+          if (a.logit_bias) s += a.logit_bias[(size_t)t * E + u];
+          a.logits[(size_t)t * E + u] = s;
+        }
+      }
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0 && atomicAdd(&s_router_done, 1) == nr - 1) s_gen = grid_arrive(&a.sync_ctr[0]);
+  }
+
+  // Output partial of this CTA: warp w owns 4-column granules g = lane + 32 * (w + 16 m).
+  float acc[2][4][TMAX];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) acc[m][c][t] = 0.f;
+  const int ngran = H / 4;
+
+  // One ring stage: gate/up dots (8 warps per unit), then every warp adds the
+  // units' down columns, scaled by the routing weight times h, to its granules.
+  // `coef_of(q, t)` gives the routing weight of stage unit q for token t (0: unused).
+  auto run_stage = [&](int s, int nunits, const float (&wq)[kStreamUnits][TMAX]) -> bool {
+    {  // every thread observes the stage's copy completion before reading it
+      volatile int never = 0;
+      if (!sm100::mbar_wait(&full[s % kStreamStages], (s / kStreamStages) & 1, a.err, &never, 4000000000LL, false))
+        s_abort = 1;
+    }
+    __syncthreads();
+    if (s_abort) return false;
+    const uint8_t* stage = ring + (size_t)(s % kStreamStages) * stage_bytes;
+    {
+      const int q = warp >> 3, w8 = warp & 7;
+      if (q < nunits) {
+        const uint8_t* g = stage + q * unit_bytes;
+        const uint8_t* u = g + (size_t)H * 2;
+        float ag[TMAX], au[TMAX];
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) ag[t] = au[t] = 0.f;
+        for (int c = lane + 32 * w8; c < H / 8; c += 256) {
+          const uint4 gv = *reinterpret_cast<const uint4*>(g + 16 * c);
+          const uint4 uv = *reinterpret_cast<const uint4*>(u + 16 * c);
+#pragma unroll
+          for (int t = 0; t < TMAX; ++t) {
+            if (t < T) {
+              const uint4 xx = *reinterpret_cast<const uint4*>(xs + t * H + 8 * c);
+              ag[t] += dot8_bf16(gv, xx);
+              au[t] += dot8_bf16(uv, xx);
+            }
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+          if (t < T) {
+            const float gs = warp_sum(ag[t]), us = warp_sum(au[t]);
+            if (lane == 0) s_part[(q * 8 + w8) * TMAX + t] = make_float2(gs, us);
+          }
+        }
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kStreamUnits; ++q) {
+      if (q < nunits) {
+        float coef[TMAX];
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+          coef[t] = 0.f;
+          if (t < T && wq[q][t] != 0.f) {
+            float gs = 0.f, us = 0.f;
+#pragma unroll
+            for (int w8 = 0; w8 < 8; ++w8) {
+              const float2 p = s_part[(q * 8 + w8) * TMAX + t];
+              gs += p.x;
+              us += p.y;
+            }
+            coef[t] = wq[q][t] * swiglu(gs, us);
+          }
+        }
+        const uint8_t* dcol = stage + q * unit_bytes + (size_t)4 * H;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int gi = lane + 32 * (warp + 16 * m);
+          if (gi < ngran) {
+            const uint2 dv = *reinterpret_cast<const uint2*>(dcol + 8 * gi);
+            const float d0 = bf16_lo(dv.x), d1 = bf16_hi(dv.x), d2 = bf16_lo(dv.y), d3 = bf16_hi(dv.y);
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+              acc[m][0][t] = fmaf(coef[t], d0, acc[m][0][t]);
+              acc[m][1][t] = fmaf(coef[t], d1, acc[m][1][t]);
+              acc[m][2][t] = fmaf(coef[t], d2, acc[m][2][t]);
+              acc[m][3][t] = fmaf(coef[t], d3, acc[m][3][t]);
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();  // the stage buffer is free again
+    return true;
+  };
+
+  // ------------------------------------------------ shared-expert units (overlap the routing barrier)
+  float wq[kStreamUnits][TMAX];
+#pragma unroll
+  for (int q = 0; q < kStreamUnits; ++q)
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) wq[q][t] = (t < T) ? 1.f : 0.f;
+  __syncthreads();
+  for (int s = 0; s < st_sh; ++s) {
+    if (!run_stage(s, min(kStreamUnits, nsh - s * kStreamUnits), wq)) return;
+    if (threadIdx.x == 0 && s + kStreamStages < st_sh) {
+      const int s2 = s + kStreamStages;
+      const int q0 = s2 * kStreamUnits, q1 = min(nsh, q0 + kStreamUnits);
+      const uint32_t bytes = (uint32_t)((q1 - q0) * unit_bytes);
+      sm100::mbar_arrive_expect_tx(&full[s2 % kStreamStages], bytes);
+      sm100::bulk_copy_g2s(ring + (size_t)(s2 % kStreamStages) * stage_bytes, a.srec + (size_t)(sh0 + q0) * 3 * H,
+                           bytes, &full[s2 % kStreamStages]);
+    }
+  }
+
+  // ------------------------------------------------ sync A: all router logits written
+  if (threadIdx.x == 0 && !grid_wait(&a.sync_ctr[0], s_gen, a.err)) s_abort = 1;
+  __syncthreads();
+  if (s_abort) return;
+
+  if (warp < T) {  // every CTA derives the routing itself (identical inputs, identical arithmetic)
+    const int t = warp;
+    constexpr int kPer = kMaxExperts / 32;
+    const int kp = (E + 31) / 32;
+    uint32_t key[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int e = lane + 32 * j;
+      key[j] = (j < kp && e < E) ? f32_order_key(ldg_cg_f32(a.logits + (size_t)t * E + e)) : 0u;
+    }
+    float v0 = 0.f, sum = 0.f, my_v = 0.f;
+    int my_e = 0;
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+      uint32_t lk = 0u;
+      int lj = 0;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        if (j < kp && key[j] > lk) { lk = key[j]; lj = j; }
+      const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, lk);
+      const uint32_t cand = (lk == gmax) ? (uint32_t)(lane + 32 * lj) : 0xFFFFFFFFu;
+      const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
+      if (lane == (int)(gidx & 31u)) {
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+          if (j == (int)(gidx >> 5)) key[j] = 0u;
+      }
+      const float val = f32_from_order_key(gmax);
+      if (r == 0) v0 = val;
+      const float ex = expf(val - v0);
+      sum += ex;
+      if (lane == r) { my_v = ex; my_e = (int)gidx; }
+    }
+    if (lane < k) {
+      const float wgt = my_v / sum;
+      s_idx[t * k + lane] = my_e;
+      s_w[t * k + lane] = wgt;
+      if (b == 0) {
+        a.idx[t * k + lane] = my_e;
+        a.weights[t * k + lane] = wgt;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int n = T * k;
+    bool first[2] = {false, false};
+    int firstpos[2] = {0, 0};
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int aidx = lane + 32 * h2;
+      if (aidx < n) {
+        const int e = s_idx[aidx];
+        int q = 0;
+        while (s_idx[q] != e) ++q;
+        first[h2] = (q == aidx);
+        firstpos[h2] = q;
+      }
+    }
+    const unsigned m0 = __ballot_sync(0xFFFFFFFFu, first[0]);
+    const unsigned m1 = __ballot_sync(0xFFFFFFFFu, first[1]);
+    const unsigned lt = (1u << lane) - 1u;
+    if (first[0]) s_slot_of[lane] = __popc(m0 & lt);
+    if (first[1]) s_slot_of[lane + 32] = __popc(m0) + __popc(m1 & lt);
+    __syncwarp();
+    const int D = __popc(m0) + __popc(m1);
+    for (int q = lane; q < D * kMaxDecodeT; q += 32) s_meta.slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = -1;
+    __syncwarp();
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int aidx = lane + 32 * h2;
+      if (aidx < n) {
+        const int slot = s_slot_of[firstpos[h2]];
+        if (first[h2]) s_meta.slot_expert[slot] = s_idx[aidx];
+        s_meta.slot_j[slot][aidx / k] = (signed char)(aidx % k);
+      }
+    }
+    if (lane == 0) s_meta.num_slots = D;
+  }
+  __syncthreads();
+  const int D = s_meta.num_slots;
+  if (b == 0) {
+    const int* src = reinterpret_cast<const int*>(&s_meta);
+    int* dst = reinterpret_cast<int*>(a.meta);
+    for (int q = threadIdx.x; q < (int)(sizeof(DecodeMeta) / 4); q += blockDim.x) dst[q] = src[q];
+  }
+
+  // ------------------------------------------------ routed units
+  const int64_t U = (int64_t)D * I;
+  const int64_t u0 = U * b / G, u1 = U * (b + 1) / G;
+  const int nst = (int)((u1 - u0 + kStreamUnits - 1) / kStreamUnits);
+  auto issue = [&](int rs) {  // routed stage rs -> ring stage st_sh + rs
+    const int s = st_sh + rs;
+    int64_t q = u0 + (int64_t)rs * kStreamUnits;
+    const int64_t qe = (u1 < q + kStreamUnits) ? u1 : q + kStreamUnits;
+    uint8_t* dst = ring + (size_t)(s % kStreamStages) * stage_bytes;
+    sm100::mbar_arrive_expect_tx(&full[s % kStreamStages], (uint32_t)((qe - q) * unit_bytes));
+    while (q < qe) {  // contiguous runs of one expert
+      const int d = (int)(q / I), i = (int)(q % I);
+      const int64_t run = (qe - q) < (int64_t)(I - i) ? (qe - q) : (int64_t)(I - i);
+      sm100::bulk_copy_g2s(dst, a.rec + ((size_t)s_meta.slot_expert[d] * I + i) * 3 * H, (uint32_t)(run * unit_bytes),
+                           &full[s % kStreamStages]);
+      dst += run * unit_bytes;
+      q += run;
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int rs = 0; rs < nst && rs < kStreamStages; ++rs) issue(rs);
+  for (int rs = 0; rs < nst; ++rs) {
+    const int64_t q0 = u0 + (int64_t)rs * kStreamUnits;
+    const int nunits = (int)((u1 - q0) < (int64_t)kStreamUnits ? (u1 - q0) : (int64_t)kStreamUnits);
+#pragma unroll
+    for (int q = 0; q < kStreamUnits; ++q) {
+      const int d = (int)((q0 + q) / I);
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        float wv = 0.f;
+        if (q < nunits && t < T) {
+          const int j = s_meta.slot_j[d][t];
+          if (j >= 0) wv = s_w[t * k + j];
+        }
+        wq[q][t] = wv;
+      }
+    }
+    if (!run_stage(st_sh + rs, nunits, wq)) return;
+    if (threadIdx.x == 0 && rs + kStreamStages < nst) issue(rs + kStreamStages);
+  }
+
+  // ------------------------------------------------ partials, sync B, column reduction
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int gi = lane + 32 * (warp + 16 * m);
+    if (gi < ngran) {
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t)
+        if (t < T)
+          *reinterpret_cast<float4*>(a.partial + ((size_t)b * T + t) * H + 4 * gi) =
+              make_float4(acc[m][0][t], acc[m][1][t], acc[m][2][t], acc[m][3][t]);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned long long gen = grid_arrive(&a.sync_ctr[1]);
+    if (!grid_wait(&a.sync_ctr[1], gen, a.err)) s_abort = 1;
+  }
+  __syncthreads();
+  if (s_abort) return;
+  const int n0 = (int)((int64_t)b * H / G), n1 = (int)((int64_t)(b + 1) * H / G), nrows = n1 - n0;
+  float* red = reinterpret_cast<float*>(ring);  // [32 groups][nrows * T]
+  const int cells = nrows * T;
+  for (int q = threadIdx.x; q < 32 * cells; q += blockDim.x) {
+    const int grp = q / cells, cell = q - grp * cells, t = cell / nrows, r = cell - t * nrows;
+    float sum = 0.f;
+    for (int p = grp; p < G; p += 32) sum += ldg_cg_f32(a.partial + ((size_t)p * T + t) * H + n0 + r);
+    red[q] = sum;
+  }
+  __syncthreads();
+  for (int cell = threadIdx.x; cell < cells; cell += blockDim.x) {
+    float sum = 0.f;
+    for (int grp = 0; grp < 32; ++grp) sum += red[grp * cells + cell];
+    const int t = cell / nrows, r = cell - t * nrows;
+    a.out[(size_t)t * H + n0 + r] = f32_to_bf16_rne(sum);
+  }
+}
+
+// ===========================================================================
 // Host launcher
 // ===========================================================================
 size_t decode_smem_bytes_down(const moe_layer* L, int T) {
@@ -746,6 +1170,51 @@ static cudaError_t launch_fused_t(moe_layer* L, const uint16_t* x, uint16_t* out
   return e;
 }
 
+constexpr int kStreamSmemMax = 220 * 1024;
+
+static size_t stream_smem_bytes(const moe_layer* L, int T) {
+  const size_t xb = ((size_t)T * L->cfg.hidden * 2 + 127) / 128 * 128;
+  const size_t ring = (size_t)kStreamStages * kStreamUnits * 3 * L->cfg.hidden * 2;
+  const size_t part = (size_t)kStreamUnits * 8 * kMaxDecodeT * sizeof(float2);
+  return xb + ring + part;
+}
+
+// The streaming kernel serves bf16 layers with H <= 4096 whose ring fits.
+static bool stream_path_ok(const moe_layer* L) {
+  return L->cfg.weight_format == MOE_WEIGHTS_BF16 && L->cfg.hidden <= kStreamMaxH &&
+         stream_smem_bytes(L, kMaxDecodeT) <= (size_t)kStreamSmemMax && L->w_rec != nullptr;
+}
+
+template <int TMAX>
+static cudaError_t launch_stream_t(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
+                                   cudaStream_t s) {
+  const auto& c = L->cfg;
+  StreamArgs a;
+  a.x = x; a.T = T; a.H = c.hidden; a.E = c.num_experts; a.k = c.top_k; a.I = c.intermediate;
+  a.Is = c.shared_intermediate;
+  a.router_t = L->router_t; a.router_bias = L->router_bias; a.logit_bias = logit_bias;
+  a.rec = L->w_rec; a.srec = L->ws_rec;
+  a.logits = L->dec.logits; a.partial = L->dec.partial;
+  a.idx = L->dec.idx; a.weights = L->dec.weights; a.meta = L->dec.meta;
+  a.sync_ctr = L->dec.sync_ctr;
+  a.out = out; a.err = L->err; a.never_set = L->never_set;
+  a.force_timeout = (c.flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L->num_sms);
+  cfg.blockDim = dim3(kGemvThreads);
+  cfg.dynamicSmemBytes = stream_smem_bytes(L, T);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs co-resident: they wait on one another
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  prof_mark(L, s);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_decode_stream_kernel<TMAX>, a);
+  prof_mark(L, s);
+  return e;
+}
+
 template <class Fmt>
 static cudaError_t set_attrs_fmt() {
   cudaError_t e = cudaSuccess;
@@ -760,7 +1229,15 @@ static cudaError_t set_attrs_fmt() {
 }
 
 cudaError_t decode_prepare(moe_layer* L) {
-  cudaError_t e = set_attrs_fmt<FmtBF16>();
+  cudaError_t e = cudaSuccess;
+  auto set = [&](const void* f) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmemMax);
+  };
+  set((const void*)moe_decode_stream_kernel<1>);
+  set((const void*)moe_decode_stream_kernel<2>);
+  set((const void*)moe_decode_stream_kernel<4>);
+  set((const void*)moe_decode_stream_kernel<8>);
+  if (e == cudaSuccess) e = set_attrs_fmt<FmtBF16>();
   if (e == cudaSuccess) e = set_attrs_fmt<FmtMXFP4>();
   return e;
 }
@@ -776,6 +1253,12 @@ static cudaError_t launch_decode_fmt(moe_layer* L, const uint16_t* x, uint16_t* 
 
 cudaError_t launch_decode(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
                           cudaStream_t s) {
+  if (stream_path_ok(L)) {
+    if (T <= 1) return launch_stream_t<1>(L, x, out, T, logit_bias, s);
+    if (T <= 2) return launch_stream_t<2>(L, x, out, T, logit_bias, s);
+    if (T <= 4) return launch_stream_t<4>(L, x, out, T, logit_bias, s);
+    return launch_stream_t<8>(L, x, out, T, logit_bias, s);
+  }
   if (L->cfg.weight_format == MOE_WEIGHTS_MXFP4) return launch_decode_fmt<FmtMXFP4>(L, x, out, T, logit_bias, s);
   return launch_decode_fmt<FmtBF16>(L, x, out, T, logit_bias, s);
 }
