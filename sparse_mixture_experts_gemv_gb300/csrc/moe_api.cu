@@ -71,25 +71,6 @@ __global__ void transpose_f32_kernel(const float* __restrict__ in, float* __rest
   }
 }
 
-// bf16 transpose of one [rows][cols] matrix into rows of `out_stride` elements:
-// out[c * out_stride + r] = in[r * cols + c] (batched over blockIdx.z).
-__global__ void transpose_bf16_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, int rows, int cols,
-                                      int64_t in_batch, int64_t out_batch, int64_t out_stride) {
-  __shared__ uint16_t tile[32][34];
-  in += blockIdx.z * in_batch;
-  out += blockIdx.z * out_batch;
-  const int c = blockIdx.x * 32 + threadIdx.x;
-  for (int r0 = 0; r0 < 32; r0 += 8) {
-    const int r = blockIdx.y * 32 + threadIdx.y + r0;
-    if (r < rows && c < cols) tile[threadIdx.y + r0][threadIdx.x] = in[(size_t)r * cols + c];
-  }
-  __syncthreads();
-  const int orow = blockIdx.x * 32 + threadIdx.y;
-  const int ocol = blockIdx.y * 32 + threadIdx.x;
-  for (int r0 = 0; r0 < 32; r0 += 8)
-    if (orow + r0 < cols && ocol < rows) out[(size_t)(orow + r0) * out_stride + ocol] = tile[threadIdx.x][threadIdx.y + r0];
-}
-
 // W = hi + mid + lo exactly, each term bf16 (8 significant bits each cover the
 // 24-bit fp32 significand; every step is an exact fp32 subtraction).
 __global__ void split3_bf16_kernel(const float* __restrict__ w, uint16_t* __restrict__ out, size_t n) {
@@ -142,7 +123,6 @@ moe_status_t alloc_workspace(LayerOwner* o) {
   GET(L.dec.h, sizeof(float) * (size_t)T8 * c.top_k * c.intermediate);
   GET(L.dec.h_shared, sizeof(float) * (size_t)T8 * std::max(c.shared_intermediate, 1));
   GET(L.dec.sync_ctr, sizeof(unsigned long long) * 2);
-  GET(L.dec.partial, sizeof(float) * (size_t)L.num_sms * T8 * c.hidden);
   GET(L.err, sizeof(int) * 4);
   GET(L.never_set, sizeof(int));
   GET(L.x_stage, sizeof(uint16_t) * (size_t)c.max_tokens * c.hidden);
@@ -191,17 +171,6 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
     MOE_CUDA(cudaMemcpy2D(L.w_gu, 2 * row, w->gate_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
     MOE_CUDA(cudaMemcpy2D(L.w_gu + row, 2 * row, w->up_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
     MOE_CUDA(cudaMemcpy(L.w_down, w->down_dev, (size_t)E * H * I * 2, cudaMemcpyDeviceToDevice));
-    // Streaming records of the decode path: for each (expert, feature i) the gate row,
-    // the up row and column i of the down projection, contiguous (3 x H bf16).
-    GET(L.w_rec, (size_t)E * I * 3 * H * 2);
-    MOE_CUDA(cudaMemcpy2D(L.w_rec, 3 * row, w->gate_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
-    MOE_CUDA(cudaMemcpy2D(L.w_rec + H, 3 * row, w->up_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
-    {
-      dim3 block(32, 8), grid((unsigned)((I + 31) / 32), (unsigned)((H + 31) / 32), (unsigned)E);
-      transpose_bf16_kernel<<<grid, block>>>((const uint16_t*)w->down_dev, L.w_rec + 2 * H, (int)H, (int)I,
-                                             H * I, I * 3 * H, 3 * H);
-      MOE_CUDA(cudaGetLastError());
-    }
   } else {
     // One record per row: codes (K/2 bytes) then scales (K/32 bytes, padded to 16).
     L.row_bytes.gu = H / 2 + pad16(H / 32);
@@ -228,16 +197,6 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
     MOE_CUDA(cudaMemcpy2D(L.ws_gu, 2 * row, w->shared_gate_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
     MOE_CUDA(cudaMemcpy2D((uint8_t*)L.ws_gu + row, 2 * row, w->shared_up_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
     MOE_CUDA(cudaMemcpy(L.ws_down, w->shared_down_dev, (size_t)H * Is * 2, cudaMemcpyDeviceToDevice));
-  }
-  GET(L.ws_rec, sizeof(uint16_t) * std::max<int64_t>(Is, 1) * 3 * H);
-  if (Is > 0) {
-    const size_t row = (size_t)H * 2;
-    MOE_CUDA(cudaMemcpy2D(L.ws_rec, 3 * row, w->shared_gate_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
-    MOE_CUDA(cudaMemcpy2D(L.ws_rec + H, 3 * row, w->shared_up_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
-    dim3 block(32, 8), grid((unsigned)((Is + 31) / 32), (unsigned)((H + 31) / 32), 1u);
-    transpose_bf16_kernel<<<grid, block>>>((const uint16_t*)w->shared_down_dev, L.ws_rec + 2 * H, (int)H, (int)Is,
-                                           0, 0, 3 * H);
-    MOE_CUDA(cudaGetLastError());
   }
 #undef GET
   return MOE_OK;

@@ -35,6 +35,7 @@
 #include "moe_common.cuh"
 #include "moe_internal.h"
 #include "moe_sm100.cuh"
+#include <cuda_fp16.h>
 
 namespace moe {
 
@@ -43,16 +44,6 @@ struct FmtMXFP4 {};
 
 constexpr int kGemvThreads = 512;
 constexpr int kLookahead = 2;  // extra rounds of gate/up units each warp keeps on their way to L2
-
-// e2m1 code values (OCP MX FP4 element): sign, 2 exponent bits (bias 1), 1 mantissa bit.
-__device__ __forceinline__ void fill_e2m1_lut(float* lut) {
-  if (threadIdx.x < 16) {
-    const int c = threadIdx.x;
-    const int e = (c >> 1) & 3, m = c & 1;
-    float mag = (e == 0) ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, e - 1);
-    lut[c] = (c & 8) ? -mag : mag;
-  }
-}
 
 __device__ __forceinline__ float e8m0_scale(uint32_t s) { return ldexpf(1.0f, (int)s - 127); }
 
@@ -82,9 +73,38 @@ __device__ __forceinline__ float dot8_bf16_f32(const uint4 w, const float4 a, co
   return s;
 }
 
-// Sum of 32 e2m1 codes (16 bytes, even element in the low nibble) times 32 bf16
-// activations starting at xs (shared memory, 16-byte aligned); unscaled.
-__device__ __forceinline__ float dot32_e2m1_bf16(const uint4 c, const uint16_t* xs, const float* lut) {
+// acc + sum of 8 bf16 weights times 8 bf16 activations, with the mixed-precision
+// FMA (bf16 inputs, fp32 accumulate; the bf16 product is exact in fp32).
+__device__ __forceinline__ float fma8_bf16(const uint4 w, const uint4 x, float acc) {
+  asm("{\n .reg .b16 w0, w1, w2, w3, w4, w5, w6, w7, x0, x1, x2, x3, x4, x5, x6, x7;\n"
+      " mov.b32 {w0, w1}, %1;\n mov.b32 {w2, w3}, %2;\n mov.b32 {w4, w5}, %3;\n mov.b32 {w6, w7}, %4;\n"
+      " mov.b32 {x0, x1}, %5;\n mov.b32 {x2, x3}, %6;\n mov.b32 {x4, x5}, %7;\n mov.b32 {x6, x7}, %8;\n"
+      " fma.rn.f32.bf16 %0, w0, x0, %0;\n fma.rn.f32.bf16 %0, w1, x1, %0;\n"
+      " fma.rn.f32.bf16 %0, w2, x2, %0;\n fma.rn.f32.bf16 %0, w3, x3, %0;\n"
+      " fma.rn.f32.bf16 %0, w4, x4, %0;\n fma.rn.f32.bf16 %0, w5, x5, %0;\n"
+      " fma.rn.f32.bf16 %0, w6, x6, %0;\n fma.rn.f32.bf16 %0, w7, x7, %0;\n}"
+      : "+f"(acc)
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w));
+  return acc;
+}
+
+// Two e2m1 codes of one byte -> f16x2 (element 2i, the low nibble, in the low half).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// acc + sum over two f16 pairs: (w.lo * x.lo + w.hi * x.hi), fp32 accumulate.
+__device__ __forceinline__ float fma2_f16(uint32_t w, uint32_t x, float acc) {
+  asm("{\n .reg .b16 w0, w1, x0, x1;\n mov.b32 {w0, w1}, %1;\n mov.b32 {x0, x1}, %2;\n"
+      " fma.rn.f32.f16 %0, w0, x0, %0;\n fma.rn.f32.f16 %0, w1, x1, %0;\n}"
+      : "+f"(acc) : "r"(w), "r"(x));
+  return acc;
+}
+
+// Unscaled sum of 32 e2m1 codes (16 bytes) times 32 f16 activations at xs (shared, 16-byte aligned).
+__device__ __forceinline__ float dot32_e2m1_f16(const uint4 c, const uint16_t* xs) {
   const uint4* xv = reinterpret_cast<const uint4*>(xs);
   const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
   float s = 0.f;
@@ -93,29 +113,7 @@ __device__ __forceinline__ float dot32_e2m1_bf16(const uint4 c, const uint16_t* 
     const uint4 x = xv[q];
     const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {     // one byte = elements 2b (low nibble), 2b+1 (high nibble)
-      const uint32_t byte = (cw[q] >> (8 * b)) & 0xFFu;
-      s = fmaf(lut[byte & 15u], bf16_lo(xw[b]), s);
-      s = fmaf(lut[byte >> 4], bf16_hi(xw[b]), s);
-    }
-  }
-  return s;
-}
-
-__device__ __forceinline__ float dot32_e2m1_f32(const uint4 c, const float* hs, const float* lut) {
-  const float4* hv = reinterpret_cast<const float4*>(hs);
-  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-  float s = 0.f;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 a = hv[2 * q], b = hv[2 * q + 1];
-    const float h8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int bb = 0; bb < 4; ++bb) {
-      const uint32_t byte = (cw[q] >> (8 * bb)) & 0xFFu;
-      s = fmaf(lut[byte & 15u], h8[2 * bb], s);
-      s = fmaf(lut[byte >> 4], h8[2 * bb + 1], s);
-    }
+    for (int b = 0; b < 4; ++b) s = fma2_f16(e2m1x2_to_f16x2(cw[q] >> (8 * b)), xw[b], s);
   }
   return s;
 }
@@ -155,8 +153,8 @@ __device__ __forceinline__ void gu_fma_bf16(const uint4 (&v)[16], int b0, int nc
       for (int t = 0; t < TMAX; ++t) {
         if (t < T) {
           const uint4 xx = *reinterpret_cast<const uint4*>(xs + t * H + 8 * c);
-          ag[t] += dot8_bf16(v[q], xx);
-          au[t] += dot8_bf16(v[8 + q], xx);
+          ag[t] = fma8_bf16(v[q], xx, ag[t]);
+          au[t] = fma8_bf16(v[8 + q], xx, au[t]);
         }
       }
     }
@@ -182,7 +180,7 @@ __device__ __forceinline__ void gu_load_mx(const uint8_t* grec, const uint8_t* u
 template <int TMAX>
 __device__ __forceinline__ void gu_fma_mx(const uint4 (&v)[16], const uint32_t (&sc)[16], int b0, int nch,
                                           const uint16_t* xs, int T, int H, float (&ag)[TMAX], float (&au)[TMAX],
-                                          const float* lut, int lane) {
+                                          int lane) {
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int c = b0 + lane + 32 * q;
@@ -191,9 +189,9 @@ __device__ __forceinline__ void gu_fma_mx(const uint4 (&v)[16], const uint32_t (
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) {
         if (t < T) {
-          const uint16_t* xp = xs + t * H + 32 * c;
-          ag[t] = fmaf(dot32_e2m1_bf16(v[q], xp, lut), sg, ag[t]);
-          au[t] = fmaf(dot32_e2m1_bf16(v[8 + q], xp, lut), su, au[t]);
+          const uint16_t* xp = xs + t * H + 32 * c;   // f16 activations
+          ag[t] = fmaf(dot32_e2m1_f16(v[q], xp), sg, ag[t]);
+          au[t] = fmaf(dot32_e2m1_f16(v[8 + q], xp), su, au[t]);
         }
       }
     }
@@ -265,7 +263,6 @@ moe_decode_fused_kernel(const FusedArgs a) {
   float* hs = reinterpret_cast<float*>(smem);         // phase 3: h [T*k][I] fp32, then h_shared [T][Is]
   uint8_t* s_shrows = smem + a.smem_r1;               // shared-expert down rows [n0, n1) x Is bf16
   uint8_t* s_rows = s_shrows + a.smem_sh;             // routed down rows, slot d at d * slot_stride
-  __shared__ float lut[16];
   __shared__ DecodeMeta s_meta;
   __shared__ float s_w[kMaxDecodeT * kMaxTopK];
   __shared__ int s_idx[kMaxDecodeT * kMaxTopK];
@@ -283,7 +280,8 @@ moe_decode_fused_kernel(const FusedArgs a) {
   const int nrows = n1 - n0;
   const int nr = (E - b + G - 1) / G;               // router rows b, b + G, ... of this CTA
   const int sh0 = (int)((int64_t)b * Is / G), sh1 = (int)((int64_t)(b + 1) * Is / G);
-  if constexpr (std::is_same<Fmt, FmtMXFP4>::value) fill_e2m1_lut(lut);
+  constexpr bool kMx = std::is_same<Fmt, FmtMXFP4>::value;
+  uint16_t* xs16 = xs + (size_t)T * H;                // MXFP4 layers: x as f16 for the e2m1 products
 
   if (threadIdx.x == 0) {
     sm100::mbar_init(&bar_sh, 1);
@@ -322,7 +320,20 @@ moe_decode_fused_kernel(const FusedArgs a) {
   {
     const uint4* src = reinterpret_cast<const uint4*>(a.x);
     uint4* dst = reinterpret_cast<uint4*>(xs);
-    for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) dst[i] = src[i];
+    for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) {
+      const uint4 v8 = src[i];
+      dst[i] = v8;
+      if (kMx) {  // exact for |x| >= 2^-14 (bf16 has fewer significand bits than f16)
+        const uint32_t w4[4] = {v8.x, v8.y, v8.z, v8.w};
+        uint32_t h4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const __half2 hh = __floats2half2_rn(bf16_lo(w4[q]), bf16_hi(w4[q]));
+          h4[q] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+        reinterpret_cast<uint4*>(xs16)[i] = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+      }
+    }
   }
   __syncthreads();
   for (int slot = warp; slot < nr + (sh1 - sh0); slot += nw) {
@@ -451,7 +462,15 @@ moe_decode_fused_kernel(const FusedArgs a) {
     }
   }
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 0 && T == 1) {  // one token: its k experts are the slots, in order
+    for (int q = lane; q < k * kMaxDecodeT; q += 32) s_meta.slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = -1;
+    __syncwarp();
+    if (lane < k) {
+      s_meta.slot_expert[lane] = s_idx[lane];
+      s_meta.slot_j[lane][0] = (signed char)lane;
+    }
+    if (lane == 0) s_meta.num_slots = k;
+  } else if (warp == 0) {
     const int n = T * k;
     bool first[2] = {false, false};
     int firstpos[2] = {0, 0};
@@ -540,7 +559,7 @@ moe_decode_fused_kernel(const FusedArgs a) {
       uint32_t sc[16];
       for (int b0 = 0; b0 < nch; b0 += 32 * 8) {
         gu_load_mx(grec, urec, H, b0, nch, v, sc, lane);
-        gu_fma_mx<TMAX>(v, sc, b0, nch, xs, T, H, ag, au, lut, lane);
+        gu_fma_mx<TMAX>(v, sc, b0, nch, xs16, T, H, ag, au, lane);
       }
     }
 #pragma unroll
@@ -571,10 +590,10 @@ moe_decode_fused_kernel(const FusedArgs a) {
   if (s_abort) return;
 
   // ------------------------------------------------ phase 3: down + combine
-  // Warp w takes expert slots w, w + 16, ... (slot D is the shared expert, weight
-  // 1) and, for each of this CTA's output rows, dots the slot's down row with the
-  // slot's SwiGLU outputs, which it reads once per 8 rows. Per-warp partial sums
-  // meet in shared memory and are added in warp order (deterministic).
+  // Work items (expert slot, block of RB output rows) are spread over all warps
+  // (slot D is the shared expert, weight 1); an item dots each of its rows with
+  // the slot's SwiGLU outputs, read once per item. Per-warp partial sums meet in
+  // shared memory and are added in warp order (deterministic).
   float* hss = hs + (size_t)T * k * I;
   float* s_part = reinterpret_cast<float*>(s_rows + (size_t)a.slots_cap * a.slot_stride);  // [nw][rows_max][T]
   {
@@ -587,11 +606,13 @@ moe_decode_fused_kernel(const FusedArgs a) {
     for (int q = threadIdx.x; q < nw * a.rows_max * T; q += blockDim.x) s_part[q] = 0.f;
   }
   __syncthreads();
-  constexpr int RB = TMAX <= 2 ? 8 : (TMAX <= 4 ? 4 : 2);   // rows per pass
-  for (int sd = warp; sd <= D; sd += nw) {
+  constexpr int RB = TMAX <= 2 ? 8 : (TMAX <= 4 ? 4 : 2);   // rows per item
+  const int npass = (nrows + RB - 1) / RB;
+  const int nslots = D + (Is > 0 ? 1 : 0);
+  for (int item = warp; item < nslots * npass; item += nw) {
+    const int sd = item / npass, r0 = (item - sd * npass) * RB;
     const bool shared = (sd == D);
-    if (shared && Is == 0) break;
-    const bool mx = !shared && !std::is_same<Fmt, FmtBF16>::value;
+    const bool mx = !shared && kMx;
     const int K = shared ? Is : I;
     const int nsub = K / 8;                    // 8-element sub-chunks of a row
     const bool in_smem = shared || sd < d_smem;
@@ -614,70 +635,73 @@ moe_decode_fused_kernel(const FusedArgs a) {
         }
       }
     }
-    for (int r0 = 0; r0 < nrows; r0 += RB) {
-      float acc[RB][TMAX];
+    float acc[RB][TMAX];
 #pragma unroll
-      for (int rr = 0; rr < RB; ++rr)
+    for (int rr = 0; rr < RB; ++rr)
 #pragma unroll
-        for (int t = 0; t < TMAX; ++t) acc[rr][t] = 0.f;
-      for (int c = lane; c < nsub; c += 32) {
-        float4 h0[TMAX], h1[TMAX];
+      for (int t = 0; t < TMAX; ++t) acc[rr][t] = 0.f;
+    for (int c = lane; c < nsub; c += 32) {
+      float4 h0[TMAX], h1[TMAX];
 #pragma unroll
-        for (int t = 0; t < TMAX; ++t) {
-          if (hrow[t]) {
-            h0[t] = *reinterpret_cast<const float4*>(hrow[t] + 8 * c);
-            h1[t] = *reinterpret_cast<const float4*>(hrow[t] + 8 * c + 4);
-          }
+      for (int t = 0; t < TMAX; ++t) {
+        if (hrow[t]) {
+          h0[t] = *reinterpret_cast<const float4*>(hrow[t] + 8 * c);
+          h1[t] = *reinterpret_cast<const float4*>(hrow[t] + 8 * c + 4);
         }
-        uint4 wv[RB];
-        uint32_t sb[RB];
+      }
+      uint4 wv[RB];
+      uint32_t sb[RB];
 #pragma unroll
-        for (int rr = 0; rr < RB; ++rr) {  // issue the row loads of this pass together
-          if (r0 + rr < nrows) {
-            const uint8_t* rec = rows_base + (r0 + rr) * rstride;
-            if (!mx) {
-              wv[rr] = in_smem ? *reinterpret_cast<const uint4*>(rec + 16 * c) : ldg_stream(rec + 16 * c);
-            } else {
-              wv[rr].x = in_smem ? *reinterpret_cast<const uint32_t*>(rec + 4 * c)
-                                 : __ldg(reinterpret_cast<const uint32_t*>(rec + 4 * c));
-              sb[rr] = in_smem ? rec[I / 2 + c / 4] : __ldg(rec + I / 2 + c / 4);
-            }
-          }
-        }
-#pragma unroll
-        for (int rr = 0; rr < RB; ++rr) {
-          if (r0 + rr < nrows) {
-            float w8[8];
-            if (!mx) {
-              w8[0] = bf16_lo(wv[rr].x); w8[1] = bf16_hi(wv[rr].x); w8[2] = bf16_lo(wv[rr].y); w8[3] = bf16_hi(wv[rr].y);
-              w8[4] = bf16_lo(wv[rr].z); w8[5] = bf16_hi(wv[rr].z); w8[6] = bf16_lo(wv[rr].w); w8[7] = bf16_hi(wv[rr].w);
-            } else {
-              const float sc = e8m0_scale(sb[rr]);
-#pragma unroll
-              for (int q = 0; q < 8; ++q) w8[q] = lut[(wv[rr].x >> (4 * q)) & 15u] * sc;
-            }
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              if (hrow[t]) {
-                float s = acc[rr][t];
-                s = fmaf(w8[0], h0[t].x, s); s = fmaf(w8[1], h0[t].y, s);
-                s = fmaf(w8[2], h0[t].z, s); s = fmaf(w8[3], h0[t].w, s);
-                s = fmaf(w8[4], h1[t].x, s); s = fmaf(w8[5], h1[t].y, s);
-                s = fmaf(w8[6], h1[t].z, s); s = fmaf(w8[7], h1[t].w, s);
-                acc[rr][t] = s;
-              }
-            }
+      for (int rr = 0; rr < RB; ++rr) {  // issue the row loads of this item together
+        if (r0 + rr < nrows) {
+          const uint8_t* rec = rows_base + (r0 + rr) * rstride;
+          if (!mx) {
+            wv[rr] = in_smem ? *reinterpret_cast<const uint4*>(rec + 16 * c) : ldg_stream(rec + 16 * c);
+          } else {
+            wv[rr].x = in_smem ? *reinterpret_cast<const uint32_t*>(rec + 4 * c)
+                               : __ldg(reinterpret_cast<const uint32_t*>(rec + 4 * c));
+            sb[rr] = in_smem ? rec[I / 2 + c / 4] : __ldg(rec + I / 2 + c / 4);
           }
         }
       }
 #pragma unroll
       for (int rr = 0; rr < RB; ++rr) {
+        if (r0 + rr < nrows) {
+          float w8[8];
+          float scale = 1.f;
+          if (!mx) {
+            w8[0] = bf16_lo(wv[rr].x); w8[1] = bf16_hi(wv[rr].x); w8[2] = bf16_lo(wv[rr].y); w8[3] = bf16_hi(wv[rr].y);
+            w8[4] = bf16_lo(wv[rr].z); w8[5] = bf16_hi(wv[rr].z); w8[6] = bf16_lo(wv[rr].w); w8[7] = bf16_hi(wv[rr].w);
+          } else {
+            scale = e8m0_scale(sb[rr]);          // one scale per 32 elements: constant over these 8
 #pragma unroll
-        for (int t = 0; t < TMAX; ++t) {
-          if (hrow[t] && r0 + rr < nrows) {   // warp-uniform conditions
-            const float sum = warp_sum(acc[rr][t]);
-            if (lane == 0) s_part[((size_t)warp * a.rows_max + r0 + rr) * T + t] += wt[t] * sum;
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t hp = e2m1x2_to_f16x2(wv[rr].x >> (8 * q));
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hp));
+              w8[2 * q] = f.x;
+              w8[2 * q + 1] = f.y;
+            }
           }
+#pragma unroll
+          for (int t = 0; t < TMAX; ++t) {
+            if (hrow[t]) {
+              float s = w8[0] * h0[t].x;
+              s = fmaf(w8[1], h0[t].y, s); s = fmaf(w8[2], h0[t].z, s); s = fmaf(w8[3], h0[t].w, s);
+              s = fmaf(w8[4], h1[t].x, s); s = fmaf(w8[5], h1[t].y, s);
+              s = fmaf(w8[6], h1[t].z, s); s = fmaf(w8[7], h1[t].w, s);
+              acc[rr][t] = fmaf(scale, s, acc[rr][t]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr) {
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (hrow[t] && r0 + rr < nrows) {   // warp-uniform conditions
+          const float sum = warp_sum(acc[rr][t]);
+          if (lane == 0) s_part[((size_t)warp * a.rows_max + r0 + rr) * T + t] += wt[t] * sum;
         }
       }
     }
@@ -687,430 +711,6 @@ moe_decode_fused_kernel(const FusedArgs a) {
     const int r = q / T, t = q - r * T;
     float sum = 0.f;
     for (int w = 0; w < nw; ++w) sum += s_part[((size_t)w * a.rows_max + r) * T + t];
-    a.out[(size_t)t * H + n0 + r] = f32_to_bf16_rne(sum);
-  }
-}
-
-// ===========================================================================
-// bf16 streaming decode kernel: gate/up and down fused per intermediate feature.
-// ===========================================================================
-// Unit = one (expert slot, intermediate feature i) record [gate row | up row |
-// down column], 3 x H bf16, contiguous. A CTA owns a balanced range of the
-// window's routed units (plus a static share of the shared expert's units),
-// streams them through a ring of shared-memory stages filled by cp.async.bulk,
-// and for each unit computes g = gate.x, u = up.x, h = silu(g) u and adds
-// w * h * down_column to its own output partial. After one grid barrier every
-// CTA adds up its slice of output columns over all CTAs' partials in CTA order.
-constexpr int kStreamUnits = 2;    // units per ring stage
-constexpr int kStreamStages = 6;   // ring depth
-constexpr int kStreamMaxH = 4096;  // two 4-column granules per lane per warp
-
-struct StreamArgs {
-  const uint16_t* x;           // bf16 [T][H]
-  int T, H, E, k, I, Is;
-  const float* router_t;       // fp32 [E][H]
-  const float* router_bias;    // fp32 [E]
-  const float* logit_bias;     // fp32 [T][E] or nullptr
-  const uint16_t* rec;         // routed records [E][I][3][H]
-  const uint16_t* srec;        // shared records [Is][3][H]
-  float* logits;               // [T][E]
-  float* partial;              // [G][T][H]
-  int* idx;                    // [T][k]     (written by CTA 0, diagnostics)
-  float* weights;              // [T][k]     (written by CTA 0, diagnostics)
-  DecodeMeta* meta;            //            (written by CTA 0, diagnostics)
-  unsigned long long* sync_ctr;
-  uint16_t* out;               // bf16 [T][H]
-  int* err;
-  const int* never_set;
-  int force_timeout;
-};
-
-template <int TMAX>
-__global__ void __launch_bounds__(kGemvThreads, 1)
-moe_decode_stream_kernel(const StreamArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int T = a.T, H = a.H, E = a.E, I = a.I, Is = a.Is, k = a.k;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int nw = kGemvThreads / 32;
-  const int G = gridDim.x, b = blockIdx.x;
-  const size_t unit_bytes = (size_t)3 * H * 2;
-  const size_t stage_bytes = kStreamUnits * unit_bytes;
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                               // [T][H]
-  uint8_t* ring = smem + ((size_t)T * H * 2 + 127) / 128 * 128;                   // kStreamStages stages
-  float2* s_part = reinterpret_cast<float2*>(ring + kStreamStages * stage_bytes); // [units][8 warps][T] (g, u)
-  __shared__ __align__(8) uint64_t full[kStreamStages];
-  __shared__ DecodeMeta s_meta;
-  __shared__ float s_w[kMaxDecodeT * kMaxTopK];
-  __shared__ int s_idx[kMaxDecodeT * kMaxTopK];
-  __shared__ int s_slot_of[kMaxDecodeT * kMaxTopK];
-  __shared__ int s_router_done, s_abort;
-  __shared__ unsigned long long s_gen;
-
-  // This CTA's units: shared-expert units [sh0, sh1) first, then routed units [u0, u1).
-  const int sh0 = (int)((int64_t)b * Is / G), sh1 = (int)((int64_t)(b + 1) * Is / G);
-  const int nsh = sh1 - sh0;
-  const int st_sh = (nsh + kStreamUnits - 1) / kStreamUnits;  // stages holding shared units
-  const int nr = (E - b + G - 1) / G;                          // router rows b, b + G, ...
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStreamStages; ++s) sm100::mbar_init(&full[s], 1);
-    sm100::fence_barrier_init();
-    s_router_done = 0;
-    s_abort = 0;
-    if (nr == 0) s_gen = grid_arrive(&a.sync_ctr[0]);
-    if (a.force_timeout && b == 0 && !bounded_wait_flag(a.never_set, 2000000LL)) set_error(a.err, kDevTimeout);
-    // shared-expert units do not depend on routing: start their copies now
-    for (int s = 0; s < st_sh && s < kStreamStages; ++s) {
-      const int q0 = s * kStreamUnits, q1 = min(nsh, q0 + kStreamUnits);
-      const uint32_t bytes = (uint32_t)((q1 - q0) * unit_bytes);
-      sm100::mbar_arrive_expect_tx(&full[s], bytes);
-      sm100::bulk_copy_g2s(ring + (size_t)s * stage_bytes, a.srec + (size_t)(sh0 + q0) * 3 * H, bytes, &full[s]);
-    }
-  }
-
-  // ------------------------------------------------ phase 1: router logits
-  uint4 v[16];
-  if (warp < nr) {
-    const float* row = a.router_t + (size_t)(b + warp * G) * H;
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int c = lane + 32 * q;
-      if (c < H / 4) v[q] = ldg_stream(row + 4 * c);
-    }
-  }
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(a.x);
-    uint4* dst = reinterpret_cast<uint4*>(xs);
-    for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) dst[i] = src[i];
-  }
-  __syncthreads();
-  for (int slot = warp; slot < nr; slot += nw) {
-    const int u = b + slot * G;
-    const float* row = a.router_t + (size_t)u * H;
-    const int nch = H / 4;
-    float acc[TMAX];
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-    for (int b0 = 0; b0 < nch; b0 += 32 * 16) {
-      if (!(slot == warp && b0 == 0)) {
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int c = b0 + lane + 32 * q;
-          if (c < nch) v[q] = ldg_stream(row + 4 * c);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int c = b0 + lane + 32 * q;
-        if (c < nch) {
-#pragma unroll
-          for (int t = 0; t < TMAX; ++t) {
-            if (t < T) {
-              const uint2 xx = *reinterpret_cast<const uint2*>(xs + t * H + 4 * c);
-              float s = acc[t];
-              s = fmaf(__uint_as_float(v[q].x), bf16_lo(xx.x), s);
-              s = fmaf(__uint_as_float(v[q].y), bf16_hi(xx.x), s);
-              s = fmaf(__uint_as_float(v[q].z), bf16_lo(xx.y), s);
-              s = fmaf(__uint_as_float(v[q].w), bf16_hi(xx.y), s);
-              acc[t] = s;
-            }
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t) {
-      if (t < T) {
-        float s = warp_sum(acc[t]);
-        if (lane == t) {
-          s += a.router_bias[u];
-          if (a.logit_bias) s += a.logit_bias[(size_t)t * E + u];
-          a.logits[(size_t)t * E + u] = s;
-        }
-      }
-    }
-    __threadfence();
-    __syncwarp();
-    if (lane == 0 && atomicAdd(&s_router_done, 1) == nr - 1) s_gen = grid_arrive(&a.sync_ctr[0]);
-  }
-
-  // Output partial of this CTA: warp w owns 4-column granules g = lane + 32 * (w + 16 m).
-  float acc[2][4][TMAX];
-#pragma unroll
-  for (int m = 0; m < 2; ++m)
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t) acc[m][c][t] = 0.f;
-  const int ngran = H / 4;
-
-  // One ring stage: gate/up dots (8 warps per unit), then every warp adds the
-  // units' down columns, scaled by the routing weight times h, to its granules.
-  // `coef_of(q, t)` gives the routing weight of stage unit q for token t (0: unused).
-  auto run_stage = [&](int s, int nunits, const float (&wq)[kStreamUnits][TMAX]) -> bool {
-    {  // every thread observes the stage's copy completion before reading it
-      volatile int never = 0;
-      if (!sm100::mbar_wait(&full[s % kStreamStages], (s / kStreamStages) & 1, a.err, &never, 4000000000LL, false))
-        s_abort = 1;
-    }
-    __syncthreads();
-    if (s_abort) return false;
-    const uint8_t* stage = ring + (size_t)(s % kStreamStages) * stage_bytes;
-    {
-      const int q = warp >> 3, w8 = warp & 7;
-      if (q < nunits) {
-        const uint8_t* g = stage + q * unit_bytes;
-        const uint8_t* u = g + (size_t)H * 2;
-        float ag[TMAX], au[TMAX];
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t) ag[t] = au[t] = 0.f;
-        for (int c = lane + 32 * w8; c < H / 8; c += 256) {
-          const uint4 gv = *reinterpret_cast<const uint4*>(g + 16 * c);
-          const uint4 uv = *reinterpret_cast<const uint4*>(u + 16 * c);
-#pragma unroll
-          for (int t = 0; t < TMAX; ++t) {
-            if (t < T) {
-              const uint4 xx = *reinterpret_cast<const uint4*>(xs + t * H + 8 * c);
-              ag[t] += dot8_bf16(gv, xx);
-              au[t] += dot8_bf16(uv, xx);
-            }
-          }
-        }
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t) {
-          if (t < T) {
-            const float gs = warp_sum(ag[t]), us = warp_sum(au[t]);
-            if (lane == 0) s_part[(q * 8 + w8) * TMAX + t] = make_float2(gs, us);
-          }
-        }
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int q = 0; q < kStreamUnits; ++q) {
-      if (q < nunits) {
-        float coef[TMAX];
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t) {
-          coef[t] = 0.f;
-          if (t < T && wq[q][t] != 0.f) {
-            float gs = 0.f, us = 0.f;
-#pragma unroll
-            for (int w8 = 0; w8 < 8; ++w8) {
-              const float2 p = s_part[(q * 8 + w8) * TMAX + t];
-              gs += p.x;
-              us += p.y;
-            }
-            coef[t] = wq[q][t] * swiglu(gs, us);
-          }
-        }
-        const uint8_t* dcol = stage + q * unit_bytes + (size_t)4 * H;
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const int gi = lane + 32 * (warp + 16 * m);
-          if (gi < ngran) {
-            const uint2 dv = *reinterpret_cast<const uint2*>(dcol + 8 * gi);
-            const float d0 = bf16_lo(dv.x), d1 = bf16_hi(dv.x), d2 = bf16_lo(dv.y), d3 = bf16_hi(dv.y);
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              acc[m][0][t] = fmaf(coef[t], d0, acc[m][0][t]);
-              acc[m][1][t] = fmaf(coef[t], d1, acc[m][1][t]);
-              acc[m][2][t] = fmaf(coef[t], d2, acc[m][2][t]);
-              acc[m][3][t] = fmaf(coef[t], d3, acc[m][3][t]);
-            }
-          }
-        }
-      }
-    }
-    __syncthreads();  // the stage buffer is free again
-    return true;
-  };
-
-  // ------------------------------------------------ shared-expert units (overlap the routing barrier)
-  float wq[kStreamUnits][TMAX];
-#pragma unroll
-  for (int q = 0; q < kStreamUnits; ++q)
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t) wq[q][t] = (t < T) ? 1.f : 0.f;
-  __syncthreads();
-  for (int s = 0; s < st_sh; ++s) {
-    if (!run_stage(s, min(kStreamUnits, nsh - s * kStreamUnits), wq)) return;
-    if (threadIdx.x == 0 && s + kStreamStages < st_sh) {
-      const int s2 = s + kStreamStages;
-      const int q0 = s2 * kStreamUnits, q1 = min(nsh, q0 + kStreamUnits);
-      const uint32_t bytes = (uint32_t)((q1 - q0) * unit_bytes);
-      sm100::mbar_arrive_expect_tx(&full[s2 % kStreamStages], bytes);
-      sm100::bulk_copy_g2s(ring + (size_t)(s2 % kStreamStages) * stage_bytes, a.srec + (size_t)(sh0 + q0) * 3 * H,
-                           bytes, &full[s2 % kStreamStages]);
-    }
-  }
-
-  // ------------------------------------------------ sync A: all router logits written
-  if (threadIdx.x == 0 && !grid_wait(&a.sync_ctr[0], s_gen, a.err)) s_abort = 1;
-  __syncthreads();
-  if (s_abort) return;
-
-  if (warp < T) {  // every CTA derives the routing itself (identical inputs, identical arithmetic)
-    const int t = warp;
-    constexpr int kPer = kMaxExperts / 32;
-    const int kp = (E + 31) / 32;
-    uint32_t key[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int e = lane + 32 * j;
-      key[j] = (j < kp && e < E) ? f32_order_key(ldg_cg_f32(a.logits + (size_t)t * E + e)) : 0u;
-    }
-    float v0 = 0.f, sum = 0.f, my_v = 0.f;
-    int my_e = 0;
-#pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-      uint32_t lk = 0u;
-      int lj = 0;
-#pragma unroll
-      for (int j = 0; j < kPer; ++j)
-        if (j < kp && key[j] > lk) { lk = key[j]; lj = j; }
-      const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, lk);
-      const uint32_t cand = (lk == gmax) ? (uint32_t)(lane + 32 * lj) : 0xFFFFFFFFu;
-      const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
-      if (lane == (int)(gidx & 31u)) {
-#pragma unroll
-        for (int j = 0; j < kPer; ++j)
-          if (j == (int)(gidx >> 5)) key[j] = 0u;
-      }
-      const float val = f32_from_order_key(gmax);
-      if (r == 0) v0 = val;
-      const float ex = expf(val - v0);
-      sum += ex;
-      if (lane == r) { my_v = ex; my_e = (int)gidx; }
-    }
-    if (lane < k) {
-      const float wgt = my_v / sum;
-      s_idx[t * k + lane] = my_e;
-      s_w[t * k + lane] = wgt;
-      if (b == 0) {
-        a.idx[t * k + lane] = my_e;
-        a.weights[t * k + lane] = wgt;
-      }
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    const int n = T * k;
-    bool first[2] = {false, false};
-    int firstpos[2] = {0, 0};
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int aidx = lane + 32 * h2;
-      if (aidx < n) {
-        const int e = s_idx[aidx];
-        int q = 0;
-        while (s_idx[q] != e) ++q;
-        first[h2] = (q == aidx);
-        firstpos[h2] = q;
-      }
-    }
-    const unsigned m0 = __ballot_sync(0xFFFFFFFFu, first[0]);
-    const unsigned m1 = __ballot_sync(0xFFFFFFFFu, first[1]);
-    const unsigned lt = (1u << lane) - 1u;
-    if (first[0]) s_slot_of[lane] = __popc(m0 & lt);
-    if (first[1]) s_slot_of[lane + 32] = __popc(m0) + __popc(m1 & lt);
-    __syncwarp();
-    const int D = __popc(m0) + __popc(m1);
-    for (int q = lane; q < D * kMaxDecodeT; q += 32) s_meta.slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = -1;
-    __syncwarp();
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int aidx = lane + 32 * h2;
-      if (aidx < n) {
-        const int slot = s_slot_of[firstpos[h2]];
-        if (first[h2]) s_meta.slot_expert[slot] = s_idx[aidx];
-        s_meta.slot_j[slot][aidx / k] = (signed char)(aidx % k);
-      }
-    }
-    if (lane == 0) s_meta.num_slots = D;
-  }
-  __syncthreads();
-  const int D = s_meta.num_slots;
-  if (b == 0) {
-    const int* src = reinterpret_cast<const int*>(&s_meta);
-    int* dst = reinterpret_cast<int*>(a.meta);
-    for (int q = threadIdx.x; q < (int)(sizeof(DecodeMeta) / 4); q += blockDim.x) dst[q] = src[q];
-  }
-
-  // ------------------------------------------------ routed units
-  const int64_t U = (int64_t)D * I;
-  const int64_t u0 = U * b / G, u1 = U * (b + 1) / G;
-  const int nst = (int)((u1 - u0 + kStreamUnits - 1) / kStreamUnits);
-  auto issue = [&](int rs) {  // routed stage rs -> ring stage st_sh + rs
-    const int s = st_sh + rs;
-    int64_t q = u0 + (int64_t)rs * kStreamUnits;
-    const int64_t qe = (u1 < q + kStreamUnits) ? u1 : q + kStreamUnits;
-    uint8_t* dst = ring + (size_t)(s % kStreamStages) * stage_bytes;
-    sm100::mbar_arrive_expect_tx(&full[s % kStreamStages], (uint32_t)((qe - q) * unit_bytes));
-    while (q < qe) {  // contiguous runs of one expert
-      const int d = (int)(q / I), i = (int)(q % I);
-      const int64_t run = (qe - q) < (int64_t)(I - i) ? (qe - q) : (int64_t)(I - i);
-      sm100::bulk_copy_g2s(dst, a.rec + ((size_t)s_meta.slot_expert[d] * I + i) * 3 * H, (uint32_t)(run * unit_bytes),
-                           &full[s % kStreamStages]);
-      dst += run * unit_bytes;
-      q += run;
-    }
-  };
-  if (threadIdx.x == 0)
-    for (int rs = 0; rs < nst && rs < kStreamStages; ++rs) issue(rs);
-  for (int rs = 0; rs < nst; ++rs) {
-    const int64_t q0 = u0 + (int64_t)rs * kStreamUnits;
-    const int nunits = (int)((u1 - q0) < (int64_t)kStreamUnits ? (u1 - q0) : (int64_t)kStreamUnits);
-#pragma unroll
-    for (int q = 0; q < kStreamUnits; ++q) {
-      const int d = (int)((q0 + q) / I);
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        float wv = 0.f;
-        if (q < nunits && t < T) {
-          const int j = s_meta.slot_j[d][t];
-          if (j >= 0) wv = s_w[t * k + j];
-        }
-        wq[q][t] = wv;
-      }
-    }
-    if (!run_stage(st_sh + rs, nunits, wq)) return;
-    if (threadIdx.x == 0 && rs + kStreamStages < nst) issue(rs + kStreamStages);
-  }
-
-  // ------------------------------------------------ partials, sync B, column reduction
-#pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    const int gi = lane + 32 * (warp + 16 * m);
-    if (gi < ngran) {
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t)
-        if (t < T)
-          *reinterpret_cast<float4*>(a.partial + ((size_t)b * T + t) * H + 4 * gi) =
-              make_float4(acc[m][0][t], acc[m][1][t], acc[m][2][t], acc[m][3][t]);
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned long long gen = grid_arrive(&a.sync_ctr[1]);
-    if (!grid_wait(&a.sync_ctr[1], gen, a.err)) s_abort = 1;
-  }
-  __syncthreads();
-  if (s_abort) return;
-  const int n0 = (int)((int64_t)b * H / G), n1 = (int)((int64_t)(b + 1) * H / G), nrows = n1 - n0;
-  float* red = reinterpret_cast<float*>(ring);  // [32 groups][nrows * T]
-  const int cells = nrows * T;
-  for (int q = threadIdx.x; q < 32 * cells; q += blockDim.x) {
-    const int grp = q / cells, cell = q - grp * cells, t = cell / nrows, r = cell - t * nrows;
-    float sum = 0.f;
-    for (int p = grp; p < G; p += 32) sum += ldg_cg_f32(a.partial + ((size_t)p * T + t) * H + n0 + r);
-    red[q] = sum;
-  }
-  __syncthreads();
-  for (int cell = threadIdx.x; cell < cells; cell += blockDim.x) {
-    float sum = 0.f;
-    for (int grp = 0; grp < 32; ++grp) sum += red[grp * cells + cell];
-    const int t = cell / nrows, r = cell - t * nrows;
     a.out[(size_t)t * H + n0 + r] = f32_to_bf16_rne(sum);
   }
 }
@@ -1138,7 +738,8 @@ static cudaError_t launch_fused_t(moe_layer* L, const uint16_t* x, uint16_t* out
   a.ws_gu = L->ws_gu; a.ws_down = L->ws_down;
   a.w_gu = L->w_gu; a.rb_gu = L->row_bytes.gu; a.w_down = L->w_down; a.rb_down = L->row_bytes.down;
   const int rows_max = (c.hidden + L->num_sms - 1) / L->num_sms;
-  const size_t xb = (size_t)T * c.hidden * sizeof(uint16_t), hb = decode_smem_bytes_down(L, T);
+  const size_t xb = (size_t)T * c.hidden * sizeof(uint16_t) * (std::is_same<Fmt, FmtMXFP4>::value ? 2 : 1);
+  const size_t hb = decode_smem_bytes_down(L, T);
   a.smem_r1 = (int)align16(xb > hb ? xb : hb);
   a.smem_sh = (int)align16((size_t)rows_max * c.shared_intermediate * 2);
   a.slot_stride = (int)((size_t)rows_max * L->row_bytes.down);
@@ -1170,51 +771,6 @@ static cudaError_t launch_fused_t(moe_layer* L, const uint16_t* x, uint16_t* out
   return e;
 }
 
-constexpr int kStreamSmemMax = 220 * 1024;
-
-static size_t stream_smem_bytes(const moe_layer* L, int T) {
-  const size_t xb = ((size_t)T * L->cfg.hidden * 2 + 127) / 128 * 128;
-  const size_t ring = (size_t)kStreamStages * kStreamUnits * 3 * L->cfg.hidden * 2;
-  const size_t part = (size_t)kStreamUnits * 8 * kMaxDecodeT * sizeof(float2);
-  return xb + ring + part;
-}
-
-// The streaming kernel serves bf16 layers with H <= 4096 whose ring fits.
-static bool stream_path_ok(const moe_layer* L) {
-  return L->cfg.weight_format == MOE_WEIGHTS_BF16 && L->cfg.hidden <= kStreamMaxH &&
-         stream_smem_bytes(L, kMaxDecodeT) <= (size_t)kStreamSmemMax && L->w_rec != nullptr;
-}
-
-template <int TMAX>
-static cudaError_t launch_stream_t(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
-                                   cudaStream_t s) {
-  const auto& c = L->cfg;
-  StreamArgs a;
-  a.x = x; a.T = T; a.H = c.hidden; a.E = c.num_experts; a.k = c.top_k; a.I = c.intermediate;
-  a.Is = c.shared_intermediate;
-  a.router_t = L->router_t; a.router_bias = L->router_bias; a.logit_bias = logit_bias;
-  a.rec = L->w_rec; a.srec = L->ws_rec;
-  a.logits = L->dec.logits; a.partial = L->dec.partial;
-  a.idx = L->dec.idx; a.weights = L->dec.weights; a.meta = L->dec.meta;
-  a.sync_ctr = L->dec.sync_ctr;
-  a.out = out; a.err = L->err; a.never_set = L->never_set;
-  a.force_timeout = (c.flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? 1 : 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(L->num_sms);
-  cfg.blockDim = dim3(kGemvThreads);
-  cfg.dynamicSmemBytes = stream_smem_bytes(L, T);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs co-resident: they wait on one another
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  prof_mark(L, s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_decode_stream_kernel<TMAX>, a);
-  prof_mark(L, s);
-  return e;
-}
-
 template <class Fmt>
 static cudaError_t set_attrs_fmt() {
   cudaError_t e = cudaSuccess;
@@ -1229,15 +785,7 @@ static cudaError_t set_attrs_fmt() {
 }
 
 cudaError_t decode_prepare(moe_layer* L) {
-  cudaError_t e = cudaSuccess;
-  auto set = [&](const void* f) {
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmemMax);
-  };
-  set((const void*)moe_decode_stream_kernel<1>);
-  set((const void*)moe_decode_stream_kernel<2>);
-  set((const void*)moe_decode_stream_kernel<4>);
-  set((const void*)moe_decode_stream_kernel<8>);
-  if (e == cudaSuccess) e = set_attrs_fmt<FmtBF16>();
+  cudaError_t e = set_attrs_fmt<FmtBF16>();
   if (e == cudaSuccess) e = set_attrs_fmt<FmtMXFP4>();
   return e;
 }
@@ -1253,12 +801,6 @@ static cudaError_t launch_decode_fmt(moe_layer* L, const uint16_t* x, uint16_t* 
 
 cudaError_t launch_decode(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
                           cudaStream_t s) {
-  if (stream_path_ok(L)) {
-    if (T <= 1) return launch_stream_t<1>(L, x, out, T, logit_bias, s);
-    if (T <= 2) return launch_stream_t<2>(L, x, out, T, logit_bias, s);
-    if (T <= 4) return launch_stream_t<4>(L, x, out, T, logit_bias, s);
-    return launch_stream_t<8>(L, x, out, T, logit_bias, s);
-  }
   if (L->cfg.weight_format == MOE_WEIGHTS_MXFP4) return launch_decode_fmt<FmtMXFP4>(L, x, out, T, logit_bias, s);
   return launch_decode_fmt<FmtBF16>(L, x, out, T, logit_bias, s);
 }

@@ -34,7 +34,6 @@ struct DecodeWorkspace {
   float* h;              // [kMaxDecodeT * k][I]   SwiGLU outputs of routed assignments (t*k+j)
   float* h_shared;       // [kMaxDecodeT][Is]
   unsigned long long* sync_ctr;   // [2] grid-sync arrival counters (monotonic)
-  float* partial;        // [num_sms][kMaxDecodeT][H] per-CTA output partial sums (streaming kernel)
 };
 
 struct GroupedWorkspace {
@@ -70,8 +69,6 @@ struct moe_layer {
   uint16_t* router_split;  // bf16 [3][E][H]  W_r^T = hi + mid + lo exactly (grouped path)
   uint8_t* w_gu;         // routed gate/up, [E][I][2][row_bytes.gu]  (gate row, up row per i)
   uint8_t* w_down;       // routed down,    [E][H][row_bytes.down]
-  uint16_t* w_rec;       // bf16 layers: routed streaming records [E][I][3][H] = gate row, up row, down column
-  uint16_t* ws_rec;      // shared-expert streaming records [Is][3][H]
   uint16_t* ws_gu;       // shared gate/up bf16 [Is][2][H]
   uint16_t* ws_down;     // shared down bf16 [H][Is]
   moe::RowBytes row_bytes;
