@@ -199,6 +199,80 @@ __device__ __forceinline__ void gu_fma_mx(const uint4 (&v)[16], const uint32_t (
 }
 
 // ===========================================================================
+// Top-k of one token's logits by one warp.
+// ===========================================================================
+// Lane l holds the logits of experts l, l + 32, ... as order-preserving keys in
+// groups of 8, each group sorted descending (ties: lower expert first) by a
+// 19-comparator network; each round then takes the warp maximum of the lane
+// heads (redux), breaks exact ties by the lowest expert index (second redux)
+// and pops the winner's head. Writes the k experts in descending order and
+// their softmax weights renormalised over the k.
+template <int G>
+__device__ __forceinline__ void ce(uint32_t (&key)[G][8], int (&jj)[G][8], int g, int a, int b) {
+  const bool sw = key[g][b] > key[g][a] || (key[g][b] == key[g][a] && jj[g][b] < jj[g][a]);
+  const uint32_t ka = key[g][a], kb = key[g][b];
+  const int ja = jj[g][a], jb = jj[g][b];
+  key[g][a] = sw ? kb : ka; key[g][b] = sw ? ka : kb;
+  jj[g][a] = sw ? jb : ja; jj[g][b] = sw ? ja : jb;
+}
+
+template <int G>
+__device__ __forceinline__ void warp_topk(const float* logits, int E, int k, int lane, int* out_e, float* out_w) {
+  uint32_t key[G][8];
+  int jj[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = 8 * g + q, e = lane + 32 * j;
+      key[g][q] = (e < E) ? f32_order_key(ldg_cg_f32(logits + e)) : 0u;
+      jj[g][q] = j;
+    }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    ce<G>(key, jj, g, 0, 1); ce<G>(key, jj, g, 2, 3); ce<G>(key, jj, g, 4, 5); ce<G>(key, jj, g, 6, 7);
+    ce<G>(key, jj, g, 0, 2); ce<G>(key, jj, g, 1, 3); ce<G>(key, jj, g, 4, 6); ce<G>(key, jj, g, 5, 7);
+    ce<G>(key, jj, g, 1, 2); ce<G>(key, jj, g, 5, 6);
+    ce<G>(key, jj, g, 0, 4); ce<G>(key, jj, g, 1, 5); ce<G>(key, jj, g, 2, 6); ce<G>(key, jj, g, 3, 7);
+    ce<G>(key, jj, g, 2, 4); ce<G>(key, jj, g, 3, 5);
+    ce<G>(key, jj, g, 1, 2); ce<G>(key, jj, g, 3, 4); ce<G>(key, jj, g, 5, 6);
+  }
+  float v0 = 0.f, sum = 0.f, my_ex = 0.f;
+  int my_e = 0;
+#pragma unroll 1
+  for (int r = 0; r < k; ++r) {
+    uint32_t hk = key[0][0];
+    int hj = jj[0][0], hg = 0;
+#pragma unroll
+    for (int g = 1; g < G; ++g)
+      if (key[g][0] > hk || (key[g][0] == hk && jj[g][0] < hj)) { hk = key[g][0]; hj = jj[g][0]; hg = g; }
+    const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, hk);
+    const uint32_t cand = (hk == gmax) ? (uint32_t)(lane + 32 * hj) : 0xFFFFFFFFu;
+    const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
+    if (lane == (int)(gidx & 31u)) {  // pop the winner's head
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (g == hg) {
+#pragma unroll
+          for (int q = 0; q < 7; ++q) { key[g][q] = key[g][q + 1]; jj[g][q] = jj[g][q + 1]; }
+          key[g][7] = 0u;
+          jj[g][7] = 1 << 20;
+        }
+      }
+    }
+    const float val = f32_from_order_key(gmax);
+    if (r == 0) v0 = val;
+    const float ex = expf(val - v0);   // renormalised softmax over the k selected logits
+    sum += ex;
+    if (lane == r) { my_ex = ex; my_e = (int)gidx; }
+  }
+  if (lane < k) {
+    out_e[lane] = my_e;
+    out_w[lane] = my_ex / sum;
+  }
+}
+
+// ===========================================================================
 // The fused decode kernel: one cooperative launch, one CTA per SM.
 // ===========================================================================
 struct FusedArgs {
@@ -260,7 +334,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 moe_decode_fused_kernel(const FusedArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);   // phases 1-2: x [T][H] bf16
-  float* hs = reinterpret_cast<float*>(smem);         // phase 3: h [T*k][I] fp32, then h_shared [T][Is]
   uint8_t* s_shrows = smem + a.smem_r1;               // shared-expert down rows [n0, n1) x Is bf16
   uint8_t* s_rows = s_shrows + a.smem_sh;             // routed down rows, slot d at d * slot_stride
   __shared__ DecodeMeta s_meta;
@@ -271,6 +344,8 @@ moe_decode_fused_kernel(const FusedArgs a) {
   __shared__ int s_abort;
   __shared__ unsigned long long s_gen;
   __shared__ __align__(8) uint64_t bar_sh, bar_rt;
+  __shared__ float s_rpart[4 * 4 * kMaxDecodeT];   // router-row quarter partials [row][quarter][t]
+  __shared__ int s_rcnt[4];
 
   const int T = a.T, H = a.H, E = a.E, I = a.I, Is = a.Is, k = a.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -289,6 +364,7 @@ moe_decode_fused_kernel(const FusedArgs a) {
     sm100::fence_barrier_init();
     s_router_done = 0;
     s_abort = 0;
+    for (int r = 0; r < 4; ++r) s_rcnt[r] = 0;
     if (nr == 0) s_gen = grid_arrive(&a.sync_ctr[0]);  // no router rows: arrive at once
   }
   __syncthreads();
@@ -301,19 +377,24 @@ moe_decode_fused_kernel(const FusedArgs a) {
   }
 
   // ------------------------------------------------ phase 1: router + shared gate/up
+  // Items: (router row r of this CTA, quarter of H) for r < nr, then this CTA's
+  // shared-expert units. The last quarter to finish a row adds the four partial
+  // sums in order and writes the logit.
+  const int nri = 4 * nr;
+  const int nch_r = H / 4;                      // 16-byte chunks (4 floats) of a router row
   uint4 v[16];
   {
-    const int slot = warp;   // first assignment of this warp: loads issued before x arrives
-    if (slot < nr) {
-      const float* row = a.router_t + (size_t)(b + slot * G) * H;
-      const int nch = H / 4;
+    const int slot = warp;   // first item of this warp: loads issued before x arrives
+    if (slot < nri) {
+      const float* row = a.router_t + (size_t)(b + (slot >> 2) * G) * H;
+      const int qlo = (slot & 3) * nch_r / 4, qhi = ((slot & 3) + 1) * nch_r / 4;
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
-        const int c = lane + 32 * q;
-        if (c < nch) v[q] = ldg_stream(row + 4 * c);
+        const int c = qlo + lane + 32 * q;
+        if (c < qhi) v[q] = ldg_stream(row + 4 * c);
       }
-    } else if (slot - nr < sh1 - sh0) {
-      const uint8_t* grec = reinterpret_cast<const uint8_t*>(a.ws_gu + (size_t)(sh0 + slot - nr) * 2 * H);
+    } else if (slot - nri < sh1 - sh0) {
+      const uint8_t* grec = reinterpret_cast<const uint8_t*>(a.ws_gu + (size_t)(sh0 + slot - nri) * 2 * H);
       gu_load_bf16(grec, grec + 2 * H, 0, H / 8, v, lane);
     }
   }
@@ -336,37 +417,38 @@ moe_decode_fused_kernel(const FusedArgs a) {
     }
   }
   __syncthreads();
-  for (int slot = warp; slot < nr + (sh1 - sh0); slot += nw) {
+  for (int slot = warp; slot < nri + (sh1 - sh0); slot += nw) {
     const bool preloaded = slot == warp;
-    if (slot < nr) {
-      const int u = b + slot * G;
+    if (slot < nri) {
+      const int rl = slot >> 2, qt = slot & 3;
+      const int u = b + rl * G;
       const float* row = a.router_t + (size_t)u * H;
-      const int nch = H / 4;
+      const int qlo = qt * nch_r / 4, qhi = (qt + 1) * nch_r / 4;
       float acc[TMAX];
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-      for (int b0 = 0; b0 < nch; b0 += 32 * 16) {
-        if (!(preloaded && b0 == 0)) {
+      for (int b0 = qlo; b0 < qhi; b0 += 32 * 16) {
+        if (!(preloaded && b0 == qlo)) {
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const int c = b0 + lane + 32 * q;
-            if (c < nch) v[q] = ldg_stream(row + 4 * c);
+            if (c < qhi) v[q] = ldg_stream(row + 4 * c);
           }
         }
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
           const int c = b0 + lane + 32 * q;
-          if (c < nch) {
+          if (c < qhi) {
 #pragma unroll
             for (int t = 0; t < TMAX; ++t) {
               if (t < T) {
                 const uint2 xx = *reinterpret_cast<const uint2*>(xs + t * H + 4 * c);
-                float s = acc[t];
-                s = fmaf(__uint_as_float(v[q].x), bf16_lo(xx.x), s);
-                s = fmaf(__uint_as_float(v[q].y), bf16_hi(xx.x), s);
-                s = fmaf(__uint_as_float(v[q].z), bf16_lo(xx.y), s);
-                s = fmaf(__uint_as_float(v[q].w), bf16_hi(xx.y), s);
-                acc[t] = s;
+                float sacc = acc[t];
+                sacc = fmaf(__uint_as_float(v[q].x), bf16_lo(xx.x), sacc);
+                sacc = fmaf(__uint_as_float(v[q].y), bf16_hi(xx.x), sacc);
+                sacc = fmaf(__uint_as_float(v[q].z), bf16_lo(xx.y), sacc);
+                sacc = fmaf(__uint_as_float(v[q].w), bf16_hi(xx.y), sacc);
+                acc[t] = sacc;
               }
             }
           }
@@ -375,20 +457,34 @@ moe_decode_fused_kernel(const FusedArgs a) {
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) {
         if (t < T) {
-          float s = warp_sum(acc[t]);
-          if (lane == t) {
-            s += a.router_bias[u];
-            if (a.logit_bias) s += a.logit_bias[(size_t)t * E + u];
-            a.logits[(size_t)t * E + u] = s;
-          }
+          const float sum = warp_sum(acc[t]);
+          if (lane == t) s_rpart[(rl * 4 + qt) * kMaxDecodeT + t] = sum;
         }
       }
-      __threadfence();
+      __threadfence_block();
       __syncwarp();
-      // the warp completing this CTA's router rows arrives for the whole CTA
-      if (lane == 0 && atomicAdd(&s_router_done, 1) == nr - 1) s_gen = grid_arrive(&a.sync_ctr[0]);
+      int last = 0;
+      if (lane == 0) last = (atomicAdd(&s_rcnt[rl], 1) == 3);
+      last = __shfl_sync(0xFFFFFFFFu, last, 0);
+      if (last) {  // all four quarters of row u are in: logit = ordered sum + biases
+        __threadfence_block();
+        if (lane < T) {
+          const volatile float* pp = s_rpart + rl * 4 * kMaxDecodeT + lane;
+          float sl = pp[0];
+          sl += pp[kMaxDecodeT];
+          sl += pp[2 * kMaxDecodeT];
+          sl += pp[3 * kMaxDecodeT];
+          sl += a.router_bias[u];
+          if (a.logit_bias) sl += a.logit_bias[(size_t)lane * E + u];
+          a.logits[(size_t)lane * E + u] = sl;
+        }
+        __threadfence();
+        __syncwarp();
+        // the warp completing this CTA's last router row arrives for the whole CTA
+        if (lane == 0 && atomicAdd(&s_router_done, 1) == nr - 1) s_gen = grid_arrive(&a.sync_ctr[0]);
+      }
     } else {
-      const int i = sh0 + slot - nr;
+      const int i = sh0 + slot - nri;
       const uint8_t* grec = reinterpret_cast<const uint8_t*>(a.ws_gu + (size_t)i * 2 * H);
       const uint8_t* urec = grec + 2 * H;
       const int nch = H / 8;
@@ -420,45 +516,12 @@ moe_decode_fused_kernel(const FusedArgs a) {
   // identical arithmetic): top-k, renormalised weights, distinct experts.
   if (warp < T) {
     const int t = warp;
-    constexpr int kPer = kMaxExperts / 32;
-    const int kp = (E + 31) / 32;
-    uint32_t key[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int e = lane + 32 * j;
-      key[j] = (j < kp && e < E) ? f32_order_key(ldg_cg_f32(a.logits + (size_t)t * E + e)) : 0u;
-    }
-    float v0 = 0.f, sum = 0.f, my_v = 0.f;
-    int my_e = 0;
-#pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-      uint32_t lk = 0u;
-      int lj = 0;
-#pragma unroll
-      for (int j = 0; j < kPer; ++j)
-        if (j < kp && key[j] > lk) { lk = key[j]; lj = j; }
-      const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, lk);
-      const uint32_t cand = (lk == gmax) ? (uint32_t)(lane + 32 * lj) : 0xFFFFFFFFu;
-      const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
-      if (lane == (int)(gidx & 31u)) {
-#pragma unroll
-        for (int j = 0; j < kPer; ++j)
-          if (j == (int)(gidx >> 5)) key[j] = 0u;
-      }
-      const float val = f32_from_order_key(gmax);
-      if (r == 0) v0 = val;
-      const float ex = expf(val - v0);   // renormalised softmax over the k selected logits
-      sum += ex;
-      if (lane == r) { my_v = ex; my_e = (int)gidx; }
-    }
-    if (lane < k) {
-      const float wgt = my_v / sum;
-      s_idx[t * k + lane] = my_e;
-      s_w[t * k + lane] = wgt;
-      if (b == 0) {
-        a.idx[t * k + lane] = my_e;
-        a.weights[t * k + lane] = wgt;
-      }
+    if (E <= 256) warp_topk<1>(a.logits + (size_t)t * E, E, k, lane, s_idx + t * k, s_w + t * k);
+    else warp_topk<2>(a.logits + (size_t)t * E, E, k, lane, s_idx + t * k, s_w + t * k);
+    __syncwarp();
+    if (b == 0 && lane < k) {
+      a.idx[t * k + lane] = s_idx[t * k + lane];
+      a.weights[t * k + lane] = s_w[t * k + lane];
     }
   }
   __syncthreads();
@@ -594,15 +657,35 @@ moe_decode_fused_kernel(const FusedArgs a) {
   // (slot D is the shared expert, weight 1); an item dots each of its rows with
   // the slot's SwiGLU outputs, read once per item. Per-warp partial sums meet in
   // shared memory and are added in warp order (deterministic).
-  float* hss = hs + (size_t)T * k * I;
+  // SwiGLU outputs as 16-bit in shared memory: bf16 for bf16 weights, f16 for
+  // MXFP4 weights (the e2m1 values are exact in f16); the shared expert is bf16.
+  uint16_t* hs16 = reinterpret_cast<uint16_t*>(smem);          // [T*k][I]
+  uint16_t* hss16 = hs16 + (size_t)T * k * I;                  // [T][Is]
   float* s_part = reinterpret_cast<float*>(s_rows + (size_t)a.slots_cap * a.slot_stride);  // [nw][rows_max][T]
   {
-    const int n16 = T * k * I / 4;
-    for (int q = threadIdx.x; q < n16; q += blockDim.x)
-      reinterpret_cast<uint4*>(hs)[q] = ldg_cg(reinterpret_cast<const uint4*>(a.h) + q);
-    const int s16 = T * Is / 4;
-    for (int q = threadIdx.x; q < s16; q += blockDim.x)
-      reinterpret_cast<uint4*>(hss)[q] = ldg_cg(reinterpret_cast<const uint4*>(a.h_shared) + q);
+    const int n4 = T * k * I / 4;
+    for (int q = threadIdx.x; q < n4; q += blockDim.x) {
+      const uint4 f = ldg_cg(reinterpret_cast<const uint4*>(a.h) + q);
+      uint2 o;
+      if (kMx) {
+        const __half2 p0 = __floats2half2_rn(__uint_as_float(f.x), __uint_as_float(f.y));
+        const __half2 p1 = __floats2half2_rn(__uint_as_float(f.z), __uint_as_float(f.w));
+        o.x = *reinterpret_cast<const uint32_t*>(&p0);
+        o.y = *reinterpret_cast<const uint32_t*>(&p1);
+      } else {
+        o.x = (uint32_t)f32_to_bf16_rne(__uint_as_float(f.x)) | ((uint32_t)f32_to_bf16_rne(__uint_as_float(f.y)) << 16);
+        o.y = (uint32_t)f32_to_bf16_rne(__uint_as_float(f.z)) | ((uint32_t)f32_to_bf16_rne(__uint_as_float(f.w)) << 16);
+      }
+      reinterpret_cast<uint2*>(hs16)[q] = o;
+    }
+    const int s4 = T * Is / 4;
+    for (int q = threadIdx.x; q < s4; q += blockDim.x) {
+      const uint4 f = ldg_cg(reinterpret_cast<const uint4*>(a.h_shared) + q);
+      uint2 o;
+      o.x = (uint32_t)f32_to_bf16_rne(__uint_as_float(f.x)) | ((uint32_t)f32_to_bf16_rne(__uint_as_float(f.y)) << 16);
+      o.y = (uint32_t)f32_to_bf16_rne(__uint_as_float(f.z)) | ((uint32_t)f32_to_bf16_rne(__uint_as_float(f.w)) << 16);
+      reinterpret_cast<uint2*>(hss16)[q] = o;
+    }
     for (int q = threadIdx.x; q < nw * a.rows_max * T; q += blockDim.x) s_part[q] = 0.f;
   }
   __syncthreads();
@@ -622,16 +705,16 @@ moe_decode_fused_kernel(const FusedArgs a) {
     else if (in_smem) { rows_base = s_rows + (size_t)sd * a.slot_stride; rstride = a.rb_down; }
     else { rows_base = a.w_down + ((int64_t)s_meta.slot_expert[sd] * H + n0) * a.rb_down; rstride = a.rb_down; }
     float wt[TMAX];
-    const float* hrow[TMAX];
+    const uint16_t* hrow[TMAX];
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) {
       wt[t] = 0.f;
       hrow[t] = nullptr;
       if (t < T) {
-        if (shared) { wt[t] = 1.f; hrow[t] = hss + (size_t)t * Is; }
+        if (shared) { wt[t] = 1.f; hrow[t] = hss16 + (size_t)t * Is; }
         else {
           const int j = s_meta.slot_j[sd][t];
-          if (j >= 0) { wt[t] = s_w[t * k + j]; hrow[t] = hs + ((size_t)t * k + j) * I; }
+          if (j >= 0) { wt[t] = s_w[t * k + j]; hrow[t] = hs16 + ((size_t)t * k + j) * I; }
         }
       }
     }
@@ -641,14 +724,10 @@ moe_decode_fused_kernel(const FusedArgs a) {
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) acc[rr][t] = 0.f;
     for (int c = lane; c < nsub; c += 32) {
-      float4 h0[TMAX], h1[TMAX];
+      uint4 hv[TMAX];
 #pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        if (hrow[t]) {
-          h0[t] = *reinterpret_cast<const float4*>(hrow[t] + 8 * c);
-          h1[t] = *reinterpret_cast<const float4*>(hrow[t] + 8 * c + 4);
-        }
-      }
+      for (int t = 0; t < TMAX; ++t)
+        if (hrow[t]) hv[t] = *reinterpret_cast<const uint4*>(hrow[t] + 8 * c);
       uint4 wv[RB];
       uint32_t sb[RB];
 #pragma unroll
@@ -667,29 +746,19 @@ moe_decode_fused_kernel(const FusedArgs a) {
 #pragma unroll
       for (int rr = 0; rr < RB; ++rr) {
         if (r0 + rr < nrows) {
-          float w8[8];
-          float scale = 1.f;
-          if (!mx) {
-            w8[0] = bf16_lo(wv[rr].x); w8[1] = bf16_hi(wv[rr].x); w8[2] = bf16_lo(wv[rr].y); w8[3] = bf16_hi(wv[rr].y);
-            w8[4] = bf16_lo(wv[rr].z); w8[5] = bf16_hi(wv[rr].z); w8[6] = bf16_lo(wv[rr].w); w8[7] = bf16_hi(wv[rr].w);
-          } else {
-            scale = e8m0_scale(sb[rr]);          // one scale per 32 elements: constant over these 8
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t hp = e2m1x2_to_f16x2(wv[rr].x >> (8 * q));
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hp));
-              w8[2 * q] = f.x;
-              w8[2 * q + 1] = f.y;
-            }
-          }
 #pragma unroll
           for (int t = 0; t < TMAX; ++t) {
             if (hrow[t]) {
-              float s = w8[0] * h0[t].x;
-              s = fmaf(w8[1], h0[t].y, s); s = fmaf(w8[2], h0[t].z, s); s = fmaf(w8[3], h0[t].w, s);
-              s = fmaf(w8[4], h1[t].x, s); s = fmaf(w8[5], h1[t].y, s);
-              s = fmaf(w8[6], h1[t].z, s); s = fmaf(w8[7], h1[t].w, s);
-              acc[rr][t] = fmaf(scale, s, acc[rr][t]);
+              if (!mx) {
+                acc[rr][t] = fma8_bf16(wv[rr], hv[t], acc[rr][t]);
+              } else {  // one scale per 32 elements: constant over these 8
+                float sdot = 0.f;
+                sdot = fma2_f16(e2m1x2_to_f16x2(wv[rr].x), hv[t].x, sdot);
+                sdot = fma2_f16(e2m1x2_to_f16x2(wv[rr].x >> 8), hv[t].y, sdot);
+                sdot = fma2_f16(e2m1x2_to_f16x2(wv[rr].x >> 16), hv[t].z, sdot);
+                sdot = fma2_f16(e2m1x2_to_f16x2(wv[rr].x >> 24), hv[t].w, sdot);
+                acc[rr][t] = fmaf(e8m0_scale(sb[rr]), sdot, acc[rr][t]);
+              }
             }
           }
         }
