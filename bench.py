@@ -363,11 +363,15 @@ def prefill_workload(B: Bench, steps: int, warmup: int, peaks):
     ms = float(np.mean(times))
     tok_s = w.T / (ms * 1e-3)
     tflops = st.flops / (ms * 1e-3) / 1e12
+    _, stages = B.time_calls(L, [x] * 3, [None] * 3, [out] * 3, profile=True)
+    st_us = np.mean(np.array(stages), axis=0) * 1e3
+    names = ["router", "dispatch", "grouped_gateup", "grouped_down", "combine"]
     return {"workload": "qwen_prefill", "T": w.T, "ms_per_call": ms, "tokens_per_s": tok_s,
             "useful_tflops": tflops, "frac_of_measured_bf16": tflops / peaks["bf16_tflops"],
             "touched_experts": st.distinct_experts, "max_expert_rows": st.max_expert_rows,
             "algorithmic_bytes": st.algorithmic_bytes,
-            "hbm_frac": st.algorithmic_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+            "hbm_frac": st.algorithmic_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "stage_us": {n: round(float(v), 2) for n, v in zip(names, st_us)}}
 
 
 def _profile_traffic(kernel: str):

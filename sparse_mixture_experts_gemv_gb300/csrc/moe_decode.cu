@@ -199,80 +199,6 @@ __device__ __forceinline__ void gu_fma_mx(const uint4 (&v)[16], const uint32_t (
 }
 
 // ===========================================================================
-// Top-k of one token's logits by one warp.
-// ===========================================================================
-// Lane l holds the logits of experts l, l + 32, ... as order-preserving keys in
-// groups of 8, each group sorted descending (ties: lower expert first) by a
-// 19-comparator network; each round then takes the warp maximum of the lane
-// heads (redux), breaks exact ties by the lowest expert index (second redux)
-// and pops the winner's head. Writes the k experts in descending order and
-// their softmax weights renormalised over the k.
-template <int G>
-__device__ __forceinline__ void ce(uint32_t (&key)[G][8], int (&jj)[G][8], int g, int a, int b) {
-  const bool sw = key[g][b] > key[g][a] || (key[g][b] == key[g][a] && jj[g][b] < jj[g][a]);
-  const uint32_t ka = key[g][a], kb = key[g][b];
-  const int ja = jj[g][a], jb = jj[g][b];
-  key[g][a] = sw ? kb : ka; key[g][b] = sw ? ka : kb;
-  jj[g][a] = sw ? jb : ja; jj[g][b] = sw ? ja : jb;
-}
-
-template <int G>
-__device__ __forceinline__ void warp_topk(const float* logits, int E, int k, int lane, int* out_e, float* out_w) {
-  uint32_t key[G][8];
-  int jj[G][8];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = 8 * g + q, e = lane + 32 * j;
-      key[g][q] = (e < E) ? f32_order_key(ldg_cg_f32(logits + e)) : 0u;
-      jj[g][q] = j;
-    }
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    ce<G>(key, jj, g, 0, 1); ce<G>(key, jj, g, 2, 3); ce<G>(key, jj, g, 4, 5); ce<G>(key, jj, g, 6, 7);
-    ce<G>(key, jj, g, 0, 2); ce<G>(key, jj, g, 1, 3); ce<G>(key, jj, g, 4, 6); ce<G>(key, jj, g, 5, 7);
-    ce<G>(key, jj, g, 1, 2); ce<G>(key, jj, g, 5, 6);
-    ce<G>(key, jj, g, 0, 4); ce<G>(key, jj, g, 1, 5); ce<G>(key, jj, g, 2, 6); ce<G>(key, jj, g, 3, 7);
-    ce<G>(key, jj, g, 2, 4); ce<G>(key, jj, g, 3, 5);
-    ce<G>(key, jj, g, 1, 2); ce<G>(key, jj, g, 3, 4); ce<G>(key, jj, g, 5, 6);
-  }
-  float v0 = 0.f, sum = 0.f, my_ex = 0.f;
-  int my_e = 0;
-#pragma unroll 1
-  for (int r = 0; r < k; ++r) {
-    uint32_t hk = key[0][0];
-    int hj = jj[0][0], hg = 0;
-#pragma unroll
-    for (int g = 1; g < G; ++g)
-      if (key[g][0] > hk || (key[g][0] == hk && jj[g][0] < hj)) { hk = key[g][0]; hj = jj[g][0]; hg = g; }
-    const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, hk);
-    const uint32_t cand = (hk == gmax) ? (uint32_t)(lane + 32 * hj) : 0xFFFFFFFFu;
-    const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
-    if (lane == (int)(gidx & 31u)) {  // pop the winner's head
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (g == hg) {
-#pragma unroll
-          for (int q = 0; q < 7; ++q) { key[g][q] = key[g][q + 1]; jj[g][q] = jj[g][q + 1]; }
-          key[g][7] = 0u;
-          jj[g][7] = 1 << 20;
-        }
-      }
-    }
-    const float val = f32_from_order_key(gmax);
-    if (r == 0) v0 = val;
-    const float ex = expf(val - v0);   // renormalised softmax over the k selected logits
-    sum += ex;
-    if (lane == r) { my_ex = ex; my_e = (int)gidx; }
-  }
-  if (lane < k) {
-    out_e[lane] = my_e;
-    out_w[lane] = my_ex / sum;
-  }
-}
-
-// ===========================================================================
 // The fused decode kernel: one cooperative launch, one CTA per SM.
 // ===========================================================================
 struct FusedArgs {

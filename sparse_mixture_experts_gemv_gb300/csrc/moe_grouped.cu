@@ -14,7 +14,8 @@
 //   grouped_gemm<ROUTER>  fp32-exact router logits on the tensor cores: W_r is
 //                         split exactly into three bf16 terms (hi + mid + lo), x is
 //                         bf16, so every product is exact and the accumulation is
-//                         fp32 (three passes over K into one TMEM accumulator).
+//                         fp32 (each staged x tile meets all three terms, all
+//                         MMAs into one TMEM accumulator).
 //   topk_hist             per-token top-k + renormalised softmax weights; per
 //                         32-token chunk expert histogram.
 //   dispatch_scan         per-expert totals, chunk bases, offsets, block map.
@@ -50,7 +51,7 @@ constexpr int kStages = 4;
 constexpr int kStageA = BM * BK * 2;     // 16 KB
 constexpr int kStageB = 256 * BK * 2;    // 32 KB (N up to 256)
 constexpr int kTmemCols = 512;           // two 256-column fp32 accumulators
-constexpr int kChunk = 32;               // tokens per dispatch chunk
+constexpr int kChunk = 32;               // tokens per dispatch chunk (one per warp of the top-k CTA)
 constexpr size_t kGemmSmem = (size_t)kStages * (kStageA + kStageB) + 1024 /*align*/ + 256 /*barriers*/;
 
 enum Epi { EPI_ROUTER = 0, EPI_SWIGLU = 1, EPI_STORE = 2 };
@@ -182,22 +183,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
-      const uint32_t bytes = (uint32_t)p.BN * BK * 2 + (GATHER ? 0u : (uint32_t)kStageA);
+      const uint32_t bytes = (uint32_t)p.BN * BK * 2 * (EPI == EPI_ROUTER ? 3 : 1) + (GATHER ? 0u : (uint32_t)kStageA);
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
         const TileInfo ti = decode_tile(p, R, tile);
         for (int kb = 0; kb < ti.ks; ++kb, ++it) {
           const int s = it % kStages;
           if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, abort_flag)) break;
           mbar_arrive_expect_tx(&full[s], bytes);
-          int kcol = kb * BK, brow;
-          if (EPI == EPI_ROUTER) {
-            const int part = kb / p.ks_part;       // 0: hi, 1: mid, 2: lo
-            kcol = (kb % p.ks_part) * BK;
-            brow = part * p.E + ti.nt * p.BN;
+          const int kcol = kb * BK;
+          if (EPI == EPI_ROUTER) {  // the three bf16 terms of W_r share this A tile
+#pragma unroll
+            for (int part = 0; part < 3; ++part)
+              tma_load_2d(sB + s * kStageB + part * p.BN * BK * 2, &mapB_r, kcol, part * p.E + ti.nt * p.BN, &full[s]);
           } else {
-            brow = (ti.shared ? 0 : ti.e * p.b_rows_per_expert) + ti.nt * p.BN;
+            const int brow = (ti.shared ? 0 : ti.e * p.b_rows_per_expert) + ti.nt * p.BN;
+            tma_load_2d(sB + s * kStageB, ti.shared ? &mapB_s : &mapB_r, kcol, brow, &full[s]);
           }
-          tma_load_2d(sB + s * kStageB, ti.shared ? &mapB_s : &mapB_r, kcol, brow, &full[s]);
           if (!GATHER) tma_load_2d(sA + s * kStageA, ti.shared ? &mapA_s : &mapA_r, kcol, ti.row0, &full[s]);
         }
       }
@@ -222,10 +223,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
           if (!mbar_wait(&full[s], (it / kStages) & 1, p.err, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + s * kStageA), b0 = smem_u32(sB + s * kStageB);
+          constexpr int kTerms = (EPI == EPI_ROUTER) ? 3 : 1;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
-                     (kb | kk) != 0 ? 1u : 0u);
+          for (int part = 0; part < kTerms; ++part) {
+            const uint32_t bp = b0 + part * p.BN * BK * 2;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(bp + kk * 32), idesc,
+                       (kb | kk | part) != 0 ? 1u : 0u);
+          }
           mma_commit(&empty[s]);
         }
         if (!ok) break;
@@ -355,7 +361,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
 // ===========================================================================
 // Routing: top-k per token, per-chunk histogram
 // ===========================================================================
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(1024)
 topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k, int* __restrict__ idx,
                  float* __restrict__ weights, int* __restrict__ chunk_counts) {
   __shared__ int s_count[kMaxExperts];
@@ -364,78 +370,56 @@ topk_hist_kernel(const float* __restrict__ logits, int T, int E, int k, int* __r
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_count[e] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int kPer = kMaxExperts / 32;
-  for (int tl = warp; tl < kChunk; tl += 8) {
+  for (int tl = warp; tl < kChunk; tl += 32) {
     const int t = blockIdx.x * kChunk + tl;
     if (t >= T) break;
-    uint32_t key[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int e = lane + 32 * j;
-      key[j] = (e < E) ? f32_order_key(logits[(size_t)t * E + e]) : 0u;
-    }
-    float sel_v[kMaxTopK];
-    int sel_e[kMaxTopK];
-#pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r) {
-      if (r < k) {
-        uint32_t lk = 0u;
-        int lj = 0;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j)
-          if (key[j] > lk) { lk = key[j]; lj = j; }
-        const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, lk);
-        const uint32_t cand = (lk == gmax) ? (uint32_t)(lane + 32 * lj) : 0xFFFFFFFFu;
-        const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
-        if (lane == (int)(gidx & 31u)) {
-#pragma unroll
-          for (int j = 0; j < kPer; ++j)
-            if (j == (int)(gidx >> 5)) key[j] = 0u;
-        }
-        sel_v[r] = f32_from_order_key(gmax);
-        sel_e[r] = (int)gidx;
-      }
-    }
-    float ex[kMaxTopK], sum = 0.f;
-#pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r)
-      if (r < k) { ex[r] = expf(sel_v[r] - sel_v[0]); sum += ex[r]; }
-#pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r) {
-      if (r < k && lane == r) {
-        idx[(size_t)t * k + r] = sel_e[r];
-        weights[(size_t)t * k + r] = ex[r] / sum;
-        atomicAdd(&s_count[sel_e[r]], 1);
-      }
-    }
+    if (E <= 256) warp_topk<1>(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, weights + (size_t)t * k);
+    else warp_topk<2>(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, weights + (size_t)t * k);
+    __syncwarp();
+    if (lane < k) atomicAdd(&s_count[idx[(size_t)t * k + lane]], 1);
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + e] = s_count[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(size_t)e * gridDim.x + blockIdx.x] = s_count[e];
 }
 
-// One CTA, one thread per expert: chunk bases, totals, offsets, block map.
-__global__ void __launch_bounds__(512)
+// One CTA. Counts are [E][chunks]: warp w scans the chunk counts of experts
+// w, w + 32, ... (exclusive, 32 chunks per pass with warp shuffles) into chunk
+// bases and expert totals; then exclusive scans over the experts give the
+// grouped-row offsets and the 128-row block map.
+__global__ void __launch_bounds__(1024)
 dispatch_scan_kernel(int* __restrict__ chunk_counts /* in: counts, out: bases */, int num_chunks, int E, int T,
                      int k, int* __restrict__ hist, int* __restrict__ offsets, int2* __restrict__ mtiles,
                      int* __restrict__ num_routed, int max_mtiles, int* __restrict__ err) {
-  __shared__ int s_tot[kMaxExperts];
-  __shared__ int s_tiles[kMaxExperts];
+  __shared__ int s_tot[1024];
+  __shared__ int s_tiles[1024];
   pdl_wait();
   pdl_launch_dependents();
-  const int e = threadIdx.x;
-  int run = 0;
-  if (e < E) {
-    for (int c = 0; c < num_chunks; ++c) {
-      int* p = chunk_counts + (size_t)c * E + e;
-      const int v = *p;
-      *p = run;
-      run += v;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = warp; e < E; e += 32) {
+    int* row = chunk_counts + (size_t)e * num_chunks;
+    int run = 0;
+    for (int c0 = 0; c0 < num_chunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < num_chunks ? row[c] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (c < num_chunks) row[c] = run + incl - v;   // exclusive base of chunk c for expert e
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
-    hist[e] = run;
+    if (lane == 0) {
+      hist[e] = run;
+      s_tot[e] = run;
+      s_tiles[e] = (run + BM - 1) / BM;
+    }
   }
-  s_tot[e] = (e < E) ? run : 0;
-  s_tiles[e] = (e < E) ? (run + BM - 1) / BM : 0;
+  for (int e = E + threadIdx.x; e < (int)blockDim.x; e += blockDim.x) { s_tot[e] = 0; s_tiles[e] = 0; }
   __syncthreads();
+  const int e = threadIdx.x;
+  const int run = (e < E) ? s_tot[e] : 0;
   // exclusive scans over experts (E <= 512, simple two-array Hillis-Steele)
   for (int d = 1; d < blockDim.x; d <<= 1) {
     int a = 0, b = 0;
@@ -461,28 +445,43 @@ dispatch_scan_kernel(int* __restrict__ chunk_counts /* in: counts, out: bases */
   }
 }
 
-// Grouped row of every assignment: offsets[e] + chunk base + rank within the chunk.
+// Grouped row of every assignment: offsets[e] + chunk base + rank within the
+// chunk, the rank counting the chunk's earlier tokens that chose e (one warp
+// walks the chunk's tokens in order; a token's k experts are distinct).
 __global__ void __launch_bounds__(256)
 dispatch_scatter_kernel(const int* __restrict__ idx, const int* __restrict__ chunk_bases,
                         const int* __restrict__ offsets, int T, int E, int k, int* __restrict__ perm,
                         int* __restrict__ pos, int* __restrict__ err) {
-  __shared__ int s_idx[kChunk * kMaxTopK];
+  __shared__ int s_next[kMaxExperts];
+  __shared__ int s_e[kChunk * kMaxTopK];
   pdl_wait();
   pdl_launch_dependents();
   const int t0 = blockIdx.x * kChunk;
-  const int n = min(kChunk, T - t0) * k;
-  for (int a = threadIdx.x; a < n; a += blockDim.x) s_idx[a] = idx[(size_t)t0 * k + a];
+  const int ntok = min(kChunk, T - t0);
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    s_next[e] = offsets[e] + chunk_bases[(size_t)e * gridDim.x + blockIdx.x];
+  for (int q = threadIdx.x; q < ntok * k; q += blockDim.x) s_e[q] = idx[(size_t)t0 * k + q];
   __syncthreads();
-  for (int a = threadIdx.x; a < n; a += blockDim.x) {
-    const int e = s_idx[a];
-    if (e < 0 || e >= E) { set_error(err, kDevCheck); continue; }
-    const int tl = a / k;
-    int rank = 0;
-    for (int b = 0; b < tl * k; ++b) rank += (s_idx[b] == e);
-    const int g = offsets[e] + chunk_bases[(size_t)blockIdx.x * E + e] + rank;
-    if (g < 0 || g >= T * k) { set_error(err, kDevCheck); continue; }
-    perm[g] = t0 * k + a;
-    pos[(size_t)t0 * k + a] = g;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    for (int tl = 0; tl < ntok; ++tl) {
+      if (lane < k) {
+        const size_t aidx = (size_t)(t0 + tl) * k + lane;
+        const int e = s_e[tl * k + lane];
+        if (e < 0 || e >= E) {
+          set_error(err, kDevCheck);
+        } else {
+          const int g = s_next[e]++;  // distinct experts within a token: no two lanes share e
+          if (g < 0 || g >= T * k) {
+            set_error(err, kDevCheck);
+          } else {
+            perm[g] = (int)aidx;
+            pos[aidx] = g;
+          }
+        }
+      }
+      __syncwarp();
+    }
   }
 }
 
@@ -500,15 +499,31 @@ combine_kernel(const uint16_t* __restrict__ y, const uint16_t* __restrict__ ys, 
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int r = pos[(size_t)t * k + j];
-      if (r < 0 || r >= T * k) { set_error(err, kDevCheck); continue; }
-      const float wt = w[(size_t)t * k + j];
-      const uint4 v = *reinterpret_cast<const uint4*>(y + (size_t)r * H + 8 * c);
-      acc[0] = fmaf(wt, bf16_lo(v.x), acc[0]); acc[1] = fmaf(wt, bf16_hi(v.x), acc[1]);
-      acc[2] = fmaf(wt, bf16_lo(v.y), acc[2]); acc[3] = fmaf(wt, bf16_hi(v.y), acc[3]);
-      acc[4] = fmaf(wt, bf16_lo(v.z), acc[4]); acc[5] = fmaf(wt, bf16_hi(v.z), acc[5]);
-      acc[6] = fmaf(wt, bf16_lo(v.w), acc[6]); acc[7] = fmaf(wt, bf16_hi(v.w), acc[7]);
+    uint4 yv[kMaxTopK];
+    float wt[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {  // issue all row loads first
+      wt[j] = 0.f;
+      if (j < k) {
+        const int r = pos[(size_t)t * k + j];
+        if (r < 0 || r >= T * k) {
+          set_error(err, kDevCheck);
+        } else {
+          wt[j] = w[(size_t)t * k + j];
+          yv[j] = *reinterpret_cast<const uint4*>(y + (size_t)r * H + 8 * c);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {  // then add them in j order
+      if (j < k && wt[j] != 0.f) {
+        const uint4 v = yv[j];
+        const float wtj = wt[j];
+        acc[0] = fmaf(wtj, bf16_lo(v.x), acc[0]); acc[1] = fmaf(wtj, bf16_hi(v.x), acc[1]);
+        acc[2] = fmaf(wtj, bf16_lo(v.y), acc[2]); acc[3] = fmaf(wtj, bf16_hi(v.y), acc[3]);
+        acc[4] = fmaf(wtj, bf16_lo(v.z), acc[4]); acc[5] = fmaf(wtj, bf16_hi(v.z), acc[5]);
+        acc[6] = fmaf(wtj, bf16_lo(v.w), acc[6]); acc[7] = fmaf(wtj, bf16_hi(v.w), acc[7]);
+      }
     }
     if (has_shared) {
       const uint4 v = *reinterpret_cast<const uint4*>(ys + (size_t)t * H + 8 * c);
@@ -676,7 +691,7 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
     GemmParams p = base;
     p.mtiles = nullptr; p.num_routed = nullptr;
     p.BN = m->router_bn;
-    p.n_routed_static = mt_tokens; p.nt_routed = E / p.BN; p.ks_part = H / BK; p.ks_routed = 3 * (H / BK);
+    p.n_routed_static = mt_tokens; p.nt_routed = E / p.BN; p.ks_part = H / BK; p.ks_routed = H / BK;
     p.n_shared_mtiles = 0; p.nt_shared = 1; p.ks_shared = 0;
     p.logits = g.logits; p.router_bias = L->router_bias; p.logit_bias = logit_bias;
     const int tiles = mt_tokens * p.nt_routed;
@@ -686,10 +701,10 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
   }
   prof_mark(L, s);
   // 2-4. top-k, histogram, scan, block map, scatter
-  e = launch_pdl(topk_hist_kernel, chunks, 256, 0, s, (const float*)g.logits, T, E, k, g.idx, g.weights,
+  e = launch_pdl(topk_hist_kernel, chunks, 1024, 0, s, (const float*)g.logits, T, E, k, g.idx, g.weights,
                  g.chunk_counts);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(dispatch_scan_kernel, 1, 512, 0, s, g.chunk_counts, chunks, E, T, k, g.hist, g.offsets,
+  e = launch_pdl(dispatch_scan_kernel, 1, 1024, 0, s, g.chunk_counts, chunks, E, T, k, g.hist, g.offsets,
                  (int2*)g.tiles, g.num_tiles, g.max_tiles, L->err);
   if (e != cudaSuccess) return e;
   e = launch_pdl(dispatch_scatter_kernel, chunks, 256, 0, s, (const int*)g.idx, (const int*)g.chunk_counts,
