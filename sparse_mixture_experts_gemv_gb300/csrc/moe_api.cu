@@ -87,6 +87,23 @@ __global__ void split3_bf16_kernel(const float* __restrict__ w, uint16_t* __rest
   }
 }
 
+// down [E][H][I] -> the third row of each record: rec[(e * I + i) * 3 + 2][n] = down[e][n][i].
+__global__ void down_to_columns_kernel(const uint16_t* __restrict__ down, uint16_t* __restrict__ rec, int H, int I) {
+  __shared__ uint16_t tile[32][33];
+  const size_t e = blockIdx.z;
+  const int i = blockIdx.x * 32 + threadIdx.x;
+  for (int r0 = 0; r0 < 32; r0 += 8) {
+    const int n = blockIdx.y * 32 + threadIdx.y + r0;
+    if (n < H && i < I) tile[threadIdx.y + r0][threadIdx.x] = down[(e * H + n) * I + i];
+  }
+  __syncthreads();
+  const int n = blockIdx.y * 32 + threadIdx.x;
+  for (int r0 = 0; r0 < 32; r0 += 8) {
+    const int io = blockIdx.x * 32 + threadIdx.y + r0;
+    if (io < I && n < H) rec[((e * I + io) * 3 + 2) * H + n] = tile[threadIdx.x][threadIdx.y + r0];
+  }
+}
+
 moe_status_t validate(const moe_layer_config_t* c, const moe_layer_weights_t* w) {
   if (!c || !w) return MOE_ERR_INVALID_ARG;
   if (c->hidden <= 0 || c->num_experts <= 0 || c->top_k <= 0 || c->intermediate <= 0 ||
@@ -122,14 +139,17 @@ moe_status_t alloc_workspace(LayerOwner* o) {
   GET(L.dec.meta, sizeof(moe::DecodeMeta));
   GET(L.dec.h, sizeof(float) * (size_t)T8 * c.top_k * c.intermediate);
   GET(L.dec.h_shared, sizeof(float) * (size_t)T8 * std::max(c.shared_intermediate, 1));
-  GET(L.dec.sync_ctr, sizeof(unsigned long long) * 2);
+  GET(L.dec.sync_ctr, sizeof(unsigned long long) * 4);
+  GET(L.dec.logit_words, sizeof(unsigned long long) * T8 * c.num_experts);
+  GET(L.dec.partial, sizeof(float) * (size_t)L.num_sms * T8 * c.hidden);
   GET(L.err, sizeof(int) * 4);
   GET(L.never_set, sizeof(int));
   GET(L.x_stage, sizeof(uint16_t) * (size_t)c.max_tokens * c.hidden);
   GET(L.out_stage, sizeof(uint16_t) * (size_t)c.max_tokens * c.hidden);
   GET(L.bias_stage, sizeof(float) * (size_t)c.max_tokens * c.num_experts);
 #undef GET
-  cudaMemset(L.dec.sync_ctr, 0, sizeof(unsigned long long) * 2);
+  cudaMemset(L.dec.sync_ctr, 0, sizeof(unsigned long long) * 4);
+  cudaMemset(L.dec.logit_words, 0, sizeof(unsigned long long) * T8 * c.num_experts);
   cudaMemset(L.err, 0, sizeof(int) * 4);
   cudaMemset(L.never_set, 0, sizeof(int));
   cudaMemset(L.dec.meta, 0, sizeof(moe::DecodeMeta));
@@ -198,6 +218,27 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
     MOE_CUDA(cudaMemcpy2D((uint8_t*)L.ws_gu + row, 2 * row, w->shared_up_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
     MOE_CUDA(cudaMemcpy(L.ws_down, w->shared_down_dev, (size_t)H * Is * 2, cudaMemcpyDeviceToDevice));
   }
+
+  // Feature records for the record-streaming decode kernel: per (expert, i)
+  // the gate row, the up row and the down column, contiguous (6H bytes).
+  if (c.weight_format == MOE_WEIGHTS_BF16 && H <= 4096) {
+    const size_t row = (size_t)H * 2, rec = 3 * row;
+    GET(L.w_rec, (size_t)E * I * rec);
+    GET(L.ws_rec, std::max<int64_t>(Is, 1) * rec);
+    MOE_CUDA(cudaMemcpy2D(L.w_rec, rec, w->gate_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
+    MOE_CUDA(cudaMemcpy2D(L.w_rec + row, rec, w->up_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
+    dim3 block(32, 8), grid((unsigned)((I + 31) / 32), (unsigned)((H + 31) / 32), (unsigned)E);
+    down_to_columns_kernel<<<grid, block>>>((const uint16_t*)w->down_dev, (uint16_t*)L.w_rec, (int)H, (int)I);
+    MOE_CUDA(cudaGetLastError());
+    if (Is > 0) {
+      MOE_CUDA(cudaMemcpy2D(L.ws_rec, rec, w->shared_gate_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
+      MOE_CUDA(cudaMemcpy2D(L.ws_rec + row, rec, w->shared_up_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
+      dim3 g1((unsigned)((Is + 31) / 32), (unsigned)((H + 31) / 32), 1u);
+      down_to_columns_kernel<<<g1, block>>>((const uint16_t*)w->shared_down_dev, (uint16_t*)L.ws_rec, (int)H,
+                                             (int)Is);
+      MOE_CUDA(cudaGetLastError());
+    }
+  }
 #undef GET
   return MOE_OK;
 }
@@ -256,6 +297,7 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
     return st;
   }
   e = moe::decode_prepare(&L);
+  if (e == cudaSuccess) e = moe::stream_prepare(&L);
   if (e == cudaSuccess) e = moe::grouped_prepare(&L);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -265,12 +307,18 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
   }
   snprintf(L.describe, sizeof(L.describe),
            "moe_layer H=%d E=%d k=%d I=%d Is=%d format=%s max_tokens=%d | "
-           "T<=%d: decode GEMV path [moe_decode_fused_kernel<%s> (cooperative: router+shared, routed gate/up, down+combine)%s] | "
+           "T<=%d: decode GEMV path [%s] | "
            "T>%d: grouped path [grouped_router_tc, dispatch, grouped_gateup_tc (tcgen05), grouped_down_tc (tcgen05), combine]%s",
            cfg->hidden, cfg->num_experts, cfg->top_k, cfg->intermediate, cfg->shared_intermediate,
            cfg->weight_format == MOE_WEIGHTS_MXFP4 ? "mxfp4" : "bf16", cfg->max_tokens,
            (cfg->flags & MOE_FLAG_FORCE_GROUPED) ? 0 : L.decode_max_t,
-           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? "mxfp4" : "bf16", "",
+           moe::stream_supported(&L, 1)
+               ? "moe_decode_stream_kernel (cooperative: router with tagged logits, per-CTA top-k, bulk-copied "
+                 "[gate|up|down column] records of the shared and routed experts with the down projection fused, "
+                 "partial-output exchange)"
+               : (cfg->weight_format == MOE_WEIGHTS_MXFP4
+                      ? "moe_decode_fused_kernel<mxfp4> (cooperative: router+shared, routed gate/up, down+combine)"
+                      : "moe_decode_fused_kernel<bf16> (cooperative: router+shared, routed gate/up, down+combine)"),
            (cfg->flags & MOE_FLAG_FORCE_GROUPED) ? 0 : L.decode_max_t,
            (cfg->flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? " [test: forced wait timeout]" : "");
   *out = &o->L;
@@ -394,7 +442,8 @@ moe_status_t moe_layer_sync_status(moe_layer_t* L, void* stream) {
   MOE_CUDA(cudaMemcpy(&code, L->err, sizeof(int), cudaMemcpyDeviceToHost));
   MOE_CUDA(cudaMemset(L->err, 0, sizeof(int)));
   if (code != 0) {  // an aborted call can leave the grid-sync counters mid-generation
-    MOE_CUDA(cudaMemset(L->dec.sync_ctr, 0, sizeof(unsigned long long) * 2));
+    MOE_CUDA(cudaMemset(L->dec.sync_ctr, 0, sizeof(unsigned long long) * 4));
+    MOE_CUDA(cudaMemset(L->dec.logit_words, 0, sizeof(unsigned long long) * moe::kMaxDecodeT * L->cfg.num_experts));
   }
   if (code == moe::kDevTimeout) return MOE_ERR_TIMEOUT;
   if (code != 0) return MOE_ERR_DEVICE_CHECK;

@@ -40,6 +40,21 @@ MOE_DEV float f32_from_order_key(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// acc + sum of 8 bf16 weights times 8 bf16 activations, with the mixed-precision
+// FMA (bf16 inputs, fp32 accumulate; the bf16 product is exact in fp32).
+MOE_DEV float fma8_bf16(const uint4 w, const uint4 x, float acc) {
+  asm("{\n .reg .b16 w0, w1, w2, w3, w4, w5, w6, w7, x0, x1, x2, x3, x4, x5, x6, x7;\n"
+      " mov.b32 {w0, w1}, %1;\n mov.b32 {w2, w3}, %2;\n mov.b32 {w4, w5}, %3;\n mov.b32 {w6, w7}, %4;\n"
+      " mov.b32 {x0, x1}, %5;\n mov.b32 {x2, x3}, %6;\n mov.b32 {x4, x5}, %7;\n mov.b32 {x6, x7}, %8;\n"
+      " fma.rn.f32.bf16 %0, w0, x0, %0;\n fma.rn.f32.bf16 %0, w1, x1, %0;\n"
+      " fma.rn.f32.bf16 %0, w2, x2, %0;\n fma.rn.f32.bf16 %0, w3, x3, %0;\n"
+      " fma.rn.f32.bf16 %0, w4, x4, %0;\n fma.rn.f32.bf16 %0, w5, x5, %0;\n"
+      " fma.rn.f32.bf16 %0, w6, x6, %0;\n fma.rn.f32.bf16 %0, w7, x7, %0;\n}"
+      : "+f"(acc)
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w));
+  return acc;
+}
+
 // ---------------------------------------------------------------------------
 // Global loads.
 // ---------------------------------------------------------------------------
@@ -125,18 +140,14 @@ MOE_DEV void ce(uint32_t (&key)[G][8], int (&jj)[G][8], int g, int a, int b) {
   jj[g][a] = sw ? jb : ja; jj[g][b] = sw ? ja : jb;
 }
 
+// Top-k from keys already in registers: key[g][q] is the order key of expert
+// lane + 32 * (8 * g + q) (0 for experts >= E); jj is scratch.
 template <int G>
-MOE_DEV void warp_topk(const float* logits, int E, int k, int lane, int* out_e, float* out_w) {
-  uint32_t key[G][8];
-  int jj[G][8];
+MOE_DEV void warp_topk_keys(uint32_t (&key)[G][8], int (&jj)[G][8], int k, int lane, int* out_e, float* out_w) {
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = 8 * g + q, e = lane + 32 * j;
-      key[g][q] = (e < E) ? f32_order_key(ldg_cg_f32(logits + e)) : 0u;
-      jj[g][q] = j;
-    }
+    for (int q = 0; q < 8; ++q) jj[g][q] = 8 * g + q;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     ce<G>(key, jj, g, 0, 1); ce<G>(key, jj, g, 2, 3); ce<G>(key, jj, g, 4, 5); ce<G>(key, jj, g, 6, 7);
@@ -179,6 +190,20 @@ MOE_DEV void warp_topk(const float* logits, int E, int k, int lane, int* out_e, 
     out_e[lane] = my_e;
     out_w[lane] = my_ex / sum;
   }
+}
+
+template <int G>
+MOE_DEV void warp_topk(const float* logits, int E, int k, int lane, int* out_e, float* out_w) {
+  uint32_t key[G][8];
+  int jj[G][8];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int e = lane + 32 * (8 * g + q);
+      key[g][q] = (e < E) ? f32_order_key(ldg_cg_f32(logits + e)) : 0u;
+    }
+  warp_topk_keys<G>(key, jj, k, lane, out_e, out_w);
 }
 
 }  // namespace moe

@@ -73,21 +73,6 @@ __device__ __forceinline__ float dot8_bf16_f32(const uint4 w, const float4 a, co
   return s;
 }
 
-// acc + sum of 8 bf16 weights times 8 bf16 activations, with the mixed-precision
-// FMA (bf16 inputs, fp32 accumulate; the bf16 product is exact in fp32).
-__device__ __forceinline__ float fma8_bf16(const uint4 w, const uint4 x, float acc) {
-  asm("{\n .reg .b16 w0, w1, w2, w3, w4, w5, w6, w7, x0, x1, x2, x3, x4, x5, x6, x7;\n"
-      " mov.b32 {w0, w1}, %1;\n mov.b32 {w2, w3}, %2;\n mov.b32 {w4, w5}, %3;\n mov.b32 {w6, w7}, %4;\n"
-      " mov.b32 {x0, x1}, %5;\n mov.b32 {x2, x3}, %6;\n mov.b32 {x4, x5}, %7;\n mov.b32 {x6, x7}, %8;\n"
-      " fma.rn.f32.bf16 %0, w0, x0, %0;\n fma.rn.f32.bf16 %0, w1, x1, %0;\n"
-      " fma.rn.f32.bf16 %0, w2, x2, %0;\n fma.rn.f32.bf16 %0, w3, x3, %0;\n"
-      " fma.rn.f32.bf16 %0, w4, x4, %0;\n fma.rn.f32.bf16 %0, w5, x5, %0;\n"
-      " fma.rn.f32.bf16 %0, w6, x6, %0;\n fma.rn.f32.bf16 %0, w7, x7, %0;\n}"
-      : "+f"(acc)
-      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w));
-  return acc;
-}
-
 // Two e2m1 codes of one byte -> f16x2 (element 2i, the low nibble, in the low half).
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   uint32_t r;
@@ -796,6 +781,7 @@ static cudaError_t launch_decode_fmt(moe_layer* L, const uint16_t* x, uint16_t* 
 
 cudaError_t launch_decode(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
                           cudaStream_t s) {
+  if (stream_supported(L, T)) return launch_stream(L, x, out, T, logit_bias, s);
   if (L->cfg.weight_format == MOE_WEIGHTS_MXFP4) return launch_decode_fmt<FmtMXFP4>(L, x, out, T, logit_bias, s);
   return launch_decode_fmt<FmtBF16>(L, x, out, T, logit_bias, s);
 }

@@ -40,7 +40,9 @@ def cuda_layer(spec: mi.LayerSpec, max_tokens: int, flags: int = 0):
     """MoeLayer for a synthetic layer (cached per (spec, max_tokens, flags) in this process)."""
     from sparse_mixture_experts_gemv_gb300 import MoeLayer
     key = (spec, max_tokens, flags)
-    if key not in _layers:
+    if key in _layers:   # most recently used last, so eviction takes the least recently used
+        _layers[key] = _layers.pop(key)
+    else:
         # keep at most two big layers alive
         if len(_layers) >= 3:
             _layers.pop(next(iter(_layers))).close()

@@ -171,4 +171,4 @@ def test_forced_device_wait_timeout_reports_status():
 def test_describe_names_the_active_path():
     L = G.cuda_layer(mi.WORKLOADS["tiny"].layer, max_tokens=64)
     d = L.describe()
-    assert "decode GEMV path" in d and "moe_decode_fused_kernel<bf16>" in d
+    assert "decode GEMV path" in d and "moe_decode_stream_kernel" in d
