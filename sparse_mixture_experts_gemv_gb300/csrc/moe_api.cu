@@ -87,8 +87,10 @@ __global__ void split3_bf16_kernel(const float* __restrict__ w, uint16_t* __rest
   }
 }
 
-// down [E][H][I] -> the third row of each record: rec[(e * I + i) * 3 + 2][n] = down[e][n][i].
-__global__ void down_to_columns_kernel(const uint16_t* __restrict__ down, uint16_t* __restrict__ rec, int H, int I) {
+// down [E][H][I] -> the down column of each record: element n of the third
+// H-row of record (e, i) (records `stride` bytes apart) = down[e][n][i].
+__global__ void down_to_columns_kernel(const uint16_t* __restrict__ down, uint8_t* __restrict__ rec, int H, int I,
+                                       int stride) {
   __shared__ uint16_t tile[32][33];
   const size_t e = blockIdx.z;
   const int i = blockIdx.x * 32 + threadIdx.x;
@@ -100,7 +102,8 @@ __global__ void down_to_columns_kernel(const uint16_t* __restrict__ down, uint16
   const int n = blockIdx.y * 32 + threadIdx.x;
   for (int r0 = 0; r0 < 32; r0 += 8) {
     const int io = blockIdx.x * 32 + threadIdx.y + r0;
-    if (io < I && n < H) rec[((e * I + io) * 3 + 2) * H + n] = tile[threadIdx.x][threadIdx.y + r0];
+    if (io < I && n < H)
+      reinterpret_cast<uint16_t*>(rec + (e * I + io) * (size_t)stride + 4 * (size_t)H)[n] = tile[threadIdx.x][threadIdx.y + r0];
   }
 }
 
@@ -141,7 +144,7 @@ moe_status_t alloc_workspace(LayerOwner* o) {
   GET(L.dec.h_shared, sizeof(float) * (size_t)T8 * std::max(c.shared_intermediate, 1));
   GET(L.dec.sync_ctr, sizeof(unsigned long long) * 4);
   GET(L.dec.logit_words, sizeof(unsigned long long) * T8 * c.num_experts);
-  GET(L.dec.partial, sizeof(float) * (size_t)L.num_sms * T8 * c.hidden);
+  GET(L.dec.partial, sizeof(unsigned long long) * (size_t)L.num_sms * T8 * c.hidden);
   GET(L.err, sizeof(int) * 4);
   GET(L.never_set, sizeof(int));
   GET(L.x_stage, sizeof(uint16_t) * (size_t)c.max_tokens * c.hidden);
@@ -150,6 +153,7 @@ moe_status_t alloc_workspace(LayerOwner* o) {
 #undef GET
   cudaMemset(L.dec.sync_ctr, 0, sizeof(unsigned long long) * 4);
   cudaMemset(L.dec.logit_words, 0, sizeof(unsigned long long) * T8 * c.num_experts);
+  cudaMemset(L.dec.partial, 0, sizeof(unsigned long long) * (size_t)L.num_sms * T8 * c.hidden);
   cudaMemset(L.err, 0, sizeof(int) * 4);
   cudaMemset(L.never_set, 0, sizeof(int));
   cudaMemset(L.dec.meta, 0, sizeof(moe::DecodeMeta));
@@ -221,21 +225,22 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
 
   // Feature records for the record-streaming decode kernel: per (expert, i)
   // the gate row, the up row and the down column, contiguous (6H bytes).
-  if (c.weight_format == MOE_WEIGHTS_BF16 && H <= 4096) {
-    const size_t row = (size_t)H * 2, rec = 3 * row;
+  if (c.weight_format == MOE_WEIGHTS_BF16 && H <= moe::kStreamMaxHidden) {
+    const size_t row = (size_t)H * 2, rec = (size_t)moe::stream_record_stride((int)H);
     GET(L.w_rec, (size_t)E * I * rec);
     GET(L.ws_rec, std::max<int64_t>(Is, 1) * rec);
+    MOE_CUDA(cudaMemset(L.w_rec, 0, (size_t)E * I * rec));
+    MOE_CUDA(cudaMemset(L.ws_rec, 0, std::max<int64_t>(Is, 1) * rec));
     MOE_CUDA(cudaMemcpy2D(L.w_rec, rec, w->gate_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
     MOE_CUDA(cudaMemcpy2D(L.w_rec + row, rec, w->up_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
     dim3 block(32, 8), grid((unsigned)((I + 31) / 32), (unsigned)((H + 31) / 32), (unsigned)E);
-    down_to_columns_kernel<<<grid, block>>>((const uint16_t*)w->down_dev, (uint16_t*)L.w_rec, (int)H, (int)I);
+    down_to_columns_kernel<<<grid, block>>>((const uint16_t*)w->down_dev, L.w_rec, (int)H, (int)I, (int)rec);
     MOE_CUDA(cudaGetLastError());
     if (Is > 0) {
       MOE_CUDA(cudaMemcpy2D(L.ws_rec, rec, w->shared_gate_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
       MOE_CUDA(cudaMemcpy2D(L.ws_rec + row, rec, w->shared_up_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
       dim3 g1((unsigned)((Is + 31) / 32), (unsigned)((H + 31) / 32), 1u);
-      down_to_columns_kernel<<<g1, block>>>((const uint16_t*)w->shared_down_dev, (uint16_t*)L.ws_rec, (int)H,
-                                             (int)Is);
+      down_to_columns_kernel<<<g1, block>>>((const uint16_t*)w->shared_down_dev, L.ws_rec, (int)H, (int)Is, (int)rec);
       MOE_CUDA(cudaGetLastError());
     }
   }
@@ -444,6 +449,8 @@ moe_status_t moe_layer_sync_status(moe_layer_t* L, void* stream) {
   if (code != 0) {  // an aborted call can leave the grid-sync counters mid-generation
     MOE_CUDA(cudaMemset(L->dec.sync_ctr, 0, sizeof(unsigned long long) * 4));
     MOE_CUDA(cudaMemset(L->dec.logit_words, 0, sizeof(unsigned long long) * moe::kMaxDecodeT * L->cfg.num_experts));
+    MOE_CUDA(cudaMemset(L->dec.partial, 0,
+                        sizeof(unsigned long long) * (size_t)L->num_sms * moe::kMaxDecodeT * L->cfg.hidden));
   }
   if (code == moe::kDevTimeout) return MOE_ERR_TIMEOUT;
   if (code != 0) return MOE_ERR_DEVICE_CHECK;

@@ -33,10 +33,10 @@ struct DecodeWorkspace {
   DecodeMeta* meta;      // one
   float* h;              // [kMaxDecodeT * k][I]   SwiGLU outputs of routed assignments (t*k+j)
   float* h_shared;       // [kMaxDecodeT][Is]
-  unsigned long long* sync_ctr;   // [4] grid-sync arrival counters (monotonic): [0], [1] the
-                                  // three-phase kernel, [2] the record-streaming kernel
+  unsigned long long* sync_ctr;   // [4] monotonic counters: [0], [1] grid syncs of the
+                                  // three-phase kernel, [2] CTA exits of the record-streaming kernel
   unsigned long long* logit_words;  // [kMaxDecodeT][E] router logits tagged with the call
-  float* partial;        // [num_sms][kMaxDecodeT][H] per-CTA partial outputs
+  unsigned long long* partial;  // [num_sms][H][kMaxDecodeT] per-CTA partial outputs, tagged words
 };
 
 struct GroupedWorkspace {
@@ -74,9 +74,10 @@ struct moe_layer {
   uint8_t* w_down;       // routed down,    [E][H][row_bytes.down]
   uint16_t* ws_gu;       // shared gate/up bf16 [Is][2][H]
   uint16_t* ws_down;     // shared down bf16 [H][Is]
-  uint8_t* w_rec;        // routed records [E][I][3][H] bf16: gate row, up row, down column
-                         // (bf16 layers with H <= 4096; nullptr otherwise)
-  uint8_t* ws_rec;       // shared-expert records [Is][3][H] bf16 (same condition)
+  uint8_t* w_rec;        // routed records [E][I], each gate row | up row | down column (bf16,
+                         // H each) + zero padding: stream_record_stride(H) bytes
+                         // (bf16 layers with H <= kStreamMaxHidden; nullptr otherwise)
+  uint8_t* ws_rec;       // shared-expert records [Is], same record format
   moe::RowBytes row_bytes;
 
   moe::DecodeWorkspace dec;
@@ -115,6 +116,8 @@ size_t decode_smem_bytes_down(const moe_layer* L, int T);
 cudaError_t decode_prepare(moe_layer* L);
 // Record-streaming decode kernel (moe_stream.cu).
 bool stream_supported(const moe_layer* L, int T);
+int stream_record_stride(int H);          // bytes per routed/shared record (6H + padding)
+constexpr int kStreamMaxHidden = 2048;    // largest H the record-streaming kernel serves
 cudaError_t stream_prepare(moe_layer* L);
 cudaError_t launch_stream(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
                           cudaStream_t s);

@@ -21,19 +21,33 @@
 //
 // One cooperative launch, one CTA per SM, 16 consumer warps + 1 producer warp:
 //   producer   bulk-copies x, then this CTA's shared-expert records, then (once
-//              routing is known) its routed records, group by group, into a
-//              ring of slot groups in shared memory (full/empty mbarriers).
+//              routing is known) its routed records into a ring of slot groups in
+//              shared memory (full/empty mbarriers). Consecutive features of one
+//              expert are adjacent in HBM, so a group of records is one or two
+//              contiguous copies.
 //   router     each CTA computes its 1-4 fp32 router logits and publishes each
 //              as a 64-bit word {call tag, value}; readers poll until every
 //              word carries the current call's tag (no separate barrier).
 //   top-k      every CTA derives the routing from the published logits
 //              (identical inputs and arithmetic on every CTA).
-//   groups     4 records per group; 4 warps per record compute the gate/up dot
-//              products over a quarter of H each; then every thread adds
-//              w * h * down[n] for its own 4-output slices.
-//   exchange   partial outputs [T][H] fp32 per CTA -> global; one bounded grid
-//              barrier; each CTA sums its slice of outputs over all CTAs in a
-//              fixed order (deterministic) and writes bf16.
+//   groups     up to 8 records per group. The gate/up dot products of the group
+//              are one 16-row x T-token tile: each warp multiplies its 1/16 of H
+//              on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 out, rows
+//              read with ldmatrix straight from the bulk-copied records), the 16
+//              partial tiles are added in warp order, and c = w * silu(g) * u is
+//              formed per (record, token). The down projection is a second tile
+//              product: out[n][t] += sum_r down_r[n] * c[r][t] (m16n8k8, c split
+//              exactly enough into two bf16 terms hi + lo), each warp owning
+//              fixed 16-row tiles of the output in registers across all groups.
+//              At batch 1 the layer is bound by HBM; the tensor cores are used
+//              here only because they do these small products in far fewer
+//              instructions than scalar FMAs, which keeps the consumers ahead of
+//              the copies.
+//   exchange   each CTA publishes its partial outputs [H][T] as 64-bit words
+//              {call tag, fp32 value}; each CTA polls the words of its slice of
+//              outputs from every CTA until all carry this call's tag (no grid
+//              barrier, no separate read), adds them in a fixed order
+//              (deterministic) and writes bf16.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -50,12 +64,14 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kStreamThreads = kConsumers + 32;     // + one producer warp
-constexpr int kWarpsPerRecord = 4;
-constexpr int kGroupRecords = kConsumerWarps / kWarpsPerRecord;   // records per ring group
+constexpr int kMaxGroupRecords = 8;                 // records per ring group (one 16-row MMA tile)
 constexpr int kMaxRingGroups = 16;
 constexpr int kMaxRouterRows = 16;                  // router rows per CTA
-constexpr int kStreamSmemMax = 220 * 1024;          // dynamic shared memory budget
-constexpr int kMaxStreamH = 4096;
+constexpr int kStreamSmemMax = 212 * 1024;          // dynamic shared memory budget
+constexpr int kMaxStreamH = kStreamMaxHidden;       // output tiles per warp kept in registers: H / 256
+constexpr int kMaxTiles = kMaxStreamH / 256;
+constexpr int kMaxKSteps = kMaxStreamH / 16 / 16;    // 16-wide k-steps per warp in the gate/up tile
+constexpr int kRecPad = 16;                         // bytes after each record (bank spread for ldmatrix)
 constexpr long long kSpinBudget = 4000000000LL;     // ~2 s of SM cycles: then give up
 
 struct StreamArgs {
@@ -64,14 +80,15 @@ struct StreamArgs {
   const float* router_t;       // fp32 [E][H]
   const float* router_bias;    // fp32 [E]
   const float* logit_bias;     // fp32 [T][E] or nullptr
-  const uint8_t* rec;          // routed records [E][I][3][H] bf16
-  const uint8_t* rec_sh;       // shared-expert records [Is][3][H] bf16
-  int rec_bytes;               // 6 * H
+  const uint8_t* rec;          // routed records [E][I] x rec_stride bytes
+  const uint8_t* rec_sh;       // shared-expert records [Is] x rec_stride bytes
+  int rec_stride;              // 6 * H + kRecPad
+  int group_records;           // records per ring group (8, or 4 when x is large)
   int ring_groups;             // slot groups in the ring
-  int x_bytes_al;              // bytes of the x region (128-aligned)
+  int x_bytes_al;              // bytes of the x region (T rows of H + 8 bf16, 128-aligned)
   unsigned long long* words;   // [kMaxDecodeT][E] tagged logits
-  float* partial;              // [G][T][H] per-CTA partial outputs
-  unsigned long long* ctr;     // monotonic arrival counter of the final exchange
+  unsigned long long* partial; // [G][H][T] per-CTA partial outputs, tagged words
+  unsigned long long* ctr;     // calls completed x G (each CTA adds 1 when it leaves)
   int* idx;                    // [T][k]  diagnostics (CTA 0)
   float* weights;              // [T][k]
   DecodeMeta* meta;
@@ -93,16 +110,36 @@ MOE_DEV unsigned long long ld_relaxed_u64_nc(const unsigned long long* p) {
   asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p));
   return v;
 }
-MOE_DEV unsigned long long ld_acquire_u64_g(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
 MOE_DEV void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
+MOE_DEV void st_relaxed_v2u64(unsigned long long* p, unsigned long long v0, unsigned long long v1) {
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" :: "l"(p), "l"(v0), "l"(v1) : "memory");
+}
+MOE_DEV void ld_relaxed_v2u64(const unsigned long long* p, unsigned long long& v0, unsigned long long& v1) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(v0), "=l"(v1) : "l"(p));
+}
+MOE_DEV unsigned long long tagged(unsigned long long tag, float v) {
+  return (tag << 32) | (unsigned long long)__float_as_uint(v);
+}
 // Barrier among the 16 consumer warps only (the producer warp never joins it).
 MOE_DEV void consumers_sync() { asm volatile("bar.sync 1, %0;" :: "n"(kConsumers) : "memory"); }
+
+// Warp-level tensor-core fragments (PTX ldmatrix / mma.sync).
+MOE_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+MOE_DEV void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+// D = A(16x16, row) * B(16x8, col) + D; bf16 inputs, fp32 accumulators.
+MOE_DEV void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+               "{%0, %1, %2, %3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 // Record range of this CTA. Shared-expert records [sh0, sh1) are known before
 // routing; routed records [u0, u1) index the window's D x I (slot, feature)
@@ -168,15 +205,16 @@ MOE_DEV bool poll_topk(const unsigned long long* words, int E, int k, unsigned l
 template <int TMAX>
 __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(const StreamArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);   // x [T][H] bf16
-  uint8_t* ring = smem + a.x_bytes_al;                // ring_groups x kGroupRecords records
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);   // x [T][H + 8] bf16 (row pitch spreads banks)
+  uint8_t* ring = smem + a.x_bytes_al;                // ring_groups x group_records records
 
   __shared__ __align__(8) uint64_t full_bar[kMaxRingGroups];
   __shared__ __align__(8) uint64_t empty_bar[kMaxRingGroups];
   __shared__ __align__(8) uint64_t x_bar;
-  __shared__ float s_rpart[kConsumerWarps][TMAX];                    // router partial sums
-  __shared__ float s_gu[kGroupRecords][kWarpsPerRecord][TMAX][2];    // gate/up partial dots
-  __shared__ float s_c[kGroupRecords][TMAX];                         // w * h per record, token
+  __shared__ float s_rpart[kConsumerWarps][TMAX];                 // router partial sums
+  __shared__ __align__(16) float s_part[kConsumerWarps][16][8];   // gate/up partial tiles [warp][row][token]
+  __shared__ __align__(16) uint16_t s_chi[8][8], s_clo[8][8];     // c = w * h as bf16 hi + lo, [token][record]
+  __shared__ __align__(16) uint16_t s_zero[8];                    // a zero row for missing records
   __shared__ int s_idx[kMaxDecodeT * kMaxTopK];
   __shared__ float s_w[kMaxDecodeT * kMaxTopK];
   __shared__ int s_slot_of[kMaxDecodeT * kMaxTopK];
@@ -186,10 +224,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
   __shared__ int s_abort;
 
   const int T = a.T, H = a.H, E = a.E, k = a.k, I = a.I, Is = a.Is;
+  const int XP = H + 8;                               // x row pitch (elements)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, b = blockIdx.x;
-  const int NG = a.ring_groups;
-  const int rec_bytes = a.rec_bytes;
+  const int NG = a.ring_groups, RG = a.group_records;
+  const int stride = a.rec_stride;
   const bool producer = (warp == kConsumerWarps);
 
   if (threadIdx.x == 0) {
@@ -200,54 +239,59 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
     sm100::mbar_init(&x_bar, 1);
     sm100::fence_barrier_init();
     s_abort = 0;
-    // Calls completed so far = arrivals at the final exchange / G; no CTA of
-    // this call arrives there before every CTA has published its logits, which
-    // each does after reading this value.
+    // Every CTA adds 1 to ctr when it leaves, so at the start of a call
+    // ctr / G = calls completed. No CTA of this call leaves before it has read
+    // every CTA's partial outputs, which each CTA publishes after reading ctr.
     s_tag = ld_relaxed_u64(a.ctr) / (unsigned long long)G + 1ull;
   }
+  if (threadIdx.x < 8) s_zero[threadIdx.x] = 0;
   __syncthreads();
   const unsigned long long tag = s_tag;
+  // Every exit path of every CTA calls this exactly once (thread 0), after the
+  // CTA has read everything of this call that other CTAs publish.
+  auto leave = [&]() { atomicAdd(a.ctr, 1ull); };
 
   const Ranges rg0 = cta_ranges(b, G, Is, 0);   // shared range does not depend on routing
   const int ns = rg0.sh1 - rg0.sh0;
-  const int nsg = (ns + kGroupRecords - 1) / kGroupRecords;    // shared groups
+  const int nsg = (ns + RG - 1) / RG;           // shared groups
 
   // ---------------------------------------------------------------- producer: x + shared records
-  // Whole producer warp: lane 0 posts the group's byte count, then lane r
-  // copies record r of the group.
+  // Whole producer warp: lane 0 posts the group's byte count and copies each
+  // contiguous run of records (a routed group may cross from one expert's last
+  // feature to the next slot's first).
   auto issue_group = [&](int grp, int u0, int nr) {
     const int sg = grp % NG;
-    int first, n;
-    if (grp < nsg) {
-      first = grp * kGroupRecords;
-      n = min(kGroupRecords, ns - first);
-    } else {
-      first = (grp - nsg) * kGroupRecords;
-      n = min(kGroupRecords, nr - first);
-    }
-    if (lane == 0) sm100::mbar_arrive_expect_tx(&full_bar[sg], (uint32_t)(n * rec_bytes));
-    __syncwarp();
-    if (lane < n) {
-      const uint8_t* src;
+    uint8_t* dst = ring + (size_t)sg * RG * stride;
+    if (lane == 0) {
       if (grp < nsg) {
-        src = a.rec_sh + (size_t)(rg0.sh0 + first + lane) * rec_bytes;
+        const int first = grp * RG, n = min(RG, ns - first);
+        sm100::mbar_arrive_expect_tx(&full_bar[sg], (uint32_t)(n * stride));
+        sm100::bulk_copy_g2s(dst, a.rec_sh + (size_t)(rg0.sh0 + first) * stride, (uint32_t)(n * stride),
+                             &full_bar[sg]);
       } else {
-        const unsigned u = (unsigned)(u0 + first + lane);
-        const unsigned d = u / (unsigned)I, i = u - d * (unsigned)I;
-        src = a.rec + ((size_t)s_meta.slot_expert[d] * I + i) * rec_bytes;
+        const int first = (grp - nsg) * RG, n = min(RG, nr - first);
+        sm100::mbar_arrive_expect_tx(&full_bar[sg], (uint32_t)(n * stride));
+        unsigned u = (unsigned)(u0 + first);
+        int left = n;
+        while (left > 0) {
+          const unsigned d = u / (unsigned)I, i = u - d * (unsigned)I;
+          const int run = min(left, I - (int)i);
+          sm100::bulk_copy_g2s(dst, a.rec + ((size_t)s_meta.slot_expert[d] * I + i) * stride, (uint32_t)(run * stride),
+                               &full_bar[sg]);
+          dst += (size_t)run * stride;
+          u += run;
+          left -= run;
+        }
       }
-      sm100::bulk_copy_g2s(ring + ((size_t)sg * kGroupRecords + lane) * rec_bytes, src, (uint32_t)rec_bytes,
-                           &full_bar[sg]);
     }
+    __syncwarp();
   };
   int issued = 0;   // groups issued (producer warp)
   if (producer) {
     if (lane == 0) {
-      const uint32_t xbytes = (uint32_t)(T * H * 2);
-      sm100::mbar_arrive_expect_tx(&x_bar, xbytes);
-      for (uint32_t off = 0; off < xbytes; off += 32768u)
-        sm100::bulk_copy_g2s(reinterpret_cast<uint8_t*>(xs) + off, reinterpret_cast<const uint8_t*>(a.x) + off,
-                             min(32768u, xbytes - off), &x_bar);
+      sm100::mbar_arrive_expect_tx(&x_bar, (uint32_t)(T * H * 2));
+      for (int t = 0; t < T; ++t)
+        sm100::bulk_copy_g2s(xs + (size_t)t * XP, a.x + (size_t)t * H, (uint32_t)(H * 2), &x_bar);
     }
     for (; issued < nsg && issued < NG; ++issued) issue_group(issued, 0, 0);
   }
@@ -288,7 +332,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
 #pragma unroll
             for (int t = 0; t < TMAX; ++t) {
               if (t < T) {
-                const uint2 xx = *reinterpret_cast<const uint2*>(xs + t * H + 4 * c);
+                const uint2 xx = *reinterpret_cast<const uint2*>(xs + t * XP + 4 * c);
                 float s = acc[t];
                 s = fmaf(__uint_as_float(v[q].x), bf16_lo(xx.x), s);
                 s = fmaf(__uint_as_float(v[q].y), bf16_hi(xx.x), s);
@@ -337,10 +381,23 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
         s_abort = 1;
       }
     }
-    consumers_sync();
+    if (T > 1) consumers_sync();
     // distinct experts of the window in first-appearance order (slots), and
     // for each slot the position j of its expert in each token's top-k
-    if (warp == 0) {
+    if (warp == 0 && T == 1) {   // one token: its k experts are the slots, in order
+      if (lane < k) {
+        const int e = s_idx[lane];
+        if (e < 0 || e >= E) {   // only NaN logits can get here
+          set_error(a.err, kDevCheck);
+          s_abort = 1;
+        }
+        s_meta.slot_expert[lane] = e;
+        s_tmask[lane] = 1u;
+#pragma unroll
+        for (int t = 0; t < kMaxDecodeT; ++t) s_meta.slot_j[lane][t] = (signed char)(t == 0 ? lane : -1);
+      }
+      if (lane == 0) s_meta.num_slots = k;
+    } else if (warp == 0) {
       const int n = T * k;
       bool first[2] = {false, false};
       int firstpos[2] = {0, 0};
@@ -390,6 +447,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
       sm100::mbar_wait(&x_bar, 0, a.err, &never, 20000000LL, false);
       for (int g2 = 0; g2 < nsg && g2 < NG; ++g2)
         sm100::mbar_wait(&full_bar[g2], 0, a.err, &never, 20000000LL, false);
+      leave();
     }
     return;
   }
@@ -397,8 +455,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
   const int D = s_meta.num_slots;
   const int U = D * I;
   const Ranges rg = cta_ranges(b, G, Is, U);
-  const int nr = (int)(rg.u1 - rg.u0);
-  const int ngroups = nsg + (nr + kGroupRecords - 1) / kGroupRecords;
+  const int nr = rg.u1 - rg.u0;
+  const int ngroups = nsg + (nr + RG - 1) / RG;
 
   if (b == 0 && !producer) {   // diagnostics copy of the routing
     for (int q = threadIdx.x; q < T * k; q += kConsumers) {
@@ -426,104 +484,98 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
   }
 
   // ---------------------------------------------------------------- consumers: groups
-  constexpr int NCH = kMaxStreamH / 4 / kConsumers;   // 4-output chunks per thread (2)
-  float acc[NCH][TMAX][4];
+  const int gq = lane >> 2, cq = lane & 3;       // mma fragment coordinates (row group, column pair)
+  const int ntile = H / 256;                      // 16-row output tiles per warp (warp w: tiles w, w + 16, ...)
+  const int kslice = H / kConsumerWarps;          // this warp's share of H in the gate/up products
+  const int k0w = warp * kslice;
+  float acc[kMaxTiles][4];
 #pragma unroll
-  for (int ci = 0; ci < NCH; ++ci)
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[ci][t][j] = 0.f;
+  for (int j = 0; j < kMaxTiles; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  const uint32_t xs_u32 = sm100::smem_u32(xs);
+  const uint32_t zero_u32 = sm100::smem_u32(s_zero);
 
-  const int H8 = H / 8, H4 = H / 4;
-  const int rr = warp / kWarpsPerRecord, qq = warp % kWarpsPerRecord;
-  const int cq0 = qq * H8 / kWarpsPerRecord, cq1 = (qq + 1) * H8 / kWarpsPerRecord;
   int grp = 0;
   for (; grp < ngroups; ++grp) {
     const int sg = grp % NG;
     const bool shared = grp < nsg;
-    const int first = shared ? grp * kGroupRecords : (grp - nsg) * kGroupRecords;
-    const int nvalid = min(kGroupRecords, (shared ? ns : nr) - first);
-    const uint8_t* gbase = ring + (size_t)sg * kGroupRecords * rec_bytes;
-    if (!sm100::mbar_wait(&full_bar[sg], (uint32_t)(grp / NG) & 1u, a.err, &s_abort, kSpinBudget)) {
-      // fall through to the barrier; every warp sees s_abort there
-    }
-    // gate/up dot products: warp (rr, qq) covers 16-byte chunks [cq0, cq1) of record rr
-    unsigned tmask = 0u;
-    if (rr < nvalid) {
-      tmask = shared ? (1u << T) - 1u : s_tmask[(unsigned)(rg.u0 + first + rr) / (unsigned)I];
-      const uint8_t* rec = gbase + (size_t)rr * rec_bytes;
-      float ag[TMAX], au[TMAX];
+    const int first = shared ? grp * RG : (grp - nsg) * RG;
+    const int nvalid = min(RG, (shared ? ns : nr) - first);
+    const uint32_t gbase = sm100::smem_u32(ring + (size_t)sg * RG * stride);
+    sm100::mbar_wait(&full_bar[sg], (uint32_t)(grp / NG) & 1u, a.err, &s_abort, kSpinBudget);
+
+    // gate/up: tile rows 0-7 = gate rows of records 0-7, rows 8-15 = their up rows;
+    // this warp covers K = [k0w, k0w + kslice)
+    {
+      const int q = lane >> 3, r = lane & 7;     // ldmatrix: lane supplies row r of matrix q
+      const uint32_t rowaddr = (r < nvalid) ? gbase + (uint32_t)(r * stride + ((q & 1) ? 2 * H : 0) + (q >> 1) * 16)
+                                            : zero_u32;
+      const bool real = r < nvalid;
+      float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // even / odd k-steps
+      const int nsteps = kslice / 16;
 #pragma unroll
-      for (int t = 0; t < TMAX; ++t) ag[t] = au[t] = 0.f;
-      for (int c = cq0 + lane; c < cq1; c += 32) {
-        const uint4 gv = *reinterpret_cast<const uint4*>(rec + 16 * c);
-        const uint4 uv = *reinterpret_cast<const uint4*>(rec + 2 * H + 16 * c);
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t) {
-          if (t < T && ((tmask >> t) & 1u)) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * H + 8 * c);
-            ag[t] = fma8_bf16(gv, xv, ag[t]);
-            au[t] = fma8_bf16(uv, xv, au[t]);
+      for (int st = 0; st < kMaxKSteps; ++st) {
+        if (st < nsteps) {
+          const int kabs = k0w + 16 * st;
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(real ? rowaddr + 2 * kabs : zero_u32, a0, a1, a2, a3);
+          uint32_t b0 = 0u, b1 = 0u;
+          if (gq < T) {
+            const uint32_t xa = xs_u32 + (uint32_t)(2 * (gq * XP + kabs + 2 * cq));
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b0) : "r"(xa));
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b1) : "r"(xa + 16));
           }
+          mma_16816(d[st & 1], a0, a1, a2, a3, b0, b1);
         }
       }
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        if (t < T && ((tmask >> t) & 1u)) {
-          const float gs = warp_sum(ag[t]);
-          const float us = warp_sum(au[t]);
-          if (lane == 0) {
-            s_gu[rr][qq][t][0] = gs;
-            s_gu[rr][qq][t][1] = us;
-          }
-        }
-      }
+      *reinterpret_cast<float2*>(&s_part[warp][gq][2 * cq]) = make_float2(d[0][0] + d[1][0], d[0][1] + d[1][1]);
+      *reinterpret_cast<float2*>(&s_part[warp][gq + 8][2 * cq]) = make_float2(d[0][2] + d[1][2], d[0][3] + d[1][3]);
     }
     consumers_sync();
-    if ((int)threadIdx.x < kGroupRecords * TMAX) {   // c = w * silu(g) * u per (record, token)
-      const int r = threadIdx.x / TMAX, t = threadIdx.x - r * TMAX;
+    if ((int)threadIdx.x < 128) {   // c = w * silu(g) * u per (record r, token t), as bf16 hi + lo
+      // two lanes per (r, t): each adds half of the 16 warp partials, then they swap
+      const int r = threadIdx.x >> 4, t = (threadIdx.x >> 1) & 7, hf = threadIdx.x & 1;
+      float g = 0.f, u = 0.f;
+#pragma unroll
+      for (int q = 0; q < kConsumerWarps / 2; ++q) {
+        g += s_part[hf * 8 + q][r][t];
+        u += s_part[hf * 8 + q][r + 8][t];
+      }
+      g += __shfl_xor_sync(0xFFFFFFFFu, g, 1);
+      u += __shfl_xor_sync(0xFFFFFFFFu, u, 1);
       float c = 0.f;
       if (r < nvalid && t < T) {
         int j = -1;
         float w = 1.f;
         if (!shared) {
-          const int d = (int)((unsigned)(rg.u0 + first + r) / (unsigned)I);
-          j = s_meta.slot_j[d][t];
+          const int dd = (int)((unsigned)(rg.u0 + first + r) / (unsigned)I);
+          j = s_meta.slot_j[dd][t];
           if (j >= 0) w = s_w[t * k + j];
         }
-        if (shared || j >= 0) {
-          float g = 0.f, u = 0.f;
-#pragma unroll
-          for (int q = 0; q < kWarpsPerRecord; ++q) {
-            g += s_gu[r][q][t][0];
-            u += s_gu[r][q][t][1];
-          }
-          c = w * swiglu(g, u);
-        }
+        if (shared || j >= 0) c = w * swiglu(g, u);
       }
-      s_c[r][t] = c;
+      if (hf == 0) {
+        const uint16_t hi = f32_to_bf16_rne(c);
+        s_chi[t][r] = hi;
+        s_clo[t][r] = f32_to_bf16_rne(c - __uint_as_float((uint32_t)hi << 16));
+      }
     }
     consumers_sync();
     if (s_abort) break;
-    // down columns: out[t][n] += c[r][t] * down_r[n] for this thread's 4-output chunks
+    // down: out[n][t] += sum_r down_r[n] * c[r][t] for this warp's output tiles
+    {
+      const uint32_t bhi = *reinterpret_cast<const uint32_t*>(&s_chi[gq][2 * cq]);
+      const uint32_t blo = *reinterpret_cast<const uint32_t*>(&s_clo[gq][2 * cq]);
+      const int r = lane & 7, half = (lane >> 3) & 1;   // ldmatrix.x2: lanes 0-15 supply rows
+      const bool real = r < nvalid;
+      const uint32_t dbase = gbase + (uint32_t)(r * stride + 4 * H + half * 16);
 #pragma unroll
-    for (int ci = 0; ci < NCH; ++ci) {
-      const int ch = threadIdx.x + ci * kConsumers;
-      if (ch < H4) {
-        for (int r = 0; r < nvalid; ++r) {
-          const uint2 dv = *reinterpret_cast<const uint2*>(gbase + (size_t)r * rec_bytes + 4 * H + 8 * ch);
-          const float d0 = bf16_lo(dv.x), d1 = bf16_hi(dv.x), d2 = bf16_lo(dv.y), d3 = bf16_hi(dv.y);
-#pragma unroll
-          for (int t = 0; t < TMAX; ++t) {
-            const float c = (t < T) ? s_c[r][t] : 0.f;
-            if (c != 0.f) {
-              acc[ci][t][0] = fmaf(c, d0, acc[ci][t][0]);
-              acc[ci][t][1] = fmaf(c, d1, acc[ci][t][1]);
-              acc[ci][t][2] = fmaf(c, d2, acc[ci][t][2]);
-              acc[ci][t][3] = fmaf(c, d3, acc[ci][t][3]);
-            }
-          }
+      for (int j = 0; j < kMaxTiles; ++j) {
+        if (j < ntile) {
+          const int n0 = 16 * (warp + kConsumerWarps * j);
+          uint32_t a0, a1;
+          ldsm_x2_trans(real ? dbase + 2 * n0 : zero_u32, a0, a1);
+          // K = 16: records 0-7 against c_hi, the same records again against c_lo
+          mma_16816(acc[j], a0, a1, a0, a1, bhi, blo);
         }
       }
     }
@@ -536,29 +588,67 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
       volatile int never = 0;
       for (int g2 = grp; g2 < ngroups && g2 < grp + NG; ++g2)
         sm100::mbar_wait(&full_bar[g2 % NG], (uint32_t)(g2 / NG) & 1u, a.err, &never, 20000000LL, false);
+      leave();
     }
     return;
   }
 
   // ---------------------------------------------------------------- exchange of partial outputs
+  // Publish: acc[j] holds rows n0 + gq (regs 0, 1) and n0 + gq + 8 (regs 2, 3)
+  // for tokens 2 cq and 2 cq + 1; word (b, n, t) sits at (b * H + n) * TP + t
+  // (TP = T rounded up to even, so each token pair is one 16-byte store).
+  const int TP = T + (T & 1);
+  if (2 * cq < T) {
 #pragma unroll
-  for (int ci = 0; ci < NCH; ++ci) {
-    const int ch = threadIdx.x + ci * kConsumers;
-    if (ch < H4) {
+    for (int j = 0; j < kMaxTiles; ++j) {
+      if (j < ntile) {
+        const int n0 = 16 * (warp + kConsumerWarps * j);
 #pragma unroll
-      for (int t = 0; t < TMAX; ++t)
-        if (t < T)
-          *reinterpret_cast<float4*>(a.partial + ((size_t)b * T + t) * H + 4 * ch) =
-              make_float4(acc[ci][t][0], acc[ci][t][1], acc[ci][t][2], acc[ci][t][3]);
+        for (int h = 0; h < 2; ++h) {
+          const int n = n0 + gq + 8 * h;
+          st_relaxed_v2u64(a.partial + ((size_t)b * H + n) * TP + 2 * cq, tagged(tag, acc[j][2 * h]),
+                           tagged(tag, acc[j][2 * h + 1]));
+        }
+      }
     }
   }
-  consumers_sync();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(a.ctr, 1ull);
-    const unsigned long long target = tag * (unsigned long long)G;
+  // Collect: this CTA owns output rows [nb0, nb1) for every token. Each thread
+  // polls its share of the G x rows x TP words (16 bytes at a time) until they
+  // carry this call's tag and stages the values in shared memory (the ring is
+  // free now); then one warp per output adds the G partials in a fixed order.
+  const int nb0 = (int)((unsigned)b * (unsigned)H / (unsigned)G);
+  const int nb1 = (int)((unsigned)(b + 1) * (unsigned)H / (unsigned)G);
+  const int nrow = nb1 - nb0;
+  const int per = nrow * TP / 2;                      // 16-byte units per CTA partial
+  const int units = G * per;
+  float* stage = reinterpret_cast<float*>(ring);      // [G][nrow][TP]
+  const unsigned long long want = tag & 0xFFFFFFFFull;
+  for (int q0 = threadIdx.x; q0 < units; q0 += 8 * kConsumers) {
     const long long t0 = clock64();
-    while (ld_acquire_u64_g(a.ctr) < target) {
+    while (true) {
+      unsigned long long v[8][2];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int q = q0 + r * kConsumers;
+        v[r][0] = v[r][1] = want << 32;
+        if (q < units) {
+          const int p = q / per, w2 = q - p * per;
+          ld_relaxed_v2u64(a.partial + ((size_t)p * H + nb0) * TP + 2 * w2, v[r][0], v[r][1]);
+        }
+      }
+      bool ok = true;   // (the pad token of odd T is written too, so both words are checked)
+#pragma unroll
+      for (int r = 0; r < 8; ++r) ok &= (v[r][0] >> 32) == want && (v[r][1] >> 32) == want;
+      if (ok) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int q = q0 + r * kConsumers;
+          if (q < units)
+            *reinterpret_cast<float2*>(stage + 2 * (size_t)q) =
+                make_float2(__uint_as_float((uint32_t)v[r][0]), __uint_as_float((uint32_t)v[r][1]));
+        }
+        break;
+      }
       if (clock64() - t0 > kSpinBudget) {
         set_error(a.err, kDevTimeout);
         s_abort = 1;
@@ -567,56 +657,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
     }
   }
   consumers_sync();
-  if (s_abort) return;
-  // This CTA's outputs: 4-output chunks [c0, c1) of the T x H/4 chunks. Every
-  // (chunk, CTA partial) float4 is loaded at once into shared memory (the ring
-  // is free now), then one warp per chunk adds the G partials in a fixed order.
-  const int NC = T * H4;
-  const int c0 = (int)((unsigned)b * (unsigned)NC / (unsigned)G);
-  const int c1 = (int)((unsigned)(b + 1) * (unsigned)NC / (unsigned)G);
-  const int npairs = (c1 - c0) * G;
-  float4* stage = reinterpret_cast<float4*>(ring);   // [c1 - c0][G]
-  for (int q0 = threadIdx.x; q0 < npairs; q0 += 8 * kConsumers) {
-    uint4 v[8];
+  if (!s_abort) {
+    for (int o = warp; o < nrow * T; o += kConsumerWarps) {
+      const int nl = o / T, t = o - nl * T;
+      float sum = 0.f;
+      for (int p = lane; p < G; p += 32) sum += stage[((size_t)p * nrow + nl) * TP + t];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int q = q0 + r * kConsumers;
-      if (q < npairs) {
-        const int cc = q / G, p = q - cc * G;
-        const int cidx = c0 + cc;
-        const int t = cidx / H4, ch = cidx - t * H4;
-        v[r] = ldg_cg(a.partial + ((size_t)p * T + t) * H + 4 * ch);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int q = q0 + r * kConsumers;
-      if (q < npairs) stage[q] = make_float4(__uint_as_float(v[r].x), __uint_as_float(v[r].y),
-                                             __uint_as_float(v[r].z), __uint_as_float(v[r].w));
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+      if (lane == 0) a.out[(size_t)t * H + nb0 + nl] = f32_to_bf16_rne(sum);
     }
   }
   consumers_sync();
-  for (int cc = warp; cc < c1 - c0; cc += kConsumerWarps) {
-    float4 sacc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p = lane; p < G; p += 32) {
-      const float4 v = stage[cc * G + p];
-      sacc.x += v.x; sacc.y += v.y; sacc.z += v.z; sacc.w += v.w;
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      sacc.x += __shfl_xor_sync(0xFFFFFFFFu, sacc.x, o);
-      sacc.y += __shfl_xor_sync(0xFFFFFFFFu, sacc.y, o);
-      sacc.z += __shfl_xor_sync(0xFFFFFFFFu, sacc.z, o);
-      sacc.w += __shfl_xor_sync(0xFFFFFFFFu, sacc.w, o);
-    }
-    if (lane == 0) {
-      const int cidx = c0 + cc;
-      const int t = cidx / H4, ch = cidx - t * H4;
-      uint2 o2;
-      o2.x = (uint32_t)f32_to_bf16_rne(sacc.x) | ((uint32_t)f32_to_bf16_rne(sacc.y) << 16);
-      o2.y = (uint32_t)f32_to_bf16_rne(sacc.z) | ((uint32_t)f32_to_bf16_rne(sacc.w) << 16);
-      *reinterpret_cast<uint2*>(a.out + (size_t)t * H + 4 * ch) = o2;
-    }
-  }
+  if (threadIdx.x == 0) leave();
 }
 
 }  // namespace
@@ -624,10 +676,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
 // ===========================================================================
 // Host side
 // ===========================================================================
+static int stream_x_bytes(int T, int H) { return (int)(((size_t)T * (H + 8) * 2 + 127) / 128 * 128); }
+int stream_record_stride(int H) { return 6 * H + kRecPad; }
+// 8 records per group when two such groups fit beside x, else 4.
+static int stream_group_records(int T, int H) {
+  const size_t room = (size_t)kStreamSmemMax - (size_t)stream_x_bytes(T, H);
+  return room >= (size_t)2 * kMaxGroupRecords * stream_record_stride(H) ? kMaxGroupRecords : kMaxGroupRecords / 2;
+}
+
 static int stream_ring_groups(const moe_layer* L, int T) {
   const int H = L->cfg.hidden;
-  const size_t xb = ((size_t)T * H * 2 + 127) / 128 * 128;
-  const size_t gb = (size_t)kGroupRecords * 6 * H;
+  const size_t xb = (size_t)stream_x_bytes(T, H);
+  const size_t gb = (size_t)stream_group_records(T, H) * (6 * H + kRecPad);
   if (xb >= (size_t)kStreamSmemMax) return 0;
   return (int)std::min<size_t>((kStreamSmemMax - xb) / gb, kMaxRingGroups);
 }
@@ -635,13 +695,15 @@ static int stream_ring_groups(const moe_layer* L, int T) {
 bool stream_supported(const moe_layer* L, int T) {
   const auto& c = L->cfg;
   if (c.weight_format != MOE_WEIGHTS_BF16 || !L->w_rec) return false;
-  if (c.hidden > kMaxStreamH || T < 1 || T > kMaxDecodeT) return false;
+  if (c.hidden > kMaxStreamH || c.hidden % 256 != 0 || T < 1 || T > kMaxDecodeT) return false;
   if ((c.num_experts + L->num_sms - 1) / L->num_sms > kMaxRouterRows) return false;
   const int ng = stream_ring_groups(L, T);
   if (ng < 2) return false;
-  // the final exchange stages this CTA's (chunk, partial) pairs in the ring
-  const size_t chunks = ((size_t)T * c.hidden / 4 + L->num_sms - 1) / L->num_sms;
-  return chunks * L->num_sms * 16 <= (size_t)ng * kGroupRecords * 6 * c.hidden;
+  // the final exchange stages G x (rows of this CTA) x TP fp32 values in the ring
+  const size_t rows = ((size_t)c.hidden + L->num_sms - 1) / L->num_sms;
+  const size_t tp = (size_t)T + (T & 1);
+  return (size_t)L->num_sms * rows * tp * 4 <=
+         (size_t)ng * stream_group_records(T, c.hidden) * stream_record_stride(c.hidden);
 }
 
 template <int TMAX>
@@ -652,9 +714,10 @@ static cudaError_t launch_stream_t(moe_layer* L, const uint16_t* x, uint16_t* ou
   a.x = x; a.T = T; a.H = c.hidden; a.E = c.num_experts; a.k = c.top_k; a.I = c.intermediate;
   a.Is = c.shared_intermediate;
   a.router_t = L->router_t; a.router_bias = L->router_bias; a.logit_bias = lb;
-  a.rec = L->w_rec; a.rec_sh = L->ws_rec; a.rec_bytes = 6 * c.hidden;
+  a.rec = L->w_rec; a.rec_sh = L->ws_rec; a.rec_stride = stream_record_stride(c.hidden);
+  a.group_records = stream_group_records(T, c.hidden);
   a.ring_groups = stream_ring_groups(L, T);
-  a.x_bytes_al = (int)(((size_t)T * c.hidden * 2 + 127) / 128 * 128);
+  a.x_bytes_al = stream_x_bytes(T, c.hidden);
   a.words = L->dec.logit_words; a.partial = L->dec.partial; a.ctr = L->dec.sync_ctr + 2;
   a.idx = L->dec.idx; a.weights = L->dec.weights; a.meta = L->dec.meta;
   a.out = out; a.err = L->err; a.never_set = L->never_set;
@@ -663,7 +726,7 @@ static cudaError_t launch_stream_t(moe_layer* L, const uint16_t* x, uint16_t* ou
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L->num_sms);
   cfg.blockDim = dim3(kStreamThreads);
-  cfg.dynamicSmemBytes = (size_t)a.x_bytes_al + (size_t)a.ring_groups * kGroupRecords * a.rec_bytes;
+  cfg.dynamicSmemBytes = (size_t)a.x_bytes_al + (size_t)a.ring_groups * a.group_records * a.rec_stride;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs co-resident: they wait on one another
