@@ -293,6 +293,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
       for (int t = 0; t < T; ++t)
         sm100::bulk_copy_g2s(xs + (size_t)t * XP, a.x + (size_t)t * H, (uint32_t)(H * 2), &x_bar);
     }
+    // The shared-expert records go out once x has landed: issued at kernel
+    // start, their copies would queue ahead of x, the router rows and the
+    // router's logit exchange, all of which are on the critical path.
+    if (lane == 0) {
+      volatile int never = 0;
+      sm100::mbar_wait(&x_bar, 0, a.err, &never, kSpinBudget, false);
+    }
+    __syncwarp();
     for (; issued < nsg && issued < NG; ++issued) issue_group(issued, 0, 0);
   }
 
