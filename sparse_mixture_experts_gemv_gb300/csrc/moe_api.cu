@@ -107,6 +107,46 @@ __global__ void down_to_columns_kernel(const uint16_t* __restrict__ down, uint8_
   }
 }
 
+// MXFP4 down codes [E][H][I/2] (element (n, i) in nibble i & 1 of byte i / 2 of
+// row n) -> the down column of each record: byte m of record (e, i)'s column
+// holds elements n = 2m (low nibble) and 2m + 1. One block: 64 features x 64 rows.
+__global__ void mx_down_to_columns_kernel(const uint8_t* __restrict__ down, uint8_t* __restrict__ rec, int H, int I,
+                                          int stride, int col_off) {
+  __shared__ uint8_t tile[64][32];            // [row n][64 features as 32 code bytes]
+  const size_t e = blockIdx.z;
+  const int i0 = blockIdx.x * 64, n0 = blockIdx.y * 64;
+  const int t = threadIdx.x;
+  {
+    const int n = t >> 2, part = t & 3;
+    *reinterpret_cast<uint2*>(&tile[n][8 * part]) =
+        *reinterpret_cast<const uint2*>(down + (e * H + n0 + n) * (size_t)(I / 2) + i0 / 2 + 8 * part);
+  }
+  __syncthreads();
+  {
+    const int il = t >> 2, part = t & 3;        // feature i0 + il, output bytes 8 * part .. + 7
+    uint8_t o[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int m = 8 * part + q;               // rows 2m, 2m + 1 of the tile
+      const uint32_t lo = (tile[2 * m][il >> 1] >> (4 * (il & 1))) & 0xFu;
+      const uint32_t hi = (tile[2 * m + 1][il >> 1] >> (4 * (il & 1))) & 0xFu;
+      o[q] = (uint8_t)(lo | (hi << 4));
+    }
+    uint8_t* dst = rec + (e * I + i0 + il) * (size_t)stride + col_off + n0 / 2 + 8 * part;
+    *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(o);
+  }
+}
+
+// MXFP4 down scales [E][H][I/32] -> [E][I/32][H] (one vector per 32 features).
+__global__ void mx_down_scales_kernel(const uint8_t* __restrict__ ds, uint8_t* __restrict__ out, int E, int H,
+                                      int nblk) {
+  const size_t total = (size_t)E * nblk * H;
+  for (size_t o = blockIdx.x * (size_t)blockDim.x + threadIdx.x; o < total; o += (size_t)gridDim.x * blockDim.x) {
+    const size_t n = o % H, eb = o / H, blk = eb % nblk, e = eb / nblk;
+    out[o] = ds[(e * H + n) * nblk + blk];
+  }
+}
+
 moe_status_t validate(const moe_layer_config_t* c, const moe_layer_weights_t* w) {
   if (!c || !w) return MOE_ERR_INVALID_ARG;
   if (c->hidden <= 0 || c->num_experts <= 0 || c->top_k <= 0 || c->intermediate <= 0 ||
@@ -225,17 +265,40 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
 
   // Feature records for the record-streaming decode kernel: per (expert, i)
   // the gate row, the up row and the down column, contiguous (6H bytes).
-  if (c.weight_format == MOE_WEIGHTS_BF16 && H <= moe::kStreamMaxHidden) {
+  const bool bf16_stream = c.weight_format == MOE_WEIGHTS_BF16 && H <= moe::kStreamMaxHidden;
+  const bool mx_stream = c.weight_format == MOE_WEIGHTS_MXFP4 && H <= moe::kStreamMxMaxHidden;
+  if (bf16_stream || mx_stream) {
     const size_t row = (size_t)H * 2, rec = (size_t)moe::stream_record_stride((int)H);
-    GET(L.w_rec, (size_t)E * I * rec);
+    dim3 block(32, 8);
+    if (bf16_stream) {
+      GET(L.w_rec, (size_t)E * I * rec);
+      MOE_CUDA(cudaMemset(L.w_rec, 0, (size_t)E * I * rec));
+      MOE_CUDA(cudaMemcpy2D(L.w_rec, rec, w->gate_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
+      MOE_CUDA(cudaMemcpy2D(L.w_rec + row, rec, w->up_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
+      dim3 grid((unsigned)((I + 31) / 32), (unsigned)((H + 31) / 32), (unsigned)E);
+      down_to_columns_kernel<<<grid, block>>>((const uint16_t*)w->down_dev, L.w_rec, (int)H, (int)I, (int)rec);
+      MOE_CUDA(cudaGetLastError());
+    } else {
+      // MXFP4 records: gate codes | gate scales | up codes | up scales | down column codes
+      const size_t mxs = (size_t)moe::stream_mx_record_stride((int)H);
+      const size_t so = (size_t)((H / 32 + 15) / 16 * 16), nblk = (size_t)I / 32;
+      GET(L.w_mx, (size_t)E * I * mxs);
+      GET(L.mx_dsc, (size_t)E * nblk * H);
+      MOE_CUDA(cudaMemset(L.w_mx, 0, (size_t)E * I * mxs));
+      const size_t rows = (size_t)E * I;
+      MOE_CUDA(cudaMemcpy2D(L.w_mx, mxs, w->gate_dev, H / 2, H / 2, rows, cudaMemcpyDeviceToDevice));
+      MOE_CUDA(cudaMemcpy2D(L.w_mx + H / 2, mxs, w->gate_scales_dev, H / 32, H / 32, rows, cudaMemcpyDeviceToDevice));
+      MOE_CUDA(cudaMemcpy2D(L.w_mx + H / 2 + so, mxs, w->up_dev, H / 2, H / 2, rows, cudaMemcpyDeviceToDevice));
+      MOE_CUDA(cudaMemcpy2D(L.w_mx + H + so, mxs, w->up_scales_dev, H / 32, H / 32, rows, cudaMemcpyDeviceToDevice));
+      dim3 g2((unsigned)(I / 64), (unsigned)(H / 64), (unsigned)E);
+      mx_down_to_columns_kernel<<<g2, 256>>>((const uint8_t*)w->down_dev, L.w_mx, (int)H, (int)I, (int)mxs,
+                                             (int)(H + 2 * so));
+      MOE_CUDA(cudaGetLastError());
+      mx_down_scales_kernel<<<1024, 256>>>(w->down_scales_dev, L.mx_dsc, (int)E, (int)H, (int)nblk);
+      MOE_CUDA(cudaGetLastError());
+    }
     GET(L.ws_rec, std::max<int64_t>(Is, 1) * rec);
-    MOE_CUDA(cudaMemset(L.w_rec, 0, (size_t)E * I * rec));
     MOE_CUDA(cudaMemset(L.ws_rec, 0, std::max<int64_t>(Is, 1) * rec));
-    MOE_CUDA(cudaMemcpy2D(L.w_rec, rec, w->gate_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
-    MOE_CUDA(cudaMemcpy2D(L.w_rec + row, rec, w->up_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
-    dim3 block(32, 8), grid((unsigned)((I + 31) / 32), (unsigned)((H + 31) / 32), (unsigned)E);
-    down_to_columns_kernel<<<grid, block>>>((const uint16_t*)w->down_dev, L.w_rec, (int)H, (int)I, (int)rec);
-    MOE_CUDA(cudaGetLastError());
     if (Is > 0) {
       MOE_CUDA(cudaMemcpy2D(L.ws_rec, rec, w->shared_gate_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
       MOE_CUDA(cudaMemcpy2D(L.ws_rec + row, rec, w->shared_up_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
@@ -303,6 +366,7 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
   }
   e = moe::decode_prepare(&L);
   if (e == cudaSuccess) e = moe::stream_prepare(&L);
+  if (e == cudaSuccess) e = moe::stream_mx_prepare(&L);
   if (e == cudaSuccess) e = moe::grouped_prepare(&L);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -320,6 +384,10 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
            moe::stream_supported(&L, 1)
                ? "moe_decode_stream_kernel (cooperative: router with tagged logits, per-CTA top-k, bulk-copied "
                  "[gate|up|down column] records of the shared and routed experts with the down projection fused, "
+                 "partial-output exchange)"
+               : moe::stream_mx_supported(&L, 1)
+               ? "moe_decode_stream_mx_kernel (cooperative: router with tagged logits, per-CTA top-k, bulk-copied "
+                 "MXFP4 [gate|up|down column] records decoded in registers, bf16 shared-expert records, "
                  "partial-output exchange)"
                : (cfg->weight_format == MOE_WEIGHTS_MXFP4
                       ? "moe_decode_fused_kernel<mxfp4> (cooperative: router+shared, routed gate/up, down+combine)"

@@ -55,6 +55,24 @@ MOE_DEV float fma8_bf16(const uint4 w, const uint4 x, float acc) {
   return acc;
 }
 
+// Two e2m1 codes of one byte -> f16x2 (element 2i, the low nibble, in the low half).
+MOE_DEV uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// acc + sum over two f16 pairs: (w.lo * x.lo + w.hi * x.hi), fp32 accumulate.
+MOE_DEV float fma2_f16(uint32_t w, uint32_t x, float acc) {
+  asm("{\n .reg .b16 w0, w1, x0, x1;\n mov.b32 {w0, w1}, %1;\n mov.b32 {x0, x1}, %2;\n"
+      " fma.rn.f32.f16 %0, w0, x0, %0;\n fma.rn.f32.f16 %0, w1, x1, %0;\n}"
+      : "+f"(acc) : "r"(w), "r"(x));
+  return acc;
+}
+
+// e8m0 scale byte -> 2^(s - 127) as fp32 (s = 255, NaN, is never stored).
+MOE_DEV float e8m0_to_f32(uint32_t s) { return __uint_as_float(s ? (s << 23) : 0x00400000u); }
+
 // ---------------------------------------------------------------------------
 // Global loads.
 // ---------------------------------------------------------------------------

@@ -73,21 +73,6 @@ __device__ __forceinline__ float dot8_bf16_f32(const uint4 w, const float4 a, co
   return s;
 }
 
-// Two e2m1 codes of one byte -> f16x2 (element 2i, the low nibble, in the low half).
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(r) : "r"(byte));
-  return r;
-}
-
-// acc + sum over two f16 pairs: (w.lo * x.lo + w.hi * x.hi), fp32 accumulate.
-__device__ __forceinline__ float fma2_f16(uint32_t w, uint32_t x, float acc) {
-  asm("{\n .reg .b16 w0, w1, x0, x1;\n mov.b32 {w0, w1}, %1;\n mov.b32 {x0, x1}, %2;\n"
-      " fma.rn.f32.f16 %0, w0, x0, %0;\n fma.rn.f32.f16 %0, w1, x1, %0;\n}"
-      : "+f"(acc) : "r"(w), "r"(x));
-  return acc;
-}
-
 // Unscaled sum of 32 e2m1 codes (16 bytes) times 32 f16 activations at xs (shared, 16-byte aligned).
 __device__ __forceinline__ float dot32_e2m1_f16(const uint4 c, const uint16_t* xs) {
   const uint4* xv = reinterpret_cast<const uint4*>(xs);
@@ -782,6 +767,7 @@ static cudaError_t launch_decode_fmt(moe_layer* L, const uint16_t* x, uint16_t* 
 cudaError_t launch_decode(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
                           cudaStream_t s) {
   if (stream_supported(L, T)) return launch_stream(L, x, out, T, logit_bias, s);
+  if (stream_mx_supported(L, T)) return launch_stream_mx(L, x, out, T, logit_bias, s);
   if (L->cfg.weight_format == MOE_WEIGHTS_MXFP4) return launch_decode_fmt<FmtMXFP4>(L, x, out, T, logit_bias, s);
   return launch_decode_fmt<FmtBF16>(L, x, out, T, logit_bias, s);
 }

@@ -77,7 +77,10 @@ struct moe_layer {
   uint8_t* w_rec;        // routed records [E][I], each gate row | up row | down column (bf16,
                          // H each) + zero padding: stream_record_stride(H) bytes
                          // (bf16 layers with H <= kStreamMaxHidden; nullptr otherwise)
-  uint8_t* ws_rec;       // shared-expert records [Is], same record format
+  uint8_t* ws_rec;       // shared-expert records [Is], same record format (also for MXFP4 layers)
+  uint8_t* w_mx;         // MXFP4 routed records [E][I], stream_mx_record_stride(H) bytes each:
+                         // gate codes | gate scales | up codes | up scales | down column codes
+  uint8_t* mx_dsc;       // MXFP4 down scales [E][I / 32][H] (one H-byte vector per 32 features)
   moe::RowBytes row_bytes;
 
   moe::DecodeWorkspace dec;
@@ -117,6 +120,13 @@ cudaError_t decode_prepare(moe_layer* L);
 // Record-streaming decode kernel (moe_stream.cu).
 bool stream_supported(const moe_layer* L, int T);
 int stream_record_stride(int H);          // bytes per routed/shared record (6H + padding)
+// Record-streaming decode kernel for MXFP4 routed experts (moe_stream_mx.cu).
+bool stream_mx_supported(const moe_layer* L, int T);
+int stream_mx_record_stride(int H);       // bytes per routed MXFP4 record
+cudaError_t stream_mx_prepare(moe_layer* L);
+cudaError_t launch_stream_mx(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
+                             cudaStream_t s);
+constexpr int kStreamMxMaxHidden = 4096;  // largest H the MXFP4 streaming kernel serves
 constexpr int kStreamMaxHidden = 2048;    // largest H the record-streaming kernel serves
 cudaError_t stream_prepare(moe_layer* L);
 cudaError_t launch_stream(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,

@@ -56,23 +56,24 @@
 #include "moe_common.cuh"
 #include "moe_internal.h"
 #include "moe_sm100.cuh"
+#include "moe_stream_common.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kConsumerWarps = 16;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kStreamThreads = kConsumers + 32;     // + one producer warp
+using stream::kConsumerWarps;
+using stream::kConsumers;
+using stream::kMaxRingGroups;
+using stream::kMaxRouterRows;
+using stream::kSpinBudget;
+constexpr int kStreamThreads = stream::kThreads;
+constexpr int kStreamSmemMax = stream::kSmemMax;
 constexpr int kMaxGroupRecords = 8;                 // records per ring group (one 16-row MMA tile)
-constexpr int kMaxRingGroups = 16;
-constexpr int kMaxRouterRows = 16;                  // router rows per CTA
-constexpr int kStreamSmemMax = 212 * 1024;          // dynamic shared memory budget
 constexpr int kMaxStreamH = kStreamMaxHidden;       // output tiles per warp kept in registers: H / 256
 constexpr int kMaxTiles = kMaxStreamH / 256;
 constexpr int kMaxKSteps = kMaxStreamH / 16 / 16;    // 16-wide k-steps per warp in the gate/up tile
 constexpr int kRecPad = 16;                         // bytes after each record (bank spread for ldmatrix)
-constexpr long long kSpinBudget = 4000000000LL;     // ~2 s of SM cycles: then give up
 
 struct StreamArgs {
   const uint16_t* x;           // bf16 [T][H]
@@ -98,32 +99,12 @@ struct StreamArgs {
   int force_timeout;
 };
 
-MOE_DEV unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-// Same load without a compiler memory barrier, so that a batch of them can be
-// issued back to back (each is still a single-copy-atomic relaxed load).
-MOE_DEV unsigned long long ld_relaxed_u64_nc(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p));
-  return v;
-}
-MOE_DEV void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
-}
-MOE_DEV void st_relaxed_v2u64(unsigned long long* p, unsigned long long v0, unsigned long long v1) {
-  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" :: "l"(p), "l"(v0), "l"(v1) : "memory");
-}
-MOE_DEV void ld_relaxed_v2u64(const unsigned long long* p, unsigned long long& v0, unsigned long long& v1) {
-  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(v0), "=l"(v1) : "l"(p));
-}
-MOE_DEV unsigned long long tagged(unsigned long long tag, float v) {
-  return (tag << 32) | (unsigned long long)__float_as_uint(v);
-}
-// Barrier among the 16 consumer warps only (the producer warp never joins it).
-MOE_DEV void consumers_sync() { asm volatile("bar.sync 1, %0;" :: "n"(kConsumers) : "memory"); }
+using stream::ld_relaxed_u64;
+using stream::st_relaxed_v2u64;
+using stream::tagged;
+using stream::consumers_sync;
+using stream::Ranges;
+using stream::cta_ranges;
 
 // Warp-level tensor-core fragments (PTX ldmatrix / mma.sync).
 MOE_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -141,67 +122,6 @@ MOE_DEV void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uin
                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Record range of this CTA. Shared-expert records [sh0, sh1) are known before
-// routing; routed records [u0, u1) index the window's D x I (slot, feature)
-// pairs. When there are at least G routed pairs the two ranges are balanced
-// jointly (a CTA with one more shared record gets one fewer routed record).
-// All counts fit 32 bits (U <= 64 slots x 4096 features, G < 1024), and the
-// kernel uses unsigned 32-bit division only: 64-bit division is a long
-// software sequence that would sit on the producer's critical path.
-struct Ranges {
-  int sh0, sh1;
-  int u0, u1;
-};
-MOE_DEV Ranges cta_ranges(unsigned b, unsigned G, unsigned Is, unsigned U) {
-  Ranges r;
-  r.sh0 = (int)(b * Is / G);
-  r.sh1 = (int)((b + 1) * Is / G);
-  if (U >= G) {
-    const unsigned N = U + Is;
-    r.u0 = (int)(b * N / G) - r.sh0;
-    r.u1 = (int)((b + 1) * N / G) - r.sh1;
-  } else {
-    r.u0 = (int)(b * U / G);
-    r.u1 = (int)((b + 1) * U / G);
-  }
-  return r;
-}
-
-// Poll one token's E tagged logit words until all carry `tag`, then select its
-// top-k (bounded: false after ~2 s without every word arriving).
-template <int GK>
-MOE_DEV bool poll_topk(const unsigned long long* words, int E, int k, unsigned long long tag, int lane, int* out_e,
-                       float* out_w) {
-  uint32_t key[GK][8];
-  int jj[GK][8];
-  const unsigned long long want = tag & 0xFFFFFFFFull;
-  const long long t0 = clock64();
-  bool ok = false;
-  while (true) {
-    unsigned long long w[GK][8];
-#pragma unroll
-    for (int g = 0; g < GK; ++g)   // every load in flight before any is used
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int e = lane + 32 * (8 * g + q);
-        w[g][q] = (e < E) ? ld_relaxed_u64_nc(words + e) : (want << 32);
-      }
-    bool mine = true;
-#pragma unroll
-    for (int g = 0; g < GK; ++g)
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int e = lane + 32 * (8 * g + q);
-        mine &= (w[g][q] >> 32) == want;
-        key[g][q] = (e < E) ? f32_order_key(__uint_as_float((uint32_t)w[g][q])) : 0u;
-      }
-    ok = __all_sync(0xFFFFFFFFu, mine);
-    if (ok || clock64() - t0 > kSpinBudget) break;
-  }
-  warp_topk_keys<GK>(key, jj, k, lane, out_e, out_w);
-  return ok;
-}
-
 template <int TMAX>
 __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(const StreamArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -215,11 +135,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
   __shared__ __align__(16) float s_part[kConsumerWarps][16][8];   // gate/up partial tiles [warp][row][token]
   __shared__ __align__(16) uint16_t s_chi[8][8], s_clo[8][8];     // c = w * h as bf16 hi + lo, [token][record]
   __shared__ __align__(16) uint16_t s_zero[8];                    // a zero row for missing records
-  __shared__ int s_idx[kMaxDecodeT * kMaxTopK];
-  __shared__ float s_w[kMaxDecodeT * kMaxTopK];
-  __shared__ int s_slot_of[kMaxDecodeT * kMaxTopK];
-  __shared__ unsigned s_tmask[kMaxSlots];
-  __shared__ DecodeMeta s_meta;
+  __shared__ stream::RouteSmem rs;
   __shared__ unsigned long long s_tag;
   __shared__ int s_abort;
 
@@ -276,7 +192,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
         while (left > 0) {
           const unsigned d = u / (unsigned)I, i = u - d * (unsigned)I;
           const int run = min(left, I - (int)i);
-          sm100::bulk_copy_g2s(dst, a.rec + ((size_t)s_meta.slot_expert[d] * I + i) * stride, (uint32_t)(run * stride),
+          sm100::bulk_copy_g2s(dst, a.rec + ((size_t)rs.meta.slot_expert[d] * I + i) * stride, (uint32_t)(run * stride),
                                &full_bar[sg]);
           dst += (size_t)run * stride;
           u += run;
@@ -304,148 +220,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
     for (; issued < nsg && issued < NG; ++issued) issue_group(issued, 0, 0);
   }
 
-  // ---------------------------------------------------------------- consumers: router logits
-  const int nr_rows = (E - b + G - 1) / G;   // router rows b, b + G, ... (<= kMaxRouterRows)
+  // ---------------------------------------------------------------- consumers: router logits, routing
   if (!producer) {
-    const int P = max(1, kConsumerWarps / max(nr_rows, 1));     // warps per row
-    const int items = nr_rows * P;
-    const int H4 = H / 4;
     if (threadIdx.x == 0 && a.force_timeout && b == 0 && !bounded_wait_flag(a.never_set, 2000000LL))
       set_error(a.err, kDevTimeout);
-    if (warp < items) {
-      const int m = warp / P, p = warp - m * P;
-      const int e = b + m * G;
-      const float* row = a.router_t + (size_t)e * H;
-      const int c0 = p * H4 / P, c1 = (p + 1) * H4 / P;
-      float acc[TMAX];
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-      bool x_ready = false;
-      for (int cb = c0; cb < c1; cb += 32 * 8) {
-        uint4 v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = cb + lane + 32 * q;
-          if (c < c1) v[q] = ldg_stream(row + 4 * c);
-        }
-        if (!x_ready) {
-          volatile int never = 0;
-          if (!sm100::mbar_wait(&x_bar, 0, a.err, &never, kSpinBudget, false)) s_abort = 1;
-          x_ready = true;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = cb + lane + 32 * q;
-          if (c < c1) {
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              if (t < T) {
-                const uint2 xx = *reinterpret_cast<const uint2*>(xs + t * XP + 4 * c);
-                float s = acc[t];
-                s = fmaf(__uint_as_float(v[q].x), bf16_lo(xx.x), s);
-                s = fmaf(__uint_as_float(v[q].y), bf16_hi(xx.x), s);
-                s = fmaf(__uint_as_float(v[q].z), bf16_lo(xx.y), s);
-                s = fmaf(__uint_as_float(v[q].w), bf16_hi(xx.y), s);
-                acc[t] = s;
-              }
-            }
-          }
-        }
-      }
-      if (!x_ready) {
-        volatile int never = 0;
-        if (!sm100::mbar_wait(&x_bar, 0, a.err, &never, kSpinBudget, false)) s_abort = 1;
-      }
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        if (t < T) {
-          const float sum = warp_sum(acc[t]);
-          if (lane == 0) s_rpart[warp][t] = sum;
-        }
-      }
-    } else {
-      volatile int never = 0;   // x is needed later by every warp
-      if (!sm100::mbar_wait(&x_bar, 0, a.err, &never, kSpinBudget, false)) s_abort = 1;
-    }
-    consumers_sync();
-    if ((int)threadIdx.x < nr_rows * T) {   // logit = partial sums in warp order + biases
-      const int m = threadIdx.x / T, t = threadIdx.x - m * T;
-      const int e = b + m * G;
-      float sl = 0.f;
-      for (int p = 0; p < P; ++p) sl += s_rpart[m * P + p][t];
-      sl += a.router_bias[e];
-      if (a.logit_bias) sl += a.logit_bias[(size_t)t * E + e];
-      st_relaxed_u64(a.words + (size_t)t * E + e, (tag << 32) | (unsigned long long)__float_as_uint(sl));
-    }
-
-    // ------------------------------------------------------------ top-k of every token, in every CTA
-    if (warp < T) {
-      const int t = warp;
-      bool ok;
-      if (E <= 256) ok = poll_topk<1>(a.words + (size_t)t * E, E, k, tag, lane, s_idx + t * k, s_w + t * k);
-      else ok = poll_topk<2>(a.words + (size_t)t * E, E, k, tag, lane, s_idx + t * k, s_w + t * k);
-      if (!ok) {
-        if (lane == 0) set_error(a.err, kDevTimeout);
-        s_abort = 1;
-      }
-    }
-    if (T > 1) consumers_sync();
-    // distinct experts of the window in first-appearance order (slots), and
-    // for each slot the position j of its expert in each token's top-k
-    if (warp == 0 && T == 1) {   // one token: its k experts are the slots, in order
-      if (lane < k) {
-        const int e = s_idx[lane];
-        if (e < 0 || e >= E) {   // only NaN logits can get here
-          set_error(a.err, kDevCheck);
-          s_abort = 1;
-        }
-        s_meta.slot_expert[lane] = e;
-        s_tmask[lane] = 1u;
-#pragma unroll
-        for (int t = 0; t < kMaxDecodeT; ++t) s_meta.slot_j[lane][t] = (signed char)(t == 0 ? lane : -1);
-      }
-      if (lane == 0) s_meta.num_slots = k;
-    } else if (warp == 0) {
-      const int n = T * k;
-      bool first[2] = {false, false};
-      int firstpos[2] = {0, 0};
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int ai = lane + 32 * h2;
-        if (ai < n) {
-          const int e = s_idx[ai];
-          if (e < 0 || e >= E) {   // only NaN logits can get here
-            set_error(a.err, kDevCheck);
-            s_abort = 1;
-          }
-          int q = 0;
-          while (s_idx[q] != e) ++q;
-          first[h2] = (q == ai);
-          firstpos[h2] = q;
-        }
-      }
-      const unsigned m0 = __ballot_sync(0xFFFFFFFFu, first[0]);
-      const unsigned m1 = __ballot_sync(0xFFFFFFFFu, first[1]);
-      const unsigned lt = (1u << lane) - 1u;
-      if (first[0]) s_slot_of[lane] = __popc(m0 & lt);
-      if (first[1]) s_slot_of[lane + 32] = __popc(m0) + __popc(m1 & lt);
-      __syncwarp();
-      const int D = __popc(m0) + __popc(m1);
-      for (int q = lane; q < D * kMaxDecodeT; q += 32) s_meta.slot_j[q / kMaxDecodeT][q % kMaxDecodeT] = -1;
-      for (int q = lane; q < D; q += 32) s_tmask[q] = 0u;
-      __syncwarp();
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int ai = lane + 32 * h2;
-        if (ai < n) {
-          const int slot = s_slot_of[firstpos[h2]];
-          if (first[h2]) s_meta.slot_expert[slot] = s_idx[ai];
-          s_meta.slot_j[slot][ai / k] = (signed char)(ai % k);
-          atomicOr(&s_tmask[slot], 1u << (ai / k));
-        }
-      }
-      if (lane == 0) s_meta.num_slots = D;
-    }
+    stream::router_publish<TMAX>(xs, XP, T, H, E, a.router_t, a.router_bias, a.logit_bias, a.words, tag, &x_bar,
+                                 a.err, &s_abort, s_rpart);
+    stream::route_window(a.words, T, E, k, tag, rs, a.err, &s_abort);
   }
   __syncthreads();   // routing known to every warp, producer included
   if (s_abort) {
@@ -460,7 +241,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
     return;
   }
 
-  const int D = s_meta.num_slots;
+  const int D = rs.meta.num_slots;
   const int U = D * I;
   const Ranges rg = cta_ranges(b, G, Is, U);
   const int nr = rg.u1 - rg.u0;
@@ -468,10 +249,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
 
   if (b == 0 && !producer) {   // diagnostics copy of the routing
     for (int q = threadIdx.x; q < T * k; q += kConsumers) {
-      a.idx[q] = s_idx[q];
-      a.weights[q] = s_w[q];
+      a.idx[q] = rs.idx[q];
+      a.weights[q] = rs.w[q];
     }
-    const int* src = reinterpret_cast<const int*>(&s_meta);
+    const int* src = reinterpret_cast<const int*>(&rs.meta);
     int* dst = reinterpret_cast<int*>(a.meta);
     for (int q = threadIdx.x; q < (int)(sizeof(DecodeMeta) / 4); q += kConsumers) dst[q] = src[q];
   }
@@ -556,8 +337,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
         float w = 1.f;
         if (!shared) {
           const int dd = (int)((unsigned)(rg.u0 + first + r) / (unsigned)I);
-          j = s_meta.slot_j[dd][t];
-          if (j >= 0) w = s_w[t * k + j];
+          j = rs.meta.slot_j[dd][t];
+          if (j >= 0) w = rs.w[t * k + j];
         }
         if (shared || j >= 0) c = w * swiglu(g, u);
       }
@@ -620,62 +401,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
       }
     }
   }
-  // Collect: this CTA owns output rows [nb0, nb1) for every token. Each thread
-  // polls its share of the G x rows x TP words (16 bytes at a time) until they
-  // carry this call's tag and stages the values in shared memory (the ring is
-  // free now); then one warp per output adds the G partials in a fixed order.
-  const int nb0 = (int)((unsigned)b * (unsigned)H / (unsigned)G);
-  const int nb1 = (int)((unsigned)(b + 1) * (unsigned)H / (unsigned)G);
-  const int nrow = nb1 - nb0;
-  const int per = nrow * TP / 2;                      // 16-byte units per CTA partial
-  const int units = G * per;
-  float* stage = reinterpret_cast<float*>(ring);      // [G][nrow][TP]
-  const unsigned long long want = tag & 0xFFFFFFFFull;
-  for (int q0 = threadIdx.x; q0 < units; q0 += 8 * kConsumers) {
-    const long long t0 = clock64();
-    while (true) {
-      unsigned long long v[8][2];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int q = q0 + r * kConsumers;
-        v[r][0] = v[r][1] = want << 32;
-        if (q < units) {
-          const int p = q / per, w2 = q - p * per;
-          ld_relaxed_v2u64(a.partial + ((size_t)p * H + nb0) * TP + 2 * w2, v[r][0], v[r][1]);
-        }
-      }
-      bool ok = true;   // (the pad token of odd T is written too, so both words are checked)
-#pragma unroll
-      for (int r = 0; r < 8; ++r) ok &= (v[r][0] >> 32) == want && (v[r][1] >> 32) == want;
-      if (ok) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int q = q0 + r * kConsumers;
-          if (q < units)
-            *reinterpret_cast<float2*>(stage + 2 * (size_t)q) =
-                make_float2(__uint_as_float((uint32_t)v[r][0]), __uint_as_float((uint32_t)v[r][1]));
-        }
-        break;
-      }
-      if (clock64() - t0 > kSpinBudget) {
-        set_error(a.err, kDevTimeout);
-        s_abort = 1;
-        break;
-      }
-    }
-  }
-  consumers_sync();
-  if (!s_abort) {
-    for (int o = warp; o < nrow * T; o += kConsumerWarps) {
-      const int nl = o / T, t = o - nl * T;
-      float sum = 0.f;
-      for (int p = lane; p < G; p += 32) sum += stage[((size_t)p * nrow + nl) * TP + t];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-      if (lane == 0) a.out[(size_t)t * H + nb0 + nl] = f32_to_bf16_rne(sum);
-    }
-  }
-  consumers_sync();
+  consumers_sync();   // every warp is done reading the ring before it stages the exchange
+  stream::collect_outputs(a.partial, reinterpret_cast<float*>(ring), tag, T, H, a.out, a.err, &s_abort);
   if (threadIdx.x == 0) leave();
 }
 
@@ -708,9 +435,7 @@ bool stream_supported(const moe_layer* L, int T) {
   const int ng = stream_ring_groups(L, T);
   if (ng < 2) return false;
   // the final exchange stages G x (rows of this CTA) x TP fp32 values in the ring
-  const size_t rows = ((size_t)c.hidden + L->num_sms - 1) / L->num_sms;
-  const size_t tp = (size_t)T + (T & 1);
-  return (size_t)L->num_sms * rows * tp * 4 <=
+  return stream::collect_stage_bytes(L->num_sms, c.hidden, T) <=
          (size_t)ng * stream_group_records(T, c.hidden) * stream_record_stride(c.hidden);
 }
 

@@ -75,6 +75,17 @@ def test_ling_mxfp4(name):
     print(name, r)
 
 
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_small_mxfp4_every_window_size(T):
+    """A small MXFP4 layer (E=16, k=4, so windows share experts and groups cross
+    expert and 32-feature scale-block boundaries) at every window size."""
+    S = mi.custom_layer(H=512, E=16, k=4, I=256, Is=128, fmt="mxfp4", seed=5)
+    L = G.cuda_layer(S.spec, max_tokens=8)
+    x = mi.tokens(S.spec, T, stream=200 + T)
+    out, idx, wt = G.run_cuda(L, x)
+    G.compare(S, x, out, idx, wt, fmt="mxfp4")
+
+
 def test_deterministic_and_batch_invariant():
     w = mi.WORKLOADS["qwen_verify"]
     L = G.cuda_layer(w.layer, max_tokens=4096)
@@ -172,3 +183,5 @@ def test_describe_names_the_active_path():
     L = G.cuda_layer(mi.WORKLOADS["tiny"].layer, max_tokens=64)
     d = L.describe()
     assert "decode GEMV path" in d and "moe_decode_stream_kernel" in d
+    S = mi.custom_layer(H=512, E=16, k=4, I=256, Is=128, fmt="mxfp4", seed=5)
+    assert "moe_decode_stream_mx_kernel" in G.cuda_layer(S.spec, max_tokens=8).describe()
