@@ -108,8 +108,9 @@ __global__ void down_to_columns_kernel(const uint16_t* __restrict__ down, uint8_
 }
 
 // MXFP4 down codes [E][H][I/2] (element (n, i) in nibble i & 1 of byte i / 2 of
-// row n) -> the down column of each record: byte m of record (e, i)'s column
-// holds elements n = 2m (low nibble) and 2m + 1. One block: 64 features x 64 rows.
+// row n) -> the down column of each record in 16-row tiles: byte 8t + g of
+// record (e, i)'s column holds rows n = 16t + g (low nibble) and 16t + g + 8.
+// One block: 64 features x 64 rows.
 __global__ void mx_down_to_columns_kernel(const uint8_t* __restrict__ down, uint8_t* __restrict__ rec, int H, int I,
                                           int stride, int col_off) {
   __shared__ uint8_t tile[64][32];            // [row n][64 features as 32 code bytes]
@@ -123,17 +124,36 @@ __global__ void mx_down_to_columns_kernel(const uint8_t* __restrict__ down, uint
   }
   __syncthreads();
   {
-    const int il = t >> 2, part = t & 3;        // feature i0 + il, output bytes 8 * part .. + 7
+    const int il = t >> 2, part = t & 3;        // feature i0 + il, 16-row tile `part` of the block
     uint8_t o[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int m = 8 * part + q;               // rows 2m, 2m + 1 of the tile
-      const uint32_t lo = (tile[2 * m][il >> 1] >> (4 * (il & 1))) & 0xFu;
-      const uint32_t hi = (tile[2 * m + 1][il >> 1] >> (4 * (il & 1))) & 0xFu;
+    for (int q = 0; q < 8; ++q) {               // byte q: rows 16 part + q and 16 part + q + 8
+      const uint32_t lo = (tile[16 * part + q][il >> 1] >> (4 * (il & 1))) & 0xFu;
+      const uint32_t hi = (tile[16 * part + q + 8][il >> 1] >> (4 * (il & 1))) & 0xFu;
       o[q] = (uint8_t)(lo | (hi << 4));
     }
     uint8_t* dst = rec + (e * I + i0 + il) * (size_t)stride + col_off + n0 / 2 + 8 * part;
     *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(o);
+  }
+}
+
+// MXFP4 gate or up codes [rows][H/2] -> the records, each 16-byte block (32
+// elements) shuffled for the tensor-core fragments: stored byte 4c + m = source
+// byte c + 4m.
+__global__ void mx_shuffle_codes_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ rec, size_t rows, int H,
+                                        int stride, int dst_off) {
+  const int nb = H / 32;
+  const size_t total = rows * nb;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < total; q += (size_t)gridDim.x * blockDim.x) {
+    const size_t row = q / nb, blk = q % nb;
+    const uint4 v = *reinterpret_cast<const uint4*>(src + row * (size_t)(H / 2) + 16 * blk);
+    const uint8_t* in = reinterpret_cast<const uint8_t*>(&v);
+    uint8_t o[16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) o[4 * c + m] = in[c + 4 * m];
+    *reinterpret_cast<uint4*>(rec + row * (size_t)stride + dst_off + 16 * blk) = *reinterpret_cast<const uint4*>(o);
   }
 }
 
@@ -266,7 +286,7 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
   // Feature records for the record-streaming decode kernel: per (expert, i)
   // the gate row, the up row and the down column, contiguous (6H bytes).
   const bool bf16_stream = c.weight_format == MOE_WEIGHTS_BF16 && H <= moe::kStreamMaxHidden;
-  const bool mx_stream = c.weight_format == MOE_WEIGHTS_MXFP4 && H <= moe::kStreamMxMaxHidden;
+  const bool mx_stream = c.weight_format == MOE_WEIGHTS_MXFP4 && H <= moe::kStreamMxMaxHidden && H % 512 == 0;
   if (bf16_stream || mx_stream) {
     const size_t row = (size_t)H * 2, rec = (size_t)moe::stream_record_stride((int)H);
     dim3 block(32, 8);
@@ -279,16 +299,18 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
       down_to_columns_kernel<<<grid, block>>>((const uint16_t*)w->down_dev, L.w_rec, (int)H, (int)I, (int)rec);
       MOE_CUDA(cudaGetLastError());
     } else {
-      // MXFP4 records: gate codes | gate scales | up codes | up scales | down column codes
+      // MXFP4 records: gate codes | up codes | gate scales | up scales | down column codes
       const size_t mxs = (size_t)moe::stream_mx_record_stride((int)H);
       const size_t so = (size_t)((H / 32 + 15) / 16 * 16), nblk = (size_t)I / 32;
       GET(L.w_mx, (size_t)E * I * mxs);
       GET(L.mx_dsc, (size_t)E * nblk * H);
       MOE_CUDA(cudaMemset(L.w_mx, 0, (size_t)E * I * mxs));
       const size_t rows = (size_t)E * I;
-      MOE_CUDA(cudaMemcpy2D(L.w_mx, mxs, w->gate_dev, H / 2, H / 2, rows, cudaMemcpyDeviceToDevice));
-      MOE_CUDA(cudaMemcpy2D(L.w_mx + H / 2, mxs, w->gate_scales_dev, H / 32, H / 32, rows, cudaMemcpyDeviceToDevice));
-      MOE_CUDA(cudaMemcpy2D(L.w_mx + H / 2 + so, mxs, w->up_dev, H / 2, H / 2, rows, cudaMemcpyDeviceToDevice));
+      mx_shuffle_codes_kernel<<<1024, 256>>>((const uint8_t*)w->gate_dev, L.w_mx, rows, (int)H, (int)mxs, 0);
+      MOE_CUDA(cudaGetLastError());
+      mx_shuffle_codes_kernel<<<1024, 256>>>((const uint8_t*)w->up_dev, L.w_mx, rows, (int)H, (int)mxs, (int)(H / 2));
+      MOE_CUDA(cudaGetLastError());
+      MOE_CUDA(cudaMemcpy2D(L.w_mx + H, mxs, w->gate_scales_dev, H / 32, H / 32, rows, cudaMemcpyDeviceToDevice));
       MOE_CUDA(cudaMemcpy2D(L.w_mx + H + so, mxs, w->up_scales_dev, H / 32, H / 32, rows, cudaMemcpyDeviceToDevice));
       dim3 g2((unsigned)(I / 64), (unsigned)(H / 64), (unsigned)E);
       mx_down_to_columns_kernel<<<g2, 256>>>((const uint8_t*)w->down_dev, L.w_mx, (int)H, (int)I, (int)mxs,

@@ -79,7 +79,8 @@ struct moe_layer {
                          // (bf16 layers with H <= kStreamMaxHidden; nullptr otherwise)
   uint8_t* ws_rec;       // shared-expert records [Is], same record format (also for MXFP4 layers)
   uint8_t* w_mx;         // MXFP4 routed records [E][I], stream_mx_record_stride(H) bytes each:
-                         // gate codes | gate scales | up codes | up scales | down column codes
+                         // gate codes | up codes | gate scales | up scales | down column codes
+                         // (code orders for the tensor-core fragments, moe_stream_common.cuh)
   uint8_t* mx_dsc;       // MXFP4 down scales [E][I / 32][H] (one H-byte vector per 32 features)
   moe::RowBytes row_bytes;
 
@@ -126,7 +127,7 @@ int stream_mx_record_stride(int H);       // bytes per routed MXFP4 record
 cudaError_t stream_mx_prepare(moe_layer* L);
 cudaError_t launch_stream_mx(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
                              cudaStream_t s);
-constexpr int kStreamMxMaxHidden = 4096;  // largest H the MXFP4 streaming kernel serves
+constexpr int kStreamMxMaxHidden = 2560;  // largest H the MXFP4 streaming kernel serves
 constexpr int kStreamMaxHidden = 2048;    // largest H the record-streaming kernel serves
 cudaError_t stream_prepare(moe_layer* L);
 cudaError_t launch_stream(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,

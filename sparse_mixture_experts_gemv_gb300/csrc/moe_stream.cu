@@ -100,27 +100,12 @@ struct StreamArgs {
 };
 
 using stream::ld_relaxed_u64;
+using stream::mma_16816;
 using stream::st_relaxed_v2u64;
 using stream::tagged;
 using stream::consumers_sync;
 using stream::Ranges;
 using stream::cta_ranges;
-
-// Warp-level tensor-core fragments (PTX ldmatrix / mma.sync).
-MOE_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-MOE_DEV void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-// D = A(16x16, row) * B(16x8, col) + D; bf16 inputs, fp32 accumulators.
-MOE_DEV void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-               "{%0, %1, %2, %3};"
-               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 template <int TMAX>
 __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(const StreamArgs a) {
@@ -295,29 +280,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
     // gate/up: tile rows 0-7 = gate rows of records 0-7, rows 8-15 = their up rows;
     // this warp covers K = [k0w, k0w + kslice)
     {
-      const int q = lane >> 3, r = lane & 7;     // ldmatrix: lane supplies row r of matrix q
-      const uint32_t rowaddr = (r < nvalid) ? gbase + (uint32_t)(r * stride + ((q & 1) ? 2 * H : 0) + (q >> 1) * 16)
-                                            : zero_u32;
-      const bool real = r < nvalid;
-      float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // even / odd k-steps
-      const int nsteps = kslice / 16;
-#pragma unroll
-      for (int st = 0; st < kMaxKSteps; ++st) {
-        if (st < nsteps) {
-          const int kabs = k0w + 16 * st;
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(real ? rowaddr + 2 * kabs : zero_u32, a0, a1, a2, a3);
-          uint32_t b0 = 0u, b1 = 0u;
-          if (gq < T) {
-            const uint32_t xa = xs_u32 + (uint32_t)(2 * (gq * XP + kabs + 2 * cq));
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b0) : "r"(xa));
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b1) : "r"(xa + 16));
-          }
-          mma_16816(d[st & 1], a0, a1, a2, a3, b0, b1);
-        }
-      }
-      *reinterpret_cast<float2*>(&s_part[warp][gq][2 * cq]) = make_float2(d[0][0] + d[1][0], d[0][1] + d[1][1]);
-      *reinterpret_cast<float2*>(&s_part[warp][gq + 8][2 * cq]) = make_float2(d[0][2] + d[1][2], d[0][3] + d[1][3]);
+      float d[4];
+      stream::bf16_gu_tile<kMaxKSteps>(gbase, stride, nvalid, H, T, XP, xs_u32, zero_u32, k0w, kslice / 16, d);
+      *reinterpret_cast<float2*>(&s_part[warp][gq][2 * cq]) = make_float2(d[0], d[1]);
+      *reinterpret_cast<float2*>(&s_part[warp][gq + 8][2 * cq]) = make_float2(d[2], d[3]);
     }
     consumers_sync();
     if ((int)threadIdx.x < 128) {   // c = w * silu(g) * u per (record r, token t), as bf16 hi + lo
@@ -351,23 +317,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
     consumers_sync();
     if (s_abort) break;
     // down: out[n][t] += sum_r down_r[n] * c[r][t] for this warp's output tiles
-    {
-      const uint32_t bhi = *reinterpret_cast<const uint32_t*>(&s_chi[gq][2 * cq]);
-      const uint32_t blo = *reinterpret_cast<const uint32_t*>(&s_clo[gq][2 * cq]);
-      const int r = lane & 7, half = (lane >> 3) & 1;   // ldmatrix.x2: lanes 0-15 supply rows
-      const bool real = r < nvalid;
-      const uint32_t dbase = gbase + (uint32_t)(r * stride + 4 * H + half * 16);
-#pragma unroll
-      for (int j = 0; j < kMaxTiles; ++j) {
-        if (j < ntile) {
-          const int n0 = 16 * (warp + kConsumerWarps * j);
-          uint32_t a0, a1;
-          ldsm_x2_trans(real ? dbase + 2 * n0 : zero_u32, a0, a1);
-          // K = 16: records 0-7 against c_hi, the same records again against c_lo
-          mma_16816(acc[j], a0, a1, a0, a1, bhi, blo);
-        }
-      }
-    }
+    stream::bf16_down_tiles<kMaxTiles>(gbase, stride, nvalid, H, ntile, zero_u32,
+                                       *reinterpret_cast<const uint32_t*>(&s_chi[gq][2 * cq]),
+                                       *reinterpret_cast<const uint32_t*>(&s_clo[gq][2 * cq]), acc);
     __syncwarp();
     if (lane == 0) sm100::mbar_arrive(&empty_bar[sg]);
   }

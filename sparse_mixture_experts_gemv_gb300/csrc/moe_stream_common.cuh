@@ -14,6 +14,7 @@
 // publishes anything.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -67,6 +68,218 @@ struct RouteSmem {
   unsigned tmask[kMaxSlots];              // tokens using each slot
   DecodeMeta meta;                        // slots: distinct experts, first-appearance order
 };
+
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core fragments (PTX ldmatrix / mma.sync).
+// ---------------------------------------------------------------------------
+MOE_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+MOE_DEV void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+// D = A(16x16, row) * B(16x8, col) + D; bf16 inputs, fp32 accumulators.
+MOE_DEV void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+               "{%0, %1, %2, %3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Same with f16 inputs.
+MOE_DEV void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                           uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+               "{%0, %1, %2, %3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Fragment coordinates of a lane in an m16n8k16 tile: row group g = lane / 4,
+// column pair c = lane % 4. C/D: rows g and g + 8, columns (tokens) 2c, 2c + 1.
+
+// One warp's part of the gate/up tile of up to 8 bf16 records (rows 0-7 = gate
+// rows of records 0-7, rows 8-15 = their up rows) at `gbase` (records `stride`
+// bytes apart; records >= nvalid read the zero row): K = [k0, k0 + 16 * nsteps)
+// of H against x (bf16, rows XP elements apart, tokens >= T read as zero).
+// Returns the partial tile (fragment layout).
+template <int MAXSTEPS>
+MOE_DEV void bf16_gu_tile(uint32_t gbase, int stride, int nvalid, int H, int T, int XP, uint32_t xs_u32,
+                          uint32_t zero_u32, int k0, int nsteps, float (&out)[4]) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
+  const int q = lane >> 3, r = lane & 7;     // ldmatrix: lane supplies row r of matrix q
+  const bool real = r < nvalid;
+  const uint32_t rowaddr = real ? gbase + (uint32_t)(r * stride + ((q & 1) ? 2 * H : 0) + (q >> 1) * 16) : zero_u32;
+  float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // even / odd k-steps
+#pragma unroll
+  for (int st = 0; st < MAXSTEPS; ++st) {
+    if (st < nsteps) {
+      const int kabs = k0 + 16 * st;
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(real ? rowaddr + 2 * kabs : zero_u32, a0, a1, a2, a3);
+      uint32_t b0 = 0u, b1 = 0u;
+      if (gq < T) {
+        const uint32_t xa = xs_u32 + (uint32_t)(2 * (gq * XP + kabs + 2 * cq));
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b0) : "r"(xa));
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(b1) : "r"(xa + 16));
+      }
+      mma_16816(d[st & 1], a0, a1, a2, a3, b0, b1);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) out[e] = d[0][e] + d[1][e];
+}
+
+// One warp's output tiles of the down projection of up to 8 bf16 records:
+// acc[j] += sum_r down_r[n] * c[r][t] for tiles n0 = 16 * (warp + 16 j), with
+// c given as bf16 hi + lo fragments (bhi, blo: c[2cq..2cq+1][token gq]). The
+// down columns start 4H bytes into each record.
+template <int MAXTILES>
+MOE_DEV void bf16_down_tiles(uint32_t gbase, int stride, int nvalid, int H, int ntile, uint32_t zero_u32, uint32_t bhi,
+                             uint32_t blo, float (&acc)[MAXTILES][4]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = lane & 7, half = (lane >> 3) & 1;   // ldmatrix.x2: lanes 0-15 supply rows
+  const bool real = r < nvalid;
+  const uint32_t dbase = gbase + (uint32_t)(r * stride + 4 * H + half * 16);
+#pragma unroll
+  for (int j = 0; j < MAXTILES; ++j) {
+    if (j < ntile) {
+      const int n0 = 16 * (warp + kConsumerWarps * j);
+      uint32_t a0, a1;
+      ldsm_x2_trans(real ? dbase + 2 * n0 : zero_u32, a0, a1);
+      // K = 16: records 0-7 against c_hi, the same records again against c_lo
+      mma_16816(acc[j], a0, a1, a0, a1, bhi, blo);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MXFP4 records on the tensor cores.
+// ---------------------------------------------------------------------------
+// Record layout (bytes; so = scale segment, pad16(H / 32)):
+//   [0, H/2)        gate codes, shuffled per 32-element block (below)
+//   [H/2, H)        up codes, shuffled the same way
+//   [H, H+so)       gate scales, one e8m0 byte per 32-element block
+//   [H+so, H+2so)   up scales
+//   [H+2so, ...)    down column codes in 16-row tiles (below)
+// Block shuffle: a 32-element block is 16 code bytes, byte j = elements 2j
+// (low nibble), 2j+1. Stored word c (bytes 4c .. 4c+3) = original bytes c, c+4,
+// c+8, c+12: exactly the four code pairs lane (g, c) of an m16n8k16 A fragment
+// needs for one row over the block's two 16-wide k-steps (k = 2c, 2c+8 of the
+// first step, then of the second).
+// Down tiles: byte 8t + g of the column = rows 16t + g (low nibble) and
+// 16t + g + 8 of the feature's down column: the pair of rows lane (g, c) holds
+// in an A fragment.
+struct MxLayout {
+  int up_codes, gate_scales, up_scales, down_tiles;
+};
+MOE_DEV MxLayout mx_layout(int H, int so) { return MxLayout{H / 2, H, H + so, H + 2 * so}; }
+
+// One warp's part of the gate/up tiles of up to 16 MXFP4 records (tile m:
+// rows 0-7 = gate rows of records 8m .. 8m+7, rows 8-15 = their up rows), over
+// 32-element blocks [blk0, blk0 + nblk) of H. Each block's two k-steps go to a
+// fresh accumulator that is then scaled by the row's block scale and added.
+// x16: f16 x, rows XP halves apart. Records >= nvalid count as zero.
+template <int MAXMT>
+MOE_DEV void mx_gu_tiles(const uint8_t* gbase, int stride, int nvalid, int nmt, const MxLayout& ly, int T, int XP,
+                         const uint16_t* x16, int blk0, int nblk, float (&out)[MAXMT][4]) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
+#pragma unroll
+  for (int m = 0; m < MAXMT; ++m) out[m][0] = out[m][1] = out[m][2] = out[m][3] = 0.f;
+  for (int bi = 0; bi < nblk; ++bi) {
+    const int blk = blk0 + bi;
+    uint32_t b[2][2] = {{0u, 0u}, {0u, 0u}};   // x fragments of the block's two k-steps
+    if (gq < T) {
+      const uint16_t* xr = x16 + gq * XP + 32 * blk + 2 * cq;
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        b[ks][0] = *reinterpret_cast<const uint32_t*>(xr + 16 * ks);
+        b[ks][1] = *reinterpret_cast<const uint32_t*>(xr + 16 * ks + 8);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MAXMT; ++m) {
+      if (m < nmt) {
+        const int r = 8 * m + gq;
+        uint32_t gw = 0u, uw = 0u;
+        float gs = 0.f, us = 0.f;
+        if (r < nvalid) {
+          const uint8_t* rec = gbase + (size_t)r * stride;
+          gw = *reinterpret_cast<const uint32_t*>(rec + 16 * blk + 4 * cq);
+          uw = *reinterpret_cast<const uint32_t*>(rec + ly.up_codes + 16 * blk + 4 * cq);
+          gs = e8m0_to_f32(rec[ly.gate_scales + blk]);
+          us = e8m0_to_f32(rec[ly.up_scales + blk]);
+        }
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          mma_16816_f16(d, e2m1x2_to_f16x2(gw >> (16 * ks)), e2m1x2_to_f16x2(uw >> (16 * ks)),
+                        e2m1x2_to_f16x2(gw >> (16 * ks + 8)), e2m1x2_to_f16x2(uw >> (16 * ks + 8)), b[ks][0],
+                        b[ks][1]);
+        out[m][0] = fmaf(gs, d[0], out[m][0]);
+        out[m][1] = fmaf(gs, d[1], out[m][1]);
+        out[m][2] = fmaf(us, d[2], out[m][2]);
+        out[m][3] = fmaf(us, d[3], out[m][3]);
+      }
+    }
+  }
+}
+
+// One warp's output tiles of the down projection of up to 16 MXFP4 records
+// (K = the records): acc[j] += sum_r code_r[n] * scale[n] * c[r][t] for tiles
+// n0 = 16 * (warp + 16 j). c comes as f16 hi + lo fragments scaled by 2^-cexp
+// (bh0, bh1: c'[2cq..2cq+1][token gq] and c'[2cq+8..2cq+9][gq]; bl0, bl1 the
+// low parts); records that use another scale vector have c = 0 here. sv: the
+// scale vector (H bytes, one per output row) of these records.
+template <int MAXTILES>
+MOE_DEV void mx_down_tiles(const uint8_t* gbase, int stride, int nvalid, const MxLayout& ly, int ntile,
+                           const uint8_t* sv, float cexp2, uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1,
+                           float (&acc)[MAXTILES][4]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gq = lane >> 2, cq = lane & 3;
+  const int ra = 2 * cq, rb = 2 * cq + 8;        // records of K columns 2cq.. and 2cq+8..
+  const uint8_t* p0 = gbase + (size_t)ra * stride + ly.down_tiles + gq;
+  const uint8_t* p1 = p0 + stride;
+  const uint8_t* p2 = gbase + (size_t)rb * stride + ly.down_tiles + gq;
+  const uint8_t* p3 = p2 + stride;
+  const bool v0 = ra < nvalid, v1 = ra + 1 < nvalid, v2 = rb < nvalid, v3 = rb + 1 < nvalid;
+#pragma unroll
+  for (int j = 0; j < MAXTILES; ++j) {
+    if (j < ntile) {
+      const int tt = warp + kConsumerWarps * j, n0 = 16 * tt;
+      const uint32_t c0 = v0 ? p0[8 * tt] : 0u, c1 = v1 ? p1[8 * tt] : 0u;
+      const uint32_t c2 = v2 ? p2[8 * tt] : 0u, c3 = v3 ? p3[8 * tt] : 0u;
+      const uint32_t a0 = e2m1x2_to_f16x2((c0 & 0xFu) | ((c1 & 0xFu) << 4));   // row n0+g
+      const uint32_t a1 = e2m1x2_to_f16x2((c0 >> 4) | (c1 & 0xF0u));          // row n0+g+8
+      const uint32_t a2 = e2m1x2_to_f16x2((c2 & 0xFu) | ((c3 & 0xFu) << 4));
+      const uint32_t a3 = e2m1x2_to_f16x2((c2 >> 4) | (c3 & 0xF0u));
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16816_f16(d, a0, a1, a2, a3, bh0, bh1);
+      mma_16816_f16(d, a0, a1, a2, a3, bl0, bl1);
+      const float f0 = e8m0_to_f32(sv[n0 + gq]) * cexp2, f1 = e8m0_to_f32(sv[n0 + gq + 8]) * cexp2;
+      acc[j][0] = fmaf(f0, d[0], acc[j][0]);
+      acc[j][1] = fmaf(f0, d[1], acc[j][1]);
+      acc[j][2] = fmaf(f1, d[2], acc[j][2]);
+      acc[j][3] = fmaf(f1, d[3], acc[j][3]);
+    }
+  }
+}
+
+// c as an f16 hi + lo pair (packed with its neighbour) after scaling by s.
+MOE_DEV void f16_hilo2(float c0, float c1, float s, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(c0 * s, c1 * s);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(c0 * s - hf.x, c1 * s - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+// c as a bf16 hi + lo pair (packed with its neighbour).
+MOE_DEV void bf16_hilo2(float c0, float c1, uint32_t& hi, uint32_t& lo) {
+  const uint16_t h0 = f32_to_bf16_rne(c0), h1 = f32_to_bf16_rne(c1);
+  const uint16_t l0 = f32_to_bf16_rne(c0 - __uint_as_float((uint32_t)h0 << 16));
+  const uint16_t l1 = f32_to_bf16_rne(c1 - __uint_as_float((uint32_t)h1 << 16));
+  hi = (uint32_t)h0 | ((uint32_t)h1 << 16);
+  lo = (uint32_t)l0 | ((uint32_t)l1 << 16);
+}
 
 // Record range of this CTA. Shared-expert records [sh0, sh1) are known before
 // routing; routed records [u0, u1) index the window's D x I (slot, feature)

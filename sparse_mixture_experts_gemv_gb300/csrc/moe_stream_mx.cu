@@ -13,29 +13,31 @@
 // "Decode weights during matrix multiplication": the codes are decoded in
 // registers as they are multiplied, never written back in a wider format.
 //
-// Records (repacked at create), per (expert e, intermediate feature i):
-//   [ gate codes (H/2 B) | gate scales (H/32 B, padded to 16) |
-//     up codes | up scales | down column codes (H/2 B) ] + 16 B padding
-// Code byte j of a row holds elements 2j (low nibble) and 2j+1 (high); a scale
-// covers 32 consecutive elements of its row. The down column of feature i
-// holds W_down[e][n][i] for n = 0..H-1, two per byte (even n low). Its scales
-// belong to (n, i / 32), i.e. to 32 consecutive features at once, so they are
-// kept apart, one H-byte vector per (e, block of 32 features), and each ring
-// group carries the one or two vectors its records need.
+// Records (repacked at create), per (expert e, intermediate feature i): gate
+// and up codes, their e8m0 scales, and the down column's codes (layout in
+// moe_stream_common.cuh, "MXFP4 records on the tensor cores"). The down
+// column's scales belong to (n, i / 32), i.e. to 32 consecutive features at
+// once, so they are kept apart, one H-byte vector per (e, block of 32
+// features), and each ring group carries the one or two vectors it needs.
 // The shared expert stays bf16 and uses the bf16 kernel's record format.
 //
-// Consumers (CUDA cores; per record the work is ~3H multiply-adds per token,
-// far below what the copies deliver per SM, so no tensor-core tiling):
-//   gate/up    16 / R warps per record of an R-record group, each over a slice
-//              of H: codes -> f16 pairs (cvt.rn.f16x2.e2m1x2), multiplied with
-//              an f16 copy of x (fma.rn.f32.f16: f16 products, fp32 sums), each
-//              8-element word scaled by its block scale; warp sums to shared
-//              memory, slices added in order, c = w * silu(g) * u per token.
-//   down       thread q owns outputs n = 8q .. 8q+7 for every token and adds
-//              c * code * scale over the group's records in record order.
+// Consumers (tensor cores, mma.sync with f16 fragments decoded from the codes
+// by cvt.rn.f16x2.e2m1x2; e2m1 values are exact in f16):
+//   gate/up    a group's 16 records are two 16-row tiles (gate rows, up rows
+//              of 8 records); each warp covers 1/16 of H, one 32-element block
+//              at a time: two k-steps into a fresh accumulator, then scaled by
+//              the row's block scale; the 16 warp parts are added in order and
+//              c = w * silu(g) * u is formed per (record, token).
+//   down       K = the group's records: A = code[n][r] (f16), B = c[r][t] as
+//              f16 hi + lo after a power-of-two shift that keeps the group's
+//              largest |c| near 2^14; each 16-row tile's result is scaled by
+//              the rows' down scales and added to the fp32 output tile.
+// At batch 1 the layer is bound by HBM; decoding e2m1 on the CUDA cores costs
+// several instructions per code byte, more than an SM's share of HBM leaves
+// time for, while a tensor-core fragment needs one cvt per two codes.
 // Readings: x is rounded to f16 for the MXFP4 products (exact for the normal
-// f16 range |x| in [2^-14, 65504]; smaller values lose bits, larger overflow),
-// the e2m1 values are exact in f16, and every sum is fp32.
+// f16 range |x| in [2^-14, 65504]; smaller values lose bits, larger overflow);
+// every sum is fp32.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -60,9 +62,12 @@ using stream::tagged;
 
 constexpr int kMaxMx = 16;             // MXFP4 records per routed group: 16 (one warp each), or 8
                                        // (two warps each) when x leaves no room for two 16-record slots
-constexpr int kShGroup = 2;            // bf16 shared-expert records per shared group (8 warps each)
-constexpr int kMxMaxH = 4096;          // one 8-output chunk per consumer thread
-constexpr int kParts = 8;              // most warps on one record (shared groups)
+constexpr int kShGroup = 4;            // bf16 shared-expert records per shared group (one MMA tile)
+constexpr int kMaxMt = kMaxMx / 8;     // 16-row gate/up tiles per group
+constexpr int kMxMaxH = kStreamMxMaxHidden;   // output tiles per warp kept in registers: H / 256
+constexpr int kMxMaxTiles = kMxMaxH / 256;
+constexpr int kMxMaxKSteps = kMxMaxH / 16 / 16;   // bf16 gate/up k-steps per warp (shared records)
+constexpr int kMxSmemMax = 204 * 1024;  // dynamic shared memory budget (the static part is ~19 KB)
 
 struct MxArgs {
   const uint16_t* x;           // bf16 [T][H]
@@ -91,21 +96,6 @@ struct MxArgs {
   int force_timeout;
 };
 
-// Record offsets (bytes) of an MXFP4 record with scale segments of `so` bytes.
-// (gate codes start at byte 0)
-MOE_DEV int mx_gate_scales(int H) { return H / 2; }
-MOE_DEV int mx_up_codes(int H, int so) { return H / 2 + so; }
-MOE_DEV int mx_up_scales(int H, int so) { return H + so; }
-MOE_DEV int mx_down_codes(int H, int so) { return H + 2 * so; }
-
-// Unscaled dot of 8 e2m1 codes (one 32-bit word, element order) with 8 f16 of x.
-MOE_DEV float dot8_e2m1(uint32_t codes, const uint4 xv) {
-  float s = fma2_f16(e2m1x2_to_f16x2(codes & 0xFFu), xv.x, 0.f);
-  s = fma2_f16(e2m1x2_to_f16x2((codes >> 8) & 0xFFu), xv.y, s);
-  s = fma2_f16(e2m1x2_to_f16x2((codes >> 16) & 0xFFu), xv.z, s);
-  return fma2_f16(e2m1x2_to_f16x2(codes >> 24), xv.w, s);
-}
-
 template <int TMAX>
 __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kernel(const MxArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -117,11 +107,10 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
   __shared__ __align__(8) uint64_t empty_bar[kMaxRingGroups];
   __shared__ __align__(8) uint64_t x_bar;
   __shared__ float s_rpart[kConsumerWarps][TMAX];                   // router partial sums
-  __shared__ float s_gu[kMaxMx][kParts][TMAX][2];                   // gate/up slice sums
-  // w * silu(g) * u per record and token, double-buffered by group parity: with
-  // one warp per record a warp writes group k+1's values while others still
-  // read group k's; group k+2 is written only after the barrier of group k+1.
-  __shared__ float s_cb[2][kMaxMx][TMAX];
+  __shared__ __align__(16) float s_part[kConsumerWarps][kMaxMt][16][8];   // gate/up partial tiles
+  __shared__ float s_cf[8][kMaxMx];                                 // c = w * silu(g) * u, [token][record]
+  __shared__ unsigned s_cmax[2];                                    // largest |c| of a group (bits), by parity
+  __shared__ __align__(16) uint16_t s_zero[8];                      // a zero row for missing bf16 records
   __shared__ stream::RouteSmem rs;
   __shared__ unsigned long long s_tag;
   __shared__ int s_abort;
@@ -148,6 +137,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
     s_abort = 0;
     s_tag = stream::ld_relaxed_u64(a.ctr) / (unsigned long long)G + 1ull;   // see moe_stream_common.cuh
   }
+  if (threadIdx.x < 8) s_zero[threadIdx.x] = 0;
   __syncthreads();
   const unsigned long long tag = s_tag;
   auto leave = [&]() { atomicAdd(a.ctr, 1ull); };   // once per CTA, on every exit path
@@ -266,15 +256,15 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
   }
 
   // ---------------------------------------------------------------- consumers: groups
-  const int Hw = H / 8;                  // 8-element words (codes) or chunks (bf16) per row
-  const int q = threadIdx.x;             // this thread's outputs: n = 8q .. 8q+7
-  const bool own = q < Hw;
-  const int GS = mx_gate_scales(H), UC = mx_up_codes(H, so), US = mx_up_scales(H, so), DC = mx_down_codes(H, so);
-  float acc[TMAX][8];
+  const int gq = lane >> 2, cq = lane & 3;            // mma fragment coordinates
+  const int ntile = H / 256;                           // output tiles per warp (warp w: tiles w, w + 16, ...)
+  const stream::MxLayout ly = stream::mx_layout(H, so);
+  const int nbw = H / 32 / kConsumerWarps;             // 32-element blocks per warp (gate/up)
+  const uint32_t xs_u32 = sm100::smem_u32(xs);
+  const uint32_t zero_u32 = sm100::smem_u32(s_zero);
+  float acc[kMxMaxTiles][4];
 #pragma unroll
-  for (int t = 0; t < TMAX; ++t)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[t][j] = 0.f;
+  for (int j = 0; j < kMxMaxTiles; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
   int grp = 0;
   for (; grp < ngroups; ++grp) {
@@ -284,151 +274,86 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
     const int first = shared ? grp * kShGroup : (grp - nsg) * RGM;
     const int nvalid = min(RG, (shared ? ns : nr) - first);
     const uint8_t* base = ring + (size_t)sg * a.slot_bytes;
-    float (*s_c)[TMAX] = s_cb[grp & 1];
+    unsigned* cmax = &s_cmax[grp & 1];
+    if (threadIdx.x == 0) *cmax = 0u;   // group grp - 2's value was last read before this group's first barrier
     sm100::mbar_wait(&full_bar[sg], (uint32_t)(grp / NG) & 1u, a.err, &s_abort, kSpinBudget);
 
-    // gate/up: P warps per record, warp part p covers words [w0, w1) of both rows.
-    // With one warp per record (P = 1) the warp's own sums are g and u, and its
-    // lane 0 forms c right away; otherwise the parts meet in shared memory.
-    const int P = kConsumerWarps / RG;
+    // gate/up tiles (tile m: gate rows of records 8m..8m+7, then their up rows), this warp's part of K
     {
-      const int r = warp / P, p = warp - r * P;
-      if (r < nvalid) {
-        const int dd = shared ? 0 : (int)((unsigned)(rg.u0 + first + r) / (unsigned)I);
-        const unsigned tmask = shared ? (1u << T) - 1u : rs.tmask[dd];
-        const int w0 = p * Hw / P, w1 = (p + 1) * Hw / P;
-        float ag[TMAX], au[TMAX];
+      float d[kMaxMt][4];
+      if (shared) {
+        stream::bf16_gu_tile<kMxMaxKSteps>(sm100::smem_u32(base), shs, nvalid, H, T, XP, xs_u32, zero_u32,
+                                           warp * (H / kConsumerWarps), H / kConsumerWarps / 16, d[0]);
+      } else {
+        stream::mx_gu_tiles<kMaxMt>(base, mxs, nvalid, (nvalid + 7) / 8, ly, T, XP, x16, warp * nbw, nbw, d);
+      }
+      const int nmt = shared ? 1 : (nvalid + 7) / 8;
 #pragma unroll
-        for (int t = 0; t < TMAX; ++t) ag[t] = au[t] = 0.f;
-        if (shared) {
-          const uint8_t* rec = base + (size_t)r * shs;
-          for (int c = w0 + lane; c < w1; c += 32) {
-            const uint4 gv = *reinterpret_cast<const uint4*>(rec + 16 * c);
-            const uint4 uv = *reinterpret_cast<const uint4*>(rec + 2 * H + 16 * c);
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              if (t < T && ((tmask >> t) & 1u)) {
-                const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * XP + 8 * c);
-                ag[t] = fma8_bf16(gv, xv, ag[t]);
-                au[t] = fma8_bf16(uv, xv, au[t]);
-              }
-            }
-          }
-        } else {
-          const uint8_t* rec = base + (size_t)r * mxs;
-          for (int c = w0 + lane; c < w1; c += 32) {
-            const uint32_t gw = *reinterpret_cast<const uint32_t*>(rec + 4 * c);
-            const uint32_t uw = *reinterpret_cast<const uint32_t*>(rec + UC + 4 * c);
-            const float gsc = e8m0_to_f32(rec[GS + c / 4]), usc = e8m0_to_f32(rec[US + c / 4]);
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              if (t < T && ((tmask >> t) & 1u)) {
-                const uint4 xv = *reinterpret_cast<const uint4*>(x16 + t * XP + 8 * c);
-                ag[t] = fmaf(gsc, dot8_e2m1(gw, xv), ag[t]);
-                au[t] = fmaf(usc, dot8_e2m1(uw, xv), au[t]);
-              }
-            }
-          }
+      for (int m = 0; m < kMaxMt; ++m) {
+        if (m < nmt) {
+          *reinterpret_cast<float2*>(&s_part[warp][m][gq][2 * cq]) = make_float2(d[m][0], d[m][1]);
+          *reinterpret_cast<float2*>(&s_part[warp][m][gq + 8][2 * cq]) = make_float2(d[m][2], d[m][3]);
         }
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t) {
-          if (t < T && ((tmask >> t) & 1u)) {
-            const float gs = warp_sum(ag[t]);
-            const float us = warp_sum(au[t]);
-            if (lane == 0) {
-              if (P == 1) {   // routed record, whole row in this warp
-                const int j = rs.meta.slot_j[dd][t];
-                s_c[r][t] = rs.w[t * k + j] * swiglu(gs, us);
-              } else {
-                s_gu[r][p][t][0] = gs;
-                s_gu[r][p][t][1] = us;
-              }
-            }
-          } else if (P == 1 && lane == 0) {
-            s_c[r][t] = 0.f;   // token t does not use this record's expert
-          }
-        }
-      } else if (P == 1 && lane == 0) {
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t) s_c[r][t] = 0.f;
       }
     }
     consumers_sync();
-    if (P > 1) {
-      if ((int)threadIdx.x < RG * TMAX) {   // c = w * silu(g) * u per (record, token)
-        const int r = threadIdx.x / TMAX, t = threadIdx.x - r * TMAX;
-        float c = 0.f;
-        if (r < nvalid && t < T) {
-          int j = -1;
-          float w = 1.f;
-          if (!shared) {
-            const int dd = (int)((unsigned)(rg.u0 + first + r) / (unsigned)I);
-            j = rs.meta.slot_j[dd][t];
-            if (j >= 0) w = rs.w[t * k + j];
-          }
-          if (shared || j >= 0) {
-            float g = 0.f, u = 0.f;
-            for (int p = 0; p < P; ++p) {
-              g += s_gu[r][p][t][0];
-              u += s_gu[r][p][t][1];
-            }
-            c = w * swiglu(g, u);
-          }
+    if ((int)threadIdx.x < 2 * kMaxMx * 8) {   // c = w * silu(g) * u per (record r, token t)
+      // two lanes per (r, t): each adds half of the 16 warp partials, then they swap
+      const int r = threadIdx.x >> 4, t = (threadIdx.x >> 1) & 7, hf = threadIdx.x & 1;
+      const int m = r >> 3, rr = r & 7;
+      float g = 0.f, u = 0.f;
+      if (r < nvalid) {
+#pragma unroll
+        for (int q = 0; q < kConsumerWarps / 2; ++q) {
+          g += s_part[hf * 8 + q][m][rr][t];
+          u += s_part[hf * 8 + q][m][rr + 8][t];
         }
-        s_c[r][t] = c;
       }
-      consumers_sync();
-    }
-    if (s_abort) break;
-    // down: out[n][t] += c[r][t] * down_r[n] for this thread's 8 outputs, records in order
-    if (own) {
-      if (shared) {
-        for (int r = 0; r < nvalid; ++r) {
-          const uint4 dv = *reinterpret_cast<const uint4*>(base + (size_t)r * shs + 4 * H + 16 * q);
-          const float v[8] = {bf16_lo(dv.x), bf16_hi(dv.x), bf16_lo(dv.y), bf16_hi(dv.y),
-                              bf16_lo(dv.z), bf16_hi(dv.z), bf16_lo(dv.w), bf16_hi(dv.w)};
-#pragma unroll
-          for (int t = 0; t < TMAX; ++t) {
-            const float c = (t < T) ? s_c[r][t] : 0.f;
-            if (c != 0.f) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) acc[t][j] = fmaf(c, v[j], acc[t][j]);
-            }
-          }
+      g += __shfl_xor_sync(0xFFFFFFFFu, g, 1);
+      u += __shfl_xor_sync(0xFFFFFFFFu, u, 1);
+      float c = 0.f;
+      if (r < nvalid && t < T) {
+        int j = -1;
+        float w = 1.f;
+        if (!shared) {
+          const int dd = (int)((unsigned)(rg.u0 + first + r) / (unsigned)I);
+          j = rs.meta.slot_j[dd][t];
+          if (j >= 0) w = rs.w[t * k + j];
         }
-      } else {
-        // Records [0, r1) use the group's first down-scale vector, [r1, nvalid)
-        // the second: the group's features are consecutive, and a new vector
-        // starts at the next multiple of 32 (slot ends are multiples of 32 too).
-        const int i0 = (rg.u0 + first) - (int)((unsigned)(rg.u0 + first) / (unsigned)I) * I;
-        const int r1 = min(nvalid, 32 - (i0 & 31));
-        auto down_records = [&](int ra, int rb, const uint8_t* sv) {
-          const uint2 sb = *reinterpret_cast<const uint2*>(sv + 8 * q);
-          float f[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] = e8m0_to_f32(((j < 4 ? sb.x : sb.y) >> (8 * (j & 3))) & 0xFFu);
-          for (int r = ra; r < rb; ++r) {
-            const uint32_t cw = *reinterpret_cast<const uint32_t*>(base + (size_t)r * mxs + DC + 4 * q);
-            float v[8];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              const uint32_t f2 = e2m1x2_to_f16x2((cw >> (8 * h)) & 0xFFu);
-              const float2 ff = __half22float2(*reinterpret_cast<const __half2*>(&f2));
-              v[2 * h] = ff.x * f[2 * h];
-              v[2 * h + 1] = ff.y * f[2 * h + 1];
-            }
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-              const float c = (t < T) ? s_c[r][t] : 0.f;
-              if (c != 0.f) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[t][j] = fmaf(c, v[j], acc[t][j]);
-              }
-            }
-          }
-        };
-        down_records(0, r1, base + sv_off);
-        if (r1 < nvalid) down_records(r1, nvalid, base + sv_off + H);
+        if (shared || j >= 0) c = w * swiglu(g, u);
+      }
+      if (hf == 0) {
+        s_cf[t][r] = c;
+        atomicMax(cmax, __float_as_uint(fabsf(c)));   // positive floats order like their bits
+      }
+    }
+    consumers_sync();
+    if (s_abort) break;
+    // down tiles: out[n][t] += sum_r down_r[n] * c[r][t]
+    if (shared) {
+      uint32_t bhi, blo;
+      stream::bf16_hilo2(s_cf[gq][2 * cq], s_cf[gq][2 * cq + 1], bhi, blo);
+      stream::bf16_down_tiles<kMxMaxTiles>(sm100::smem_u32(base), shs, nvalid, H, ntile, zero_u32, bhi, blo, acc);
+    } else {
+      // c' = c * 2^-e with the group's largest |c'| in [2^14, 2^15): far inside
+      // the f16 range, and hi + lo keep ~22 significant bits of every c.
+      const unsigned mb = *cmax;
+      const int e = mb ? (int)((mb >> 23) & 0xFFu) - 127 - 14 : 0;
+      const int ec = max(-120, min(120, e));
+      const float down = __uint_as_float((uint32_t)(127 - ec) << 23), up = __uint_as_float((uint32_t)(127 + ec) << 23);
+      // records [0, r1) use the group's first down-scale vector, [r1, nvalid)
+      // the second: a new vector starts at the next multiple of 32 features
+      const int i0 = (rg.u0 + first) - (int)((unsigned)(rg.u0 + first) / (unsigned)I) * I;
+      const int r1 = min(nvalid, 32 - (i0 & 31));
+      const float* cr = s_cf[gq];
+      for (int v = 0; v < (r1 < nvalid ? 2 : 1); ++v) {
+        const int lo_r = v ? r1 : 0, hi_r = v ? nvalid : r1;
+        auto cv = [&](int r) { return (r >= lo_r && r < hi_r) ? cr[r] : 0.f; };
+        uint32_t bh0, bl0, bh1, bl1;
+        stream::f16_hilo2(cv(2 * cq), cv(2 * cq + 1), down, bh0, bl0);
+        stream::f16_hilo2(cv(2 * cq + 8), cv(2 * cq + 9), down, bh1, bl1);
+        stream::mx_down_tiles<kMxMaxTiles>(base, mxs, nvalid, ly, ntile, base + sv_off + v * H, up, bh0, bh1, bl0,
+                                           bl1, acc);
       }
     }
     __syncwarp();
@@ -446,17 +371,18 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
   }
 
   // ---------------------------------------------------------------- exchange of partial outputs
+  // acc[j]: rows n0 + gq (regs 0, 1) and n0 + gq + 8 (regs 2, 3), tokens 2 cq and 2 cq + 1;
+  // word (b, n, t) at (b * H + n) * TP + t (TP = T rounded up to even)
   const int TP = T + (T & 1);
-  if (own) {
+  if (2 * cq < T) {
 #pragma unroll
-    for (int t = 0; t < TMAX; t += 2) {
-      if (t < T) {
+    for (int j = 0; j < kMxMaxTiles; ++j) {
+      if (j < ntile) {
+        const int n0 = 16 * (warp + kConsumerWarps * j);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float v1 = (t + 1 < TMAX) ? acc[t + 1 < TMAX ? t + 1 : t][j] : 0.f;
-          stream::st_relaxed_v2u64(a.partial + ((size_t)b * H + 8 * q + j) * TP + t, tagged(tag, acc[t][j]),
-                                   tagged(tag, v1));
-        }
+        for (int h = 0; h < 2; ++h)
+          stream::st_relaxed_v2u64(a.partial + ((size_t)b * H + n0 + gq + 8 * h) * TP + 2 * cq,
+                                   tagged(tag, acc[j][2 * h]), tagged(tag, acc[j][2 * h + 1]));
       }
     }
   }
@@ -480,20 +406,21 @@ static int mx_slot_bytes(int H, int rgm) {
 }
 // 16 MXFP4 records per routed group when two such slots fit beside the two x copies, else 8.
 static int mx_group_records(int T, int H) {
-  const size_t room = (size_t)stream::kSmemMax - 2 * (size_t)mx_x_bytes(T, H);
+  const size_t room = (size_t)kMxSmemMax - 2 * (size_t)mx_x_bytes(T, H);
   return room >= 2 * (size_t)mx_slot_bytes(H, kMaxMx) ? kMaxMx : kMaxMx / 2;
 }
 static int mx_ring_groups(const moe_layer* L, int T) {
   const int H = L->cfg.hidden;
   const size_t xb = 2 * (size_t)mx_x_bytes(T, H);
-  if (xb >= (size_t)stream::kSmemMax) return 0;
-  return (int)std::min<size_t>((stream::kSmemMax - xb) / mx_slot_bytes(H, mx_group_records(T, H)), kMaxRingGroups);
+  if (xb >= (size_t)kMxSmemMax) return 0;
+  return (int)std::min<size_t>((kMxSmemMax - xb) / mx_slot_bytes(H, mx_group_records(T, H)), kMaxRingGroups);
 }
 
 bool stream_mx_supported(const moe_layer* L, int T) {
   const auto& c = L->cfg;
   if (c.weight_format != MOE_WEIGHTS_MXFP4 || !L->w_mx || !L->mx_dsc || !L->ws_rec) return false;
-  if (c.hidden > kMxMaxH || c.hidden % 256 != 0 || T < 1 || T > kMaxDecodeT) return false;
+  // 16 warps x whole 32-element blocks of H in the gate/up tiles
+  if (c.hidden > kMxMaxH || c.hidden % 512 != 0 || T < 1 || T > kMaxDecodeT) return false;
   if ((c.num_experts + L->num_sms - 1) / L->num_sms > stream::kMaxRouterRows) return false;
   const int ng = mx_ring_groups(L, T);
   if (ng < 2) return false;
@@ -542,7 +469,7 @@ cudaError_t stream_mx_prepare(moe_layer* L) {
   (void)L;
   cudaError_t e = cudaSuccess;
   auto set = [&](const void* f) {
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, stream::kSmemMax);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmemMax);
   };
   set((const void*)moe_decode_stream_mx_kernel<1>);
   set((const void*)moe_decode_stream_mx_kernel<2>);
