@@ -286,8 +286,8 @@ def run_ours(args):
     alg_bytes = float(np.mean([s.algorithmic_bytes for s in stats]))
     distinct = float(np.mean([s.distinct_experts for s in stats]))
 
-    # the decode path is one fused kernel per call: time that launch with CUDA
-    # events recorded on the launching stream around it
+    # the decode path is one kernel per call (moe_decode_stream_kernel): time that
+    # launch with CUDA events recorded on the launching stream around it
     stage_all = []
     for _ in range(max(1, args.steps // 2)):
         _, st = B.time_calls(L, xs, lbs, outs, profile=True)
@@ -310,7 +310,7 @@ def run_ours(args):
                   "warm_us_per_call": warm_us, "us_p50": float(np.median(times) * 1e3),
                   "us_p90": float(np.percentile(times, 90) * 1e3),
                   "distinct_experts_mean": distinct},
-        "roofline": {"kernel": "moe_decode_fused_kernel<1,bf16>", "bound": "hbm", "achieved": round(achieved, 1),
+        "roofline": {"kernel": "moe_decode_stream_kernel<1>", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": None, "peak_source": peaks["source"],
                      "bytes_per_launch": alg_bytes, "launch_us": round(k_us, 3)},
@@ -320,7 +320,7 @@ def run_ours(args):
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),
     }
-    traffic = _profile_traffic("moe_decode_fused_kernel")
+    traffic = _profile_traffic("moe_decode_stream_kernel")
     if traffic is not None:
         result["roofline"]["traffic"] = traffic
 
