@@ -226,15 +226,16 @@ MOE_DEV void mx_gu_tiles(const uint8_t* gbase, int stride, int nvalid, int nmt, 
 }
 
 // One warp's output tiles of the down projection of up to 16 MXFP4 records
-// (K = the records): acc[j] += sum_r code_r[n] * scale[n] * c[r][t] for tiles
-// n0 = 16 * (warp + 16 j). c comes as f16 hi + lo fragments scaled by 2^-cexp
-// (bh0, bh1: c'[2cq..2cq+1][token gq] and c'[2cq+8..2cq+9][gq]; bl0, bl1 the
-// low parts); records that use another scale vector have c = 0 here. sv: the
-// scale vector (H bytes, one per output row) of these records.
+// (K = the records): acc[j] += sum_r code_r[n] * scale_v(r)[n] * c[r][t] for
+// tiles n0 = 16 * (warp + 16 j). The records use one or two down-scale
+// vectors (nv; sv0, sv1: H bytes, one per output row). For vector v, c comes
+// as f16 hi + lo fragments scaled by 2^-cexp, with c = 0 for the records of
+// the other vector (bh[v][0..1]: c'[2cq..2cq+1][token gq], c'[2cq+8..2cq+9][gq];
+// bl[v] the low parts). A fragments are built once per tile for both vectors.
 template <int MAXTILES>
-MOE_DEV void mx_down_tiles(const uint8_t* gbase, int stride, int nvalid, const MxLayout& ly, int ntile,
-                           const uint8_t* sv, float cexp2, uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1,
-                           float (&acc)[MAXTILES][4]) {
+MOE_DEV void mx_down_tiles(const uint8_t* gbase, int stride, int nvalid, const MxLayout& ly, int ntile, int nv,
+                           const uint8_t* sv0, const uint8_t* sv1, float cexp2, const uint32_t (&bh)[2][2],
+                           const uint32_t (&bl)[2][2], float (&acc)[MAXTILES][4]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gq = lane >> 2, cq = lane & 3;
   const int ra = 2 * cq, rb = 2 * cq + 8;        // records of K columns 2cq.. and 2cq+8..
   const uint8_t* p0 = gbase + (size_t)ra * stride + ly.down_tiles + gq;
@@ -252,14 +253,20 @@ MOE_DEV void mx_down_tiles(const uint8_t* gbase, int stride, int nvalid, const M
       const uint32_t a1 = e2m1x2_to_f16x2((c0 >> 4) | (c1 & 0xF0u));          // row n0+g+8
       const uint32_t a2 = e2m1x2_to_f16x2((c2 & 0xFu) | ((c3 & 0xFu) << 4));
       const uint32_t a3 = e2m1x2_to_f16x2((c2 >> 4) | (c3 & 0xF0u));
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16816_f16(d, a0, a1, a2, a3, bh0, bh1);
-      mma_16816_f16(d, a0, a1, a2, a3, bl0, bl1);
-      const float f0 = e8m0_to_f32(sv[n0 + gq]) * cexp2, f1 = e8m0_to_f32(sv[n0 + gq + 8]) * cexp2;
-      acc[j][0] = fmaf(f0, d[0], acc[j][0]);
-      acc[j][1] = fmaf(f0, d[1], acc[j][1]);
-      acc[j][2] = fmaf(f1, d[2], acc[j][2]);
-      acc[j][3] = fmaf(f1, d[3], acc[j][3]);
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        if (v < nv) {
+          const uint8_t* sv = v ? sv1 : sv0;
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_16816_f16(d, a0, a1, a2, a3, bh[v][0], bh[v][1]);
+          mma_16816_f16(d, a0, a1, a2, a3, bl[v][0], bl[v][1]);
+          const float f0 = e8m0_to_f32(sv[n0 + gq]) * cexp2, f1 = e8m0_to_f32(sv[n0 + gq + 8]) * cexp2;
+          acc[j][0] = fmaf(f0, d[0], acc[j][0]);
+          acc[j][1] = fmaf(f0, d[1], acc[j][1]);
+          acc[j][2] = fmaf(f1, d[2], acc[j][2]);
+          acc[j][3] = fmaf(f1, d[3], acc[j][3]);
+        }
+      }
     }
   }
 }

@@ -346,15 +346,17 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
       const int i0 = (rg.u0 + first) - (int)((unsigned)(rg.u0 + first) / (unsigned)I) * I;
       const int r1 = min(nvalid, 32 - (i0 & 31));
       const float* cr = s_cf[gq];
-      for (int v = 0; v < (r1 < nvalid ? 2 : 1); ++v) {
+      const int nv = r1 < nvalid ? 2 : 1;
+      uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
         const int lo_r = v ? r1 : 0, hi_r = v ? nvalid : r1;
         auto cv = [&](int r) { return (r >= lo_r && r < hi_r) ? cr[r] : 0.f; };
-        uint32_t bh0, bl0, bh1, bl1;
-        stream::f16_hilo2(cv(2 * cq), cv(2 * cq + 1), down, bh0, bl0);
-        stream::f16_hilo2(cv(2 * cq + 8), cv(2 * cq + 9), down, bh1, bl1);
-        stream::mx_down_tiles<kMxMaxTiles>(base, mxs, nvalid, ly, ntile, base + sv_off + v * H, up, bh0, bh1, bl0,
-                                           bl1, acc);
+        stream::f16_hilo2(cv(2 * cq), cv(2 * cq + 1), down, bh[v][0], bl[v][0]);
+        stream::f16_hilo2(cv(2 * cq + 8), cv(2 * cq + 9), down, bh[v][1], bl[v][1]);
       }
+      stream::mx_down_tiles<kMxMaxTiles>(base, mxs, nvalid, ly, ntile, nv, base + sv_off, base + sv_off + H, up, bh,
+                                         bl, acc);
     }
     __syncwarp();
     if (lane == 0) sm100::mbar_arrive(&empty_bar[sg]);
