@@ -285,7 +285,8 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
         stream::bf16_gu_tile<kMxMaxKSteps>(sm100::smem_u32(base), shs, nvalid, H, T, XP, xs_u32, zero_u32,
                                            warp * (H / kConsumerWarps), H / kConsumerWarps / 16, d[0]);
       } else {
-        stream::mx_gu_tiles<kMaxMt>(base, mxs, nvalid, (nvalid + 7) / 8, ly, T, XP, x16, warp * nbw, nbw, d);
+        stream::mx_gu_tiles<kMaxMt, kMxMaxH / 512>(base, mxs, nvalid, (nvalid + 7) / 8, ly, T, XP, x16, warp * nbw,
+                                                   nbw, d);
       }
       const int nmt = shared ? 1 : (nvalid + 7) / 8;
 #pragma unroll
