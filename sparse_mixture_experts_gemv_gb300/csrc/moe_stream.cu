@@ -335,26 +335,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
   }
 
   // ---------------------------------------------------------------- exchange of partial outputs
-  // Publish: acc[j] holds rows n0 + gq (regs 0, 1) and n0 + gq + 8 (regs 2, 3)
-  // for tokens 2 cq and 2 cq + 1; word (b, n, t) sits at (b * H + n) * TP + t
-  // (TP = T rounded up to even, so each token pair is one 16-byte store).
-  const int TP = T + (T & 1);
-  if (2 * cq < T) {
 #pragma unroll
-    for (int j = 0; j < kMaxTiles; ++j) {
-      if (j < ntile) {
-        const int n0 = 16 * (warp + kConsumerWarps * j);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int n = n0 + gq + 8 * h;
-          st_relaxed_v2u64(a.partial + ((size_t)b * H + n) * TP + 2 * cq, tagged(tag, acc[j][2 * h]),
-                           tagged(tag, acc[j][2 * h + 1]));
-        }
-      }
-    }
-  }
-  consumers_sync();   // every warp is done reading the ring before it stages the exchange
-  stream::collect_outputs(a.partial, reinterpret_cast<float*>(ring), tag, T, H, a.out, a.err, &s_abort);
+  for (int j = 0; j < kMaxTiles; ++j)
+    if (j < ntile) stream::publish_tile(a.partial, b, H, T, 16 * (warp + kConsumerWarps * j), acc[j], tag);
+  consumers_sync();
+  stream::collect_outputs(a.partial, reinterpret_cast<unsigned long long*>(ring), (size_t)NG * RG * stride, tag, T, H, a.out, a.err, &s_abort);
   if (threadIdx.x == 0) leave();
 }
 
@@ -387,8 +372,7 @@ bool stream_supported(const moe_layer* L, int T) {
   const int ng = stream_ring_groups(L, T);
   if (ng < 2) return false;
   // the final exchange stages G x (rows of this CTA) x TP fp32 values in the ring
-  return stream::collect_stage_bytes(L->num_sms, c.hidden, T) <=
-         (size_t)ng * stream_group_records(T, c.hidden) * stream_record_stride(c.hidden);
+  return stream::collect_fits(L->num_sms, c.hidden, T, (size_t)ng * stream_group_records(T, c.hidden) * stream_record_stride(c.hidden));
 }
 
 template <int TMAX>

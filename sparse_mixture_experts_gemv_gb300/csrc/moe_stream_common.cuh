@@ -59,6 +59,14 @@ MOE_DEV unsigned long long tagged(unsigned long long tag, float v) {
 }
 // Barrier among the 16 consumer warps only (the producer warp never joins it).
 MOE_DEV void consumers_sync() { asm volatile("bar.sync 1, %0;" :: "n"(kConsumers) : "memory"); }
+// Consumer barrier that also returns whether any consumer thread passed a true v.
+MOE_DEV bool consumers_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, %2, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r) : "r"((uint32_t)v), "n"(kConsumers) : "memory");
+  return r != 0;
+}
 
 // Routing of the window, in shared memory.
 struct RouteSmem {
@@ -81,7 +89,7 @@ MOE_DEV void ldsm_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
 }
 // D = A(16x16, row) * B(16x8, col) + D; bf16 inputs, fp32 accumulators.
 MOE_DEV void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
                "{%0, %1, %2, %3};"
                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -89,7 +97,7 @@ MOE_DEV void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uin
 // Same with f16 inputs.
 MOE_DEV void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                            uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
                "{%0, %1, %2, %3};"
                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -177,18 +185,17 @@ MOE_DEV MxLayout mx_layout(int H, int so) { return MxLayout{H / 2, H, H + so, H 
 
 // One warp's part of the gate/up tiles of up to 16 MXFP4 records (tile m:
 // rows 0-7 = gate rows of records 8m .. 8m+7, rows 8-15 = their up rows), over
-// 32-element blocks [blk0, blk0 + nblk) of H. Each block's two k-steps go to a
+// 32-element blocks [blk0, blk0 + NBLK) of H. Each block's two k-steps go to a
 // fresh accumulator that is then scaled by the row's block scale and added.
 // x16: f16 x, rows XP halves apart. Records >= nvalid count as zero.
-template <int MAXMT, int MAXBLK>
+template <int MAXMT, int NBLK>
 MOE_DEV void mx_gu_tiles(const uint8_t* gbase, int stride, int nvalid, int nmt, const MxLayout& ly, int T, int XP,
-                         const uint16_t* x16, int blk0, int nblk, float (&out)[MAXMT][4]) {
+                         const uint16_t* x16, int blk0, float (&out)[MAXMT][4]) {
   const int lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
 #pragma unroll
   for (int m = 0; m < MAXMT; ++m) out[m][0] = out[m][1] = out[m][2] = out[m][3] = 0.f;
 #pragma unroll
-  for (int bi = 0; bi < MAXBLK; ++bi) {
-    if (bi >= nblk) break;
+  for (int bi = 0; bi < NBLK; ++bi) {
     const int blk = blk0 + bi;
     uint32_t b[2][2] = {{0u, 0u}, {0u, 0u}};   // x fragments of the block's two k-steps
     if (gq < T) {
@@ -229,15 +236,15 @@ MOE_DEV void mx_gu_tiles(const uint8_t* gbase, int stride, int nvalid, int nmt, 
 
 // One warp's output tiles of the down projection of up to 16 MXFP4 records
 // (K = the records): acc[j] += sum_r code_r[n] * scale_v(r)[n] * c[r][t] for
-// tiles n0 = 16 * (warp + 16 j). The records use one or two down-scale
+// tiles n0 = 16 * (warp + 16 j), j < NTILE = H / 256. The records use one or two down-scale
 // vectors (nv; sv0, sv1: H bytes, one per output row). For vector v, c comes
 // as f16 hi + lo fragments scaled by 2^-cexp, with c = 0 for the records of
 // the other vector (bh[v][0..1]: c'[2cq..2cq+1][token gq], c'[2cq+8..2cq+9][gq];
 // bl[v] the low parts). A fragments are built once per tile for both vectors.
-template <int MAXTILES>
-MOE_DEV void mx_down_tiles(const uint8_t* gbase, int stride, int nvalid, const MxLayout& ly, int ntile, int nv,
+template <int NTILE>
+MOE_DEV void mx_down_tiles(const uint8_t* gbase, int stride, int nvalid, const MxLayout& ly, int nv,
                            const uint8_t* sv0, const uint8_t* sv1, float cexp2, const uint32_t (&bh)[2][2],
-                           const uint32_t (&bl)[2][2], float (&acc)[MAXTILES][4]) {
+                           const uint32_t (&bl)[2][2], float (&acc)[NTILE][4]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gq = lane >> 2, cq = lane & 3;
   const int ra = 2 * cq, rb = 2 * cq + 8;        // records of K columns 2cq.. and 2cq+8..
   const uint8_t* p0 = gbase + (size_t)ra * stride + ly.down_tiles + gq;
@@ -246,8 +253,8 @@ MOE_DEV void mx_down_tiles(const uint8_t* gbase, int stride, int nvalid, const M
   const uint8_t* p3 = p2 + stride;
   const bool v0 = ra < nvalid, v1 = ra + 1 < nvalid, v2 = rb < nvalid, v3 = rb + 1 < nvalid;
 #pragma unroll
-  for (int j = 0; j < MAXTILES; ++j) {
-    if (j < ntile) {
+  for (int j = 0; j < NTILE; ++j) {
+    {
       const int tt = warp + kConsumerWarps * j, n0 = 16 * tt;
       const uint32_t c0 = v0 ? p0[8 * tt] : 0u, c1 = v1 ? p1[8 * tt] : 0u;
       const uint32_t c2 = v2 ? p2[8 * tt] : 0u, c3 = v3 ? p3[8 * tt] : 0u;
@@ -506,74 +513,145 @@ MOE_DEV void route_window(const unsigned long long* words, int T, int E, int k, 
   if (lane == 0) rs.meta.num_slots = D;
 }
 
-// Consumer warps, after this CTA published its partial outputs as tagged
-// words at partial[(b * H + n) * TP + t] (TP = T rounded up to even): this
-// CTA owns output rows [nb0, nb1) for every token. Each thread polls its share
-// of the G x rows x TP words (16 bytes at a time) until they carry this call's
-// tag and stages the values in shared memory (`stage`, G x rows x TP floats);
-// then one warp per output adds the G partials in a fixed order and writes
-// bf16. Ends with a consumer barrier.
-MOE_DEV void collect_outputs(const unsigned long long* partial, float* stage, unsigned long long tag, int T, int H,
-                             uint16_t* out, int* err, int* s_abort) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// ---------------------------------------------------------------------------
+// Exchange of partial outputs. Every CTA holds fp32 partial sums of all H
+// output rows over the records it streamed; the output is their sum over the
+// G CTAs. Each CTA publishes its partials as tagged words, word (b, n, t) at
+// (b * H + n) * TP + t, TP = exchange_pitch(T); CTA b then reduces the rows
+// [8 u0, 8 u1) of the 8-row units split evenly over the grid, for every token.
+// ---------------------------------------------------------------------------
+// Words per output row: T itself for one token, else T rounded up to even so
+// that a token pair is one 16-byte store.
+MOE_DEV int exchange_pitch(int T) { return T == 1 ? 1 : T + (T & 1); }
+
+struct RowSlice {
+  int n0, nrow;
+};
+MOE_DEV RowSlice exchange_rows(int b, int G, int H) {
+  const unsigned U = (unsigned)H / 8u;
+  const int u0 = (int)((unsigned)b * U / (unsigned)G), u1 = (int)((unsigned)(b + 1) * U / (unsigned)G);
+  return {8 * u0, 8 * (u1 - u0)};
+}
+
+// One output tile of this CTA's partials, straight from an mma accumulator
+// fragment: acc rows n0 + gq (regs 0, 1) and n0 + gq + 8 (regs 2, 3), tokens
+// 2 cq and 2 cq + 1. For odd T >= 3 the pad token's word is written too.
+MOE_DEV void publish_tile(unsigned long long* partial, int b, int H, int T, int n0, const float (&acc)[4],
+                          unsigned long long tag) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
+  const int TP = exchange_pitch(T);
+  if (T == 1) {
+    if (cq == 0) {
+      st_relaxed_u64(partial + (size_t)b * H + n0 + gq, tagged(tag, acc[0]));
+      st_relaxed_u64(partial + (size_t)b * H + n0 + gq + 8, tagged(tag, acc[2]));
+    }
+  } else if (2 * cq < T) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      st_relaxed_v2u64(partial + ((size_t)b * H + n0 + gq + 8 * h) * TP + 2 * cq, tagged(tag, acc[2 * h]),
+                       tagged(tag, acc[2 * h + 1]));
+  }
+}
+
+// Consumer warps, after every warp of this CTA has published its tiles: 16-byte
+// asynchronous copies (cp.async, no registers held) bring the published blocks
+// of this CTA's rows from all G CTAs into shared memory (`stage`, `stage_bytes`
+// of it; as many sources per pass as fit), all in flight at once. A pass in
+// which any word still carries an older tag is copied again. (One bulk copy
+// per source block was tried: the copy engine works through the G small
+// copies one after another, several microseconds in all.) Each output (row, token) is added by four
+// threads, thread i over the sources [iG/4, (i+1)G/4) in order, and the four
+// sums are combined as (s0 + s1) + (s2 + s3): a fixed order, so the result
+// does not depend on timing. Ends with a consumer barrier.
+MOE_DEV void collect_outputs(const unsigned long long* partial, unsigned long long* stage, size_t stage_bytes,
+                             unsigned long long tag, int T, int H, uint16_t* out, int* err, int* s_abort) {
   const int G = gridDim.x, b = blockIdx.x;
-  const int TP = T + (T & 1);
-  const int nb0 = (int)((unsigned)b * (unsigned)H / (unsigned)G);
-  const int nb1 = (int)((unsigned)(b + 1) * (unsigned)H / (unsigned)G);
-  const int nrow = nb1 - nb0;
-  const int per = nrow * TP / 2;                      // 16-byte units per CTA partial
-  const int units = G * per;
+  const int TP = exchange_pitch(T);
+  const RowSlice rs = exchange_rows(b, G, H);
+  const int blk_words = rs.nrow * TP;
+  const uint32_t blk_bytes = (uint32_t)blk_words * 8u;
+  const int nout = rs.nrow * T;
   const unsigned long long want = tag & 0xFFFFFFFFull;
-  for (int q0 = threadIdx.x; q0 < units; q0 += 8 * kConsumers) {
+  const int per_pass = (int)min((size_t)G, stage_bytes / (blk_bytes ? blk_bytes : 1u));
+  constexpr int kOut = 2;   // outputs per thread: 4 * nout <= kOut * kConsumers
+  float sum[kOut] = {0.f, 0.f};
+  bool aborted = *s_abort != 0;   // read after the caller's consumer barrier: the same in every thread
+  if (nout > 0) {
     const long long t0 = clock64();
-    while (true) {
-      unsigned long long v[8][2];
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int q = q0 + r * kConsumers;
-        v[r][0] = v[r][1] = want << 32;
-        if (q < units) {
-          const int p = q / per, w2 = q - p * per;
-          ld_relaxed_v2u64(partial + ((size_t)p * H + nb0) * TP + 2 * w2, v[r][0], v[r][1]);
+    for (int c0 = 0; c0 < G && !aborted; c0 += per_pass) {
+      const int pc = min(per_pass, G - c0);
+      while (true) {
+        const unsigned bu = (unsigned)blk_words / 2u;   // 16-byte units per source block
+        for (int u = threadIdx.x; u < pc * (int)bu; u += kConsumers) {
+          const int q = (int)((unsigned)u / bu), w = u - q * (int)bu;
+          sm100::cp_async_16(stage + (size_t)q * blk_words + 2 * w,
+                             partial + ((size_t)(c0 + q) * H + rs.n0) * TP + 2 * w, 16u);
         }
-      }
-      bool ok = true;   // (the pad token of odd T is written too, so both words are checked)
+        sm100::cp_async_commit();
+        sm100::cp_async_wait<0>();
+        consumers_sync();   // every thread's copies have landed
+        int stale = 0;
+        float add[kOut] = {0.f, 0.f};
 #pragma unroll
-      for (int r = 0; r < 8; ++r) ok &= (v[r][0] >> 32) == want && (v[r][1] >> 32) == want;
-      if (ok) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int q = q0 + r * kConsumers;
-          if (q < units)
-            *reinterpret_cast<float2*>(stage + 2 * (size_t)q) =
-                make_float2(__uint_as_float((uint32_t)v[r][0]), __uint_as_float((uint32_t)v[r][1]));
+        for (int r = 0; r < kOut; ++r) {
+          const int o4 = (int)threadIdx.x + r * kConsumers;
+          if (o4 < 4 * nout) {
+            const int o = o4 >> 2, i = o4 & 3;
+            const int nl = o / T, t = o - nl * T;
+            const int p0 = max(c0, (int)((unsigned)i * (unsigned)G / 4u));
+            const int p1 = min(c0 + pc, (int)((unsigned)(i + 1) * (unsigned)G / 4u));
+            const unsigned long long* src = stage + nl * TP + t;
+            float acc = 0.f;
+            for (int p = p0; p < p1; ++p) {
+              const unsigned long long w = src[(size_t)(p - c0) * blk_words];
+              stale |= (w >> 32) != want;
+              acc += __uint_as_float((uint32_t)w);
+            }
+            add[r] = acc;
+          }
         }
-        break;
-      }
-      if (clock64() - t0 > kSpinBudget) {
-        set_error(err, kDevTimeout);
-        *s_abort = 1;
-        break;
+        const bool give_up = threadIdx.x == 0 && clock64() - t0 > kSpinBudget;
+        // both reductions are barriers: every thread is done reading the stage
+        // before warp 0 copies into it again
+        if (consumers_sync_or(give_up)) {
+          if (threadIdx.x == 0) set_error(err, kDevTimeout);
+          aborted = true;
+          break;
+        }
+        if (!consumers_sync_or(stale)) {
+#pragma unroll
+          for (int r = 0; r < kOut; ++r) sum[r] += add[r];
+          break;
+        }
       }
     }
+    if (aborted && threadIdx.x == 0) *s_abort = 1;
   }
   consumers_sync();
-  if (!*s_abort) {
-    for (int o = warp; o < nrow * T; o += kConsumerWarps) {
-      const int nl = o / T, t = o - nl * T;
-      float sum = 0.f;
-      for (int p = lane; p < G; p += 32) sum += stage[((size_t)p * nrow + nl) * TP + t];
+  if (!aborted) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-      if (lane == 0) out[(size_t)t * H + nb0 + nl] = f32_to_bf16_rne(sum);
+    for (int r = 0; r < kOut; ++r) {
+      const int o4 = (int)threadIdx.x + r * kConsumers;   // lanes 4o .. 4o + 3 share one output
+      float v = sum[r];
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+      if (o4 < 4 * nout && (o4 & 3) == 0) {
+        const int o = o4 >> 2, nl = o / T, t = o - nl * T;
+        out[(size_t)t * H + rs.n0 + nl] = f32_to_bf16_rne(v);
+      }
     }
   }
   consumers_sync();
 }
 
-// Bytes of shared memory the exchange stages: G x ceil(H / G) x TP floats.
-inline size_t collect_stage_bytes(int G, int H, int T) {
-  return (size_t)G * ((size_t)(H + G - 1) / G) * (size_t)(T + (T & 1)) * 4;
+// Whether the exchange can run: one source's block of this CTA's rows fits in
+// the `stage_bytes` it is given, and four threads per output (row, token)
+// need at most two outputs per consumer thread.
+inline bool collect_fits(int G, int H, int T, size_t stage_bytes) {
+  const int U = H / 8;
+  const int nrow = 8 * ((U + G - 1) / G);
+  const int TP = T == 1 ? 1 : T + (T & 1);
+  return (size_t)nrow * TP * 8 <= stage_bytes && 4 * nrow * T <= 2 * kConsumers;
 }
 
 }  // namespace stream

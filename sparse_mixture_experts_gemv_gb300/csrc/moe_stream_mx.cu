@@ -65,8 +65,6 @@ constexpr int kMaxMx = 16;             // MXFP4 records per routed group: 16 (on
 constexpr int kShGroup = 4;            // bf16 shared-expert records per shared group (one MMA tile)
 constexpr int kMaxMt = kMaxMx / 8;     // 16-row gate/up tiles per group
 constexpr int kMxMaxH = kStreamMxMaxHidden;   // output tiles per warp kept in registers: H / 256
-constexpr int kMxMaxTiles = kMxMaxH / 256;
-constexpr int kMxMaxKSteps = kMxMaxH / 16 / 16;   // bf16 gate/up k-steps per warp (shared records)
 constexpr int kMxSmemMax = 204 * 1024;  // dynamic shared memory budget (the static part is ~19 KB)
 
 struct MxArgs {
@@ -96,7 +94,10 @@ struct MxArgs {
   int force_timeout;
 };
 
-template <int TMAX>
+// NT = H / 256: output tiles per warp, bf16 gate/up k-steps per warp (shared
+// records) and twice the MXFP4 blocks per warp, fixed at compile time so that
+// the tile loops are straight-line code.
+template <int TMAX, int NT>
 __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kernel(const MxArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                 // x [T][H + 8] bf16
@@ -257,14 +258,13 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
 
   // ---------------------------------------------------------------- consumers: groups
   const int gq = lane >> 2, cq = lane & 3;            // mma fragment coordinates
-  const int ntile = H / 256;                           // output tiles per warp (warp w: tiles w, w + 16, ...)
   const stream::MxLayout ly = stream::mx_layout(H, so);
-  const int nbw = H / 32 / kConsumerWarps;             // 32-element blocks per warp (gate/up)
+  constexpr int nbw = NT / 2;                          // 32-element blocks per warp (gate/up)
   const uint32_t xs_u32 = sm100::smem_u32(xs);
   const uint32_t zero_u32 = sm100::smem_u32(s_zero);
-  float acc[kMxMaxTiles][4];
+  float acc[NT][4];   // output tiles w, w + 16, ... of warp w
 #pragma unroll
-  for (int j = 0; j < kMxMaxTiles; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
   int grp = 0;
   for (; grp < ngroups; ++grp) {
@@ -282,11 +282,10 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
     {
       float d[kMaxMt][4];
       if (shared) {
-        stream::bf16_gu_tile<kMxMaxKSteps>(sm100::smem_u32(base), shs, nvalid, H, T, XP, xs_u32, zero_u32,
-                                           warp * (H / kConsumerWarps), H / kConsumerWarps / 16, d[0]);
+        stream::bf16_gu_tile<NT>(sm100::smem_u32(base), shs, nvalid, H, T, XP, xs_u32, zero_u32,
+                                 warp * (H / kConsumerWarps), NT, d[0]);
       } else {
-        stream::mx_gu_tiles<kMaxMt, kMxMaxH / 512>(base, mxs, nvalid, (nvalid + 7) / 8, ly, T, XP, x16, warp * nbw,
-                                                   nbw, d);
+        stream::mx_gu_tiles<kMaxMt, nbw>(base, mxs, nvalid, (nvalid + 7) / 8, ly, T, XP, x16, warp * nbw, d);
       }
       const int nmt = shared ? 1 : (nvalid + 7) / 8;
 #pragma unroll
@@ -334,7 +333,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
     if (shared) {
       uint32_t bhi, blo;
       stream::bf16_hilo2(s_cf[gq][2 * cq], s_cf[gq][2 * cq + 1], bhi, blo);
-      stream::bf16_down_tiles<kMxMaxTiles>(sm100::smem_u32(base), shs, nvalid, H, ntile, zero_u32, bhi, blo, acc);
+      stream::bf16_down_tiles<NT>(sm100::smem_u32(base), shs, nvalid, H, NT, zero_u32, bhi, blo, acc);
     } else {
       // c' = c * 2^-e with the group's largest |c'| in [2^14, 2^15): far inside
       // the f16 range, and hi + lo keep ~22 significant bits of every c.
@@ -356,7 +355,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
         stream::f16_hilo2(cv(2 * cq), cv(2 * cq + 1), down, bh[v][0], bl[v][0]);
         stream::f16_hilo2(cv(2 * cq + 8), cv(2 * cq + 9), down, bh[v][1], bl[v][1]);
       }
-      stream::mx_down_tiles<kMxMaxTiles>(base, mxs, nvalid, ly, ntile, nv, base + sv_off, base + sv_off + H, up, bh,
+      stream::mx_down_tiles<NT>(base, mxs, nvalid, ly, nv, base + sv_off, base + sv_off + H, up, bh,
                                          bl, acc);
     }
     __syncwarp();
@@ -374,23 +373,11 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
   }
 
   // ---------------------------------------------------------------- exchange of partial outputs
-  // acc[j]: rows n0 + gq (regs 0, 1) and n0 + gq + 8 (regs 2, 3), tokens 2 cq and 2 cq + 1;
-  // word (b, n, t) at (b * H + n) * TP + t (TP = T rounded up to even)
-  const int TP = T + (T & 1);
-  if (2 * cq < T) {
 #pragma unroll
-    for (int j = 0; j < kMxMaxTiles; ++j) {
-      if (j < ntile) {
-        const int n0 = 16 * (warp + kConsumerWarps * j);
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          stream::st_relaxed_v2u64(a.partial + ((size_t)b * H + n0 + gq + 8 * h) * TP + 2 * cq,
-                                   tagged(tag, acc[j][2 * h]), tagged(tag, acc[j][2 * h + 1]));
-      }
-    }
-  }
-  consumers_sync();   // every warp is done reading the ring before it stages the exchange
-  stream::collect_outputs(a.partial, reinterpret_cast<float*>(ring), tag, T, H, a.out, a.err, &s_abort);
+  for (int j = 0; j < NT; ++j)
+    stream::publish_tile(a.partial, b, H, T, 16 * (warp + kConsumerWarps * j), acc[j], tag);
+  consumers_sync();
+  stream::collect_outputs(a.partial, reinterpret_cast<unsigned long long*>(ring), (size_t)NG * a.slot_bytes, tag, T, H, a.out, a.err, &s_abort);
   if (threadIdx.x == 0) leave();
 }
 
@@ -427,11 +414,10 @@ bool stream_mx_supported(const moe_layer* L, int T) {
   if ((c.num_experts + L->num_sms - 1) / L->num_sms > stream::kMaxRouterRows) return false;
   const int ng = mx_ring_groups(L, T);
   if (ng < 2) return false;
-  return stream::collect_stage_bytes(L->num_sms, c.hidden, T) <=
-         (size_t)ng * mx_slot_bytes(c.hidden, mx_group_records(T, c.hidden));
+  return stream::collect_fits(L->num_sms, c.hidden, T, (size_t)ng * mx_slot_bytes(c.hidden, mx_group_records(T, c.hidden)));
 }
 
-template <int TMAX>
+template <int TMAX, int NT>
 static cudaError_t launch_stream_mx_t(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* lb,
                                       cudaStream_t s) {
   const auto& c = L->cfg;
@@ -463,9 +449,17 @@ static cudaError_t launch_stream_mx_t(moe_layer* L, const uint16_t* x, uint16_t*
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   prof_mark(L, s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_decode_stream_mx_kernel<TMAX>, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_decode_stream_mx_kernel<TMAX, NT>, a);
   prof_mark(L, s);
   return e;
+}
+
+template <int NT, typename F>
+static void set_all(F& set) {
+  set((const void*)moe_decode_stream_mx_kernel<1, NT>);
+  set((const void*)moe_decode_stream_mx_kernel<2, NT>);
+  set((const void*)moe_decode_stream_mx_kernel<4, NT>);
+  set((const void*)moe_decode_stream_mx_kernel<8, NT>);
 }
 
 cudaError_t stream_mx_prepare(moe_layer* L) {
@@ -474,18 +468,32 @@ cudaError_t stream_mx_prepare(moe_layer* L) {
   auto set = [&](const void* f) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmemMax);
   };
-  set((const void*)moe_decode_stream_mx_kernel<1>);
-  set((const void*)moe_decode_stream_mx_kernel<2>);
-  set((const void*)moe_decode_stream_mx_kernel<4>);
-  set((const void*)moe_decode_stream_mx_kernel<8>);
+  set_all<2>(set);
+  set_all<4>(set);
+  set_all<6>(set);
+  set_all<8>(set);
+  set_all<10>(set);
   return e;
 }
 
+template <int NT>
+static cudaError_t launch_stream_mx_nt(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* lb,
+                                       cudaStream_t s) {
+  if (T <= 1) return launch_stream_mx_t<1, NT>(L, x, out, T, lb, s);
+  if (T <= 2) return launch_stream_mx_t<2, NT>(L, x, out, T, lb, s);
+  if (T <= 4) return launch_stream_mx_t<4, NT>(L, x, out, T, lb, s);
+  return launch_stream_mx_t<8, NT>(L, x, out, T, lb, s);
+}
+
 cudaError_t launch_stream_mx(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* lb, cudaStream_t s) {
-  if (T <= 1) return launch_stream_mx_t<1>(L, x, out, T, lb, s);
-  if (T <= 2) return launch_stream_mx_t<2>(L, x, out, T, lb, s);
-  if (T <= 4) return launch_stream_mx_t<4>(L, x, out, T, lb, s);
-  return launch_stream_mx_t<8>(L, x, out, T, lb, s);
+  switch (L->cfg.hidden / 256) {   // H % 512 == 0, H <= 2560 (stream_mx_supported)
+    case 2: return launch_stream_mx_nt<2>(L, x, out, T, lb, s);
+    case 4: return launch_stream_mx_nt<4>(L, x, out, T, lb, s);
+    case 6: return launch_stream_mx_nt<6>(L, x, out, T, lb, s);
+    case 8: return launch_stream_mx_nt<8>(L, x, out, T, lb, s);
+    case 10: return launch_stream_mx_nt<10>(L, x, out, T, lb, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace moe

@@ -86,6 +86,18 @@ def test_small_mxfp4_every_window_size(T):
     G.compare(S, x, out, idx, wt, fmt="mxfp4")
 
 
+@pytest.mark.parametrize("H,fmt,T", [(4096, "bf16", 1), (4096, "bf16", 5), (768, "mxfp4", 1), (768, "mxfp4", 3)])
+def test_three_phase_kernel_shapes(H, fmt, T):
+    """Shapes the record-streaming kernels do not take (bf16 with H > 2048, MXFP4 with H not a
+    multiple of 512) run on the three-phase decode kernel; same parity bar."""
+    S = mi.custom_layer(H=H, E=8, k=2, I=128, Is=128, fmt=fmt, seed=11)
+    L = G.cuda_layer(S.spec, max_tokens=8)
+    assert "moe_decode_fused_kernel" in L.describe()
+    x = mi.tokens(S.spec, T, stream=300 + T)
+    out, idx, wt = G.run_cuda(L, x)
+    G.compare(S, x, out, idx, wt, fmt=fmt)
+
+
 def test_deterministic_and_batch_invariant():
     w = mi.WORKLOADS["qwen_verify"]
     L = G.cuda_layer(w.layer, max_tokens=4096)
