@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
   for (int j = 0; j < kMaxTiles; ++j)
     if (j < ntile) stream::publish_tile(a.partial, b, H, T, 16 * (warp + kConsumerWarps * j), acc[j], tag);
   consumers_sync();
-  stream::collect_outputs(a.partial, reinterpret_cast<unsigned long long*>(ring), (size_t)NG * RG * stride, tag, T, H, a.out, a.err, &s_abort);
+  stream::collect_outputs<true>(a.partial, reinterpret_cast<unsigned long long*>(ring), (size_t)NG * RG * stride, tag, T, H, a.out, a.err, &s_abort);
   if (threadIdx.x == 0) leave();
 }
 

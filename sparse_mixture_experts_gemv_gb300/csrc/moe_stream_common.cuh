@@ -556,15 +556,21 @@ MOE_DEV void publish_tile(unsigned long long* partial, int b, int H, int T, int 
 // Consumer warps, after every warp of this CTA has published its tiles: 16-byte
 // asynchronous copies (cp.async, no registers held) bring the published blocks
 // of this CTA's rows from all G CTAs into shared memory (`stage`, `stage_bytes`
-// of it; as many sources per pass as fit), all in flight at once. A pass in
-// which any word still carries an older tag is copied again. (One bulk copy
-// per source block was tried: the copy engine works through the G small
-// copies one after another, several microseconds in all.) Each output (row, token) is added by four
-// threads, thread i over the sources [iG/4, (i+1)G/4) in order, and the four
-// sums are combined as (s0 + s1) + (s2 + s3): a fixed order, so the result
-// does not depend on timing. Ends with a consumer barrier.
+// of it; as many sources per pass as fit); a copy that still carries an older
+// tag is made again. Two ways to retry: PER_WARP -- warp w owns the sources
+// p = w mod 16 of a pass and copies again the ones that are not current, on its
+// own, so that a late CTA's block is picked up one round trip after it lands;
+// otherwise the whole pass is copied again after a consumer barrier (fewer
+// registers; faster in the MXFP4 kernel, measured). (One bulk copy per source
+// block was tried: the copy engine works through the G small copies one after
+// another, several microseconds in all.) Each output (row, token) is then added
+// by four threads, thread i over the sources [iG/4, (i+1)G/4) in order, and the
+// four sums are combined as (s0 + s1) + (s2 + s3): a fixed order, so the
+// result does not depend on timing. Ends with a consumer barrier.
+template <bool PER_WARP>
 MOE_DEV void collect_outputs(const unsigned long long* partial, unsigned long long* stage, size_t stage_bytes,
                              unsigned long long tag, int T, int H, uint16_t* out, int* err, int* s_abort) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, b = blockIdx.x;
   const int TP = exchange_pitch(T);
   const RowSlice rs = exchange_rows(b, G, H);
@@ -573,6 +579,7 @@ MOE_DEV void collect_outputs(const unsigned long long* partial, unsigned long lo
   const int nout = rs.nrow * T;
   const unsigned long long want = tag & 0xFFFFFFFFull;
   const int per_pass = (int)min((size_t)G, stage_bytes / (blk_bytes ? blk_bytes : 1u));
+  const unsigned bu = (unsigned)blk_words / 2u;   // 16-byte units per source block
   constexpr int kOut = 2;   // outputs per thread: 4 * nout <= kOut * kConsumers
   float sum[kOut] = {0.f, 0.f};
   bool aborted = *s_abort != 0;   // read after the caller's consumer barrier: the same in every thread
@@ -580,50 +587,80 @@ MOE_DEV void collect_outputs(const unsigned long long* partial, unsigned long lo
     const long long t0 = clock64();
     for (int c0 = 0; c0 < G && !aborted; c0 += per_pass) {
       const int pc = min(per_pass, G - c0);
-      while (true) {
-        const unsigned bu = (unsigned)blk_words / 2u;   // 16-byte units per source block
-        for (int u = threadIdx.x; u < pc * (int)bu; u += kConsumers) {
-          const int q = (int)((unsigned)u / bu), w = u - q * (int)bu;
-          sm100::cp_async_16(stage + (size_t)q * blk_words + 2 * w,
-                             partial + ((size_t)(c0 + q) * H + rs.n0) * TP + 2 * w, 16u);
-        }
-        sm100::cp_async_commit();
-        sm100::cp_async_wait<0>();
-        consumers_sync();   // every thread's copies have landed
-        int stale = 0;
-        float add[kOut] = {0.f, 0.f};
-#pragma unroll
-        for (int r = 0; r < kOut; ++r) {
-          const int o4 = (int)threadIdx.x + r * kConsumers;
-          if (o4 < 4 * nout) {
-            const int o = o4 >> 2, i = o4 & 3;
-            const int nl = o / T, t = o - nl * T;
-            const int p0 = max(c0, (int)((unsigned)i * (unsigned)G / 4u));
-            const int p1 = min(c0 + pc, (int)((unsigned)(i + 1) * (unsigned)G / 4u));
-            const unsigned long long* src = stage + nl * TP + t;
-            float acc = 0.f;
-            for (int p = p0; p < p1; ++p) {
-              const unsigned long long w = src[(size_t)(p - c0) * blk_words];
-              stale |= (w >> 32) != want;
-              acc += __uint_as_float((uint32_t)w);
+      bool timed_out = false;
+      if constexpr (PER_WARP) {
+        // this warp's sources q = warp, warp + 16, ... of the pass: copy until every word is current
+        const int nq = (pc - warp + kConsumerWarps - 1) / kConsumerWarps;
+        uint32_t todo = nq > 0 ? (nq >= 32 ? 0xFFFFFFFFu : (1u << nq) - 1u) : 0u;   // bit j: source warp + 16 j
+        while (todo) {
+          for (unsigned u = (unsigned)lane; u < (unsigned)nq * bu; u += 32u) {
+            const int jq = (int)(u / bu), w = (int)(u - (unsigned)jq * bu);
+            if ((todo >> jq) & 1u) {
+              const int q = warp + kConsumerWarps * jq;
+              sm100::cp_async_16(stage + (size_t)q * blk_words + 2 * w,
+                                 partial + ((size_t)(c0 + q) * H + rs.n0) * TP + 2 * w, 16u);
             }
-            add[r] = acc;
+          }
+          sm100::cp_async_commit();
+          sm100::cp_async_wait<0>();
+          __syncwarp();   // the warp's copies have landed
+          uint32_t stale = 0u;
+          for (unsigned u = (unsigned)lane; u < (unsigned)nq * (unsigned)blk_words; u += 32u) {
+            const int jq = (int)(u / (unsigned)blk_words), w = (int)(u - (unsigned)jq * (unsigned)blk_words);
+            if ((todo >> jq) & 1u) {
+              const int q = warp + kConsumerWarps * jq;
+              if ((stage[(size_t)q * blk_words + w] >> 32) != want) stale |= 1u << jq;
+            }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) stale |= __shfl_xor_sync(0xFFFFFFFFu, stale, o);
+          todo = stale;
+          if (todo && clock64() - t0 > kSpinBudget) {
+            timed_out = true;
+            break;
           }
         }
-        const bool give_up = threadIdx.x == 0 && clock64() - t0 > kSpinBudget;
-        // both reductions are barriers: every thread is done reading the stage
-        // before warp 0 copies into it again
-        if (consumers_sync_or(give_up)) {
-          if (threadIdx.x == 0) set_error(err, kDevTimeout);
-          aborted = true;
-          break;
-        }
-        if (!consumers_sync_or(stale)) {
-#pragma unroll
-          for (int r = 0; r < kOut; ++r) sum[r] += add[r];
-          break;
+      } else {
+        while (true) {
+          for (int u = threadIdx.x; u < pc * (int)bu; u += kConsumers) {
+            const int q = (int)((unsigned)u / bu), w = u - q * (int)bu;
+            sm100::cp_async_16(stage + (size_t)q * blk_words + 2 * w,
+                               partial + ((size_t)(c0 + q) * H + rs.n0) * TP + 2 * w, 16u);
+          }
+          sm100::cp_async_commit();
+          sm100::cp_async_wait<0>();
+          consumers_sync();   // every thread's copies have landed
+          bool stale = false;
+          for (int u = threadIdx.x; u < pc * blk_words; u += kConsumers) stale |= (stage[u] >> 32) != want;
+          // a barrier: every thread is done reading the stage before it is copied into again
+          if (!consumers_sync_or(stale)) break;
+          if (consumers_sync_or(threadIdx.x == 0 && clock64() - t0 > kSpinBudget)) {   // one decision for all
+            timed_out = true;
+            break;
+          }
         }
       }
+      // the pass is complete in every warp; the stage is read, then copied into again
+      if (consumers_sync_or(timed_out)) {
+        if (threadIdx.x == 0) set_error(err, kDevTimeout);
+        aborted = true;
+        break;
+      }
+#pragma unroll
+      for (int r = 0; r < kOut; ++r) {
+        const int o4 = (int)threadIdx.x + r * kConsumers;
+        if (o4 < 4 * nout) {
+          const int o = o4 >> 2, i = o4 & 3;
+          const int nl = o / T, t = o - nl * T;
+          const int p0 = max(c0, (int)((unsigned)i * (unsigned)G / 4u));
+          const int p1 = min(c0 + pc, (int)((unsigned)(i + 1) * (unsigned)G / 4u));
+          const unsigned long long* src = stage + nl * TP + t;
+          float acc = sum[r];
+          for (int p = p0; p < p1; ++p) acc += __uint_as_float((uint32_t)src[(size_t)(p - c0) * blk_words]);
+          sum[r] = acc;
+        }
+      }
+      if (c0 + pc < G) consumers_sync();
     }
     if (aborted && threadIdx.x == 0) *s_abort = 1;
   }

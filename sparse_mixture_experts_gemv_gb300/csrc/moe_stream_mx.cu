@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
   for (int j = 0; j < NT; ++j)
     stream::publish_tile(a.partial, b, H, T, 16 * (warp + kConsumerWarps * j), acc[j], tag);
   consumers_sync();
-  stream::collect_outputs(a.partial, reinterpret_cast<unsigned long long*>(ring), (size_t)NG * a.slot_bytes, tag, T, H, a.out, a.err, &s_abort);
+  stream::collect_outputs<false>(a.partial, reinterpret_cast<unsigned long long*>(ring), (size_t)NG * a.slot_bytes, tag, T, H, a.out, a.err, &s_abort);
   if (threadIdx.x == 0) leave();
 }
 
