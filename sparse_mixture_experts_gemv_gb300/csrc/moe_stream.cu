@@ -154,40 +154,56 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
 
   const Ranges rg0 = cta_ranges(b, G, Is, 0);   // shared range does not depend on routing
   const int ns = rg0.sh1 - rg0.sh0;
-  const int nsg = (ns + RG - 1) / RG;           // shared groups
+  // A CTA's records are its ns shared-expert records, then its routed records,
+  // cut into groups of RG: groups [0, ns / RG) are all shared and go out before
+  // routing; a group that starts in the shared part and ends in the routed part
+  // ("mixed") has its shared records copied before routing and the rest after.
+  const int nfull_sh = ns / RG;                 // all-shared groups
+  const int gmix = (ns % RG) ? nfull_sh : -1;   // the mixed group, if any
 
   // ---------------------------------------------------------------- producer: x + shared records
-  // Whole producer warp: lane 0 posts the group's byte count and copies each
-  // contiguous run of records (a routed group may cross from one expert's last
+  // Lane 0 of the producer warp posts a group's byte count and copies each
+  // contiguous run of records (routed records may cross from one expert's last
   // feature to the next slot's first).
-  auto issue_group = [&](int grp, int u0, int nr) {
+  auto copy_shared = [&](uint8_t* dst, int p0, int cnt, uint64_t* bar) {
+    sm100::bulk_copy_g2s(dst, a.rec_sh + (size_t)(rg0.sh0 + p0) * stride, (uint32_t)(cnt * stride), bar);
+  };
+  auto copy_routed = [&](uint8_t* dst, int u, int cnt, uint64_t* bar) {
+    while (cnt > 0) {
+      const unsigned d = (unsigned)u / (unsigned)I, i = (unsigned)u - d * (unsigned)I;
+      const int run = min(cnt, I - (int)i);
+      sm100::bulk_copy_g2s(dst, a.rec + ((size_t)rs.meta.slot_expert[d] * I + i) * stride, (uint32_t)(run * stride),
+                           bar);
+      dst += (size_t)run * stride;
+      u += run;
+      cnt -= run;
+    }
+  };
+  // part: 0 = all of the group, 1 = its shared records only (before routing), 2 = the rest
+  auto issue_group = [&](int grp, int part, int u0, int nr) {
     const int sg = grp % NG;
     uint8_t* dst = ring + (size_t)sg * RG * stride;
     if (lane == 0) {
-      if (grp < nsg) {
-        const int first = grp * RG, n = min(RG, ns - first);
-        sm100::mbar_arrive_expect_tx(&full_bar[sg], (uint32_t)(n * stride));
-        sm100::bulk_copy_g2s(dst, a.rec_sh + (size_t)(rg0.sh0 + first) * stride, (uint32_t)(n * stride),
-                             &full_bar[sg]);
+      const int p0 = grp * RG;
+      const int p1 = part == 1 ? min(ns, p0 + RG) : min(ns + nr, p0 + RG);
+      const int sh_n = max(0, min(ns, p1) - p0);
+      const int rt_n = part == 1 ? 0 : (p1 - p0) - sh_n;
+      if (part == 1) {
+        if (grp == gmix) sm100::mbar_expect_tx(&full_bar[sg], (uint32_t)(sh_n * stride));
+        else sm100::mbar_arrive_expect_tx(&full_bar[sg], (uint32_t)(sh_n * stride));
+        copy_shared(dst, p0, sh_n, &full_bar[sg]);
+      } else if (part == 2) {
+        sm100::mbar_arrive_expect_tx(&full_bar[sg], (uint32_t)(rt_n * stride));
+        copy_routed(dst + (size_t)sh_n * stride, u0 + max(0, p0 - ns), rt_n, &full_bar[sg]);
       } else {
-        const int first = (grp - nsg) * RG, n = min(RG, nr - first);
-        sm100::mbar_arrive_expect_tx(&full_bar[sg], (uint32_t)(n * stride));
-        unsigned u = (unsigned)(u0 + first);
-        int left = n;
-        while (left > 0) {
-          const unsigned d = u / (unsigned)I, i = u - d * (unsigned)I;
-          const int run = min(left, I - (int)i);
-          sm100::bulk_copy_g2s(dst, a.rec + ((size_t)rs.meta.slot_expert[d] * I + i) * stride, (uint32_t)(run * stride),
-                               &full_bar[sg]);
-          dst += (size_t)run * stride;
-          u += run;
-          left -= run;
-        }
+        sm100::mbar_arrive_expect_tx(&full_bar[sg], (uint32_t)((sh_n + rt_n) * stride));
+        if (sh_n > 0) copy_shared(dst, p0, sh_n, &full_bar[sg]);
+        copy_routed(dst + (size_t)sh_n * stride, u0 + max(0, p0 - ns), rt_n, &full_bar[sg]);
       }
     }
     __syncwarp();
   };
-  int issued = 0;   // groups issued (producer warp)
+  const int npre = min(NG, nfull_sh + (gmix >= 0 ? 1 : 0));   // groups whose shared records go out before routing
   if (producer) {
     if (lane == 0) {
       sm100::mbar_arrive_expect_tx(&x_bar, (uint32_t)(T * H * 2));
@@ -202,7 +218,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
       sm100::mbar_wait(&x_bar, 0, a.err, &never, kSpinBudget, false);
     }
     __syncwarp();
-    for (; issued < nsg && issued < NG; ++issued) issue_group(issued, 0, 0);
+    for (int g = 0; g < npre; ++g) issue_group(g, 1, 0, 0);
   }
 
   // ---------------------------------------------------------------- consumers: router logits, routing
@@ -216,11 +232,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
   __syncthreads();   // routing known to every warp, producer included
   if (s_abort) {
     // nothing routed was issued; let x and the shared-expert copies land first
+    // (the mixed group's phase still needs its arrival)
     if (threadIdx.x == 0) {
       volatile int never = 0;
       sm100::mbar_wait(&x_bar, 0, a.err, &never, 20000000LL, false);
-      for (int g2 = 0; g2 < nsg && g2 < NG; ++g2)
+      for (int g2 = 0; g2 < npre; ++g2) {
+        if (g2 == gmix) sm100::mbar_arrive(&full_bar[g2]);
         sm100::mbar_wait(&full_bar[g2], 0, a.err, &never, 20000000LL, false);
+      }
       leave();
     }
     return;
@@ -230,7 +249,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
   const int U = D * I;
   const Ranges rg = cta_ranges(b, G, Is, U);
   const int nr = rg.u1 - rg.u0;
-  const int ngroups = nsg + (nr + RG - 1) / RG;
+  const int ngroups = (ns + nr + RG - 1) / RG;
 
   if (b == 0 && !producer) {   // diagnostics copy of the routing
     for (int q = threadIdx.x; q < T * k; q += kConsumers) {
@@ -244,7 +263,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
 
   // ---------------------------------------------------------------- producer: routed records
   if (producer) {
-    for (; issued < ngroups; ++issued) {
+    if (gmix >= 0 && gmix < npre) issue_group(gmix, 2, rg.u0, nr);   // the mixed group's routed records
+    for (int issued = npre; issued < ngroups; ++issued) {
       bool go = !s_abort;
       if (go && issued >= NG && lane == 0) {
         const int sg = issued % NG;
@@ -252,7 +272,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
         go = sm100::mbar_wait(&empty_bar[sg], par, a.err, &s_abort, kSpinBudget);
       }
       if (!__shfl_sync(0xFFFFFFFFu, go, 0)) break;
-      issue_group(issued, rg.u0, nr);
+      issue_group(issued, 0, rg.u0, nr);
     }
     return;   // the consumers outlive every copy issued here (they wait for each)
   }
@@ -271,9 +291,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
   int grp = 0;
   for (; grp < ngroups; ++grp) {
     const int sg = grp % NG;
-    const bool shared = grp < nsg;
-    const int first = shared ? grp * RG : (grp - nsg) * RG;
-    const int nvalid = min(RG, (shared ? ns : nr) - first);
+    const int first = grp * RG;                    // position of the group's first record in the CTA's list
+    const int nvalid = min(RG, ns + nr - first);
     const uint32_t gbase = sm100::smem_u32(ring + (size_t)sg * RG * stride);
     sm100::mbar_wait(&full_bar[sg], (uint32_t)(grp / NG) & 1u, a.err, &s_abort, kSpinBudget);
 
@@ -299,10 +318,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
       u += __shfl_xor_sync(0xFFFFFFFFu, u, 1);
       float c = 0.f;
       if (r < nvalid && t < T) {
+        const bool shared = first + r < ns;
         int j = -1;
         float w = 1.f;
         if (!shared) {
-          const int dd = (int)((unsigned)(rg.u0 + first + r) / (unsigned)I);
+          const int dd = (int)((unsigned)(rg.u0 + first + r - ns) / (unsigned)I);
           j = rs.meta.slot_j[dd][t];
           if (j >= 0) w = rs.w[t * k + j];
         }
