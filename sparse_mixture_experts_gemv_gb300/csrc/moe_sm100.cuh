@@ -49,12 +49,20 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait until the phase with the given parity has completed. Gives up after
 // ~`budget_cycles` SM cycles: records MOE_ERR_TIMEOUT in *err and sets *abort so
 // that every role of the CTA winds down instead of hanging the GPU.
+// try_wait that lets the thread sleep until the phase completes (or ~20 us pass)
+MOE_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(20000u) : "memory");
+  return ok != 0;
+}
 MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, volatile int* abort,
                        long long budget_cycles = 4000000000LL, bool stop_on_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (stop_on_abort && *abort) return false;
     if (clock64() - t0 > budget_cycles) {
       set_error(err, kDevTimeout);
