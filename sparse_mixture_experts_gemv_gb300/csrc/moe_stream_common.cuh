@@ -473,22 +473,29 @@ MOE_DEV void route_window(const unsigned long long* words, int T, int E, int k, 
     return;
   }
   const int n = T * k;
-  bool first[2] = {false, false};
-  int firstpos[2] = {0, 0};
+  // assignment ai = lane + 32 h2; its expert's first position in the window:
+  // __match_any_sync finds it among positions 0-31 (and, for h2 = 1, among
+  // 32-63), a shuffle scan checks positions 0-31 for h2 = 1 (T * k > 32 only)
+  int e2[2];
 #pragma unroll
   for (int h2 = 0; h2 < 2; ++h2) {
     const int ai = lane + 32 * h2;
-    if (ai < n) {
-      const int e = rs.idx[ai];
-      if (e < 0 || e >= E) {
-        set_error(err, kDevCheck);
-        *s_abort = 1;
-      }
-      int q = 0;
-      while (rs.idx[q] != e) ++q;
-      first[h2] = (q == ai);
-      firstpos[h2] = q;
+    e2[h2] = ai < n ? rs.idx[ai] : -1 - ai;   // a value no other lane holds
+    if (ai < n && (e2[h2] < 0 || e2[h2] >= E)) {
+      set_error(err, kDevCheck);
+      *s_abort = 1;
     }
+  }
+  bool first[2] = {false, false};
+  int firstpos[2] = {0, 0};
+  firstpos[0] = __ffs(__match_any_sync(0xFFFFFFFFu, e2[0])) - 1;
+  first[0] = lane < n && firstpos[0] == lane;
+  if (n > 32) {
+    int pos = 32 + __ffs(__match_any_sync(0xFFFFFFFFu, e2[1])) - 1;
+    for (int j = 31; j >= 0; --j)
+      if (__shfl_sync(0xFFFFFFFFu, e2[0], j) == e2[1]) pos = j;
+    firstpos[1] = pos;
+    first[1] = lane + 32 < n && pos == lane + 32;
   }
   const unsigned m0 = __ballot_sync(0xFFFFFFFFu, first[0]);
   const unsigned m1 = __ballot_sync(0xFFFFFFFFu, first[1]);
