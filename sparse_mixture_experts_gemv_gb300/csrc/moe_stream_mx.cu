@@ -42,6 +42,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "moe_common.cuh"
 #include "moe_internal.h"
 #include "moe_sm100.cuh"
@@ -266,10 +268,12 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
 #pragma unroll
   for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
-  int grp = 0;
-  for (; grp < ngroups; ++grp) {
+  // One group; the shared (bf16) and routed (MXFP4) groups run in two loops so
+  // that each loop body holds one kind's code (the loop stays in the
+  // instruction cache). Returns false when the CTA aborts.
+  auto run_group = [&](auto kind, int grp) -> bool {
+    constexpr bool shared = decltype(kind)::value;
     const int sg = grp % NG;
-    const bool shared = grp < nsg;
     const int RG = shared ? kShGroup : RGM;
     const int first = shared ? grp * kShGroup : (grp - nsg) * RGM;
     const int nvalid = min(RG, (shared ? ns : nr) - first);
@@ -281,7 +285,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
     // gate/up tiles (tile m: gate rows of records 8m..8m+7, then their up rows), this warp's part of K
     {
       float d[kMaxMt][4];
-      if (shared) {
+      if constexpr (shared) {
         stream::bf16_gu_tile<NT>(sm100::smem_u32(base), shs, nvalid, H, T, XP, xs_u32, zero_u32,
                                  warp * (H / kConsumerWarps), NT, d[0]);
       } else {
@@ -328,9 +332,9 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
       }
     }
     consumers_sync();
-    if (s_abort) break;
+    if (s_abort) return false;
     // down tiles: out[n][t] += sum_r down_r[n] * c[r][t]
-    if (shared) {
+    if constexpr (shared) {
       uint32_t bhi, blo;
       stream::bf16_hilo2(s_cf[gq][2 * cq], s_cf[gq][2 * cq + 1], bhi, blo);
       stream::bf16_down_tiles<NT>(sm100::smem_u32(base), shs, nvalid, H, NT, zero_u32, bhi, blo, acc);
@@ -360,7 +364,14 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
     }
     __syncwarp();
     if (lane == 0) sm100::mbar_arrive(&empty_bar[sg]);
-  }
+    return true;
+  };
+  int grp = 0;
+  for (; grp < nsg; ++grp)
+    if (!run_group(std::true_type{}, grp)) break;
+  if (!s_abort)
+    for (; grp < ngroups; ++grp)
+      if (!run_group(std::false_type{}, grp)) break;
   if (s_abort) {
     // let copies still in flight land before the CTA's shared memory goes away
     if (threadIdx.x == 0) {
