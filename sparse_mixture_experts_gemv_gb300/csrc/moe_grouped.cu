@@ -395,25 +395,67 @@ dispatch_scan_kernel(int* __restrict__ chunk_counts /* in: counts, out: bases */
   pdl_wait();
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int e = warp; e < E; e += 32) {
-    int* row = chunk_counts + (size_t)e * num_chunks;
-    int run = 0;
-    for (int c0 = 0; c0 < num_chunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = c < num_chunks ? row[c] : 0;
-      int incl = v;
+  // Scan of one expert's chunk counts; v holds chunks c0 + lane, c0 + 32 + lane, ...
+  auto scan_row = [&](int e, int* row, int c0, int nq, const int (&v)[4], int& run) {
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += n;
+    for (int q = 0; q < 4; ++q) {
+      if (q < nq) {
+        const int c = c0 + 32 * q + lane;
+        int incl = v[q];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        if (c < num_chunks) row[c] = run + incl - v[q];   // exclusive base of chunk c for expert e
+        run += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
-      if (c < num_chunks) row[c] = run + incl - v;   // exclusive base of chunk c for expert e
-      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
-    if (lane == 0) {
-      hist[e] = run;
-      s_tot[e] = run;
-      s_tiles[e] = (run + BM - 1) / BM;
+  };
+  if (num_chunks <= 128) {
+    // up to 128 chunks: the four rows a warp scans at a time are loaded at once
+    // (one round trip for 16 loads a lane instead of one per 32 chunks)
+    for (int e0 = warp; e0 < E; e0 += 32 * 4) {
+      int v[4][4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = e0 + 32 * x, c = 32 * q + lane;
+          v[x][q] = (e < E && c < num_chunks) ? chunk_counts[(size_t)e * num_chunks + c] : 0;
+        }
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int e = e0 + 32 * x;
+        if (e < E) {
+          int run = 0;
+          scan_row(e, chunk_counts + (size_t)e * num_chunks, 0, 4, v[x], run);
+          if (lane == 0) {
+            hist[e] = run;
+            s_tot[e] = run;
+            s_tiles[e] = (run + BM - 1) / BM;
+          }
+        }
+      }
+    }
+  } else {
+    for (int e = warp; e < E; e += 32) {
+      int* row = chunk_counts + (size_t)e * num_chunks;
+      int run = 0;
+      for (int c0 = 0; c0 < num_chunks; c0 += 128) {
+        int v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c = c0 + 32 * q + lane;
+          v[q] = c < num_chunks ? row[c] : 0;
+        }
+        scan_row(e, row, c0, 4, v, run);
+      }
+      if (lane == 0) {
+        hist[e] = run;
+        s_tot[e] = run;
+        s_tiles[e] = (run + BM - 1) / BM;
+      }
     }
   }
   for (int e = E + threadIdx.x; e < (int)blockDim.x; e += blockDim.x) { s_tot[e] = 0; s_tiles[e] = 0; }
