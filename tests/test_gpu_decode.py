@@ -86,6 +86,30 @@ def test_small_mxfp4_every_window_size(T):
     G.compare(S, x, out, idx, wt, fmt="mxfp4")
 
 
+@pytest.mark.parametrize("H,T", [(1024, 1), (1536, 3), (2048, 2)])
+def test_mxfp4_stream_every_tile_count(H, T):
+    """The MXFP4 stream kernel is compiled per H / 256 (2, 4, 6, 8, 10 output tiles per
+    warp); H = 512 and 2560 are covered above, these are the other three."""
+    S = mi.custom_layer(H=H, E=16, k=4, I=256, Is=128, fmt="mxfp4", seed=17)
+    L = G.cuda_layer(S.spec, max_tokens=8)
+    assert "moe_decode_stream_mx_kernel" in L.describe()
+    x = mi.tokens(S.spec, T, stream=400 + T)
+    out, idx, wt = G.run_cuda(L, x)
+    G.compare(S, x, out, idx, wt, fmt="mxfp4")
+
+
+def test_single_routed_expert_window():
+    """k = 1, T = 1: one routed expert of 128 features spread over 152 CTAs, so most
+    CTAs have no routed record and the group holding their shared tail has no routed
+    part; the rest have one or two."""
+    S = mi.custom_layer(H=512, E=8, k=1, I=128, Is=256, seed=21)
+    L = G.cuda_layer(S.spec, max_tokens=8)
+    for stream in range(3):
+        x = mi.tokens(S.spec, 1, stream=500 + stream)
+        out, idx, wt = G.run_cuda(L, x)
+        G.compare(S, x, out, idx, wt)
+
+
 @pytest.mark.parametrize("H,fmt,T", [(4096, "bf16", 1), (4096, "bf16", 5), (768, "mxfp4", 1), (768, "mxfp4", 3)])
 def test_three_phase_kernel_shapes(H, fmt, T):
     """Shapes the record-streaming kernels do not take (bf16 with H > 2048, MXFP4 with H not a
