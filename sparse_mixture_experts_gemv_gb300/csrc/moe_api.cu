@@ -108,12 +108,17 @@ __global__ void down_to_columns_kernel(const uint16_t* __restrict__ down, uint8_
 }
 
 // MXFP4 down codes [E][H][I/2] (element (n, i) in nibble i & 1 of byte i / 2 of
-// row n) -> the down column of each record in 16-row tiles: byte 8t + g of
-// record (e, i)'s column holds rows n = 16t + g (low nibble) and 16t + g + 8.
-// One block: 64 features x 64 rows.
+// row n) -> the down columns of each pair of records (features 2p, 2p + 1) in
+// 16-row tiles. Byte i / 2 of row n already holds both features' codes for
+// that row (feature 2p in the low nibble), which is the code pair one lane of
+// an m16n8k16 A fragment needs (k = 2c, 2c + 1). For tile t (rows 16t ..
+// 16t + 15) and g < 8, bytes 2g and 2g + 1 of the tile's 16 are rows 16t + g
+// and 16t + g + 8; the first H / 32 tiles of the pair sit in record 2p's column,
+// the rest in record 2p + 1's (each record keeps H / 2 bytes).
+// One block: 64 features (32 pairs) x 64 rows.
 __global__ void mx_down_to_columns_kernel(const uint8_t* __restrict__ down, uint8_t* __restrict__ rec, int H, int I,
                                           int stride, int col_off) {
-  __shared__ uint8_t tile[64][32];            // [row n][64 features as 32 code bytes]
+  __shared__ uint8_t tile[64][32];            // [row n][pair]
   const size_t e = blockIdx.z;
   const int i0 = blockIdx.x * 64, n0 = blockIdx.y * 64;
   const int t = threadIdx.x;
@@ -124,15 +129,17 @@ __global__ void mx_down_to_columns_kernel(const uint8_t* __restrict__ down, uint
   }
   __syncthreads();
   {
-    const int il = t >> 2, part = t & 3;        // feature i0 + il, 16-row tile `part` of the block
+    const int pl = t >> 3, part = (t >> 1) & 3, h = t & 1;   // pair, 16-row tile of the block, half of its bytes
+    const int tile_abs = n0 / 16 + part, half_tiles = H / 32;
+    const int sel = tile_abs >= half_tiles ? 1 : 0;
     uint8_t o[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {               // byte q: rows 16 part + q and 16 part + q + 8
-      const uint32_t lo = (tile[16 * part + q][il >> 1] >> (4 * (il & 1))) & 0xFu;
-      const uint32_t hi = (tile[16 * part + q + 8][il >> 1] >> (4 * (il & 1))) & 0xFu;
-      o[q] = (uint8_t)(lo | (hi << 4));
+    for (int q = 0; q < 4; ++q) {               // g = 4h + q: rows 16 part + g and 16 part + g + 8
+      o[2 * q] = tile[16 * part + 4 * h + q][pl];
+      o[2 * q + 1] = tile[16 * part + 4 * h + q + 8][pl];
     }
-    uint8_t* dst = rec + (e * I + i0 + il) * (size_t)stride + col_off + n0 / 2 + 8 * part;
+    uint8_t* dst = rec + (e * I + i0 + 2 * pl + sel) * (size_t)stride + col_off +
+                   16 * (tile_abs - sel * half_tiles) + 8 * h;
     *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(o);
   }
 }

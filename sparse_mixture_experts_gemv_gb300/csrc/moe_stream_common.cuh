@@ -175,9 +175,12 @@ MOE_DEV void bf16_down_tiles(uint32_t gbase, int stride, int nvalid, int H, int 
 // c+8, c+12: exactly the four code pairs lane (g, c) of an m16n8k16 A fragment
 // needs for one row over the block's two 16-wide k-steps (k = 2c, 2c+8 of the
 // first step, then of the second).
-// Down tiles: byte 8t + g of the column = rows 16t + g (low nibble) and
-// 16t + g + 8 of the feature's down column: the pair of rows lane (g, c) holds
-// in an A fragment.
+// Down tiles, per pair of records (features 2p, 2p + 1; groups and CTA ranges
+// start at even features): for 16-row tile t and g < 8, bytes 16t' + 2g and
+// 16t' + 2g + 1 hold rows 16t + g and 16t + g + 8, each byte both features'
+// codes of that row (feature 2p in the low nibble) -- the code pair lane (g, c)
+// of an A fragment needs for K columns 2c, 2c + 1. Tiles t < H / 32 are in
+// record 2p's column (t' = t), the rest in record 2p + 1's (t' = t - H / 32).
 struct MxLayout {
   int up_codes, gate_scales, up_scales, down_tiles;
 };
@@ -246,22 +249,25 @@ MOE_DEV void mx_down_tiles(const uint8_t* gbase, int stride, int nvalid, const M
                            const uint8_t* sv0, const uint8_t* sv1, float cexp2, const uint32_t (&bh)[2][2],
                            const uint32_t (&bl)[2][2], float (&acc)[NTILE][4]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gq = lane >> 2, cq = lane & 3;
-  const int ra = 2 * cq, rb = 2 * cq + 8;        // records of K columns 2cq.. and 2cq+8..
-  const uint8_t* p0 = gbase + (size_t)ra * stride + ly.down_tiles + gq;
-  const uint8_t* p1 = p0 + stride;
-  const uint8_t* p2 = gbase + (size_t)rb * stride + ly.down_tiles + gq;
-  const uint8_t* p3 = p2 + stride;
-  const bool v0 = ra < nvalid, v1 = ra + 1 < nvalid, v2 = rb < nvalid, v3 = rb + 1 < nvalid;
+  // pairs cq (records 2cq, 2cq + 1: K columns 2cq, 2cq + 1) and cq + 4 (K columns 2cq + 8, 2cq + 9);
+  // nvalid is even, so a pair is present or absent as a whole
+  const uint8_t* pa = gbase + (size_t)(2 * cq) * stride + ly.down_tiles + 2 * gq;
+  const uint8_t* pb = pa + (size_t)8 * stride;
+  const bool va = 2 * cq < nvalid, vb = 2 * cq + 8 < nvalid;
 #pragma unroll
   for (int j = 0; j < NTILE; ++j) {
     {
       const int tt = warp + kConsumerWarps * j, n0 = 16 * tt;
-      const uint32_t c0 = v0 ? p0[8 * tt] : 0u, c1 = v1 ? p1[8 * tt] : 0u;
-      const uint32_t c2 = v2 ? p2[8 * tt] : 0u, c3 = v3 ? p3[8 * tt] : 0u;
-      const uint32_t a0 = e2m1x2_to_f16x2((c0 & 0xFu) | ((c1 & 0xFu) << 4));   // row n0+g
-      const uint32_t a1 = e2m1x2_to_f16x2((c0 >> 4) | (c1 & 0xF0u));          // row n0+g+8
-      const uint32_t a2 = e2m1x2_to_f16x2((c2 & 0xFu) | ((c3 & 0xFu) << 4));
-      const uint32_t a3 = e2m1x2_to_f16x2((c2 >> 4) | (c3 & 0xF0u));
+      // tiles tt < H / 32 = 8 NTILE (j < NTILE / 2) in the pair's first record, the rest in its second
+      constexpr int kHalf = NTILE / 2;
+      const int sel = j >= kHalf ? 1 : 0;
+      const int off = sel * stride + 16 * (warp + kConsumerWarps * (j - sel * kHalf));
+      const uint32_t ua = va ? *reinterpret_cast<const uint16_t*>(pa + off) : 0u;
+      const uint32_t ub = vb ? *reinterpret_cast<const uint16_t*>(pb + off) : 0u;
+      const uint32_t a0 = e2m1x2_to_f16x2(ua);        // row n0+g
+      const uint32_t a1 = e2m1x2_to_f16x2(ua >> 8);   // row n0+g+8
+      const uint32_t a2 = e2m1x2_to_f16x2(ub);
+      const uint32_t a3 = e2m1x2_to_f16x2(ub >> 8);
 #pragma unroll
       for (int v = 0; v < 2; ++v) {
         if (v < nv) {

@@ -230,7 +230,9 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
     return;
   }
   const int D = rs.meta.num_slots;
-  const Ranges rg = cta_ranges(b, G, Is, D * I);
+  Ranges rg = cta_ranges(b, G, Is, D * I);
+  rg.u0 &= ~1;   // routed ranges start at even features: the down columns come in pairs of records
+  rg.u1 &= ~1;   // (the same rounding on both sides of every boundary; D * I is even)
   const int nr = rg.u1 - rg.u0;
   const int ngroups = nsg + (nr + RGM - 1) / RGM;
 
