@@ -332,10 +332,11 @@ def run_ours(args):
                 extra[wname] = decode_workload(B, wname, max(2, args.steps // 2), 2, peaks)
             except Exception as ex:  # report, never hide
                 extra[wname] = {"error": repr(ex)}
-        try:
-            extra["qwen_prefill"] = prefill_workload(B, max(2, args.steps // 2), 2, peaks)
-        except Exception as ex:
-            extra["qwen_prefill"] = {"error": repr(ex)}
+        for wname in ("qwen_prefill", "ling_mxfp4_prefill"):
+            try:
+                extra[wname] = prefill_workload(B, wname, max(2, args.steps // 2), 2, peaks)
+            except Exception as ex:
+                extra[wname] = {"error": repr(ex)}
     result["workloads"] = extra
 
     if rank == 0 and not args.no_cpu_baseline:
@@ -346,9 +347,9 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def prefill_workload(B: Bench, steps: int, warmup: int, peaks):
+def prefill_workload(B: Bench, wname: str, steps: int, warmup: int, peaks):
     torch = B.torch
-    w = mi.WORKLOADS["qwen_prefill"]
+    w = mi.WORKLOADS[wname]
     L = B.layer(w.layer, max_tokens=4096)
     x = torch.from_numpy(mi.workload_tokens(w, 0).view(np.int16)).to(B.dev)
     out = torch.empty_like(x)
@@ -366,8 +367,10 @@ def prefill_workload(B: Bench, steps: int, warmup: int, peaks):
     _, stages = B.time_calls(L, [x] * 3, [None] * 3, [out] * 3, profile=True)
     st_us = np.mean(np.array(stages), axis=0) * 1e3
     names = ["router", "dispatch", "grouped_gateup", "grouped_down", "combine"]
-    return {"workload": "qwen_prefill", "T": w.T, "ms_per_call": ms, "tokens_per_s": tok_s,
+    return {"workload": wname, "T": w.T, "ms_per_call": ms, "tokens_per_s": tok_s,
             "useful_tflops": tflops, "frac_of_measured_bf16": tflops / peaks["bf16_tflops"],
+            "mma": ("routed f16 x f16 (MXFP4 rows decoded in the GEMM), shared bf16 x bf16"
+                    if w.layer.fmt == "mxfp4" else "bf16 x bf16"),
             "touched_experts": st.distinct_experts, "max_expert_rows": st.max_expert_rows,
             "algorithmic_bytes": st.algorithmic_bytes,
             "hbm_frac": st.algorithmic_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],

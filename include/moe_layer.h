@@ -73,8 +73,12 @@ typedef enum {
 /* Largest T served by the weight-streaming (GEMV) path; larger T use the grouped
    tensor-core path. Verify windows of 2-5 rows and 2-token-per-draft batches fit.
    (The limit is lower when T*(k*I + Is)*4 bytes of SwiGLU outputs would exceed
-   200 KB, see moe_layer_describe.) The grouped path needs bf16 routed experts and
-   E a multiple of 16; other layers return MOE_ERR_UNSUPPORTED for larger T. */
+   200 KB, see moe_layer_describe.) The grouped path needs E a multiple of 16;
+   other layers return MOE_ERR_UNSUPPORTED for larger T. It serves both weight
+   formats: MXFP4 routed rows are decoded inside the tensor-core GEMMs to f16 (e2m1
+   times 2^(scale - the row's largest scale), exact for blocks within 2^23 of the
+   row's largest), with x and the routed SwiGLU outputs in f16 there (exact for
+   |x| in [2^-14, 65504]; larger magnitudes overflow to infinity). */
 #define MOE_DECODE_MAX_T 8
 
 typedef struct {

@@ -91,6 +91,10 @@ WORKLOADS = {
         "ling_mxfp4_t4", LayerSpec(H=2560, E=512, k=8, I=768, Is=768, fmt="mxfp4", seed=0),
         T=4, calls=16,
         description="Ling-shaped MXFP4 decode H=2560 E=512 top-8 I=768 + shared, T=4"),
+    "ling_mxfp4_prefill": Workload(
+        "ling_mxfp4_prefill", LayerSpec(H=2560, E=512, k=8, I=768, Is=768, fmt="mxfp4", seed=0),
+        T=4096, calls=1,
+        description="Ling-shaped MXFP4 prefill chunk H=2560 E=512 top-8 I=768 + shared, T=4096"),
     "qwen_prefill": Workload(
         "qwen_prefill", LayerSpec(H=2048, E=256, k=8, I=512, Is=512, fmt="bf16", seed=0,
                                   router_bias="zipf"), T=4096, calls=1,

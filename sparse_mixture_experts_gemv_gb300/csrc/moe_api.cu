@@ -406,7 +406,8 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
   snprintf(L.describe, sizeof(L.describe),
            "moe_layer H=%d E=%d k=%d I=%d Is=%d format=%s max_tokens=%d | "
            "T<=%d: decode GEMV path [%s] | "
-           "T>%d: grouped path [grouped_router_tc, dispatch, grouped_gateup_tc (tcgen05), grouped_down_tc (tcgen05), combine]%s",
+           "T>%d: grouped path [grouped_router_tc, dispatch, grouped_gateup_tc (tcgen05%s), grouped_down_tc (tcgen05%s), "
+           "combine]%s",
            cfg->hidden, cfg->num_experts, cfg->top_k, cfg->intermediate, cfg->shared_intermediate,
            cfg->weight_format == MOE_WEIGHTS_MXFP4 ? "mxfp4" : "bf16", cfg->max_tokens,
            (cfg->flags & MOE_FLAG_FORCE_GROUPED) ? 0 : L.decode_max_t,
@@ -422,6 +423,8 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
                       ? "moe_decode_fused_kernel<mxfp4> (cooperative: router+shared, routed gate/up, down+combine)"
                       : "moe_decode_fused_kernel<bf16> (cooperative: router+shared, routed gate/up, down+combine)"),
            (cfg->flags & MOE_FLAG_FORCE_GROUPED) ? 0 : L.decode_max_t,
+           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? ", MXFP4 B rows decoded to f16 in the kernel" : "",
+           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? ", MXFP4 B rows decoded to f16 in the kernel" : "",
            (cfg->flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? " [test: forced wait timeout]" : "");
   *out = &o->L;
   return MOE_OK;
@@ -439,9 +442,8 @@ moe_status_t moe_layer_forward_ex(moe_layer_t* L, const void* x, void* out, int3
   if (logit_bias && ((uintptr_t)logit_bias & 3)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   const bool grouped = (L->cfg.flags & MOE_FLAG_FORCE_GROUPED) || T > L->decode_max_t;
-  // The grouped path serves bf16 routed experts with E a multiple of 16.
-  if (grouped && (L->cfg.weight_format == MOE_WEIGHTS_MXFP4 || L->cfg.num_experts % 16 != 0))
-    return MOE_ERR_UNSUPPORTED;
+  // The grouped path's router takes E in multiples of 16.
+  if (grouped && L->cfg.num_experts % 16 != 0) return MOE_ERR_UNSUPPORTED;
   L->prof_n = 0;
   cudaError_t e = grouped ? moe::launch_grouped(L, (const uint16_t*)x, (uint16_t*)out, T, logit_bias, s)
                           : moe::launch_decode(L, (const uint16_t*)x, (uint16_t*)out, T, logit_bias, s);

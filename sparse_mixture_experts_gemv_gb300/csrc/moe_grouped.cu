@@ -53,6 +53,15 @@ constexpr int kStageB = 256 * BK * 2;    // 32 KB (N up to 256)
 constexpr int kTmemCols = 512;           // two 256-column fp32 accumulators
 constexpr int kChunk = 32;               // tokens per dispatch chunk (one per warp of the top-k CTA)
 constexpr size_t kGemmSmem = (size_t)kStages * (kStageA + kStageB) + 1024 /*align*/ + 256 /*barriers*/;
+// MXFP4 B operands: a separate ring of raw stages (e2m1 codes of 256 B rows x 64
+// K, 32 bytes a row, then the rows' scale pairs) that converter warps decode into
+// the f16 B stage of the main ring.
+constexpr int kRaw = 3;
+constexpr int kRawCodes = 256 * (BK / 2);  // 8 KB
+constexpr int kRawScales = 256 * 2;        // 512 B: blocks 2kb, 2kb + 1 of each row
+constexpr int kRawStage = kRawCodes + kRawScales;
+constexpr size_t kGemmSmemMx = kGemmSmem + (size_t)kRaw * kRawStage;
+constexpr int kConvThreads = 256;          // one B row per converter thread
 
 enum Epi { EPI_ROUTER = 0, EPI_SWIGLU = 1, EPI_STORE = 2 };
 
@@ -83,6 +92,11 @@ struct GemmParams {
   uint16_t* out_shared; int ld_shared;
   float* logits; const float* router_bias; const float* logit_bias;
   int* err;
+  // MXFP4 routed experts (B rows decoded in the kernel): routed A operands are f16
+  // (x16 for the gathered gate/up rows, f16 h for the down rows).
+  const uint16_t* x16;      // f16 [T][H]
+  const uint16_t* mx_sc;    // scale pairs [E][K / 64][b_rows_per_expert]
+  const uint8_t* mx_sref;   // reference exponent of each B row [E][b_rows_per_expert]
 };
 
 struct TileInfo {
@@ -126,32 +140,79 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int R, int 
   return ti;
 }
 
-template <int EPI, bool GATHER>
-__global__ void __launch_bounds__(GATHER ? 320 : 192, 1)
+// Instruction descriptor of kind::f16 with f16 A and B (format 0), fp32
+// accumulation, both operands K-major, shape M x N.
+constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// 2^d as a pair of f16 (d <= 15): normal down to 2^-14, subnormal down to 2^-24,
+// zero below.
+__device__ __forceinline__ uint32_t pow2_f16x2(int d) {
+  d = min(d, 15);
+  const uint32_t h = d >= -14 ? (uint32_t)(d + 15) << 10 : (d >= -24 ? 1u << (d + 24) : 0u);
+  return h | (h << 16);
+}
+__device__ __forceinline__ uint32_t hmul2_f16(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// Two fp32 -> f16 pair, lo in the low half (round to nearest even).
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Eight e2m1 codes (one 32-bit word, element 2i in the low nibble of byte i)
+// times the f16 pair f -> eight f16 in element order.
+__device__ __forceinline__ uint4 e2m1x8_to_f16(uint32_t w, uint32_t f) {
+  return make_uint4(hmul2_f16(e2m1x2_to_f16x2(w), f), hmul2_f16(e2m1x2_to_f16x2(w >> 8), f),
+                    hmul2_f16(e2m1x2_to_f16x2(w >> 16), f), hmul2_f16(e2m1x2_to_f16x2(w >> 24), f));
+}
+
+// MXB: routed B rows are MXFP4 (e2m1 codes + one e8m0 scale per 32 K). The
+// producer copies each stage's codes (TMA, 32 bytes x 256 rows) and the rows'
+// scale pairs (one bulk copy) into a raw ring; converter warps decode them into
+// the f16 B stage: e2m1 -> f16 (exact) times 2^(s - sref), sref being the row's
+// largest scale, so the stage is exact f16 for blocks within 2^23 of the row's
+// largest; the epilogue multiplies column n by 2^(sref[n] - 127). Routed A rows
+// are f16 then (x16 for gate/up, f16 h for down) and the MMA kind is f16 x f16;
+// shared-expert tiles stay bf16 x bf16 through TMA.
+template <int EPI, bool GATHER, bool MXB>
+__global__ void __launch_bounds__((GATHER ? 320 : 192) + (MXB ? kConvThreads : 0), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_constant__ CUtensorMap mapA_s,
                     const __grid_constant__ CUtensorMap mapB_r, const __grid_constant__ CUtensorMap mapB_s,
                     const GemmParams p) {
+  constexpr int kConvWarp0 = GATHER ? 10 : 6;  // first converter warp (MXB)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kStageA;
-  uint64_t* full = (uint64_t*)(sB + kStages * kStageB);
+  uint8_t* sRaw = sB + kStages * kStageB;  // MXB: raw ring
+  uint64_t* full = (uint64_t*)(sRaw + (MXB ? kRaw * kRawStage : 0));
   uint64_t* empty = full + kStages;
   uint64_t* acc_full = empty + kStages;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* drain = acc_empty + 2;
+  uint64_t* raw_full = acc_empty + 2;
+  uint64_t* raw_empty = raw_full + kRaw;
+  uint64_t* drain = raw_empty + kRaw;
   uint32_t* tmem_slot = (uint32_t*)(drain + 1);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1 + (GATHER ? 128 : 0));
+      mbar_init(&full[s], 1 + (GATHER ? 128 : 0) + (MXB ? kConvThreads : 0));
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], 128);
+    }
+    for (int q = 0; q < kRaw; ++q) {
+      mbar_init(&raw_full[q], 1);
+      mbar_init(&raw_empty[q], kConvThreads);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -177,25 +238,37 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
     R = 0;
   }
   const int total = R * p.nt_routed + p.n_shared_mtiles * p.nt_shared;
-  const uint32_t idesc = idesc_bf16_f32(BM, p.BN);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t it = 0;
-      const uint32_t bytes = (uint32_t)p.BN * BK * 2 * (EPI == EPI_ROUTER ? 3 : 1) + (GATHER ? 0u : (uint32_t)kStageA);
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+      uint32_t it = 0, rit = 0;
+      bool stop = false;
+      for (int tile = blockIdx.x; tile < total && !stop && !*abort_flag; tile += gridDim.x) {
         const TileInfo ti = decode_tile(p, R, tile);
+        const bool mxt = MXB && !ti.shared;
         for (int kb = 0; kb < ti.ks; ++kb, ++it) {
-          const int s = it % kStages;
-          if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, abort_flag)) break;
-          mbar_arrive_expect_tx(&full[s], bytes);
           const int kcol = kb * BK;
+          if (mxt) {  // raw codes and scale pairs of this stage's 256 B rows
+            const int q = rit % kRaw;
+            if (!mbar_wait(&raw_empty[q], ((rit / kRaw) & 1) ^ 1, p.err, abort_flag)) { stop = true; break; }
+            mbar_arrive_expect_tx(&raw_full[q], (uint32_t)kRawStage);
+            const int brow = ti.e * p.b_rows_per_expert + ti.nt * 256;
+            tma_load_2d(sRaw + q * kRawStage, &mapB_r, kb * (BK / 2), brow, &raw_full[q]);
+            bulk_copy_g2s(sRaw + q * kRawStage + kRawCodes,
+                          p.mx_sc + ((size_t)ti.e * ti.ks + kb) * p.b_rows_per_expert + ti.nt * 256,
+                          (uint32_t)kRawScales, &raw_full[q]);
+            ++rit;
+          }
+          const int s = it % kStages;
+          if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, abort_flag)) { stop = true; break; }
+          const uint32_t bbytes = mxt ? 0u : (uint32_t)p.BN * BK * 2 * (EPI == EPI_ROUTER ? 3 : 1);
+          mbar_arrive_expect_tx(&full[s], bbytes + (GATHER ? 0u : (uint32_t)kStageA));
           if (EPI == EPI_ROUTER) {  // the three bf16 terms of W_r share this A tile
 #pragma unroll
             for (int part = 0; part < 3; ++part)
               tma_load_2d(sB + s * kStageB + part * p.BN * BK * 2, &mapB_r, kcol, part * p.E + ti.nt * p.BN, &full[s]);
-          } else {
+          } else if (!mxt) {
             const int brow = (ti.shared ? 0 : ti.e * p.b_rows_per_expert) + ti.nt * p.BN;
             tma_load_2d(sB + s * kStageB, ti.shared ? &mapB_s : &mapB_r, kcol, brow, &full[s]);
           }
@@ -205,14 +278,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
       if (*abort_flag) {  // let copies already issued land before the CTA exits
         for (uint32_t q = (it > (uint32_t)kStages ? it - kStages : 0); q < it; ++q)
           mbar_wait(&full[q % kStages], (q / kStages) & 1, p.err, abort_flag, 20000000LL, false);
+        if (MXB)
+          for (uint32_t q = (rit > (uint32_t)kRaw ? rit - kRaw : 0); q < rit; ++q)
+            mbar_wait(&raw_full[q % kRaw], (q / kRaw) & 1, p.err, abort_flag, 20000000LL, false);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      const uint32_t idesc_bf = idesc_bf16_f32(BM, p.BN), idesc_h = idesc_f16_f32(BM, p.BN);
       uint32_t it = 0, tc = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++tc) {
         const TileInfo ti = decode_tile(p, R, tile);
+        const uint32_t idesc = (MXB && !ti.shared) ? idesc_h : idesc_bf;
         const int ab = tc & 1;
         if (!mbar_wait(&acc_empty[ab], ((tc >> 1) & 1) ^ 1, p.err, abort_flag)) break;
         tc_fence_after();
@@ -248,6 +326,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
     uint32_t tc = 0;
     for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++tc) {
       const TileInfo ti = decode_tile(p, R, tile);
+      const bool mxt = MXB && !ti.shared;
       const int ab = tc & 1;
       if (!mbar_wait(&acc_full[ab], (tc >> 1) & 1, p.err, abort_flag)) break;
       tc_fence_after();
@@ -258,6 +337,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
         uint32_t v[32];
         tmem_ld32(taddr + c0, v);
         if (!valid) continue;
+        if (mxt) {  // column n of a decoded MXFP4 tile carries 2^(127 - sref[n])
+          const uint4* sr = reinterpret_cast<const uint4*>(p.mx_sref + (size_t)ti.e * p.b_rows_per_expert +
+                                                           ti.nt * p.BN + c0);
+          const uint4 s0 = __ldg(sr), s1 = __ldg(sr + 1);
+          const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            v[i] = __float_as_uint(__uint_as_float(v[i]) * e8m0_to_f32((sw[i >> 2] >> (8 * (i & 3))) & 0xFFu));
+        }
         if (EPI == EPI_SWIGLU) {
           // columns alternate gate / up of intermediate features i0 + c0/2 + (0..15)
           uint32_t packed[8];
@@ -265,7 +353,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
           for (int i = 0; i < 8; ++i) {
             const float h0 = swiglu(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]));
             const float h1 = swiglu(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-            packed[i] = (uint32_t)f32_to_bf16_rne(h0) | ((uint32_t)f32_to_bf16_rne(h1) << 16);
+            packed[i] = mxt ? f32x2_to_f16x2(h0, h1)   // f16 A of the MXFP4 down GEMM
+                            : (uint32_t)f32_to_bf16_rne(h0) | ((uint32_t)f32_to_bf16_rne(h1) << 16);
           }
           uint16_t* dst = ti.shared ? p.out_shared + (size_t)gr * p.ld_shared
                                     : p.out_routed + (size_t)gr * p.ld_routed;
@@ -304,49 +393,85 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
       tc_fence_before();
       mbar_arrive(&acc_empty[ab]);
     }
-  } else {
+  } else if (GATHER && warp < 10) {
     // ------------------------------------------------------------ A gather (gate/up)
-    if (GATHER) {
-      const int r = threadIdx.x - 192;   // tile row this thread copies
-      uint32_t it = 0;
-      int pending = -1;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(p, R, tile);
-        const int gr = ti.row0 + r;
-        int token = -1;
-        if (gr < ti.row_end) {
-          if (ti.shared) {
-            token = gr;
-          } else {
-            const int a = p.perm[gr];
-            if (a >= 0 && a < p.T * p.k) token = a / p.k;
-            else set_error(p.err, kDevCheck);
-          }
+    const int r = threadIdx.x - 192;   // tile row this thread copies
+    uint32_t it = 0;
+    int pending = -1;
+    for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(p, R, tile);
+      const int gr = ti.row0 + r;
+      int token = -1;
+      if (gr < ti.row_end) {
+        if (ti.shared) {
+          token = gr;
+        } else {
+          const int a = p.perm[gr];
+          if (a >= 0 && a < p.T * p.k) token = a / p.k;
+          else set_error(p.err, kDevCheck);
         }
-        const uint16_t* src = p.x + (size_t)(token < 0 ? 0 : token) * p.H;
-        const uint32_t nbytes = token < 0 ? 0u : 16u;
-        bool ok = true;
-        for (int kb = 0; kb < ti.ks; ++kb, ++it) {
-          const int s = it % kStages;
-          if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
-          uint8_t* dst = sA + s * kStageA + r * 128;
+      }
+      const uint16_t* xa = (MXB && !ti.shared) ? p.x16 : p.x;  // routed MXFP4 tiles take f16 rows
+      const uint16_t* src = xa + (size_t)(token < 0 ? 0 : token) * p.H;
+      const uint32_t nbytes = token < 0 ? 0u : 16u;
+      bool ok = true;
+      for (int kb = 0; kb < ti.ks; ++kb, ++it) {
+        const int s = it % kStages;
+        if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
+        uint8_t* dst = sA + s * kStageA + r * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) cp_async_16(dst + ((j ^ (r & 7)) << 4), src + kb * BK + j * 8, nbytes);
-          cp_async_commit();
-          if (pending >= 0) {
-            cp_async_wait<1>();
-            fence_proxy_async_smem();
-            mbar_arrive(&full[pending]);
-          }
-          pending = s;
+        for (int j = 0; j < 8; ++j) cp_async_16(dst + ((j ^ (r & 7)) << 4), src + kb * BK + j * 8, nbytes);
+        cp_async_commit();
+        if (pending >= 0) {
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(&full[pending]);
         }
-        if (!ok) break;
+        pending = s;
       }
-      cp_async_wait<0>();
-      if (pending >= 0) {
-        fence_proxy_async_smem();
-        mbar_arrive(&full[pending]);
+      if (!ok) break;
+    }
+    cp_async_wait<0>();
+    if (pending >= 0) {
+      fence_proxy_async_smem();
+      mbar_arrive(&full[pending]);
+    }
+  } else if (MXB) {
+    // ------------------------------------------------------------ MXFP4 B converter
+    const int r = threadIdx.x - kConvWarp0 * 32;   // B row of the tile this thread decodes
+    uint32_t it = 0, rit = 0;
+    for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(p, R, tile);
+      const bool mxt = !ti.shared;
+      const int sref = mxt ? (int)__ldg(p.mx_sref + (size_t)ti.e * p.b_rows_per_expert + ti.nt * 256 + r) : 0;
+      bool ok = true;
+      for (int kb = 0; kb < ti.ks; ++kb, ++it) {
+        const int s = it % kStages;
+        if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
+        if (mxt) {
+          const int q = rit % kRaw;
+          if (!mbar_wait(&raw_full[q], (rit / kRaw) & 1, p.err, abort_flag)) { ok = false; break; }
+          const uint8_t* rb = sRaw + q * kRawStage;
+          const uint4 c0 = *reinterpret_cast<const uint4*>(rb + r * 32);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(rb + r * 32 + 16);
+          const uint32_t sc = *reinterpret_cast<const uint16_t*>(rb + kRawCodes + 2 * r);
+          ++rit;
+          const uint32_t f0 = pow2_f16x2((int)(sc & 0xFFu) - sref), f1 = pow2_f16x2((int)(sc >> 8) - sref);
+          const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint8_t* dst = sB + s * kStageB + r * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)   // 16-byte chunk j = K elements 8j..8j+7 (block 2kb for j < 4)
+            *reinterpret_cast<uint4*>(dst + ((j ^ (r & 7)) << 4)) = e2m1x8_to_f16(w[j], j < 4 ? f0 : f1);
+          fence_proxy_async_smem();
+          // The raw slot is released only once its values have been used: an
+          // arrival issued right after the loads can be observed (and the slot
+          // refilled by the next bulk copy) before those loads have read shared
+          // memory, which showed as stale rows of whole converter warps.
+          mbar_arrive(&raw_empty[q]);
+        }
+        mbar_arrive(&full[s]);
       }
+      if (!ok) break;
     }
   }
 
@@ -581,16 +706,53 @@ combine_kernel(const uint16_t* __restrict__ y, const uint16_t* __restrict__ ys, 
   }
 }
 
+// x (bf16) -> f16 for the routed rows of MXFP4 layers (8 values a thread-step;
+// exact for |x| in [2^-14, 65504], rounded to nearest even below).
+__global__ void __launch_bounds__(256)
+bf16_to_f16_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y, size_t n8) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n8; q += (size_t)gridDim.x * blockDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(x)[q];
+    reinterpret_cast<uint4*>(y)[q] =
+        make_uint4(f32x2_to_f16x2(bf16_lo(v.x), bf16_hi(v.x)), f32x2_to_f16x2(bf16_lo(v.y), bf16_hi(v.y)),
+                   f32x2_to_f16x2(bf16_lo(v.z), bf16_hi(v.z)), f32x2_to_f16x2(bf16_lo(v.w), bf16_hi(v.w)));
+  }
+}
+
+// Scale tables of an MXFP4 matrix for the grouped GEMMs. Rows are `row_bytes`
+// apart, each K / 2 code bytes then K / 32 e8m0 scale bytes; `rpe` rows per
+// expert. sref[row] = the row's largest scale byte; sc[e][kb][row in expert] =
+// the scales of blocks 2kb (low byte) and 2kb + 1, so one stage's 256 rows are
+// 512 contiguous bytes.
+__global__ void mx_grouped_scales_kernel(const uint8_t* __restrict__ w, int64_t row_bytes, int K, int rpe,
+                                         size_t rows, uint16_t* __restrict__ sc, uint8_t* __restrict__ sref) {
+  const int nkb = K / 64;
+  for (size_t row = blockIdx.x * (size_t)blockDim.x + threadIdx.x; row < rows; row += (size_t)gridDim.x * blockDim.x) {
+    const uint8_t* s = w + row * row_bytes + K / 2;
+    const size_t e = row / rpe, rr = row % rpe;
+    uint32_t mx = 0;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const uint32_t a = s[2 * kb], b = s[2 * kb + 1];
+      mx = max(mx, max(a, b));
+      sc[(e * nkb + kb) * rpe + rr] = (uint16_t)(a | (b << 8));
+    }
+    sref[row] = (uint8_t)mx;
+  }
+}
+
 // ===========================================================================
 // Host side
 // ===========================================================================
 struct GroupedMaps {
   CUtensorMap router_split;  // B router: [3E][H] bf16, box {64, BNr}
   CUtensorMap w_gu;          // B gate/up routed: [E*2I][H], box {64, 256}
+                             // (MXFP4: code bytes [E*2I][row], box {32, 256})
   CUtensorMap ws_gu;         // B gate/up shared: [2Is][H], box {64, 256}
   CUtensorMap h;             // A down routed: [Tmax*k][I], box {64, 128}
   CUtensorMap hs;            // A down shared: [Tmax][Is], box {64, 128}
   CUtensorMap w_down;        // B down routed: [E*H][I], box {64, 256}
+                             // (MXFP4: code bytes [E*H][row], box {32, 256})
   CUtensorMap ws_down;       // B down shared: [H][Is], box {64, 256}
   int router_bn;
 };
@@ -616,6 +778,19 @@ cudaError_t encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// 2-D byte map over [rows][row_bytes] (MXFP4 code rows), box {32 bytes, 256 rows},
+// no swizzle: one stage's codes land as 256 dense 32-byte rows.
+cudaError_t encode_codes(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes) {
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)(BK / 2), 256};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -667,6 +842,20 @@ cudaError_t grouped_prepare(moe_layer* L) {
   GALLOC(g.hs, sizeof(uint16_t) * (size_t)Tm * (Is > 0 ? Is : 1));
   GALLOC(g.y, sizeof(uint16_t) * TK * H);
   GALLOC(g.ys, sizeof(uint16_t) * (size_t)Tm * H);
+  const bool mx = c.weight_format == MOE_WEIGHTS_MXFP4;
+  if (mx) {
+    GALLOC(g.x16, sizeof(uint16_t) * (size_t)Tm * H);
+    GALLOC(g.mx_gu_sc, sizeof(uint16_t) * (size_t)E * (H / 64) * 2 * I);
+    GALLOC(g.mx_dn_sc, sizeof(uint16_t) * (size_t)E * (I / 64) * H);
+    GALLOC(g.mx_gu_sref, (size_t)E * 2 * I);
+    GALLOC(g.mx_dn_sref, (size_t)E * H);
+    mx_grouped_scales_kernel<<<1024, 256>>>(L->w_gu, L->row_bytes.gu, H, 2 * I, (size_t)E * 2 * I, g.mx_gu_sc,
+                                            g.mx_gu_sref);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    mx_grouped_scales_kernel<<<1024, 256>>>(L->w_down, L->row_bytes.down, I, H, (size_t)E * H, g.mx_dn_sc,
+                                            g.mx_dn_sref);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
 #undef GALLOC
 
   if ((e = get_encoder()) != cudaSuccess) return e;
@@ -675,12 +864,13 @@ cudaError_t grouped_prepare(moe_layer* L) {
   m->router_bn = (E % 64 == 0) ? 64 : (E % 32 == 0 ? 32 : 16);  // N tile dividing E (E % 16 == 0)
   if ((e = encode_2d(&m->router_split, L->router_split, 3ull * E, H, m->router_bn)) != cudaSuccess) return e;
   if ((e = encode_2d(&m->h, g.h, TK, I, BM)) != cudaSuccess) return e;
-  if (c.weight_format == MOE_WEIGHTS_BF16) {  // the grouped path serves bf16 routed experts
+  if (!mx) {
     if ((e = encode_2d(&m->w_gu, L->w_gu, (uint64_t)E * 2 * I, H, 256)) != cudaSuccess) return e;
     if ((e = encode_2d(&m->w_down, L->w_down, (uint64_t)E * H, I, 256)) != cudaSuccess) return e;
   } else {
-    m->w_gu = m->h;
-    m->w_down = m->h;
+    if ((e = encode_codes(&m->w_gu, L->w_gu, (uint64_t)E * 2 * I, (uint64_t)L->row_bytes.gu)) != cudaSuccess) return e;
+    if ((e = encode_codes(&m->w_down, L->w_down, (uint64_t)E * H, (uint64_t)L->row_bytes.down)) != cudaSuccess)
+      return e;
   }
   if (Is > 0) {
     if ((e = encode_2d(&m->ws_gu, L->ws_gu, 2ull * Is, H, 256)) != cudaSuccess) return e;
@@ -691,18 +881,22 @@ cudaError_t grouped_prepare(moe_layer* L) {
     m->hs = m->h;
     m->ws_down = m->w_down;
   }
-  e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_ROUTER, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_SWIGLU, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_STORE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+  constexpr auto kSmemAttr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_ROUTER, false, false>, kSmemAttr, (int)kGemmSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_SWIGLU, true, false>, kSmemAttr, (int)kGemmSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_STORE, false, false>, kSmemAttr, (int)kGemmSmem);
+  if (e == cudaSuccess && mx)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_SWIGLU, true, true>, kSmemAttr, (int)kGemmSmemMx);
+  if (e == cudaSuccess && mx)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_STORE, false, true>, kSmemAttr, (int)kGemmSmemMx);
   return e;
 }
 
 void grouped_release(moe_layer* L) {
   auto& g = L->grp;
   void* ptrs[] = {g.logits, g.idx, g.weights, g.hist, g.offsets, g.chunk_counts, g.perm, g.pos,
-                  g.tiles, g.num_tiles, g.h, g.hs, g.y, g.ys};
+                  g.tiles, g.num_tiles, g.h, g.hs, g.y, g.ys, g.x16, g.mx_gu_sc, g.mx_dn_sc,
+                  g.mx_gu_sref, g.mx_dn_sref};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   memset(&g, 0, sizeof(g));
@@ -726,9 +920,18 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
   GemmParams base;
   memset(&base, 0, sizeof(base));
   base.E = E; base.T = T; base.k = k; base.H = H; base.err = L->err; base.max_mtiles = g.max_tiles;
+  const bool mx = c.weight_format == MOE_WEIGHTS_MXFP4;
 
-  // 1. router logits (tensor cores, exact 3-term split of W_r)
+  // 1. router logits (tensor cores, exact 3-term split of W_r); MXFP4 layers
+  //    first convert x to f16 for the routed gate/up rows.
   prof_mark(L, s);
+  if (mx) {
+    const size_t n8 = (size_t)T * H / 8;
+    int grid = (int)((n8 + 255) / 256);
+    if (grid > 4 * L->num_sms) grid = 4 * L->num_sms;
+    e = launch_pdl(bf16_to_f16_kernel, grid, 256, 0, s, x, g.x16, n8);
+    if (e != cudaSuccess) return e;
+  }
   {
     GemmParams p = base;
     p.mtiles = nullptr; p.num_routed = nullptr;
@@ -737,7 +940,7 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
     p.n_shared_mtiles = 0; p.nt_shared = 1; p.ks_shared = 0;
     p.logits = g.logits; p.router_bias = L->router_bias; p.logit_bias = logit_bias;
     const int tiles = mt_tokens * p.nt_routed;
-    e = launch_pdl(grouped_gemm_kernel<EPI_ROUTER, false>, tiles < L->num_sms ? tiles : L->num_sms, 192,
+    e = launch_pdl(grouped_gemm_kernel<EPI_ROUTER, false, false>, tiles < L->num_sms ? tiles : L->num_sms, 192,
                    kGemmSmem, s, map_x, map_x, m->router_split, m->router_split, p);
     if (e != cudaSuccess) return e;
   }
@@ -762,8 +965,14 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
     p.n_shared_mtiles = Is > 0 ? mt_tokens : 0; p.nt_shared = Is > 0 ? 2 * Is / 256 : 1; p.ks_shared = H / BK;
     p.x = x; p.perm = g.perm; p.b_rows_per_expert = 2 * I;
     p.out_routed = g.h; p.ld_routed = I; p.out_shared = g.hs; p.ld_shared = Is;
-    e = launch_pdl(grouped_gemm_kernel<EPI_SWIGLU, true>, L->num_sms, 320, kGemmSmem, s, map_x, map_x, m->w_gu,
-                   m->ws_gu, p);
+    if (mx) {
+      p.x16 = g.x16; p.mx_sc = g.mx_gu_sc; p.mx_sref = g.mx_gu_sref;
+      e = launch_pdl(grouped_gemm_kernel<EPI_SWIGLU, true, true>, L->num_sms, 320 + kConvThreads, kGemmSmemMx, s,
+                     map_x, map_x, m->w_gu, m->ws_gu, p);
+    } else {
+      e = launch_pdl(grouped_gemm_kernel<EPI_SWIGLU, true, false>, L->num_sms, 320, kGemmSmem, s, map_x, map_x,
+                     m->w_gu, m->ws_gu, p);
+    }
     if (e != cudaSuccess) return e;
   }
   prof_mark(L, s);
@@ -776,8 +985,14 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
     p.n_shared_mtiles = Is > 0 ? mt_tokens : 0; p.nt_shared = H / 256; p.ks_shared = Is > 0 ? Is / BK : 1;
     p.b_rows_per_expert = H;
     p.out_routed = g.y; p.ld_routed = H; p.out_shared = g.ys; p.ld_shared = H;
-    e = launch_pdl(grouped_gemm_kernel<EPI_STORE, false>, L->num_sms, 192, kGemmSmem, s, m->h, m->hs, m->w_down,
-                   m->ws_down, p);
+    if (mx) {
+      p.mx_sc = g.mx_dn_sc; p.mx_sref = g.mx_dn_sref;
+      e = launch_pdl(grouped_gemm_kernel<EPI_STORE, false, true>, L->num_sms, 192 + kConvThreads, kGemmSmemMx, s, m->h,
+                     m->hs, m->w_down, m->ws_down, p);
+    } else {
+      e = launch_pdl(grouped_gemm_kernel<EPI_STORE, false, false>, L->num_sms, 192, kGemmSmem, s, m->h, m->hs,
+                     m->w_down, m->ws_down, p);
+    }
     if (e != cudaSuccess) return e;
   }
   prof_mark(L, s);

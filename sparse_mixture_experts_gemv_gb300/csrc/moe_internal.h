@@ -56,6 +56,12 @@ struct GroupedWorkspace {
   uint16_t* hs;          // bf16 [T][Is]   shared-expert SwiGLU outputs
   uint16_t* y;           // bf16 [T*k][H]  down outputs in grouped order
   uint16_t* ys;          // bf16 [T][H]    shared-expert down outputs
+  // MXFP4 layers (routed B rows decoded inside the grouped GEMMs):
+  uint16_t* x16;         // f16 [T][H]  x for the routed gate/up rows (h is f16 for routed rows)
+  uint16_t* mx_gu_sc;    // gate/up scale pairs [E][H / 64][2I]: blocks 2kb (low byte), 2kb + 1
+  uint16_t* mx_dn_sc;    // down scale pairs [E][I / 64][H]
+  uint8_t* mx_gu_sref;   // largest scale byte of each gate/up row [E][2I]
+  uint8_t* mx_dn_sref;   // largest scale byte of each down row [E][H]
 };
 
 }  // namespace moe

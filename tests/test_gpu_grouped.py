@@ -94,3 +94,85 @@ def test_grouped_matches_decode_path():
     b, ib, _ = G.run_cuda(Lg, x)
     assert (ia == ib).all()
     assert np.abs(G.bits_to_f64(a) - G.bits_to_f64(b)).max() <= 2 * G.BF16_MAX_ABS
+
+
+# ---------------------------------------------------------------- MXFP4 routed experts
+def _mx_small():
+    return mi.custom_layer(H=512, E=16, k=4, I=256, Is=128, fmt="mxfp4", seed=5).spec
+
+
+@pytest.mark.parametrize("T", [1, 8, 9, 100, 129, 300])
+def test_small_mxfp4_grouped(T):
+    """MXFP4 routed experts decoded inside the grouped tcgen05 GEMMs (forced grouped
+    path at small T, ragged 128-row blocks), against the oracle."""
+    spec = _mx_small()
+    L = G.cuda_layer(spec, max_tokens=512, flags=FORCE)
+    x = mi.tokens(spec, T, stream=3000 + T)
+    out, idx, wt = G.run_cuda(L, x)
+    assert L.stats().path == 2
+    G.compare(G.synth(spec), x, out, idx, wt, fmt="mxfp4")
+    _check_dispatch(L, T, spec.k, spec.E, idx)
+
+
+def test_mxfp4_grouped_wide_scale_range():
+    """Scale exponents spread over 24 binades inside each row (the in-kernel f16
+    stage holds e2m1 x 2^(s - largest scale of the row), exact down to 2^-23),
+    on both gate/up and down rows."""
+    from sparse_mixture_experts_gemv_gb300 import MoeLayer, weights_from_raw
+    from tests.layer_helpers import ModifiedLayer
+
+    base = mi.custom_layer(H=512, E=16, k=4, I=256, Is=128, fmt="mxfp4", seed=9)
+    spec = base.spec
+
+    def widen(r):
+        out = dict(r)
+        for name in ("gate_scales", "up_scales", "down_scales"):
+            s = r[name].astype(np.int64)
+            rows, nb = s.shape
+            spread = (np.arange(rows)[:, None] * 7 + np.arange(nb)[None, :] * 5) % 24
+            out[name] = (127 - 2 - spread).astype(np.uint8)   # exponents -2 ... -25
+        return out
+
+    S = ModifiedLayer(base, expert_fn=widen)
+    raws = [S.expert_raw(e) for e in range(spec.E)]
+    stacked = {n: np.stack([r[n] for r in raws]) for n in raws[0]}
+    weights = weights_from_raw(S.router(), S.router_bias(), stacked, S.shared_raw())
+    L = MoeLayer(spec.H, spec.E, spec.k, spec.I, spec.Is, weights, fmt="mxfp4", max_tokens=512, flags=FORCE)
+    try:
+        x = mi.tokens(spec, 200, stream=41)
+        out, idx, wt = G.run_cuda(L, x)
+        G.compare(S, x, out, idx, wt, fmt="mxfp4")
+    finally:
+        L.close()
+
+
+def test_mxfp4_grouped_matches_decode_path():
+    """T=7 MXFP4 window: the record-streaming decode kernel and the grouped GEMMs
+    select the same experts and agree to a few output roundings."""
+    spec = _mx_small()
+    Ld = G.cuda_layer(spec, max_tokens=64)
+    Lg = G.cuda_layer(spec, max_tokens=512, flags=FORCE)
+    x = mi.tokens(spec, 7, stream=32)
+    a, ia, _ = G.run_cuda(Ld, x)
+    b, ib, _ = G.run_cuda(Lg, x)
+    assert (ia == ib).all()
+    da, db = G.bits_to_f64(a), G.bits_to_f64(b)
+    rms = np.sqrt((da ** 2).mean())
+    assert np.abs(da - db).max() / rms <= 2 * G.MXFP4_MAX_ABS_NORM
+
+
+def test_ling_mxfp4_prefill_sampled_rows():
+    """Ling-shaped MXFP4 prefill chunk (T=4096, H=2560, E=512, top-8, I=768):
+    dispatch checked on all rows, outputs on a seeded sample of 64 rows."""
+    w = mi.WORKLOADS["ling_mxfp4_prefill"]
+    L = G.cuda_layer(w.layer, max_tokens=4096)
+    S = G.synth(w.layer)
+    x = mi.workload_tokens(w, 0)
+    out, idx, wt = G.run_cuda(L, x)
+    st = L.stats()
+    assert st.path == 2
+    _check_dispatch(L, 4096, 8, 512, idx)
+    rows = np.sort(np.random.default_rng(1).choice(4096, size=64, replace=False))
+    ref = o.moe_forward(S, x[rows])
+    r = G.compare(S, x[rows], out[rows], idx[rows], wt[rows], fmt="mxfp4", ref=ref)
+    print("ling mxfp4 prefill sampled rows", r, "touched", st.distinct_experts)
