@@ -172,6 +172,26 @@ moe_status_t moe_layer_forward_ex(moe_layer_t* layer, const void* x_dev, void* o
                                   const float* logit_bias_dev, void* stream);
 
 /*
+ * Long-prompt forward in chunks ("Optimizing on-device inference for Apple
+ * Silicon", section on prompt chunking: a long prompt is pushed through the layer
+ * a chunk of rows at a time, so the workspace stays sized for one chunk).
+ * x_dev, out_dev: bf16 [T, H] device, 16-byte aligned, not overlapping; T >= 0
+ * may exceed max_tokens. chunk: rows per chunk, 1 <= chunk <= max_tokens, or 0
+ * for max_tokens. logit_bias_dev: optional fp32 [T, E] (NULL = none). Every chunk,
+ * including a short last one, runs the grouped tensor-core path, whose result for
+ * a token does not depend on the other tokens of its chunk: the output is
+ * bit-identical for every chunk size (and equal to one moe_layer_forward call with
+ * MOE_FLAG_FORCE_GROUPED when T fits max_tokens). Chunks are enqueued back to back
+ * on `stream` and reuse the layer's workspace in stream order; no allocation, no
+ * host synchronisation. Diagnostics (get_stats, get_routing, get_dispatch) then
+ * describe the last chunk. Errors: MOE_ERR_INVALID_ARG (layer NULL, T < 0, chunk
+ * out of range, bad pointers), MOE_ERR_UNSUPPORTED (E not a multiple of 16),
+ * MOE_ERR_CUDA (launch failure; earlier chunks may have been enqueued).
+ */
+moe_status_t moe_layer_forward_chunked(moe_layer_t* layer, const void* x_dev, void* out_dev, int32_t T,
+                                       int32_t chunk, const float* logit_bias_dev, void* stream);
+
+/*
  * Host-buffer forward: copies x_host (bf16 [T, H]) to the device, runs the layer
  * on `stream`, copies the result to out_host (bf16 [T, H]) and synchronises the
  * stream before returning. Pinned (page-locked) host buffers give asynchronous

@@ -71,6 +71,8 @@ _SIGNATURES = {
                                          ctypes.c_void_p]),
     "moe_layer_forward_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                             ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_layer_forward_chunked": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
     "moe_layer_forward_host": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                               ctypes.c_void_p, ctypes.c_void_p]),
     "moe_layer_get_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(moe_stats_t)]),
@@ -145,6 +147,11 @@ def moe_layer_forward(layer: int, x_dev: int, out_dev: int, T: int, stream: int 
 
 def moe_layer_forward_ex(layer: int, x_dev: int, out_dev: int, T: int, logit_bias_dev, stream: int = 0) -> int:
     return load().moe_layer_forward_ex(layer, x_dev, out_dev, T, logit_bias_dev, stream)
+
+
+def moe_layer_forward_chunked(layer: int, x_dev: int, out_dev: int, T: int, chunk: int = 0, logit_bias_dev=None,
+                              stream: int = 0) -> int:
+    return load().moe_layer_forward_chunked(layer, x_dev, out_dev, T, chunk, logit_bias_dev, stream)
 
 
 def moe_layer_forward_host(layer: int, x_host: int, out_host: int, T: int, logit_bias_host=None,

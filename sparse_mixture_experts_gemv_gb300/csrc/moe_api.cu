@@ -454,6 +454,36 @@ moe_status_t moe_layer_forward_ex(moe_layer_t* L, const void* x, void* out, int3
   return MOE_OK;
 }
 
+moe_status_t moe_layer_forward_chunked(moe_layer_t* L, const void* x, void* out, int32_t T, int32_t chunk,
+                                       const float* logit_bias, void* stream) {
+  if (!L || T < 0) return MOE_ERR_INVALID_ARG;
+  if (chunk == 0) chunk = L->cfg.max_tokens;
+  if (chunk < 1 || chunk > L->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !out || ((uintptr_t)x & 15) || ((uintptr_t)out & 15)) return MOE_ERR_INVALID_ARG;
+  if (logit_bias && ((uintptr_t)logit_bias & 3)) return MOE_ERR_INVALID_ARG;
+  const size_t H = (size_t)L->cfg.hidden, E = (size_t)L->cfg.num_experts;
+  const size_t bytes = (size_t)T * H * 2;
+  const uintptr_t xa = (uintptr_t)x, oa = (uintptr_t)out;
+  if (xa < oa + bytes && oa < xa + bytes) return MOE_ERR_INVALID_ARG;  // overlap
+  if (L->cfg.num_experts % 16 != 0) return MOE_ERR_UNSUPPORTED;        // grouped router tiles
+  cudaStream_t s = (cudaStream_t)stream;
+  L->prof_n = 0;
+  for (int32_t t0 = 0; t0 < T; t0 += chunk) {
+    const int32_t n = T - t0 < chunk ? T - t0 : chunk;
+    const uint16_t* xc = (const uint16_t*)x + (size_t)t0 * H;   // H % 256 == 0: chunks stay 16-byte aligned
+    uint16_t* oc = (uint16_t*)out + (size_t)t0 * H;
+    const float* lb = logit_bias ? logit_bias + (size_t)t0 * E : nullptr;
+    if (L->profile) L->prof_n = 0;  // stage timings describe the last chunk
+    cudaError_t e = moe::launch_grouped(L, xc, oc, n, lb, s);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_layer_forward_chunked");
+    L->last_path = MOE_PATH_GROUPED;
+    L->last_T = n;
+    L->last_logit_bias = lb;
+  }
+  return MOE_OK;
+}
+
 moe_status_t moe_layer_forward(moe_layer_t* L, const void* x, void* out, int32_t T, void* stream) {
   return moe_layer_forward_ex(L, x, out, T, nullptr, stream);
 }

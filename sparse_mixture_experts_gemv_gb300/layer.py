@@ -78,6 +78,20 @@ class MoeLayer:
             raise N.MoeError(st, "moe_layer_forward_ex")
         return out
 
+    def forward_chunked(self, x: torch.Tensor, chunk: int = 0, out: torch.Tensor = None,
+                        logit_bias: torch.Tensor = None, stream: torch.cuda.Stream = None) -> torch.Tensor:
+        """Any number of rows, pushed through the grouped path `chunk` rows at a time
+        (0 = max_tokens); bit-identical for every chunk size."""
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty_like(x)
+        s = (stream or torch.cuda.current_stream(self.device)).cuda_stream
+        lb = logit_bias.data_ptr() if logit_bias is not None else None
+        st = N.moe_layer_forward_chunked(self.handle, x.data_ptr(), out.data_ptr(), T, chunk, lb, s)
+        if st != N.MOE_OK:
+            raise N.MoeError(st, "moe_layer_forward_chunked")
+        return out
+
     def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor, logit_bias_host=None,
                      stream: torch.cuda.Stream = None):
         s = (stream or torch.cuda.current_stream(self.device)).cuda_stream
