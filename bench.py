@@ -327,9 +327,12 @@ def run_ours(args):
     # ---- secondary workloads
     extra = {}
     if not args.quick:
-        for wname in ("qwen_verify", "ling_mxfp4_t1", "ling_mxfp4_t4"):
+        for wname in ("qwen_verify", "qwen_tsweep", "ling_mxfp4_t1", "ling_mxfp4_t4"):
             try:
-                extra[wname] = decode_workload(B, wname, max(2, args.steps // 2), 2, peaks)
+                if wname == "qwen_tsweep":   # same layer as the headline: runs before the Ling layer replaces it
+                    extra[wname] = tsweep_workload(B, max(2, args.steps // 4), peaks)
+                else:
+                    extra[wname] = decode_workload(B, wname, max(2, args.steps // 2), 2, peaks)
             except Exception as ex:  # report, never hide
                 extra[wname] = {"error": repr(ex)}
         for wname in ("qwen_prefill", "ling_mxfp4_prefill"):
@@ -345,6 +348,36 @@ def run_ours(args):
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def tsweep_workload(B: Bench, steps: int, peaks, tmax: int = 8, calls: int = 16):
+    """Per-call time of the Qwen-shaped layer for windows of T = 1..tmax rows (verify
+    windows of 2-5 rows, 2-token MTP batches), L2 flushed before every call; T > the
+    weight-streaming limit would take the grouped path and is reported as such."""
+    torch = B.torch
+    spec = mi.QWEN_LAYER
+    L = B.layer(spec, max_tokens=4096)
+    rows = []
+    for T in range(1, tmax + 1):
+        xs = [torch.from_numpy(mi.tokens(spec, T, stream=900_000 + 100 * T + c).view(np.int16)).to(B.dev)
+              for c in range(calls)]
+        outs = [torch.empty_like(x) for x in xs]
+        stats = []
+        for i in range(calls):
+            L.forward(xs[i], outs[i])
+            stats.append(L.stats())
+        B.time_calls(L, xs, [None] * calls, outs)
+        times = []
+        for _ in range(steps):
+            times += B.time_calls(L, xs, [None] * calls, outs)[0]
+        us = float(np.mean(times) * 1e3)
+        alg = float(np.mean([s.algorithmic_bytes for s in stats]))
+        rows.append({"T": T, "us_per_call": round(us, 3), "path": int(stats[0].path),
+                     "distinct_experts_mean": float(np.mean([s.distinct_experts for s in stats])),
+                     "algorithmic_bytes": alg, "frac_of_hbm": round(alg / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                     "us_per_token": round(us / T, 3)})
+    return {"workload": "qwen_tsweep: Qwen-shaped layer, T = 1..8 seeded tokens per call (no logit bias)",
+            "calls_per_T": calls, "rows": rows}
 
 
 def prefill_workload(B: Bench, wname: str, steps: int, warmup: int, peaks):

@@ -33,7 +33,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 # Stream purposes (second element of every seed key).
-_P_ROUTER, _P_EXPERT, _P_SHARED, _P_TOKENS, _P_LOGIT_BIAS, _P_ROUTER_BIAS = range(6)
+_P_ROUTER, _P_EXPERT, _P_SHARED, _P_TOKENS, _P_LOGIT_BIAS, _P_ROUTER_BIAS, _P_LMHEAD = range(7)
 
 WEIGHT_STD = np.float32(0.02)
 
@@ -244,3 +244,52 @@ def hash_stream(name: str, call: int) -> int:
 def custom_layer(H, E, k, I, Is, fmt="bf16", seed=0, router_bias="none") -> SynthLayer:
     return SynthLayer(LayerSpec(H=H, E=E, k=k, I=I, Is=Is, fmt=fmt, seed=seed,
                                 router_bias=router_bias))
+
+
+# ---------------------------------------------------------------------------
+# Output projection (LM head) of the Ling-shaped model: "Three ways to speed up
+# MoE inference on DGX Spark", section "Optimization 2": the head projects the
+# hidden size 2,560 onto a vocabulary of 157,184 tokens and is stored in bf16.
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class LmHeadSpec:
+    V: int = 157_184
+    H: int = 2560
+    seed: int = 0
+
+
+LMHEAD = LmHeadSpec()
+_LMHEAD_BLOCK = 4096  # rows per random stream
+
+
+def lmhead_rows(spec: LmHeadSpec, r0: int, r1: int) -> np.ndarray:
+    """bf16 bits of rows [r0, r1) of W [V, H] ~ N(0, 0.02); one stream per 4096-row block."""
+    out = np.empty((r1 - r0, spec.H), dtype=np.uint16)
+    b = r0 // _LMHEAD_BLOCK
+    while b * _LMHEAD_BLOCK < r1:
+        lo, hi = b * _LMHEAD_BLOCK, min((b + 1) * _LMHEAD_BLOCK, spec.V)
+        blk = _normal_bf16(_rng(spec.seed, _P_LMHEAD, b), (hi - lo, spec.H))
+        a, z = max(lo, r0), min(hi, r1)
+        out[a - r0:z - r0] = blk[a - lo:z - lo]
+        b += 1
+    return out
+
+
+def lmhead_weights(spec: LmHeadSpec, threads: int | None = None) -> np.ndarray:
+    """All of W [V, H] as bf16 bits (blocks drawn in parallel)."""
+    out = np.empty((spec.V, spec.H), dtype=np.uint16)
+    nb = (spec.V + _LMHEAD_BLOCK - 1) // _LMHEAD_BLOCK
+
+    def fill(b):
+        lo, hi = b * _LMHEAD_BLOCK, min((b + 1) * _LMHEAD_BLOCK, spec.V)
+        out[lo:hi] = _normal_bf16(_rng(spec.seed, _P_LMHEAD, b), (hi - lo, spec.H))
+
+    with _cf.ThreadPoolExecutor(threads or min(32, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, range(nb)))
+    return out
+
+
+def lmhead_tokens(spec: LmHeadSpec, n: int, stream: int = 0) -> np.ndarray:
+    """n hidden-state rows x ~ N(0, 1) as bf16 bits [n, H]."""
+    return _normal_bf16(_rng(spec.seed, _P_TOKENS, 7_000_000 + stream), (n, spec.H), std=1.0)
+
