@@ -335,6 +335,10 @@ def run_ours(args):
                     extra[wname] = decode_workload(B, wname, max(2, args.steps // 2), 2, peaks)
             except Exception as ex:  # report, never hide
                 extra[wname] = {"error": repr(ex)}
+        try:
+            extra["lmhead_fp8"] = lmhead_workload(B, max(2, args.steps // 4), peaks)
+        except Exception as ex:
+            extra["lmhead_fp8"] = {"error": repr(ex)}
         for wname in ("qwen_prefill", "ling_mxfp4_prefill"):
             try:
                 extra[wname] = prefill_workload(B, wname, max(2, args.steps // 2), 2, peaks)
@@ -378,6 +382,43 @@ def tsweep_workload(B: Bench, steps: int, peaks, tmax: int = 8, calls: int = 16)
                      "us_per_token": round(us / T, 3)})
     return {"workload": "qwen_tsweep: Qwen-shaped layer, T = 1..8 seeded tokens per call (no logit bias)",
             "calls_per_T": calls, "rows": rows}
+
+
+def lmhead_workload(B: Bench, steps: int, peaks, calls: int = 16):
+    """Online-FP8 LM head, 157,184 x 2,560, T = 1 and 4: per-call time with the L2
+    flushed before every call; algorithmic bytes = codes + scales + x + logits."""
+    torch = B.torch
+    from sparse_mixture_experts_gemv_gb300 import LmHead
+    spec = mi.LMHEAD
+    head = LmHead(mi.lmhead_weights(spec), device=B.dev)
+    res = {"workload": f"lmhead_fp8: online-FP8 (E4M3, per-row fp32 scale) output projection "
+                       f"{spec.V} x {spec.H}, bf16 activations", "rows": []}
+    try:
+        for T in (1, 4):
+            xs = [torch.from_numpy(mi.lmhead_tokens(spec, T, stream=100 * T + c).view(np.int16)).to(B.dev)
+                  for c in range(calls)]
+            outs = [torch.empty((T, spec.V), dtype=torch.float32, device=B.dev) for _ in range(calls)]
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+            times = []
+            for it in range(steps + 1):
+                torch.cuda._sleep(20_000_000)
+                for i in range(calls):
+                    B.flush_l2()
+                    ev[i][0].record()
+                    head.forward(xs[i], outs[i])
+                    ev[i][1].record()
+                torch.cuda.synchronize()
+                if it:  # the first pass warms up
+                    times += [a.elapsed_time(b) for a, b in ev]
+            us = float(np.mean(times) * 1e3)
+            alg = spec.V * spec.H + 4 * spec.V + 2 * T * spec.H + 4 * T * spec.V
+            gbs = alg / (us * 1e-6) / 1e9
+            res["rows"].append({"T": T, "us_per_call": round(us, 3), "algorithmic_bytes": alg,
+                                "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                                "launches_per_call": 1})
+    finally:
+        head.close()
+    return res
 
 
 def prefill_workload(B: Bench, wname: str, steps: int, warmup: int, peaks):
@@ -500,6 +541,17 @@ def run_profile_driver(args):
     import torch
     dev = torch.device("cuda", 0)
     B = Bench(dev)
+    if args.profile == "lmhead_fp8":   # the online-FP8 LM head GEMV at T=1
+        from sparse_mixture_experts_gemv_gb300 import LmHead
+        head = LmHead(mi.lmhead_weights(mi.LMHEAD), device=dev)
+        x = torch.from_numpy(mi.lmhead_tokens(mi.LMHEAD, 1, stream=3).view(np.int16)).to(dev)
+        for c in range(args.profile_calls):
+            B.flush_l2()
+            head.forward(x)
+        torch.cuda.synchronize()
+        head.close()
+        print(json.dumps({"profile_driver": args.profile, "calls": args.profile_calls, "status": 0}))
+        return
     w = mi.WORKLOADS[args.profile]
     L = B.layer(w.layer, max_tokens=max(8, w.T) if w.layer.fmt != "bf16" else 4096)
     xs, lbs = B.inputs(w, min(w.calls, args.profile_calls))
@@ -523,7 +575,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-calls-per-step", type=int, default=8)
-    ap.add_argument("--profile", default=None, choices=sorted(mi.WORKLOADS),
+    ap.add_argument("--profile", default=None, choices=sorted(mi.WORKLOADS) + ["lmhead_fp8"],
                     help="untimed calls of one workload, for ncu captures")
     ap.add_argument("--profile-calls", type=int, default=6)
     args = ap.parse_args()

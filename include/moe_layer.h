@@ -283,6 +283,49 @@ moe_status_t moe_route_topk_noalloc(const void* x_dev, const float* router_t_dev
                                     const float* logit_bias_dev, int32_t T, int32_t H, int32_t E, int32_t k,
                                     int32_t* idx_dev, float* weights_dev, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Online-FP8 output projection (LM head), a second GEMV on the same engine
+ * ("Three ways to speed up MoE inference on DGX Spark", section "Optimization
+ * 2": the bf16 head, hidden 2,560 -> 157,184 vocabulary entries, is read in full
+ * for every decoded token; quantizing it to FP8 when it is built halves those
+ * bytes). Codes are FP8 E4M3 (OCP: bias 7, largest finite 448, no infinities),
+ * one fp32 scale per output row s_v = amax_h |W[v, h]| / 448 (1 for an all-zero
+ * row), q = E4M3(W / s_v) rounded to nearest even with saturation to +-448.
+ * logits[t, v] = s_v * sum_h E4M3(q[v, h]) * x[t, h], accumulated in fp32;
+ * activations stay bf16.
+ * ------------------------------------------------------------------------ */
+typedef struct moe_lmhead moe_lmhead_t;
+#define MOE_LMHEAD_MAX_T 4          /* tokens per forward (decode, verify windows) */
+#define MOE_LMHEAD_MAX_HIDDEN 8192
+
+/*
+ * Quantize W (w_dev: bf16 [vocab, hidden] device, row-major, 16-byte aligned) into
+ * codes and scales the head owns; the caller may free w_dev afterwards.
+ * Synchronous. hidden must be a multiple of 256 and <= MOE_LMHEAD_MAX_HIDDEN
+ * (else MOE_ERR_UNSUPPORTED); vocab >= 1. Errors: MOE_ERR_INVALID_ARG,
+ * MOE_ERR_OOM, MOE_ERR_CUDA. On failure *out is NULL and nothing stays allocated.
+ */
+moe_status_t moe_lmhead_create(int32_t hidden, int32_t vocab, const void* w_dev, moe_lmhead_t** out);
+
+/*
+ * logits_dev fp32 [T, vocab] = head(x_dev bf16 [T, hidden]); 0 <= T <=
+ * MOE_LMHEAD_MAX_T (T == 0 is a no-op). x_dev 16-byte aligned, logits_dev 4-byte
+ * aligned, not overlapping. One kernel enqueued on `stream`; no allocation, no
+ * host synchronisation. Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA.
+ */
+moe_status_t moe_lmhead_forward(moe_lmhead_t* head, const void* x_dev, float* logits_dev, int32_t T,
+                                void* stream);
+
+/*
+ * Copy the quantized weights out (diagnostic): codes_dev uint8 [vocab, hidden],
+ * scales_dev fp32 [vocab] (device pointers; either may be NULL). Enqueued on
+ * `stream`.
+ */
+moe_status_t moe_lmhead_get_weights(moe_lmhead_t* head, void* codes_dev, float* scales_dev, void* stream);
+
+/* Free the head (synchronises the device first). NULL is accepted. */
+void moe_lmhead_destroy(moe_lmhead_t* head);
+
 /* Name of a status code (static string). */
 const char* moe_status_string(moe_status_t status);
 

@@ -8,3 +8,4 @@ first call raises ImportError (there is no fallback implementation).
 from ._native import *  # noqa: F401,F403  (C names: moe_layer_create, moe_layer_forward, ...)
 from ._native import load  # noqa: F401
 from .layer import MoeLayer, weights_from_raw  # noqa: F401
+from .lmhead import LmHead  # noqa: F401

@@ -85,6 +85,12 @@ _SIGNATURES = {
                                               ctypes.POINTER(ctypes.c_int32)]),
     "moe_route_topk_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int32] * 4 +
                                [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_lmhead_create": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                         ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_lmhead_forward": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                          ctypes.c_void_p]),
+    "moe_lmhead_get_weights": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "moe_lmhead_destroy": (None, [ctypes.c_void_p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_last_cuda_error": (ctypes.c_char_p, []),
 }
@@ -205,3 +211,27 @@ def moe_route_topk_noalloc(x_dev, router_t_dev, router_bias_dev, logit_bias_dev,
 
 def moe_layer_describe(layer: int) -> str:
     return load().moe_layer_describe(layer).decode()
+
+
+MOE_LMHEAD_MAX_T = 4
+MOE_LMHEAD_MAX_HIDDEN = 8192
+
+
+def moe_lmhead_create(hidden: int, vocab: int, w_dev: int):
+    """Returns (status, handle or None)."""
+    h = ctypes.c_void_p()
+    st = load().moe_lmhead_create(hidden, vocab, w_dev, ctypes.byref(h))
+    return st, h.value
+
+
+def moe_lmhead_forward(head: int, x_dev: int, logits_dev: int, T: int, stream: int = 0) -> int:
+    return load().moe_lmhead_forward(head, x_dev, logits_dev, T, stream)
+
+
+def moe_lmhead_get_weights(head: int, codes_dev, scales_dev, stream: int = 0) -> int:
+    return load().moe_lmhead_get_weights(head, codes_dev, scales_dev, stream)
+
+
+def moe_lmhead_destroy(head: int) -> None:
+    load().moe_lmhead_destroy(head)
+

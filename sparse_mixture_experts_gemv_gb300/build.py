@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
-SOURCES = ["moe_api.cu", "moe_decode.cu", "moe_stream.cu", "moe_stream_mx.cu", "moe_grouped.cu", "moe_noalloc.cu"]
+SOURCES = ["moe_api.cu", "moe_decode.cu", "moe_stream.cu", "moe_stream_mx.cu", "moe_grouped.cu", "moe_noalloc.cu",
+           "moe_lmhead.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-O3"]

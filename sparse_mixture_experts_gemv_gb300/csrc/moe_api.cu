@@ -21,6 +21,14 @@ moe_status_t cuda_fail(cudaError_t e, const char* what) {
   return MOE_ERR_CUDA;
 }
 
+}  // namespace
+
+namespace moe {
+moe_status_t record_cuda_failure(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+}  // namespace moe
+
+namespace {
+
 #define MOE_CUDA(call)                                           \
   do {                                                           \
     cudaError_t e_ = (call);                                     \

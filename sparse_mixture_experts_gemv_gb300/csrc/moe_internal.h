@@ -111,6 +111,8 @@ struct moe_layer {
 };
 
 namespace moe {
+// Keeps the text of a CUDA failure for moe_last_cuda_error; returns MOE_ERR_CUDA.
+moe_status_t record_cuda_failure(cudaError_t e, const char* what);
 // Records the next profiling event on s (no-op unless profiling is enabled).
 inline void prof_mark(moe_layer* L, cudaStream_t s) {
   if (L->profile && L->prof_n < 8) cudaEventRecord(L->prof_ev[L->prof_n++], s);
