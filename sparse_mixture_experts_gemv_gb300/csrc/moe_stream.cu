@@ -68,7 +68,12 @@ using stream::kMaxRingGroups;
 using stream::kMaxRouterRows;
 using stream::kSpinBudget;
 constexpr int kStreamThreads = stream::kThreads;
-constexpr int kStreamSmemMax = stream::kSmemMax;
+// Dynamic shared memory budget: the kernel's static part is at most 11,136 bytes
+// (TMAX = 8), and a block may hold 232,448 bytes in all. 216 KB keeps two
+// 8-record ring groups beside x up to 5 tokens at H = 2048 (6 and more take
+// three 4-record groups).
+constexpr int kStreamSmemMax = 216 * 1024;
+static_assert(kStreamSmemMax + 11136 <= 232448, "static + dynamic shared memory of one block");
 constexpr int kMaxGroupRecords = 8;                 // records per ring group (one 16-row MMA tile)
 constexpr int kMaxStreamH = kStreamMaxHidden;       // output tiles per warp kept in registers: H / 256
 constexpr int kMaxTiles = kMaxStreamH / 256;

@@ -30,7 +30,6 @@ constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;            // + one producer warp
 constexpr int kMaxRingGroups = 16;
 constexpr int kMaxRouterRows = 16;                   // router rows per CTA
-constexpr int kSmemMax = 212 * 1024;                 // dynamic shared memory budget
 constexpr long long kSpinBudget = 4000000000LL;      // ~2 s of SM cycles: then give up
 
 MOE_DEV unsigned long long ld_relaxed_u64(const unsigned long long* p) {

@@ -67,7 +67,11 @@ constexpr int kMaxMx = 16;             // MXFP4 records per routed group: 16 (on
 constexpr int kShGroup = 4;            // bf16 shared-expert records per shared group (one MMA tile)
 constexpr int kMaxMt = kMaxMx / 8;     // 16-row gate/up tiles per group
 constexpr int kMxMaxH = kStreamMxMaxHidden;   // output tiles per warp kept in registers: H / 256
-constexpr int kMxSmemMax = 204 * 1024;  // dynamic shared memory budget (the static part is ~19 KB)
+// Dynamic shared memory budget: the static part is at most 19,584 bytes and a
+// block may hold 232,448 bytes in all; 207 KB keeps 16-record groups up to 7
+// tokens at H = 2560.
+constexpr int kMxSmemMax = 207 * 1024;
+static_assert(kMxSmemMax + 19584 <= 232448, "static + dynamic shared memory of one block");
 
 struct MxArgs {
   const uint16_t* x;           // bf16 [T][H]

@@ -75,6 +75,32 @@ def test_ling_mxfp4(name):
     print(name, r)
 
 
+@pytest.mark.parametrize("T", [5, 6, 8])
+def test_qwen_windows_beyond_four(T):
+    """Qwen-shaped windows of 5-8 tokens on the weight-streaming kernel (5 tokens keep
+    two 8-record ring groups beside x; 6 and 8 take three 4-record groups)."""
+    spec = mi.QWEN_LAYER
+    L = G.cuda_layer(spec, max_tokens=4096)
+    S = G.synth(spec)
+    for call in range(2):
+        x = mi.tokens(spec, T, stream=6000 + 10 * T + call)
+        out, idx, wt = G.run_cuda(L, x)
+        assert L.stats().path == 1
+        G.compare(S, x, out, idx, wt)
+
+
+def test_ling_mxfp4_window_of_seven():
+    """The largest weight-streaming window of the Ling-shaped MXFP4 layer (7 tokens,
+    16-record MXFP4 groups)."""
+    w = mi.WORKLOADS["ling_mxfp4_t4"]
+    L = G.cuda_layer(w.layer, max_tokens=8)
+    S = G.synth(w.layer)
+    x = mi.tokens(w.layer, 7, stream=6070)
+    out, idx, wt = G.run_cuda(L, x)
+    assert L.stats().path == 1
+    G.compare(S, x, out, idx, wt, fmt="mxfp4")
+
+
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_small_mxfp4_every_window_size(T):
     """A small MXFP4 layer (E=16, k=4, so windows share experts and groups cross
