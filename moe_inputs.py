@@ -121,6 +121,21 @@ def _mxfp4_matrix(rng: np.random.Generator, rows: int, K: int):
     return codes, scales
 
 
+def _int4_matrix(rng: np.random.Generator, rows: int, K: int):
+    """Groupwise affine int4 (group 64 along K): codes uniform over 0..15 (a uniform
+    byte holds two independent uniform nibbles); per group a bf16 scale
+    s = 0.02 * (4 / 15) * u, u uniform in [0.5, 1.5), and a bf16 bias
+    b = -7.5 * s * (1 + 0.1 z), z ~ N(0, 1), so q * s + b spans about +-0.04 around 0,
+    the spread of the bf16 layers' N(0, 0.02) weights."""
+    codes = rng.integers(0, 256, size=(rows, K // 2), dtype=np.uint8)
+    u = rng.uniform(0.5, 1.5, size=(rows, K // 64)).astype(np.float32)
+    z = rng.standard_normal((rows, K // 64), dtype=np.float32)
+    s = f32_to_bf16_bits(np.float32(0.02 * 4 / 15) * u)
+    s_f = (s.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    b = f32_to_bf16_bits(np.float32(-7.5) * s_f * (np.float32(1) + np.float32(0.1) * z))
+    return codes, s, b
+
+
 class SynthLayer:
     """Lazily drawn weights of one synthetic MoE layer, in storage format.
 
@@ -128,6 +143,8 @@ class SynthLayer:
       bf16:  gate [I,H] u16, up [I,H] u16, down [H,I] u16   (bf16 bit patterns)
       mxfp4: gate_codes [I,H/2] u8, gate_scales [I,H/32] u8, same for up,
              down_codes [H,I/2] u8, down_scales [H,I/32] u8
+      int4:  gate_codes [I,H/2] u8, gate_scales and gate_biases [I,H/64] (bf16 bits),
+             same for up, down_codes [H,I/2] u8, down_scales / down_biases [H,I/64]
     shared_raw() returns gate [Is,H], up [Is,H], down [H,Is] as bf16 bits.
     router() returns W_r [H,E] float32; router_bias() returns [E] float32 or None.
     """
@@ -178,6 +195,12 @@ class SynthLayer:
             dc, ds = _mxfp4_matrix(rng, s.H, s.I)
             return {"gate_codes": gc, "gate_scales": gs, "up_codes": uc, "up_scales": us,
                     "down_codes": dc, "down_scales": ds}
+        if s.fmt == "int4":
+            out = {}
+            for m, (rows, K) in (("gate", (s.I, s.H)), ("up", (s.I, s.H)), ("down", (s.H, s.I))):
+                c, sc, b = _int4_matrix(rng, rows, K)
+                out[f"{m}_codes"], out[f"{m}_scales"], out[f"{m}_biases"] = c, sc, b
+            return out
         raise ValueError(f"unknown weight format {s.fmt!r}")
 
     def shared_raw(self) -> dict:

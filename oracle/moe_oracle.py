@@ -84,6 +84,21 @@ def mxfp4_to_f64(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return vals * sc
 
 
+def int4_affine_to_f64(codes: np.ndarray, scales: np.ndarray, biases: np.ndarray) -> np.ndarray:
+    """Decode a groupwise affine int4 matrix ("Optimizing on-device inference for
+    Apple Silicon", section "Decode weights during matrix multiplication": 4-bit
+    weights in groups of 64 with a bf16 scale and a bf16 bias per group): codes
+    [..., K/2] (two unsigned 4-bit q per byte, even element in the low nibble),
+    scales and biases [..., K/64] as bf16 bits -> q * scale + bias in fp64 [..., K]."""
+    codes = np.asarray(codes)
+    lo = codes & 0x0F
+    hi = codes >> 4
+    q = np.stack([lo, hi], axis=-1).reshape(codes.shape[:-1] + (codes.shape[-1] * 2,)).astype(np.float64)
+    s = np.repeat(bf16_bits_to_f64(scales), 64, axis=-1)
+    b = np.repeat(bf16_bits_to_f64(biases), 64, axis=-1)
+    return q * s + b
+
+
 def round_f64_to_bf16_bits(v: np.ndarray) -> np.ndarray:
     """Round fp64 values to the nearest bf16 (ties to even) in one step; return uint16 bits.
 
@@ -166,6 +181,9 @@ def decode_expert(layer, e: int):
         return (mxfp4_to_f64(raw["gate_codes"], raw["gate_scales"]),
                 mxfp4_to_f64(raw["up_codes"], raw["up_scales"]),
                 mxfp4_to_f64(raw["down_codes"], raw["down_scales"]))
+    if layer.spec.fmt == "int4":
+        return tuple(int4_affine_to_f64(raw[f"{m}_codes"], raw[f"{m}_scales"], raw[f"{m}_biases"])
+                     for m in ("gate", "up", "down"))
     raise ValueError(layer.spec.fmt)
 
 

@@ -11,7 +11,8 @@ from tests import test_oracle_pins as pins
 
 _orig = {name: getattr(o, name) for name in
          ("swiglu_expert", "routing_weights", "select_topk", "mxfp4_to_f64", "e8m0_value",
-          "bf16_bits_to_f64", "router_logits", "moe_forward", "dispatch", "e2m1_value", "silu")}
+          "bf16_bits_to_f64", "router_logits", "moe_forward", "dispatch", "e2m1_value", "silu",
+         "int4_affine_to_f64")}
 
 
 def _silu_on_up(X, wg, wu, wd):
@@ -72,7 +73,33 @@ def _dispatch_reverse_tokens(idx, E, block_rows):
     return d
 
 
+def _int4_nibbles_swapped(codes, scales, biases):
+    c = np.asarray(codes)
+    return _orig["int4_affine_to_f64"](((c & 0x0F) << 4) | (c >> 4), scales, biases)
+
+
+def _int4_group_32(codes, scales, biases):
+    c = np.asarray(codes)
+    q = np.stack([c & 0x0F, c >> 4], axis=-1).reshape(c.shape[:-1] + (c.shape[-1] * 2,)).astype(np.float64)
+    s = np.repeat(o.bf16_bits_to_f64(scales), 32, axis=-1)
+    b = np.repeat(o.bf16_bits_to_f64(biases), 32, axis=-1)
+    n = min(q.shape[-1], s.shape[-1])
+    return q[..., :n] * s[..., :n] + b[..., :n]
+
+
+def _int4_signed_codes(codes, scales, biases):
+    c = np.asarray(codes)
+    q = np.stack([c & 0x0F, c >> 4], axis=-1).reshape(c.shape[:-1] + (c.shape[-1] * 2,)).astype(np.float64)
+    q = np.where(q >= 8, q - 16, q)                  # read as two's complement
+    s = np.repeat(o.bf16_bits_to_f64(scales), 64, axis=-1)
+    b = np.repeat(o.bf16_bits_to_f64(biases), 64, axis=-1)
+    return q * s + b
+
+
 MUTATIONS = {
+    "int4_nibbles_swapped": ("int4_affine_to_f64", _int4_nibbles_swapped),
+    "int4_group_of_32": ("int4_affine_to_f64", _int4_group_32),
+    "int4_signed_codes": ("int4_affine_to_f64", _int4_signed_codes),
     "silu_on_up": ("swiglu_expert", _silu_on_up),
     "weights_not_renormalised": ("routing_weights", _no_renorm),
     "topk_smallest": ("select_topk", _topk_ascending),
@@ -98,6 +125,8 @@ PIN_TESTS = [
     lambda: pins.test_worked_example_mxfp4(),
     lambda: pins.test_single_expert_is_plain_swiglu_mlp(),
     lambda: pins.test_dispatch_invariants_and_brute_force(),
+    lambda: pins.test_int4_affine_decode_all_bytes(),
+    lambda: pins.test_int4_scale_and_bias_apply_per_64_group(),
 ]
 
 

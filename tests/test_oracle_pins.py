@@ -84,6 +84,30 @@ def test_mxfp4_scale_applies_per_32_block():
     assert (got[0, :32] == 1.0).all() and (got[0, 32:] == 8.0).all()
 
 
+def test_int4_affine_decode_all_bytes():
+    """Every byte in every position of a 64-element group: element 2i is the low
+    nibble q0, 2i+1 the high nibble q1, value = q * scale + bias (scale 0.5 = bf16
+    0x3F00, bias -4 = bf16 0xC080): byte 0x3A -> 10 * 0.5 - 4 = 1.0 and 3 * 0.5 - 4 = -2.5."""
+    codes = np.arange(256, dtype=np.uint8).reshape(8, 32)      # 8 rows x 64 elements
+    sc = np.full((8, 1), 0x3F00, dtype=np.uint16)
+    bi = np.full((8, 1), 0xC080, dtype=np.uint16)
+    got = o.int4_affine_to_f64(codes, sc, bi)
+    for r in range(8):
+        for byte_i in range(32):
+            b = int(codes[r, byte_i])
+            assert got[r, 2 * byte_i] == (b & 15) * 0.5 - 4.0
+            assert got[r, 2 * byte_i + 1] == (b >> 4) * 0.5 - 4.0
+    assert got[0x3A // 32, 2 * (0x3A % 32)] == 1.0 and got[0x3A // 32, 2 * (0x3A % 32) + 1] == -2.5
+
+
+def test_int4_scale_and_bias_apply_per_64_group():
+    codes = np.full((1, 96), 0x11, dtype=np.uint8)             # 192 elements with q = 1
+    sc = np.array([[0x3F80, 0x4000, 0x4080]], dtype=np.uint16)  # 1, 2, 4
+    bi = np.array([[0x0000, 0x4120, 0x42C8]], dtype=np.uint16)  # 0, 10, 100
+    got = o.int4_affine_to_f64(codes, sc, bi)
+    assert (got[0, :64] == 1.0).all() and (got[0, 64:128] == 12.0).all() and (got[0, 128:] == 104.0).all()
+
+
 # ---------------------------------------------------------------- router
 
 def _brute_topk(row, k):
@@ -213,11 +237,11 @@ def test_k_equals_E_is_dense_softmax_mixture():
     np.testing.assert_allclose(r["out"], want, rtol=1e-12, atol=1e-14)
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "mxfp4"])
+@pytest.mark.parametrize("fmt", ["bf16", "mxfp4", "int4"])
 def test_dense_masked_equals_sparse(fmt):
     """Evaluate every expert on every token, weight by w on the selected experts and 0
     elsewhere: equals the sparse path."""
-    H, I = (64, 32)
+    H, I = (64, 32) if fmt != "int4" else (128, 64)   # int4 groups are 64 wide
     layer = random_layer(H=H, E=7, k=3, I=I, Is=32, seed=7, fmt=fmt)
     x = bf16(np.random.default_rng(2).normal(size=(9, H)))
     r = o.moe_forward(layer, x)
