@@ -339,7 +339,12 @@ def run_ours(args):
             extra["lmhead_fp8"] = lmhead_workload(B, max(2, args.steps // 4), peaks)
         except Exception as ex:
             extra["lmhead_fp8"] = {"error": repr(ex)}
-        for wname in ("qwen_prefill", "ling_mxfp4_prefill"):
+        for wname in ("qwen_int4_decode",):
+            try:
+                extra[wname] = decode_workload(B, wname, max(2, args.steps // 2), 2, peaks)
+            except Exception as ex:
+                extra[wname] = {"error": repr(ex)}
+        for wname in ("qwen_prefill", "qwen_int4_prefill", "ling_mxfp4_prefill"):
             try:
                 extra[wname] = prefill_workload(B, wname, max(2, args.steps // 2), 2, peaks)
             except Exception as ex:

@@ -55,11 +55,20 @@ typedef enum {
 
 typedef enum {
   MOE_WEIGHTS_BF16 = 0,      /* routed experts in bf16                                     */
-  MOE_WEIGHTS_MXFP4 = 1      /* routed experts in MXFP4: e2m1 codes, two per byte with the
+  MOE_WEIGHTS_MXFP4 = 1,     /* routed experts in MXFP4: e2m1 codes, two per byte with the
                                 even element in the low nibble, plus one e8m0 scale byte per
                                 32 consecutive elements along the contraction dimension;
                                 value = e2m1(code) * 2^(scale-127). The shared expert stays
                                 bf16 and the router fp32.                                  */
+  MOE_WEIGHTS_INT4 = 2       /* routed experts in groupwise affine int4 ("Optimizing
+                                on-device inference for Apple Silicon", section "Decode
+                                weights during matrix multiplication"): unsigned 4-bit q, two
+                                per byte with the even element in the low nibble, one bf16
+                                scale s and one bf16 bias b per 64 consecutive elements along
+                                the contraction dimension; value = q * s + b. The shared
+                                expert stays bf16 and the router fp32. Served by the
+                                three-phase decode kernel and the grouped path (decoded to f16
+                                there: one rounding of q * s + b).                          */
 } moe_weight_format_t;
 
 /* Create-time flags (moe_layer_config_t.flags). */
@@ -105,6 +114,11 @@ typedef struct {
  *   MXFP4 format:
  *     gate_dev, up_dev   uint8 codes [E, I, H/2];  gate_scales_dev, up_scales_dev uint8 [E, I, H/32]
  *     down_dev           uint8 codes [E, H, I/2];  down_scales_dev uint8 [E, H, I/32]
+ *   INT4 format (H and I multiples of 64):
+ *     gate_dev, up_dev   uint8 codes [E, I, H/2];  gate/up scales and biases bf16 [E, I, H/64]
+ *                        (gate_scales_dev, gate_biases_dev, ...: byte pointers to bf16 data)
+ *     down_dev           uint8 codes [E, H, I/2];  down scales and biases bf16 [E, H, I/64]
+ *   *_biases_dev are used by the INT4 format only (NULL otherwise).
  *   shared_gate_dev, shared_up_dev  bf16 [Is, H];  shared_down_dev bf16 [H, Is]
  */
 typedef struct {
@@ -119,6 +133,9 @@ typedef struct {
   const void* shared_gate_dev;
   const void* shared_up_dev;
   const void* shared_down_dev;
+  const void* gate_biases_dev;
+  const void* up_biases_dev;
+  const void* down_biases_dev;
 } moe_layer_weights_t;
 
 typedef struct moe_layer moe_layer_t;

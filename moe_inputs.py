@@ -95,6 +95,13 @@ WORKLOADS = {
         "ling_mxfp4_prefill", LayerSpec(H=2560, E=512, k=8, I=768, Is=768, fmt="mxfp4", seed=0),
         T=4096, calls=1,
         description="Ling-shaped MXFP4 prefill chunk H=2560 E=512 top-8 I=768 + shared, T=4096"),
+    "qwen_int4_decode": Workload(
+        "qwen_int4_decode", LayerSpec(H=2048, E=256, k=8, I=512, Is=512, fmt="int4", seed=0), T=1, calls=64,
+        description="Qwen-shaped decode with groupwise affine int4 routed experts (group 64, bf16 scale + bias)"),
+    "qwen_int4_prefill": Workload(
+        "qwen_int4_prefill", LayerSpec(H=2048, E=256, k=8, I=512, Is=512, fmt="int4", seed=0,
+                                       router_bias="zipf"), T=4096, calls=1,
+        description="Qwen-shaped prefill T=4096 with int4 routed experts, Zipf(1.1) per-expert router bias"),
     "qwen_prefill": Workload(
         "qwen_prefill", LayerSpec(H=2048, E=256, k=8, I=512, Is=512, fmt="bf16", seed=0,
                                   router_bias="zipf"), T=4096, calls=1,

@@ -23,6 +23,7 @@ MOE_ERR_DEVICE_CHECK = 6
 
 MOE_WEIGHTS_BF16 = 0
 MOE_WEIGHTS_MXFP4 = 1
+MOE_WEIGHTS_INT4 = 2
 
 MOE_FLAG_FORCE_GROUPED = 0x1
 MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT = 0x100
@@ -42,7 +43,8 @@ class moe_layer_config_t(ctypes.Structure):
 class moe_layer_weights_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "router_dev", "router_bias_dev", "gate_dev", "up_dev", "down_dev", "gate_scales_dev",
-        "up_scales_dev", "down_scales_dev", "shared_gate_dev", "shared_up_dev", "shared_down_dev")]
+        "up_scales_dev", "down_scales_dev", "shared_gate_dev", "shared_up_dev", "shared_down_dev",
+        "gate_biases_dev", "up_biases_dev", "down_biases_dev")]
 
 
 class moe_stats_t(ctypes.Structure):

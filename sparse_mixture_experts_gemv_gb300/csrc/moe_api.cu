@@ -182,13 +182,26 @@ __global__ void mx_down_scales_kernel(const uint8_t* __restrict__ ds, uint8_t* _
   }
 }
 
+// Groupwise affine int4: the (scale, bias) bf16 pair of group g of each row goes
+// to bytes [off + 4g, off + 4g + 4) of the row's record (scale first).
+__global__ void i4_group_params_kernel(const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
+                                       uint8_t* __restrict__ rec, size_t rows, int ngroups, int64_t rb, int64_t off) {
+  const size_t total = rows * ngroups;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < total; q += (size_t)gridDim.x * blockDim.x) {
+    const size_t row = q / ngroups, g = q % ngroups;
+    *reinterpret_cast<uint32_t*>(rec + row * rb + off + 4 * g) = (uint32_t)scales[q] | ((uint32_t)biases[q] << 16);
+  }
+}
+
 moe_status_t validate(const moe_layer_config_t* c, const moe_layer_weights_t* w) {
   if (!c || !w) return MOE_ERR_INVALID_ARG;
   if (c->hidden <= 0 || c->num_experts <= 0 || c->top_k <= 0 || c->intermediate <= 0 ||
       c->shared_intermediate < 0 || c->max_tokens <= 0)
     return MOE_ERR_INVALID_ARG;
   if (c->top_k > c->num_experts) return MOE_ERR_INVALID_ARG;
-  if (c->weight_format != MOE_WEIGHTS_BF16 && c->weight_format != MOE_WEIGHTS_MXFP4) return MOE_ERR_INVALID_ARG;
+  if (c->weight_format != MOE_WEIGHTS_BF16 && c->weight_format != MOE_WEIGHTS_MXFP4 &&
+      c->weight_format != MOE_WEIGHTS_INT4)
+    return MOE_ERR_INVALID_ARG;
   if (c->flags & ~(uint32_t)(MOE_FLAG_FORCE_GROUPED | MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT)) return MOE_ERR_INVALID_ARG;
   if (c->hidden % 256 != 0 || c->hidden > 8192) return MOE_ERR_UNSUPPORTED;
   if (c->intermediate % 128 != 0 || c->intermediate > 4096) return MOE_ERR_UNSUPPORTED;
@@ -198,8 +211,11 @@ moe_status_t validate(const moe_layer_config_t* c, const moe_layer_weights_t* w)
   if (!w->router_dev || !w->gate_dev || !w->up_dev || !w->down_dev) return MOE_ERR_INVALID_ARG;
   if (c->shared_intermediate > 0 && (!w->shared_gate_dev || !w->shared_up_dev || !w->shared_down_dev))
     return MOE_ERR_INVALID_ARG;
-  if (c->weight_format == MOE_WEIGHTS_MXFP4 &&
+  if (c->weight_format != MOE_WEIGHTS_BF16 &&
       (!w->gate_scales_dev || !w->up_scales_dev || !w->down_scales_dev))
+    return MOE_ERR_INVALID_ARG;
+  if (c->weight_format == MOE_WEIGHTS_INT4 &&
+      (!w->gate_biases_dev || !w->up_biases_dev || !w->down_biases_dev))
     return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
@@ -270,6 +286,30 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
     MOE_CUDA(cudaMemcpy2D(L.w_gu, 2 * row, w->gate_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
     MOE_CUDA(cudaMemcpy2D(L.w_gu + row, 2 * row, w->up_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
     MOE_CUDA(cudaMemcpy(L.w_down, w->down_dev, (size_t)E * H * I * 2, cudaMemcpyDeviceToDevice));
+  } else if (c.weight_format == MOE_WEIGHTS_INT4) {
+    // One record per row: codes (K/2 bytes) then (scale, bias) bf16 pairs of the
+    // K/64 groups (4 bytes each, padded to 16).
+    L.row_bytes.gu = H / 2 + pad16(H / 16);
+    L.row_bytes.down = I / 2 + pad16(I / 16);
+    GET(L.w_gu, (size_t)E * I * 2 * L.row_bytes.gu);
+    GET(L.w_down, (size_t)E * H * L.row_bytes.down);
+    MOE_CUDA(cudaMemset(L.w_gu, 0, (size_t)E * I * 2 * L.row_bytes.gu));
+    MOE_CUDA(cudaMemset(L.w_down, 0, (size_t)E * H * L.row_bytes.down));
+    const size_t rg = (size_t)L.row_bytes.gu, rd = (size_t)L.row_bytes.down;
+    const size_t rows_gu = (size_t)E * I, rows_d = (size_t)E * H;
+    MOE_CUDA(cudaMemcpy2D(L.w_gu, 2 * rg, w->gate_dev, H / 2, H / 2, rows_gu, cudaMemcpyDeviceToDevice));
+    MOE_CUDA(cudaMemcpy2D(L.w_gu + rg, 2 * rg, w->up_dev, H / 2, H / 2, rows_gu, cudaMemcpyDeviceToDevice));
+    MOE_CUDA(cudaMemcpy2D(L.w_down, rd, w->down_dev, I / 2, I / 2, rows_d, cudaMemcpyDeviceToDevice));
+    // gate rows are records 2i, up rows 2i + 1 (stride 2 * rg from the first of each)
+    i4_group_params_kernel<<<1024, 256>>>((const uint16_t*)w->gate_scales_dev, (const uint16_t*)w->gate_biases_dev,
+                                          L.w_gu, rows_gu, (int)(H / 64), (int64_t)(2 * rg), H / 2);
+    MOE_CUDA(cudaGetLastError());
+    i4_group_params_kernel<<<1024, 256>>>((const uint16_t*)w->up_scales_dev, (const uint16_t*)w->up_biases_dev,
+                                          L.w_gu + rg, rows_gu, (int)(H / 64), (int64_t)(2 * rg), H / 2);
+    MOE_CUDA(cudaGetLastError());
+    i4_group_params_kernel<<<1024, 256>>>((const uint16_t*)w->down_scales_dev, (const uint16_t*)w->down_biases_dev,
+                                          L.w_down, rows_d, (int)(I / 64), (int64_t)rd, I / 2);
+    MOE_CUDA(cudaGetLastError());
   } else {
     // One record per row: codes (K/2 bytes) then scales (K/32 bytes, padded to 16).
     L.row_bytes.gu = H / 2 + pad16(H / 32);
@@ -417,7 +457,8 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
            "T>%d: grouped path [grouped_router_tc, dispatch, grouped_gateup_tc (tcgen05%s), grouped_down_tc (tcgen05%s), "
            "combine]%s",
            cfg->hidden, cfg->num_experts, cfg->top_k, cfg->intermediate, cfg->shared_intermediate,
-           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? "mxfp4" : "bf16", cfg->max_tokens,
+           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? "mxfp4" : cfg->weight_format == MOE_WEIGHTS_INT4 ? "int4" : "bf16",
+           cfg->max_tokens,
            (cfg->flags & MOE_FLAG_FORCE_GROUPED) ? 0 : L.decode_max_t,
            moe::stream_supported(&L, 1)
                ? "moe_decode_stream_kernel (cooperative: router with tagged logits, per-CTA top-k, bulk-copied "
@@ -429,10 +470,15 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
                  "partial-output exchange)"
                : (cfg->weight_format == MOE_WEIGHTS_MXFP4
                       ? "moe_decode_fused_kernel<mxfp4> (cooperative: router+shared, routed gate/up, down+combine)"
+                      : cfg->weight_format == MOE_WEIGHTS_INT4
+                      ? "moe_decode_fused_kernel<int4> (cooperative: router+shared, routed gate/up, down+combine; "
+                        "per group s * sum(q x) + b * sum(x))"
                       : "moe_decode_fused_kernel<bf16> (cooperative: router+shared, routed gate/up, down+combine)"),
            (cfg->flags & MOE_FLAG_FORCE_GROUPED) ? 0 : L.decode_max_t,
-           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? ", MXFP4 B rows decoded to f16 in the kernel" : "",
-           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? ", MXFP4 B rows decoded to f16 in the kernel" : "",
+           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? ", MXFP4 B rows decoded to f16 in the kernel"
+           : cfg->weight_format == MOE_WEIGHTS_INT4 ? ", int4 B rows decoded to f16 in the kernel" : "",
+           cfg->weight_format == MOE_WEIGHTS_MXFP4 ? ", MXFP4 B rows decoded to f16 in the kernel"
+           : cfg->weight_format == MOE_WEIGHTS_INT4 ? ", int4 B rows decoded to f16 in the kernel" : "",
            (cfg->flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? " [test: forced wait timeout]" : "");
   *out = &o->L;
   return MOE_OK;

@@ -41,6 +41,7 @@ namespace moe {
 
 struct FmtBF16 {};
 struct FmtMXFP4 {};
+struct FmtInt4 {};   // groupwise affine int4: q * s + b, one (s, b) bf16 pair per 64 elements
 
 constexpr int kGemvThreads = 512;
 constexpr int kLookahead = 2;  // extra rounds of gate/up units each warp keeps on their way to L2
@@ -84,6 +85,30 @@ __device__ __forceinline__ float dot32_e2m1_f16(const uint4 c, const uint16_t* x
     const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int b = 0; b < 4; ++b) s = fma2_f16(e2m1x2_to_f16x2(cw[q] >> (8 * b)), xw[b], s);
+  }
+  return s;
+}
+
+// Two unsigned 4-bit codes of one byte (element 2i in the low nibble) -> f16x2,
+// exact: 0x6400 | q is the f16 1024 + q, and 1024 is subtracted in f16.
+__device__ __forceinline__ uint32_t u4x2_to_f16x2(uint32_t byte) {
+  const uint32_t w = 0x64006400u | (byte & 0x0Fu) | ((byte & 0xF0u) << 12);
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0x64006400u));
+  return r;
+}
+
+// Unscaled sum of 32 int4 codes (16 bytes) times 32 f16 activations at xs.
+__device__ __forceinline__ float dot32_u4_f16(const uint4 c, const uint16_t* xs) {
+  const uint4* xv = reinterpret_cast<const uint4*>(xs);
+  const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+  float s = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 x = xv[q];
+    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int b = 0; b < 4; ++b) s = fma2_f16(u4x2_to_f16x2(cw[q] >> (8 * b)), xw[b], s);
   }
   return s;
 }
@@ -162,6 +187,47 @@ __device__ __forceinline__ void gu_fma_mx(const uint4 (&v)[16], const uint32_t (
           const uint16_t* xp = xs + t * H + 32 * c;   // f16 activations
           ag[t] = fmaf(dot32_e2m1_f16(v[q], xp), sg, ag[t]);
           au[t] = fmaf(dot32_e2m1_f16(v[8 + q], xp), su, au[t]);
+        }
+      }
+    }
+  }
+}
+
+// Int4 row pair: each 16-byte chunk holds 32 codes = half a 64-element group;
+// the (scale, bias) pairs follow the codes in the row record.
+__device__ __forceinline__ void gu_load_i4(const uint8_t* grec, const uint8_t* urec, int H, int b0, int nch,
+                                           uint4 (&v)[16], uint32_t (&par)[16], int lane) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int c = b0 + lane + 32 * q;
+    if (c < nch) {
+      v[q] = ldg_stream(grec + 16 * c);
+      v[8 + q] = ldg_stream(urec + 16 * c);
+      par[q] = __ldg(reinterpret_cast<const uint32_t*>(grec + H / 2 + 4 * (c >> 1)));
+      par[8 + q] = __ldg(reinterpret_cast<const uint32_t*>(urec + H / 2 + 4 * (c >> 1)));
+    }
+  }
+}
+
+// sum over a chunk of (q s + b) x = s * sum(q x) + b * sum(x); sum(x) of every
+// 32-element chunk of every token is staged in xsum [T][H / 32].
+template <int TMAX>
+__device__ __forceinline__ void gu_fma_i4(const uint4 (&v)[16], const uint32_t (&par)[16], int b0, int nch,
+                                          const uint16_t* xs, const float* xsum, int T, int H, float (&ag)[TMAX],
+                                          float (&au)[TMAX], int lane) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int c = b0 + lane + 32 * q;
+    if (c < nch) {
+      const float sg = bf16_lo(par[q]), bg = bf16_hi(par[q]);
+      const float su = bf16_lo(par[8 + q]), bu = bf16_hi(par[8 + q]);
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (t < T) {
+          const uint16_t* xp = xs + t * H + 32 * c;   // f16 activations
+          const float xsm = xsum[t * nch + c];
+          ag[t] = fmaf(bg, xsm, fmaf(sg, dot32_u4_f16(v[q], xp), ag[t]));
+          au[t] = fmaf(bu, xsm, fmaf(su, dot32_u4_f16(v[8 + q], xp), au[t]));
         }
       }
     }
@@ -252,7 +318,9 @@ moe_decode_fused_kernel(const FusedArgs a) {
   const int nr = (E - b + G - 1) / G;               // router rows b, b + G, ... of this CTA
   const int sh0 = (int)((int64_t)b * Is / G), sh1 = (int)((int64_t)(b + 1) * Is / G);
   constexpr bool kMx = std::is_same<Fmt, FmtMXFP4>::value;
-  uint16_t* xs16 = xs + (size_t)T * H;                // MXFP4 layers: x as f16 for the e2m1 products
+  constexpr bool kI4 = std::is_same<Fmt, FmtInt4>::value;
+  uint16_t* xs16 = xs + (size_t)T * H;                // MXFP4 / int4 layers: x as f16 for the code products
+  float* xsum = reinterpret_cast<float*>(xs16 + (size_t)T * H);  // int4: sum of x per 32 elements [T][H/32]
 
   if (threadIdx.x == 0) {
     sm100::mbar_init(&bar_sh, 1);
@@ -300,7 +368,7 @@ moe_decode_fused_kernel(const FusedArgs a) {
     for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) {
       const uint4 v8 = src[i];
       dst[i] = v8;
-      if (kMx) {  // exact for |x| >= 2^-14 (bf16 has fewer significand bits than f16)
+      if (kMx || kI4) {  // exact for |x| >= 2^-14 (bf16 has fewer significand bits than f16)
         const uint32_t w4[4] = {v8.x, v8.y, v8.z, v8.w};
         uint32_t h4[4];
 #pragma unroll
@@ -313,6 +381,16 @@ moe_decode_fused_kernel(const FusedArgs a) {
     }
   }
   __syncthreads();
+  if (kI4) {  // fixed-order fp32 sums of the bf16 x values, 32 at a time
+    for (int q = threadIdx.x; q < T * (H / 32); q += blockDim.x) {
+      const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs) + 16 * q;
+      float sm = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sm += bf16_lo(xw[i]) + bf16_hi(xw[i]);
+      xsum[q] = sm;
+    }
+    __syncthreads();
+  }
   for (int slot = warp; slot < nri + (sh1 - sh0); slot += nw) {
     const bool preloaded = slot == warp;
     if (slot < nri) {
@@ -513,12 +591,19 @@ moe_decode_fused_kernel(const FusedArgs a) {
         gu_load_bf16(grec, urec, b0, nch, v, lane);
         gu_fma_bf16<TMAX>(v, b0, nch, xs, T, H, ag, au, lane);
       }
-    } else {
+    } else if constexpr (std::is_same<Fmt, FmtMXFP4>::value) {
       const int nch = H / 32;
       uint32_t sc[16];
       for (int b0 = 0; b0 < nch; b0 += 32 * 8) {
         gu_load_mx(grec, urec, H, b0, nch, v, sc, lane);
         gu_fma_mx<TMAX>(v, sc, b0, nch, xs16, T, H, ag, au, lane);
+      }
+    } else {
+      const int nch = H / 32;
+      uint32_t par[16];
+      for (int b0 = 0; b0 < nch; b0 += 32 * 8) {
+        gu_load_i4(grec, urec, H, b0, nch, v, par, lane);
+        gu_fma_i4<TMAX>(v, par, b0, nch, xs16, xsum, T, H, ag, au, lane);
       }
     }
 #pragma unroll
@@ -563,7 +648,7 @@ moe_decode_fused_kernel(const FusedArgs a) {
     for (int q = threadIdx.x; q < n4; q += blockDim.x) {
       const uint4 f = ldg_cg(reinterpret_cast<const uint4*>(a.h) + q);
       uint2 o;
-      if (kMx) {
+      if (kMx || kI4) {
         const __half2 p0 = __floats2half2_rn(__uint_as_float(f.x), __uint_as_float(f.y));
         const __half2 p1 = __floats2half2_rn(__uint_as_float(f.z), __uint_as_float(f.w));
         o.x = *reinterpret_cast<const uint32_t*>(&p0);
@@ -592,6 +677,7 @@ moe_decode_fused_kernel(const FusedArgs a) {
     const int sd = item / npass, r0 = (item - sd * npass) * RB;
     const bool shared = (sd == D);
     const bool mx = !shared && kMx;
+    const bool i4 = !shared && kI4;
     const int K = shared ? Is : I;
     const int nsub = K / 8;                    // 8-element sub-chunks of a row
     const bool in_smem = shared || sd < d_smem;
@@ -621,16 +707,34 @@ moe_decode_fused_kernel(const FusedArgs a) {
       for (int t = 0; t < TMAX; ++t) acc[rr][t] = 0.f;
     for (int c = lane; c < nsub; c += 32) {
       uint4 hv[TMAX];
+      float hsum[TMAX];   // int4: sum of the 8 f16 SwiGLU outputs of this sub-chunk
 #pragma unroll
-      for (int t = 0; t < TMAX; ++t)
-        if (hrow[t]) hv[t] = *reinterpret_cast<const uint4*>(hrow[t] + 8 * c);
+      for (int t = 0; t < TMAX; ++t) {
+        hsum[t] = 0.f;
+        if (hrow[t]) {
+          hv[t] = *reinterpret_cast<const uint4*>(hrow[t] + 8 * c);
+          if (i4) {
+            float sm = 0.f;
+            sm = fma2_f16(0x3C003C00u, hv[t].x, sm);   // 1.0 x each pair
+            sm = fma2_f16(0x3C003C00u, hv[t].y, sm);
+            sm = fma2_f16(0x3C003C00u, hv[t].z, sm);
+            sm = fma2_f16(0x3C003C00u, hv[t].w, sm);
+            hsum[t] = sm;
+          }
+        }
+      }
       uint4 wv[RB];
       uint32_t sb[RB];
 #pragma unroll
       for (int rr = 0; rr < RB; ++rr) {  // issue the row loads of this item together
         if (r0 + rr < nrows) {
           const uint8_t* rec = rows_base + (r0 + rr) * rstride;
-          if (!mx) {
+          if (i4) {   // 8 codes; the (scale, bias) pair of group c / 8
+            wv[rr].x = in_smem ? *reinterpret_cast<const uint32_t*>(rec + 4 * c)
+                               : __ldg(reinterpret_cast<const uint32_t*>(rec + 4 * c));
+            sb[rr] = in_smem ? *reinterpret_cast<const uint32_t*>(rec + I / 2 + 4 * (c >> 3))
+                             : __ldg(reinterpret_cast<const uint32_t*>(rec + I / 2 + 4 * (c >> 3)));
+          } else if (!mx) {
             wv[rr] = in_smem ? *reinterpret_cast<const uint4*>(rec + 16 * c) : ldg_stream(rec + 16 * c);
           } else {
             wv[rr].x = in_smem ? *reinterpret_cast<const uint32_t*>(rec + 4 * c)
@@ -645,7 +749,14 @@ moe_decode_fused_kernel(const FusedArgs a) {
 #pragma unroll
           for (int t = 0; t < TMAX; ++t) {
             if (hrow[t]) {
-              if (!mx) {
+              if (i4) {
+                float sdot = 0.f;
+                sdot = fma2_f16(u4x2_to_f16x2(wv[rr].x), hv[t].x, sdot);
+                sdot = fma2_f16(u4x2_to_f16x2(wv[rr].x >> 8), hv[t].y, sdot);
+                sdot = fma2_f16(u4x2_to_f16x2(wv[rr].x >> 16), hv[t].z, sdot);
+                sdot = fma2_f16(u4x2_to_f16x2(wv[rr].x >> 24), hv[t].w, sdot);
+                acc[rr][t] = fmaf(bf16_hi(sb[rr]), hsum[t], fmaf(bf16_lo(sb[rr]), sdot, acc[rr][t]));
+              } else if (!mx) {
                 acc[rr][t] = fma8_bf16(wv[rr], hv[t], acc[rr][t]);
               } else {  // one scale per 32 elements: constant over these 8
                 float sdot = 0.f;
@@ -703,7 +814,9 @@ static cudaError_t launch_fused_t(moe_layer* L, const uint16_t* x, uint16_t* out
   a.ws_gu = L->ws_gu; a.ws_down = L->ws_down;
   a.w_gu = L->w_gu; a.rb_gu = L->row_bytes.gu; a.w_down = L->w_down; a.rb_down = L->row_bytes.down;
   const int rows_max = (c.hidden + L->num_sms - 1) / L->num_sms;
-  const size_t xb = (size_t)T * c.hidden * sizeof(uint16_t) * (std::is_same<Fmt, FmtMXFP4>::value ? 2 : 1);
+  constexpr bool kI4 = std::is_same<Fmt, FmtInt4>::value;
+  const size_t xb = (size_t)T * c.hidden * sizeof(uint16_t) * (std::is_same<Fmt, FmtMXFP4>::value || kI4 ? 2 : 1) +
+                    (kI4 ? (size_t)T * (c.hidden / 32) * sizeof(float) : 0);
   const size_t hb = decode_smem_bytes_down(L, T);
   a.smem_r1 = (int)align16(xb > hb ? xb : hb);
   a.smem_sh = (int)align16((size_t)rows_max * c.shared_intermediate * 2);
@@ -752,6 +865,7 @@ static cudaError_t set_attrs_fmt() {
 cudaError_t decode_prepare(moe_layer* L) {
   cudaError_t e = set_attrs_fmt<FmtBF16>();
   if (e == cudaSuccess) e = set_attrs_fmt<FmtMXFP4>();
+  if (e == cudaSuccess) e = set_attrs_fmt<FmtInt4>();
   return e;
 }
 
@@ -769,6 +883,7 @@ cudaError_t launch_decode(moe_layer* L, const uint16_t* x, uint16_t* out, int T,
   if (stream_supported(L, T)) return launch_stream(L, x, out, T, logit_bias, s);
   if (stream_mx_supported(L, T)) return launch_stream_mx(L, x, out, T, logit_bias, s);
   if (L->cfg.weight_format == MOE_WEIGHTS_MXFP4) return launch_decode_fmt<FmtMXFP4>(L, x, out, T, logit_bias, s);
+  if (L->cfg.weight_format == MOE_WEIGHTS_INT4) return launch_decode_fmt<FmtInt4>(L, x, out, T, logit_bias, s);
   return launch_decode_fmt<FmtBF16>(L, x, out, T, logit_bias, s);
 }
 

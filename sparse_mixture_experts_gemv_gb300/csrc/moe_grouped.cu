@@ -58,8 +58,10 @@ constexpr size_t kGemmSmem = (size_t)kStages * (kStageA + kStageB) + 1024 /*alig
 // the f16 B stage of the main ring.
 constexpr int kRaw = 3;
 constexpr int kRawCodes = 256 * (BK / 2);  // 8 KB
-constexpr int kRawScales = 256 * 2;        // 512 B: blocks 2kb, 2kb + 1 of each row
-constexpr int kRawStage = kRawCodes + kRawScales;
+constexpr int kRawParMax = 256 * 4;        // per-row stage parameters: MXFP4 2 scale bytes, int4 (s, b) bf16
+constexpr int kRawStage = kRawCodes + kRawParMax;
+// B operand kinds of the grouped GEMM: bf16 rows by TMA, or 4-bit rows decoded in the kernel.
+enum BKind { B_BF16 = 0, B_MXFP4 = 1, B_INT4 = 2 };
 constexpr size_t kGemmSmemMx = kGemmSmem + (size_t)kRaw * kRawStage;
 constexpr int kConvThreads = 256;          // one B row per converter thread
 
@@ -92,11 +94,12 @@ struct GemmParams {
   uint16_t* out_shared; int ld_shared;
   float* logits; const float* router_bias; const float* logit_bias;
   int* err;
-  // MXFP4 routed experts (B rows decoded in the kernel): routed A operands are f16
+  // 4-bit routed experts (B rows decoded in the kernel): routed A operands are f16
   // (x16 for the gathered gate/up rows, f16 h for the down rows).
   const uint16_t* x16;      // f16 [T][H]
-  const uint16_t* mx_sc;    // scale pairs [E][K / 64][b_rows_per_expert]
-  const uint8_t* mx_sref;   // reference exponent of each B row [E][b_rows_per_expert]
+  const void* q_par;        // per-stage row parameters [E][K / 64][b_rows_per_expert]:
+                            // MXFP4 uint16 scale pairs, int4 uint32 (scale, bias) bf16 pairs
+  const uint8_t* mx_sref;   // MXFP4: reference exponent of each B row [E][b_rows_per_expert]
 };
 
 struct TileInfo {
@@ -171,19 +174,39 @@ __device__ __forceinline__ uint4 e2m1x8_to_f16(uint32_t w, uint32_t f) {
                     hmul2_f16(e2m1x2_to_f16x2(w >> 16), f), hmul2_f16(e2m1x2_to_f16x2(w >> 24), f));
 }
 
-// MXB: routed B rows are MXFP4 (e2m1 codes + one e8m0 scale per 32 K). The
+// Eight unsigned 4-bit codes (one word, element 2i in the low nibble of byte i)
+// -> f16(q * s + b) for the f16 pairs s2 = {s, s}, b2 = {b, b}: q is made exact in
+// f16 as (0x6400 | q) - 1024, then one fused multiply-add rounds once.
+__device__ __forceinline__ uint32_t u4x2_affine_f16x2(uint32_t byte, uint32_t s2, uint32_t b2) {
+  const uint32_t w = 0x64006400u | (byte & 0x0Fu) | ((byte & 0xF0u) << 12);
+  uint32_t q, r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(q) : "r"(w), "r"(0x64006400u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(q), "r"(s2), "r"(b2));
+  return r;
+}
+__device__ __forceinline__ uint4 u4x8_affine_f16(uint32_t w, uint32_t s2, uint32_t b2) {
+  return make_uint4(u4x2_affine_f16x2(w, s2, b2), u4x2_affine_f16x2(w >> 8, s2, b2),
+                    u4x2_affine_f16x2(w >> 16, s2, b2), u4x2_affine_f16x2(w >> 24, s2, b2));
+}
+
+// BQ = B_MXFP4: routed B rows are MXFP4 (e2m1 codes + one e8m0 scale per 32 K). The
 // producer copies each stage's codes (TMA, 32 bytes x 256 rows) and the rows'
 // scale pairs (one bulk copy) into a raw ring; converter warps decode them into
 // the f16 B stage: e2m1 -> f16 (exact) times 2^(s - sref), sref being the row's
 // largest scale, so the stage is exact f16 for blocks within 2^23 of the row's
 // largest; the epilogue multiplies column n by 2^(sref[n] - 127). Routed A rows
 // are f16 then (x16 for gate/up, f16 h for down) and the MMA kind is f16 x f16;
-// shared-expert tiles stay bf16 x bf16 through TMA.
-template <int EPI, bool GATHER, bool MXB>
-__global__ void __launch_bounds__((GATHER ? 320 : 192) + (MXB ? kConvThreads : 0), 1)
+// shared-expert tiles stay bf16 x bf16 through TMA. BQ = B_INT4: the same
+// pipeline with groupwise affine int4 rows; one stage of K = 64 is one group,
+// and the converter writes f16(q * s + b) with one fused multiply-add (one
+// rounding); no column factor.
+template <int EPI, bool GATHER, int BQ>
+__global__ void __launch_bounds__((GATHER ? 320 : 192) + (BQ != B_BF16 ? kConvThreads : 0), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_constant__ CUtensorMap mapA_s,
                     const __grid_constant__ CUtensorMap mapB_r, const __grid_constant__ CUtensorMap mapB_s,
                     const GemmParams p) {
+  constexpr bool MXB = BQ != B_BF16;           // B rows decoded by converter warps
+  constexpr int kParBytes = BQ == B_INT4 ? 4 : 2;   // stage parameters per B row
   constexpr int kConvWarp0 = GATHER ? 10 : 6;  // first converter warp (MXB)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -252,12 +275,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
           if (mxt) {  // raw codes and scale pairs of this stage's 256 B rows
             const int q = rit % kRaw;
             if (!mbar_wait(&raw_empty[q], ((rit / kRaw) & 1) ^ 1, p.err, abort_flag)) { stop = true; break; }
-            mbar_arrive_expect_tx(&raw_full[q], (uint32_t)kRawStage);
+            mbar_arrive_expect_tx(&raw_full[q], (uint32_t)(kRawCodes + 256 * kParBytes));
             const int brow = ti.e * p.b_rows_per_expert + ti.nt * 256;
             tma_load_2d(sRaw + q * kRawStage, &mapB_r, kb * (BK / 2), brow, &raw_full[q]);
             bulk_copy_g2s(sRaw + q * kRawStage + kRawCodes,
-                          p.mx_sc + ((size_t)ti.e * ti.ks + kb) * p.b_rows_per_expert + ti.nt * 256,
-                          (uint32_t)kRawScales, &raw_full[q]);
+                          reinterpret_cast<const uint8_t*>(p.q_par) +
+                              (((size_t)ti.e * ti.ks + kb) * p.b_rows_per_expert + ti.nt * 256) * kParBytes,
+                          (uint32_t)(256 * kParBytes), &raw_full[q]);
             ++rit;
           }
           const int s = it % kStages;
@@ -337,7 +361,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
         uint32_t v[32];
         tmem_ld32(taddr + c0, v);
         if (!valid) continue;
-        if (mxt) {  // column n of a decoded MXFP4 tile carries 2^(127 - sref[n])
+        if (BQ == B_MXFP4 && mxt) {  // column n of a decoded MXFP4 tile carries 2^(127 - sref[n])
           const uint4* sr = reinterpret_cast<const uint4*>(p.mx_sref + (size_t)ti.e * p.b_rows_per_expert +
                                                            ti.nt * p.BN + c0);
           const uint4 s0 = __ldg(sr), s1 = __ldg(sr + 1);
@@ -411,7 +435,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
           else set_error(p.err, kDevCheck);
         }
       }
-      const uint16_t* xa = (MXB && !ti.shared) ? p.x16 : p.x;  // routed MXFP4 tiles take f16 rows
+      const uint16_t* xa = (MXB && !ti.shared) ? p.x16 : p.x;  // routed 4-bit tiles take f16 rows
       const uint16_t* src = xa + (size_t)(token < 0 ? 0 : token) * p.H;
       const uint32_t nbytes = token < 0 ? 0u : 16u;
       bool ok = true;
@@ -443,7 +467,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
     for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
       const TileInfo ti = decode_tile(p, R, tile);
       const bool mxt = !ti.shared;
-      const int sref = mxt ? (int)__ldg(p.mx_sref + (size_t)ti.e * p.b_rows_per_expert + ti.nt * 256 + r) : 0;
+      const int sref = (BQ == B_MXFP4 && mxt)
+                           ? (int)__ldg(p.mx_sref + (size_t)ti.e * p.b_rows_per_expert + ti.nt * 256 + r) : 0;
       bool ok = true;
       for (int kb = 0; kb < ti.ks; ++kb, ++it) {
         const int s = it % kStages;
@@ -454,14 +479,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
           const uint8_t* rb = sRaw + q * kRawStage;
           const uint4 c0 = *reinterpret_cast<const uint4*>(rb + r * 32);
           const uint4 c1 = *reinterpret_cast<const uint4*>(rb + r * 32 + 16);
-          const uint32_t sc = *reinterpret_cast<const uint16_t*>(rb + kRawCodes + 2 * r);
           ++rit;
-          const uint32_t f0 = pow2_f16x2((int)(sc & 0xFFu) - sref), f1 = pow2_f16x2((int)(sc >> 8) - sref);
           const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint8_t* dst = sB + s * kStageB + r * 128;
+          if (BQ == B_MXFP4) {
+            const uint32_t sc = *reinterpret_cast<const uint16_t*>(rb + kRawCodes + 2 * r);
+            const uint32_t f0 = pow2_f16x2((int)(sc & 0xFFu) - sref), f1 = pow2_f16x2((int)(sc >> 8) - sref);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)   // 16-byte chunk j = K elements 8j..8j+7 (block 2kb for j < 4)
-            *reinterpret_cast<uint4*>(dst + ((j ^ (r & 7)) << 4)) = e2m1x8_to_f16(w[j], j < 4 ? f0 : f1);
+            for (int j = 0; j < 8; ++j)   // 16-byte chunk j = K elements 8j..8j+7 (block 2kb for j < 4)
+              *reinterpret_cast<uint4*>(dst + ((j ^ (r & 7)) << 4)) = e2m1x8_to_f16(w[j], j < 4 ? f0 : f1);
+          } else {   // int4: this stage is group kb of the row
+            const uint32_t sb = *reinterpret_cast<const uint32_t*>(rb + kRawCodes + 4 * r);
+            const uint32_t s2 = f32x2_to_f16x2(bf16_lo(sb), bf16_lo(sb)), b2 = f32x2_to_f16x2(bf16_hi(sb), bf16_hi(sb));
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(dst + ((j ^ (r & 7)) << 4)) = u4x8_affine_f16(w[j], s2, b2);
+          }
           fence_proxy_async_smem();
           // The raw slot is released only once its values have been used: an
           // arrival issued right after the loads can be observed (and the slot
@@ -741,6 +774,20 @@ __global__ void mx_grouped_scales_kernel(const uint8_t* __restrict__ w, int64_t 
   }
 }
 
+// Per-stage (scale, bias) pairs of an int4 matrix for the grouped GEMMs: rows are
+// `row_bytes` apart, each K / 2 code bytes then K / 64 (scale, bias) bf16 pairs;
+// par[e][kb][row in expert] = the pair of group kb, so one stage's 256 rows are
+// 1 KB contiguous.
+__global__ void i4_grouped_params_kernel(const uint8_t* __restrict__ w, int64_t row_bytes, int K, int rpe,
+                                         size_t rows, uint32_t* __restrict__ par) {
+  const int nkb = K / 64;
+  for (size_t row = blockIdx.x * (size_t)blockDim.x + threadIdx.x; row < rows; row += (size_t)gridDim.x * blockDim.x) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(w + row * row_bytes + K / 2);
+    const size_t e = row / rpe, rr = row % rpe;
+    for (int kb = 0; kb < nkb; ++kb) par[(e * nkb + kb) * rpe + rr] = src[kb];
+  }
+}
+
 // ===========================================================================
 // Host side
 // ===========================================================================
@@ -843,6 +890,16 @@ cudaError_t grouped_prepare(moe_layer* L) {
   GALLOC(g.y, sizeof(uint16_t) * TK * H);
   GALLOC(g.ys, sizeof(uint16_t) * (size_t)Tm * H);
   const bool mx = c.weight_format == MOE_WEIGHTS_MXFP4;
+  const bool i4 = c.weight_format == MOE_WEIGHTS_INT4;
+  if (i4) {
+    GALLOC(g.x16, sizeof(uint16_t) * (size_t)Tm * H);
+    GALLOC(g.i4_gu_par, sizeof(uint32_t) * (size_t)E * (H / 64) * 2 * I);
+    GALLOC(g.i4_dn_par, sizeof(uint32_t) * (size_t)E * (I / 64) * H);
+    i4_grouped_params_kernel<<<1024, 256>>>(L->w_gu, L->row_bytes.gu, H, 2 * I, (size_t)E * 2 * I, g.i4_gu_par);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    i4_grouped_params_kernel<<<1024, 256>>>(L->w_down, L->row_bytes.down, I, H, (size_t)E * H, g.i4_dn_par);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (mx) {
     GALLOC(g.x16, sizeof(uint16_t) * (size_t)Tm * H);
     GALLOC(g.mx_gu_sc, sizeof(uint16_t) * (size_t)E * (H / 64) * 2 * I);
@@ -864,7 +921,7 @@ cudaError_t grouped_prepare(moe_layer* L) {
   m->router_bn = (E % 64 == 0) ? 64 : (E % 32 == 0 ? 32 : 16);  // N tile dividing E (E % 16 == 0)
   if ((e = encode_2d(&m->router_split, L->router_split, 3ull * E, H, m->router_bn)) != cudaSuccess) return e;
   if ((e = encode_2d(&m->h, g.h, TK, I, BM)) != cudaSuccess) return e;
-  if (!mx) {
+  if (!mx && !i4) {
     if ((e = encode_2d(&m->w_gu, L->w_gu, (uint64_t)E * 2 * I, H, 256)) != cudaSuccess) return e;
     if ((e = encode_2d(&m->w_down, L->w_down, (uint64_t)E * H, I, 256)) != cudaSuccess) return e;
   } else {
@@ -882,20 +939,24 @@ cudaError_t grouped_prepare(moe_layer* L) {
     m->ws_down = m->w_down;
   }
   constexpr auto kSmemAttr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_ROUTER, false, false>, kSmemAttr, (int)kGemmSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_SWIGLU, true, false>, kSmemAttr, (int)kGemmSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_STORE, false, false>, kSmemAttr, (int)kGemmSmem);
+  e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_ROUTER, false, B_BF16>, kSmemAttr, (int)kGemmSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_SWIGLU, true, B_BF16>, kSmemAttr, (int)kGemmSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_STORE, false, B_BF16>, kSmemAttr, (int)kGemmSmem);
   if (e == cudaSuccess && mx)
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_SWIGLU, true, true>, kSmemAttr, (int)kGemmSmemMx);
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_SWIGLU, true, B_MXFP4>, kSmemAttr, (int)kGemmSmemMx);
   if (e == cudaSuccess && mx)
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_STORE, false, true>, kSmemAttr, (int)kGemmSmemMx);
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_STORE, false, B_MXFP4>, kSmemAttr, (int)kGemmSmemMx);
+  if (e == cudaSuccess && i4)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_SWIGLU, true, B_INT4>, kSmemAttr, (int)kGemmSmemMx);
+  if (e == cudaSuccess && i4)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_STORE, false, B_INT4>, kSmemAttr, (int)kGemmSmemMx);
   return e;
 }
 
 void grouped_release(moe_layer* L) {
   auto& g = L->grp;
   void* ptrs[] = {g.logits, g.idx, g.weights, g.hist, g.offsets, g.chunk_counts, g.perm, g.pos,
-                  g.tiles, g.num_tiles, g.h, g.hs, g.y, g.ys, g.x16, g.mx_gu_sc, g.mx_dn_sc,
+                  g.tiles, g.num_tiles, g.h, g.hs, g.y, g.ys, g.x16, g.mx_gu_sc, g.mx_dn_sc, g.i4_gu_par, g.i4_dn_par,
                   g.mx_gu_sref, g.mx_dn_sref};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -921,11 +982,12 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
   memset(&base, 0, sizeof(base));
   base.E = E; base.T = T; base.k = k; base.H = H; base.err = L->err; base.max_mtiles = g.max_tiles;
   const bool mx = c.weight_format == MOE_WEIGHTS_MXFP4;
+  const bool i4 = c.weight_format == MOE_WEIGHTS_INT4;
 
   // 1. router logits (tensor cores, exact 3-term split of W_r); MXFP4 layers
   //    first convert x to f16 for the routed gate/up rows.
   prof_mark(L, s);
-  if (mx) {
+  if (mx || i4) {
     const size_t n8 = (size_t)T * H / 8;
     int grid = (int)((n8 + 255) / 256);
     if (grid > 4 * L->num_sms) grid = 4 * L->num_sms;
@@ -940,7 +1002,7 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
     p.n_shared_mtiles = 0; p.nt_shared = 1; p.ks_shared = 0;
     p.logits = g.logits; p.router_bias = L->router_bias; p.logit_bias = logit_bias;
     const int tiles = mt_tokens * p.nt_routed;
-    e = launch_pdl(grouped_gemm_kernel<EPI_ROUTER, false, false>, tiles < L->num_sms ? tiles : L->num_sms, 192,
+    e = launch_pdl(grouped_gemm_kernel<EPI_ROUTER, false, B_BF16>, tiles < L->num_sms ? tiles : L->num_sms, 192,
                    kGemmSmem, s, map_x, map_x, m->router_split, m->router_split, p);
     if (e != cudaSuccess) return e;
   }
@@ -966,11 +1028,15 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
     p.x = x; p.perm = g.perm; p.b_rows_per_expert = 2 * I;
     p.out_routed = g.h; p.ld_routed = I; p.out_shared = g.hs; p.ld_shared = Is;
     if (mx) {
-      p.x16 = g.x16; p.mx_sc = g.mx_gu_sc; p.mx_sref = g.mx_gu_sref;
-      e = launch_pdl(grouped_gemm_kernel<EPI_SWIGLU, true, true>, L->num_sms, 320 + kConvThreads, kGemmSmemMx, s,
+      p.x16 = g.x16; p.q_par = g.mx_gu_sc; p.mx_sref = g.mx_gu_sref;
+      e = launch_pdl(grouped_gemm_kernel<EPI_SWIGLU, true, B_MXFP4>, L->num_sms, 320 + kConvThreads, kGemmSmemMx, s,
+                     map_x, map_x, m->w_gu, m->ws_gu, p);
+    } else if (i4) {
+      p.x16 = g.x16; p.q_par = g.i4_gu_par;
+      e = launch_pdl(grouped_gemm_kernel<EPI_SWIGLU, true, B_INT4>, L->num_sms, 320 + kConvThreads, kGemmSmemMx, s,
                      map_x, map_x, m->w_gu, m->ws_gu, p);
     } else {
-      e = launch_pdl(grouped_gemm_kernel<EPI_SWIGLU, true, false>, L->num_sms, 320, kGemmSmem, s, map_x, map_x,
+      e = launch_pdl(grouped_gemm_kernel<EPI_SWIGLU, true, B_BF16>, L->num_sms, 320, kGemmSmem, s, map_x, map_x,
                      m->w_gu, m->ws_gu, p);
     }
     if (e != cudaSuccess) return e;
@@ -986,11 +1052,15 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
     p.b_rows_per_expert = H;
     p.out_routed = g.y; p.ld_routed = H; p.out_shared = g.ys; p.ld_shared = H;
     if (mx) {
-      p.mx_sc = g.mx_dn_sc; p.mx_sref = g.mx_dn_sref;
-      e = launch_pdl(grouped_gemm_kernel<EPI_STORE, false, true>, L->num_sms, 192 + kConvThreads, kGemmSmemMx, s, m->h,
-                     m->hs, m->w_down, m->ws_down, p);
+      p.q_par = g.mx_dn_sc; p.mx_sref = g.mx_dn_sref;
+      e = launch_pdl(grouped_gemm_kernel<EPI_STORE, false, B_MXFP4>, L->num_sms, 192 + kConvThreads, kGemmSmemMx, s,
+                     m->h, m->hs, m->w_down, m->ws_down, p);
+    } else if (i4) {
+      p.q_par = g.i4_dn_par;
+      e = launch_pdl(grouped_gemm_kernel<EPI_STORE, false, B_INT4>, L->num_sms, 192 + kConvThreads, kGemmSmemMx, s,
+                     m->h, m->hs, m->w_down, m->ws_down, p);
     } else {
-      e = launch_pdl(grouped_gemm_kernel<EPI_STORE, false, false>, L->num_sms, 192, kGemmSmem, s, m->h, m->hs,
+      e = launch_pdl(grouped_gemm_kernel<EPI_STORE, false, B_BF16>, L->num_sms, 192, kGemmSmem, s, m->h, m->hs,
                      m->w_down, m->ws_down, p);
     }
     if (e != cudaSuccess) return e;

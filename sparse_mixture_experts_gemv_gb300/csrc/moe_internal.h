@@ -62,6 +62,9 @@ struct GroupedWorkspace {
   uint16_t* mx_dn_sc;    // down scale pairs [E][I / 64][H]
   uint8_t* mx_gu_sref;   // largest scale byte of each gate/up row [E][2I]
   uint8_t* mx_dn_sref;   // largest scale byte of each down row [E][H]
+  // int4 layers: (scale, bias) bf16 pairs per stage [E][K / 64][rows] (uint32 each)
+  uint32_t* i4_gu_par;   // [E][H / 64][2I]
+  uint32_t* i4_dn_par;   // [E][I / 64][H]
 };
 
 }  // namespace moe

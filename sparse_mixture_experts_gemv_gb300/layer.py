@@ -28,6 +28,8 @@ class MoeLayer:
       bf16 format:  gate [E,I,H] u16, up [E,I,H] u16, down [E,H,I] u16 (bf16 bits)
       mxfp4 format: gate_codes [E,I,H/2] u8, gate_scales [E,I,H/32] u8, up_codes, up_scales,
                     down_codes [E,H,I/2] u8, down_scales [E,H,I/32] u8
+      int4 format:  gate_codes [E,I,H/2] u8, gate_scales / gate_biases [E,I,H/64] (bf16 bits),
+                    the same for up, down_codes [E,H,I/2] u8, down_scales / down_biases [E,H,I/64]
       shared_gate [Is,H], shared_up [Is,H], shared_down [H,Is] (bf16 bits)
     """
 
@@ -37,8 +39,8 @@ class MoeLayer:
         self.fmt = fmt
         self.max_tokens = max_tokens
         self.device = torch.device(device)
-        cfg = N.moe_layer_config_t(H, E, k, I, Is, max_tokens,
-                                   N.MOE_WEIGHTS_MXFP4 if fmt == "mxfp4" else N.MOE_WEIGHTS_BF16, flags)
+        code = {"bf16": N.MOE_WEIGHTS_BF16, "mxfp4": N.MOE_WEIGHTS_MXFP4, "int4": N.MOE_WEIGHTS_INT4}[fmt]
+        cfg = N.moe_layer_config_t(H, E, k, I, Is, max_tokens, code, flags)
         keep = {}
 
         def up(name):
@@ -51,10 +53,13 @@ class MoeLayer:
         w = N.moe_layer_weights_t()
         w.router_dev = up("router")
         w.router_bias_dev = up("router_bias")
-        if fmt == "mxfp4":
+        if fmt in ("mxfp4", "int4"):
             w.gate_dev, w.up_dev, w.down_dev = up("gate_codes"), up("up_codes"), up("down_codes")
             w.gate_scales_dev, w.up_scales_dev = up("gate_scales"), up("up_scales")
             w.down_scales_dev = up("down_scales")
+            if fmt == "int4":
+                w.gate_biases_dev, w.up_biases_dev = up("gate_biases"), up("up_biases")
+                w.down_biases_dev = up("down_biases")
         else:
             w.gate_dev, w.up_dev, w.down_dev = up("gate"), up("up"), up("down")
         w.shared_gate_dev, w.shared_up_dev = up("shared_gate"), up("shared_up")

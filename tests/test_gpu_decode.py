@@ -247,3 +247,28 @@ def test_describe_names_the_active_path():
     assert "decode GEMV path" in d and "moe_decode_stream_kernel" in d
     S = mi.custom_layer(H=512, E=16, k=4, I=256, Is=128, fmt="mxfp4", seed=5)
     assert "moe_decode_stream_mx_kernel" in G.cuda_layer(S.spec, max_tokens=8).describe()
+
+
+# ---------------------------------------------------------------- int4 routed experts
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8])
+def test_small_int4_every_window_size(T):
+    """Groupwise affine int4 routed experts on the three-phase decode kernel
+    (per group s * sum(q x) + b * sum(x)), against the oracle."""
+    S = mi.custom_layer(H=512, E=16, k=4, I=256, Is=128, fmt="int4", seed=5)
+    L = G.cuda_layer(S.spec, max_tokens=64)
+    x = mi.tokens(S.spec, T, stream=7000 + T)
+    out, idx, wt = G.run_cuda(L, x)
+    assert L.stats().path == 1
+    G.compare(G.synth(S.spec), x, out, idx, wt)
+    assert "int4" in L.describe()
+
+
+def test_qwen_int4_decode():
+    w = mi.WORKLOADS["qwen_int4_decode"]
+    L = G.cuda_layer(w.layer, max_tokens=8)
+    S = G.synth(w.layer)
+    for call in range(3):
+        x = mi.workload_tokens(w, call)
+        out, idx, wt = G.run_cuda(L, x)
+        r = G.compare(S, x, out, idx, wt)
+    print("qwen int4 decode", r)

@@ -176,3 +176,45 @@ def test_ling_mxfp4_prefill_sampled_rows():
     ref = o.moe_forward(S, x[rows])
     r = G.compare(S, x[rows], out[rows], idx[rows], wt[rows], fmt="mxfp4", ref=ref)
     print("ling mxfp4 prefill sampled rows", r, "touched", st.distinct_experts)
+
+
+# ---------------------------------------------------------------- int4 routed experts
+@pytest.mark.parametrize("T", [9, 100, 300])
+def test_small_int4_grouped(T):
+    """int4 routed experts decoded to f16 (one rounding of q * s + b) inside the
+    grouped tcgen05 GEMMs, against the oracle."""
+    spec = mi.custom_layer(H=512, E=16, k=4, I=256, Is=128, fmt="int4", seed=5).spec
+    L = G.cuda_layer(spec, max_tokens=512, flags=FORCE)
+    x = mi.tokens(spec, T, stream=8000 + T)
+    out, idx, wt = G.run_cuda(L, x)
+    assert L.stats().path == 2
+    G.compare(G.synth(spec), x, out, idx, wt)
+    _check_dispatch(L, T, spec.k, spec.E, idx)
+
+
+def test_int4_grouped_deterministic_and_matches_decode():
+    spec = mi.custom_layer(H=512, E=16, k=4, I=256, Is=128, fmt="int4", seed=5).spec
+    Lg = G.cuda_layer(spec, max_tokens=512, flags=FORCE)
+    x = mi.tokens(spec, 300, stream=99)
+    a = G.run_cuda(Lg, x)[0]
+    b = G.run_cuda(Lg, x)[0]
+    assert (a == b).all()
+    Ld = G.cuda_layer(spec, max_tokens=64)
+    xs = x[:6]
+    d, i_d, _ = G.run_cuda(Ld, xs)
+    g, i_g, _ = G.run_cuda(Lg, xs)
+    assert (i_d == i_g).all()
+    assert np.abs(G.bits_to_f64(d) - G.bits_to_f64(g)).max() <= 2 * G.BF16_MAX_ABS
+
+
+def test_qwen_int4_prefill_sampled_rows():
+    w = mi.WORKLOADS["qwen_int4_prefill"]
+    L = G.cuda_layer(w.layer, max_tokens=4096)
+    S = G.synth(w.layer)
+    x = mi.workload_tokens(w, 0)
+    out, idx, wt = G.run_cuda(L, x)
+    assert L.stats().path == 2
+    _check_dispatch(L, 4096, 8, 256, idx)
+    rows = np.sort(np.random.default_rng(2).choice(4096, size=128, replace=False))
+    r = G.compare(S, x[rows], out[rows], idx[rows], wt[rows], ref=o.moe_forward(S, x[rows]))
+    print("qwen int4 prefill sampled rows", r)
