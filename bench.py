@@ -4,8 +4,10 @@ Headline: Qwen-shaped decode layer (H=2048, E=256 routed experts, top-8,
 SwiGLU intermediate 512, one shared expert, bf16 experts, fp32 router), T=1:
 microseconds per layer call, over 64 different seeded tokens per step, with
 the L2 cache flushed (a 256 MiB write) before every call, outside the timed
-events. The same line also reports the verify window (T=4), the MXFP4 Ling
-layer (T=1, T=4) and the prefill chunk (T=4096) as secondary workloads.
+events. The same line also reports, as secondary workloads: the verify window (T=4),
+a decode T-sweep 1..8, the MXFP4 Ling layer (T=1, T=4), int4 routed experts
+(T=1), the online-FP8 LM head (T=1, 4) and the prefill chunks (T=4096: bf16,
+int4 and MXFP4 routed experts).
 
   python bench.py [--steps K] [--warmup W] [--impl ours|reference] [--quick]
 
@@ -239,6 +241,18 @@ def decode_workload(B: Bench, wname: str, steps: int, warmup: int, peaks, profil
     return res
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of a list of floats over all ranks (the slowest replica
+    sets the job's time); the identity when no process group is running."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
 def run_ours(args):
     import torch
     peaks = _peaks()
@@ -279,10 +293,7 @@ def run_ours(args):
         torch.distributed.barrier()
     us = float(np.mean(times) * 1e3)
     step_ms = float(np.sum(times) / args.steps)
-    if world > 1:
-        t = torch.tensor([us, step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        us, step_ms = float(t[0]), float(t[1])
+    us, step_ms = max_over_ranks([us, step_ms], dev)
     alg_bytes = float(np.mean([s.algorithmic_bytes for s in stats]))
     distinct = float(np.mean([s.distinct_experts for s in stats]))
 
