@@ -445,6 +445,7 @@ def prefill_workload(B: Bench, wname: str, steps: int, warmup: int, peaks):
     out = torch.empty_like(x)
     L.forward(x, out)
     st = L.stats()
+    hist = L.dispatch(w.T)[0].cpu().numpy()          # rows routed to each expert by this chunk
     for _ in range(warmup):
         L.forward(x, out)
     times = []
@@ -462,6 +463,9 @@ def prefill_workload(B: Bench, wname: str, steps: int, warmup: int, peaks):
             "mma": ("routed f16 x f16 (MXFP4 rows decoded in the GEMM), shared bf16 x bf16"
                     if w.layer.fmt == "mxfp4" else "bf16 x bf16"),
             "touched_experts": st.distinct_experts, "max_expert_rows": st.max_expert_rows,
+            "expert_rows_summary": {"min": int(hist.min()), "median": float(np.median(hist)), "max": int(hist.max()),
+                                    "mean": float(hist.mean()), "experts_over_128_rows": int((hist > 128).sum())},
+            "expert_rows_histogram": [int(v) for v in hist],
             "algorithmic_bytes": st.algorithmic_bytes,
             "hbm_frac": st.algorithmic_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "stage_us": {n: round(float(v), 2) for n, v in zip(names, st_us)}}
