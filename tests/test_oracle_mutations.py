@@ -127,6 +127,7 @@ PIN_TESTS = [
     lambda: pins.test_dispatch_invariants_and_brute_force(),
     lambda: pins.test_int4_affine_decode_all_bytes(),
     lambda: pins.test_int4_scale_and_bias_apply_per_64_group(),
+    lambda: pins.test_worked_example_int4(),
 ]
 
 

@@ -367,3 +367,33 @@ def test_synthetic_layer_shapes():
     assert rm["gate_scales"].min() == 119 and rm["gate_scales"].max() == 123
     zb = mi.SynthLayer(mi.WORKLOADS["qwen_prefill"].layer).router_bias()
     assert zb.shape == (256,) and abs(float(zb.mean())) < 1e-5
+
+
+def test_worked_example_int4():
+    ex = {e["name"]: e for e in json.load(open(os.path.join(GOLDEN, "worked_examples.json")))["examples"]}["int4_single_expert"]
+    H, I = ex["H"], ex["I"]
+    spec = Spec(H=H, E=1, k=1, I=I, Is=1, fmt="int4")
+
+    def mat(rows, K, entries):
+        c = np.zeros((rows, K // 2), np.uint8)
+        s = np.zeros((rows, K // 64), np.uint16)
+        b = np.zeros((rows, K // 64), np.uint16)
+        for r, e in entries:
+            c[r, 0], s[r, 0], b[r, 0] = e["byte0"], e["scale_bf16"], e["bias_bf16"]
+        return c, s, b
+
+    gc, gs, gb = mat(I, H, [(0, ex["gate_row0"])])
+    uc, us, ub = mat(I, H, [(0, ex["up_row0"])])
+    dc, ds, db = mat(H, I, [(0, ex["down_row0"]), (1, ex["down_row1"])])
+    expert = {"gate_codes": gc, "gate_scales": gs, "gate_biases": gb, "up_codes": uc, "up_scales": us,
+              "up_biases": ub, "down_codes": dc, "down_scales": ds, "down_biases": db}
+    zero = {"gate": bf16(np.zeros((1, H))), "up": bf16(np.zeros((1, H))), "down": bf16(np.zeros((H, 1)))}
+    layer = ArrayLayer(spec, np.zeros((H, 1)), [expert], zero)
+    x = np.zeros((1, H))
+    for i, v in ex["x_nonzero"].items():
+        x[0, int(i)] = v
+    r = o.moe_forward(layer, bf16(x))
+    want = np.zeros((1, H))
+    for i, s in ex["out_nonzero"].items():
+        want[0, int(i)] = _expr(s)
+    np.testing.assert_allclose(r["out"], want, rtol=1e-14, atol=1e-15)
