@@ -38,3 +38,34 @@ def test_create_rejects_bad_config_before_touching_the_device():
     cfg = N.moe_layer_config_t(256, 16, 2, 128, 128, 8, 7, 0)  # unknown format
     st, h = N.moe_layer_create_status(cfg, N.moe_layer_weights_t())
     assert st == N.MOE_ERR_INVALID_ARG
+
+
+def test_header_is_plain_c99(tmp_path):
+    """include/moe_layer.h compiles as C99 with warnings as errors (a C caller needs
+    no C++ or CUDA headers), and a C program links against libmoe.so."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        import pytest
+        pytest.skip("gcc not available")
+    src = tmp_path / "use_header.c"
+    src.write_text(
+        '#include "moe_layer.h"\n'
+        "int main(void) {\n"
+        "  moe_layer_config_t c = {0};\n"
+        "  moe_layer_t* L = 0;\n"
+        "  (void)c;\n"
+        "  if (moe_layer_create(0, 0, &L) != MOE_ERR_INVALID_ARG) return 1;\n"
+        "  return moe_status_string(MOE_OK)[0] == 'M' ? 0 : 2;\n"
+        "}\n")
+    inc = os.path.join(ROOT, "include")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, "-fsyntax-only",
+                        str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    from sparse_mixture_experts_gemv_gb300 import build as b
+    lib = b.build()
+    exe = tmp_path / "use_header"
+    r = subprocess.run([gcc, "-std=c99", "-I", inc, str(src), "-o", str(exe), lib,
+                        "-Wl,-rpath," + os.path.dirname(lib)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
