@@ -69,3 +69,30 @@ def test_header_is_plain_c99(tmp_path):
     r = subprocess.run([gcc, "-std=c99", "-I", inc, str(src), "-o", str(exe), lib,
                         "-Wl,-rpath," + os.path.dirname(lib)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_new_entry_points_reject_bad_arguments_before_touching_the_device():
+    import ctypes
+    from sparse_mixture_experts_gemv_gb300 import _native as N
+    fake = 0x10000   # never dereferenced: every case below fails validation first
+    # chunked forward without a layer
+    assert N.moe_layer_forward_chunked(None, fake, fake, 10, 0, None, 0) == N.MOE_ERR_INVALID_ARG
+    # LM head: hidden not a multiple of 256, empty vocabulary, missing or misaligned weights
+    assert N.moe_lmhead_create(250, 10, fake)[0] == N.MOE_ERR_UNSUPPORTED
+    assert N.moe_lmhead_create(256 * 33, 10, fake)[0] == N.MOE_ERR_UNSUPPORTED   # above the hidden limit
+    assert N.moe_lmhead_create(256, 0, fake)[0] == N.MOE_ERR_INVALID_ARG
+    assert N.moe_lmhead_create(256, 10, 0)[0] == N.MOE_ERR_INVALID_ARG
+    assert N.moe_lmhead_create(256, 10, fake + 2)[0] == N.MOE_ERR_INVALID_ARG
+    assert N.moe_lmhead_forward(None, fake, fake, 1, 0) == N.MOE_ERR_INVALID_ARG
+    assert N.moe_lmhead_get_weights(None, None, None, 0) == N.MOE_ERR_INVALID_ARG
+    N.moe_lmhead_destroy(None)
+    # int4 layers need scales and biases
+    cfg = N.moe_layer_config_t(256, 16, 2, 128, 128, 8, N.MOE_WEIGHTS_INT4, 0)
+    w = N.moe_layer_weights_t()
+    for f in ("router_dev", "gate_dev", "up_dev", "down_dev", "gate_scales_dev", "up_scales_dev",
+              "down_scales_dev", "shared_gate_dev", "shared_up_dev", "shared_down_dev"):
+        setattr(w, f, fake)
+    st, h = N.moe_layer_create_status(cfg, w)
+    assert st == N.MOE_ERR_INVALID_ARG and h is None
+    cfg3 = N.moe_layer_config_t(256, 16, 2, 128, 128, 8, 3, 0)   # no format 3
+    assert N.moe_layer_create_status(cfg3, w)[0] == N.MOE_ERR_INVALID_ARG
