@@ -29,6 +29,10 @@
 // Latency, not arithmetic, sets the time of a batch-1 layer: warps issue their
 // weight loads in batches of 16 x 16 bytes per lane before using any of them,
 // and kernel boundaries are replaced by the two in-kernel synchronisations.
+// The kernel is templated on the routed weight format: bf16, MXFP4 (e2m1 codes
+// with e8m0 scales per 32) and groupwise affine int4 (q * s + b per 64, summed
+// as s * sum(q x) + b * sum(x)). The record-streaming kernels serve bf16 and
+// MXFP4 layers within their limits; this one serves the rest.
 #include <cuda_runtime.h>
 #include <stdint.h>
 

@@ -25,11 +25,20 @@
 //                         SwiGLU in the epilogue, bf16 h in grouped order.
 //   grouped_gemm<STORE>   down projection of every group (TMA A = h), bf16 y.
 //   combine               out[t] = sum_j w[t,j] y[pos[t,j]] + y_shared[t].
+// A chunked forward (moe_layer_forward_chunked) repeats this chain per chunk.
 //
 // The grouped GEMM is a persistent, warp-specialised tcgen05 kernel: warp 0
 // issues TMA loads, warp 1 owns tensor memory and issues the MMAs, warps 2-5
 // drain the double-buffered TMEM accumulators; for gathered A, warps 6-9 copy
 // the token rows with cp.async into the 128-byte-swizzled layout.
+//
+// 4-bit routed experts ("Optimizing on-device inference for Apple Silicon",
+// section "Decode weights during matrix multiplication"; "Three ways to speed up
+// MoE inference on DGX Spark", section "Optimization 1"): for MXFP4 and
+// groupwise affine int4 layers, eight more converter warps turn each stage's
+// 4-bit rows (copied into a raw ring) into the f16 B tile in shared memory, and
+// the routed MMAs are f16 x f16 (x and the SwiGLU outputs in f16); x is
+// converted once per call by bf16_to_f16 before the router.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
