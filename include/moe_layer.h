@@ -50,7 +50,9 @@ typedef enum {
   MOE_ERR_OOM = 3,           /* device allocation failed; nothing is left allocated        */
   MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed; see moe_last_cuda_error()      */
   MOE_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out; outputs are undefined  */
-  MOE_ERR_DEVICE_CHECK = 6   /* a device-side index check failed; outputs are undefined    */
+  MOE_ERR_DEVICE_CHECK = 6   /* a device-side check failed: an index out of range, or (MXFP4
+                                and int4 layers) an activation beyond the f16 range of their
+                                f16 operands; outputs are undefined                        */
 } moe_status_t;
 
 typedef enum {
@@ -87,7 +89,10 @@ typedef enum {
    formats: MXFP4 routed rows are decoded inside the tensor-core GEMMs to f16 (e2m1
    times 2^(scale - the row's largest scale), exact for blocks within 2^23 of the
    row's largest), with x and the routed SwiGLU outputs in f16 there (exact for
-   |x| in [2^-14, 65504]; larger magnitudes overflow to infinity). */
+   |x| in [2^-14, 65504]). A finite x or routed SwiGLU output above 65504 in
+   magnitude would not fit those f16 operands: the call then reports
+   MOE_ERR_DEVICE_CHECK (through moe_layer_sync_status) instead of returning
+   infinities. The same holds for the f16 x of the MXFP4 and int4 decode kernels. */
 #define MOE_DECODE_MAX_T 8
 
 typedef struct {
@@ -176,7 +181,10 @@ void moe_layer_destroy(moe_layer_t* layer);
  * of routing decisions. The workspace is owned by the layer, so calls on one layer
  * must be ordered (same stream, or ordered by events). A device-side error from
  * an earlier call (MOE_ERR_TIMEOUT / MOE_ERR_DEVICE_CHECK) is returned by
- * moe_layer_sync_status.
+ * moe_layer_sync_status. After such an error the outputs of every later call are
+ * undefined until moe_layer_sync_status has been called: the weight-streaming
+ * kernels then return at once instead of computing (and instead of waiting out
+ * their time limits on counters the failed call left mid-generation).
  */
 moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x_dev, void* out_dev, int32_t T,
                                void* stream);
@@ -243,6 +251,24 @@ moe_status_t moe_layer_get_dispatch(moe_layer_t* layer, int32_t* hist_dev, int32
                                     int32_t* perm_dev, int32_t* pos_dev, void* stream);
 
 /*
+ * Copy the block map of the last grouped-path forward (MOE_ERR_INVALID_ARG after a
+ * decode-path forward): the list of 128-row blocks of grouped routed rows that the
+ * grouped GEMMs take as their M tiles ("Optimizing on-device inference for Apple
+ * Silicon", section "Keep expert routing on the GPU": the dispatch writes the block
+ * list on the GPU). Block b covers grouped rows [row0, min(row0 + 128, offsets[e+1]))
+ * of expert e; blocks are in increasing expert order, then increasing row0.
+ *   blocks_dev      int32 [max_blocks][2] device: (e, row0) of each block; the first
+ *                   min(max_blocks, capacity) entries are copied, where capacity is
+ *                   ceil(max_tokens * k / 128) + E + 1; entries at or after the
+ *                   block count are unspecified
+ *   num_blocks_dev  int32 [1] device: the block count written by the dispatch
+ * Either pointer may be NULL. max_blocks < 0 is MOE_ERR_INVALID_ARG. Enqueued on
+ * `stream`.
+ */
+moe_status_t moe_layer_get_block_map(moe_layer_t* layer, int32_t* blocks_dev, int32_t max_blocks,
+                                     int32_t* num_blocks_dev, void* stream);
+
+/*
  * Synchronise `stream`, then read and clear the device error word: MOE_OK,
  * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK (or MOE_ERR_CUDA if the stream itself
  * failed).
@@ -272,8 +298,9 @@ moe_status_t moe_layer_profile_read(moe_layer_t* layer, float* stage_ms, int32_t
 /*
  * Routing without any device allocation (no counterpart on the pages; this is
  * an entry point of this library for callers that cannot call cudaMalloc, for
- * example code running while a CUDA graph is captured, or a host framework
- * that owns all device memory through its own pool).
+ * example a host framework that owns all device memory through its own pool and
+ * forbids raw allocations, or a real-time caller that must not allocate once it
+ * is running).
  *
  * Computes, for T tokens, the fp32 router logits x . W_r (+ router_bias[e])
  * (+ logit_bias[t][e]), the top-k experts (descending, exact ties to the lower
@@ -291,8 +318,9 @@ moe_status_t moe_layer_profile_read(moe_layer_t* layer, float* stage_ms, int32_t
  * before reading it, so nothing needs clearing, but all calls share the array:
  * calls that overlap on the GPU (unordered streams, or several host threads)
  * race. The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
- * Enqueued on `stream`; no host synchronisation.
+ * (cudaGetSymbolAddress); make that first call before any stream capture. The
+ * address is kept per device and per CUDA context: after a device reset the next
+ * call looks it up again. Enqueued on `stream`; no host synchronisation.
  */
 #define MOE_NOALLOC_MAX_TOKENS 8
 #define MOE_NOALLOC_MAX_EXPERTS 512

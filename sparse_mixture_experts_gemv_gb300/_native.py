@@ -80,6 +80,8 @@ _SIGNATURES = {
     "moe_layer_get_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(moe_stats_t)]),
     "moe_layer_get_routing": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "moe_layer_get_dispatch": (ctypes.c_int, [ctypes.c_void_p] + [ctypes.c_void_p] * 4 + [ctypes.c_void_p]),
+    "moe_layer_get_block_map": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                               ctypes.c_void_p]),
     "moe_layer_sync_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "moe_layer_describe": (ctypes.c_char_p, [ctypes.c_void_p]),
     "moe_layer_profile_enable": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
@@ -181,6 +183,10 @@ def moe_layer_get_routing(layer: int, idx_dev, w_dev, stream: int = 0) -> int:
 
 def moe_layer_get_dispatch(layer: int, hist_dev, offsets_dev, perm_dev, pos_dev, stream: int = 0) -> int:
     return load().moe_layer_get_dispatch(layer, hist_dev, offsets_dev, perm_dev, pos_dev, stream)
+
+
+def moe_layer_get_block_map(layer: int, blocks_dev, max_blocks: int, num_blocks_dev, stream: int = 0) -> int:
+    return load().moe_layer_get_block_map(layer, blocks_dev, max_blocks, num_blocks_dev, stream)
 
 
 def moe_layer_sync_status(layer: int, stream: int = 0) -> int:

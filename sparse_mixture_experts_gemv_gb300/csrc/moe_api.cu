@@ -587,6 +587,16 @@ moe_status_t moe_layer_get_dispatch(moe_layer_t* L, int32_t* hist, int32_t* offs
   return MOE_OK;
 }
 
+moe_status_t moe_layer_get_block_map(moe_layer_t* L, int32_t* blocks, int32_t max_blocks, int32_t* num_blocks,
+                                     void* stream) {
+  if (!L || L->last_path != MOE_PATH_GROUPED || max_blocks < 0) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t n = (size_t)std::min(max_blocks, L->grp.max_tiles);
+  if (blocks && n) MOE_CUDA(cudaMemcpyAsync(blocks, L->grp.tiles, n * 2 * sizeof(int), cudaMemcpyDeviceToDevice, s));
+  if (num_blocks) MOE_CUDA(cudaMemcpyAsync(num_blocks, L->grp.num_tiles, sizeof(int), cudaMemcpyDeviceToDevice, s));
+  return MOE_OK;
+}
+
 moe_status_t moe_layer_get_stats(moe_layer_t* L, void* stream, moe_stats_t* st) {
   if (!L || !st) return MOE_ERR_INVALID_ARG;
   memset(st, 0, sizeof(*st));

@@ -128,6 +128,18 @@ class MoeLayer:
             raise N.MoeError(st, "moe_layer_get_dispatch")
         return hist, offs, perm, pos
 
+    def block_map(self, T: int, stream=None):
+        """(blocks int32 [n, 2] of (expert, first grouped row), n) of the last grouped forward."""
+        cap = (self.max_tokens * self.k + 127) // 128 + self.E + 1
+        blocks = torch.full((cap, 2), -1, dtype=torch.int32, device=self.device)
+        n = torch.zeros(1, dtype=torch.int32, device=self.device)
+        s = (stream or torch.cuda.current_stream(self.device)).cuda_stream
+        st = N.moe_layer_get_block_map(self.handle, blocks.data_ptr(), cap, n.data_ptr(), s)
+        if st != N.MOE_OK:
+            raise N.MoeError(st, "moe_layer_get_block_map")
+        nb = int(n.item())
+        return blocks[:nb], nb
+
     def stats(self, stream=None) -> N.moe_stats_t:
         s = (stream or torch.cuda.current_stream(self.device)).cuda_stream
         return N.moe_layer_get_stats(self.handle, s)

@@ -21,6 +21,10 @@ def _check_dispatch(L, T, k, E, idx):
     assert (offs == ref["offsets"]).all()
     assert (perm == ref["perm"]).all()           # bit-exact: token order within each expert
     assert (pos == ref["pos"].reshape(-1)).all()
+    # the block map the grouped GEMMs take as M tiles: (expert, first grouped row), bit-exact
+    blocks, nb = L.block_map(T)
+    assert nb == len(ref["blocks"]), (nb, len(ref["blocks"]))
+    assert (blocks.cpu().numpy().astype(np.int64) == ref["blocks"]).all()
 
 
 def test_tiny_forced_grouped_t8():
@@ -34,7 +38,7 @@ def test_tiny_forced_grouped_t8():
     _check_dispatch(L, 8, 2, 16, idx)
 
 
-@pytest.mark.parametrize("T", [1, 9, 100, 129, 300, 512])
+@pytest.mark.parametrize("T", [1, 9, 100, 127, 128, 129, 300, 512])
 def test_tiny_grouped_ragged(T):
     spec = mi.WORKLOADS["tiny"].layer
     L = G.cuda_layer(spec, max_tokens=512, flags=FORCE)
