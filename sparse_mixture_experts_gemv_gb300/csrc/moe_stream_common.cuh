@@ -366,7 +366,11 @@ MOE_DEV bool poll_topk(const unsigned long long* words, int E, int k, unsigned l
 // Consumer warps: this CTA's router logits (rows b, b + G, ... of the fp32
 // router, at most kMaxRouterRows), split into parts over the 16 warps, summed
 // in warp order, plus the router bias and the optional per-token logit bias,
-// published as tagged words [t][E]. The row loads are issued before waiting
+// published as tagged words [t][E]. The number of parts P follows from the
+// largest row count of any CTA, not from this CTA's own, so that every logit
+// of the layer is the same sequence of fp32 operations: two experts with equal
+// router columns get bitwise equal logits, and the exact-tie rule (lower index
+// first) then decides between them. The row loads are issued before waiting
 // for x (x_bar). Every consumer thread has waited on x_bar when this returns.
 template <int TMAX>
 MOE_DEV void router_publish(const uint16_t* xs, int XP, int T, int H, int E, const float* router_t,
@@ -376,9 +380,18 @@ MOE_DEV void router_publish(const uint16_t* xs, int XP, int T, int H, int E, con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, b = blockIdx.x;
   const int nr_rows = (E - b + G - 1) / G;
-  const int P = max(1, kConsumerWarps / max(nr_rows, 1));     // warps per row
+  const int P = max(1, kConsumerWarps / ((E + G - 1) / G));   // warps per row, the same in every CTA
   const int items = nr_rows * P;
   const int H4 = H / 4;
+  // the bias terms are loaded now, so that they do not add a memory round trip
+  // after the dot products
+  float rbias = 0.f, lbias = 0.f;
+  if ((int)threadIdx.x < nr_rows * T) {
+    const int m = threadIdx.x / T, t = threadIdx.x - m * T;
+    const int e = b + m * G;
+    rbias = router_bias[e];
+    if (logit_bias) lbias = logit_bias[(size_t)t * E + e];
+  }
   bool x_ready = false;
   if (warp < items) {
     const int m = warp / P, p = warp - m * P;
@@ -436,8 +449,8 @@ MOE_DEV void router_publish(const uint16_t* xs, int XP, int T, int H, int E, con
     const int e = b + m * G;
     float sl = 0.f;
     for (int p = 0; p < P; ++p) sl += s_rpart[m * P + p][t];
-    sl += router_bias[e];
-    if (logit_bias) sl += logit_bias[(size_t)t * E + e];
+    sl += rbias;
+    if (logit_bias) sl += lbias;
     st_relaxed_u64(words + (size_t)t * E + e, tagged(tag, sl));
   }
 }
