@@ -70,6 +70,11 @@ MOE_DEV float fma2_f16(uint32_t w, uint32_t x, float acc) {
   return acc;
 }
 
+// True when a finite fp32 value lies outside the f16 range (its f16 rounding
+// would be infinite). Infinite or NaN inputs are not flagged: they propagate as
+// they would through fp32 arithmetic.
+MOE_DEV bool f16_overflows(float v) { return fabsf(v) > 65504.0f && fabsf(v) < __int_as_float(0x7F800000); }
+
 // e8m0 scale byte -> 2^(s - 127) as fp32 (s = 255, NaN, is never stored).
 MOE_DEV float e8m0_to_f32(uint32_t s) { return __uint_as_float(s ? (s << 23) : 0x00400000u); }
 

@@ -299,6 +299,11 @@ template <int TMAX, class Fmt>
 __global__ void __launch_bounds__(kGemvThreads, 1)
 moe_decode_fused_kernel(const FusedArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // An error word left set by an earlier call means the layer's cross-CTA
+  // counters and tagged words may be mid-generation: do nothing (outputs stay
+  // undefined) until moe_layer_sync_status has read and cleared it. Every CTA
+  // reads the same value: it was written before this launch began.
+  if (*reinterpret_cast<const volatile int*>(a.err) != 0) return;
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);   // phases 1-2: x [T][H] bf16
   uint8_t* s_shrows = smem + a.smem_r1;               // shared-expert down rows [n0, n1) x Is bf16
   uint8_t* s_rows = s_shrows + a.smem_sh;             // routed down rows, slot d at d * slot_stride
@@ -375,11 +380,14 @@ moe_decode_fused_kernel(const FusedArgs a) {
       if (kMx || kI4) {  // exact for |x| >= 2^-14 (bf16 has fewer significand bits than f16)
         const uint32_t w4[4] = {v8.x, v8.y, v8.z, v8.w};
         uint32_t h4[4];
+        bool x_range = false;   // |x| above the f16 range: reported, never rounded to infinity silently
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
+          x_range |= f16_overflows(bf16_lo(w4[q])) || f16_overflows(bf16_hi(w4[q]));
           const __half2 hh = __floats2half2_rn(bf16_lo(w4[q]), bf16_hi(w4[q]));
           h4[q] = *reinterpret_cast<const uint32_t*>(&hh);
         }
+        if (x_range) set_error(a.err, kDevCheck);
         reinterpret_cast<uint4*>(xs16)[i] = make_uint4(h4[0], h4[1], h4[2], h4[3]);
       }
     }
@@ -649,10 +657,13 @@ moe_decode_fused_kernel(const FusedArgs a) {
   float* s_part = reinterpret_cast<float*>(s_rows + (size_t)a.slots_cap * a.slot_stride);  // [nw][rows_max][T]
   {
     const int n4 = T * k * I / 4;
+    bool h_range = false;   // an f16 SwiGLU output above the f16 range: reported, never silently infinite
     for (int q = threadIdx.x; q < n4; q += blockDim.x) {
       const uint4 f = ldg_cg(reinterpret_cast<const uint4*>(a.h) + q);
       uint2 o;
       if (kMx || kI4) {
+        h_range |= f16_overflows(__uint_as_float(f.x)) || f16_overflows(__uint_as_float(f.y)) ||
+                   f16_overflows(__uint_as_float(f.z)) || f16_overflows(__uint_as_float(f.w));
         const __half2 p0 = __floats2half2_rn(__uint_as_float(f.x), __uint_as_float(f.y));
         const __half2 p1 = __floats2half2_rn(__uint_as_float(f.z), __uint_as_float(f.w));
         o.x = *reinterpret_cast<const uint32_t*>(&p0);
@@ -663,6 +674,7 @@ moe_decode_fused_kernel(const FusedArgs a) {
       }
       reinterpret_cast<uint2*>(hs16)[q] = o;
     }
+    if (h_range) set_error(a.err, kDevCheck);
     const int s4 = T * Is / 4;
     for (int q = threadIdx.x; q < s4; q += blockDim.x) {
       const uint4 f = ldg_cg(reinterpret_cast<const uint4*>(a.h_shared) + q);

@@ -382,13 +382,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
         if (EPI == EPI_SWIGLU) {
           // columns alternate gate / up of intermediate features i0 + c0/2 + (0..15)
           uint32_t packed[8];
+          bool h_range = false;   // a routed f16 h above the f16 range: reported, never silently infinite
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float h0 = swiglu(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]));
             const float h1 = swiglu(__uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            if (mxt) h_range |= f16_overflows(h0) || f16_overflows(h1);
             packed[i] = mxt ? f32x2_to_f16x2(h0, h1)   // f16 A of the MXFP4 down GEMM
                             : (uint32_t)f32_to_bf16_rne(h0) | ((uint32_t)f32_to_bf16_rne(h1) << 16);
           }
+          if (h_range) set_error(p.err, kDevCheck);
           uint16_t* dst = ti.shared ? p.out_shared + (size_t)gr * p.ld_shared
                                     : p.out_routed + (size_t)gr * p.ld_routed;
           dst += ti.nt * (p.BN / 2) + c0 / 2;
@@ -751,15 +754,20 @@ combine_kernel(const uint16_t* __restrict__ y, const uint16_t* __restrict__ ys, 
 // x (bf16) -> f16 for the routed rows of MXFP4 layers (8 values a thread-step;
 // exact for |x| in [2^-14, 65504], rounded to nearest even below).
 __global__ void __launch_bounds__(256)
-bf16_to_f16_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y, size_t n8) {
+bf16_to_f16_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ y, size_t n8, int* __restrict__ err) {
   pdl_wait();
   pdl_launch_dependents();
+  bool x_range = false;   // |x| above the f16 range: reported, never rounded to infinity silently
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n8; q += (size_t)gridDim.x * blockDim.x) {
     const uint4 v = reinterpret_cast<const uint4*>(x)[q];
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x_range |= f16_overflows(bf16_lo(w4[i])) || f16_overflows(bf16_hi(w4[i]));
     reinterpret_cast<uint4*>(y)[q] =
         make_uint4(f32x2_to_f16x2(bf16_lo(v.x), bf16_hi(v.x)), f32x2_to_f16x2(bf16_lo(v.y), bf16_hi(v.y)),
                    f32x2_to_f16x2(bf16_lo(v.z), bf16_hi(v.z)), f32x2_to_f16x2(bf16_lo(v.w), bf16_hi(v.w)));
   }
+  if (x_range) set_error(err, kDevCheck);
 }
 
 // Scale tables of an MXFP4 matrix for the grouped GEMMs. Rows are `row_bytes`
@@ -1000,7 +1008,7 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
     const size_t n8 = (size_t)T * H / 8;
     int grid = (int)((n8 + 255) / 256);
     if (grid > 4 * L->num_sms) grid = 4 * L->num_sms;
-    e = launch_pdl(bf16_to_f16_kernel, grid, 256, 0, s, x, g.x16, n8);
+    e = launch_pdl(bf16_to_f16_kernel, grid, 256, 0, s, x, g.x16, n8, L->err);
     if (e != cudaSuccess) return e;
   }
   {

@@ -115,6 +115,11 @@ using stream::cta_ranges;
 template <int TMAX>
 __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(const StreamArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // An error word left set by an earlier call means the layer's cross-CTA
+  // counters and tagged words may be mid-generation: do nothing (outputs stay
+  // undefined) until moe_layer_sync_status has read and cleared it. Every CTA
+  // reads the same value: it was written before this launch began.
+  if (*reinterpret_cast<const volatile int*>(a.err) != 0) return;
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);   // x [T][H + 8] bf16 (row pitch spreads banks)
   uint8_t* ring = smem + a.x_bytes_al;                // ring_groups x group_records records
 

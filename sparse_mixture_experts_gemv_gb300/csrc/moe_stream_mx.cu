@@ -106,6 +106,11 @@ struct MxArgs {
 template <int TMAX, int NT>
 __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kernel(const MxArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // An error word left set by an earlier call means the layer's cross-CTA
+  // counters and tagged words may be mid-generation: do nothing (outputs stay
+  // undefined) until moe_layer_sync_status has read and cleared it. Every CTA
+  // reads the same value: it was written before this launch began.
+  if (*reinterpret_cast<const volatile int*>(a.err) != 0) return;
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                 // x [T][H + 8] bf16
   uint16_t* x16 = reinterpret_cast<uint16_t*>(smem + a.x_bytes_al); // x [T][H + 8] f16
   uint8_t* ring = smem + 2 * a.x_bytes_al;                          // ring_groups x slot_bytes
@@ -214,12 +219,15 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
       set_error(a.err, kDevTimeout);
     stream::router_publish<TMAX>(xs, XP, T, H, E, a.router_t, a.router_bias, a.logit_bias, a.words, tag, &x_bar,
                                  a.err, &s_abort, s_rpart);
+    bool x_range = false;   // an |x| above the f16 range: reported, never rounded to infinity silently
     for (int q = threadIdx.x; q < T * H / 2; q += kConsumers) {   // bf16 pairs -> f16 pairs
       const int t = q / (H / 2), c = q - t * (H / 2);
       const uint32_t v = *reinterpret_cast<const uint32_t*>(xs + t * XP + 2 * c);
+      x_range |= f16_overflows(bf16_lo(v)) || f16_overflows(bf16_hi(v));
       const __half2 h = __floats2half2_rn(bf16_lo(v), bf16_hi(v));
       *reinterpret_cast<__half2*>(x16 + t * XP + 2 * c) = h;
     }
+    if (x_range) set_error(a.err, kDevCheck);
     stream::route_window(a.words, T, E, k, tag, rs, a.err, &s_abort);
   }
   __syncthreads();   // routing and the f16 x known to every warp

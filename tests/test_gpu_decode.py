@@ -231,6 +231,14 @@ def test_forced_device_wait_timeout_reports_status():
     assert "forced wait timeout" in L.describe()
     x = torch.from_numpy(mi.tokens(S.spec, 2, 9).view(np.int16)).cuda()
     L.forward(x)
+    torch.cuda.synchronize()
+    # later calls fail fast: each would otherwise wait ~2 ms on the forced flag again
+    import time
+    t0 = time.perf_counter()
+    for _ in range(8):
+        L.forward(x)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 8e-3
     assert L.sync_status() == N.MOE_ERR_TIMEOUT
     assert L.sync_status() == N.MOE_OK   # cleared
     L.close()
