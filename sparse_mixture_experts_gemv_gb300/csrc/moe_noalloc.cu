@@ -1,12 +1,13 @@
 // Routing (router logits + top-k + renormalised weights) that allocates no
-// device memory, for callers that cannot call cudaMalloc: code running while a
-// CUDA graph is being captured (allocation is not a capturable operation), code
-// inside a host framework that owns all device memory through its own pool and
-// forbids raw allocations, or real-time paths that must not allocate after
-// start-up. The caller passes every input and output buffer; the only scratch
+// device memory, for callers that cannot call cudaMalloc: code inside a host
+// framework that owns all device memory through its own pool and forbids raw
+// allocations, or real-time paths that must not allocate (nor risk an
+// allocation failure) once they are running. The caller passes every input and
+// output buffer; the only scratch
 // memory (the fp32 router logits between the two kernels) is the file-scope
 // device array below, which every GPU that loads this library holds until the
 // process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -28,10 +29,44 @@ constexpr int kNoAllocMaxK = 8;
 static __device__ __align__(256) float g_noalloc_logits[kNoAllocMaxT * kNoAllocMaxE];
 
 // Device address of g_noalloc_logits per device (host code cannot use the
-// symbol's name as a device address).
+// symbol's name as a device address), with the unique id of the context it was
+// looked up in: after a device reset the module is loaded again, possibly at
+// another address, so a new context makes the next call look the address up
+// again instead of launching with a stale one.
 constexpr int kMaxDevices = 64;
-float* g_scratch_ptr[kMaxDevices] = {nullptr};
+struct ScratchAddr {
+  float* ptr;
+  unsigned long long ctx_id;   // 0: unknown (look up again on every call)
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 std::mutex g_scratch_mu;
+
+// Driver entry points through the runtime, so that the library does not link
+// libcuda directly (it still loads on machines without a driver).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  if (!get_current || !get_id) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+      return 0;
+    get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+    get_id = reinterpret_cast<CtxGetIdFn>(f2);
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 cudaError_t scratch_for_current_device(float** out) {
   int dev = 0;
@@ -39,13 +74,15 @@ cudaError_t scratch_for_current_device(float** out) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  const unsigned long long id = current_context_id();
+  if (g_scratch[dev].ptr == nullptr || id == 0 || g_scratch[dev].ctx_id != id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_logits);
+    e = cudaGetSymbolAddress(&p, g_noalloc_logits);   // also makes the device's context current
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
+    g_scratch[dev].ptr = static_cast<float*>(p);
+    g_scratch[dev].ctx_id = current_context_id();
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   return cudaSuccess;
 }
 

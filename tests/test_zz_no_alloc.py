@@ -1,11 +1,13 @@
 """The allocation-free routing entry point (moe_route_topk_noalloc) against the
-routing moe_layer_forward computes, through the C ABI, on two calls in a row.
+routing moe_layer_forward computes, through the C ABI, on two calls in a row,
+and its weights against the fp64 oracle's renormalised softmax.
 
-Callers that cannot allocate device memory (code running under CUDA graph
-capture, or frameworks that own all device memory) use this entry point; its
-only scratch is a fixed array inside the library, shared by all calls. This
-file is collected last so that a run stopping at the first failure has
-already run every other test; it also passes on its own in a fresh process.
+Callers that cannot allocate device memory (a host framework that owns all
+device memory through its own pool, or a real-time path that must not allocate
+once running) use this entry point; its only scratch is a fixed array inside the
+library, shared by all calls. This file is collected last so that a run stopping
+at the first failure has already run every other test; it also passes on its own
+in a fresh process.
 """
 import numpy as np
 import pytest
@@ -19,12 +21,14 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-def test_noalloc_routing_matches_layer_forward_twice():
+@pytest.mark.parametrize("H,E", [(1024, 128), (2560, 512)])
+def test_noalloc_routing_matches_layer_forward_twice(H, E):
+    """E=512 is the scratch array's limit and takes the 16-keys-per-lane top-k."""
     from sparse_mixture_experts_gemv_gb300 import MoeLayer, _native as N
-    S = mi.custom_layer(H=1024, E=128, k=8, I=128, Is=128, seed=21)
-    L = MoeLayer(1024, 128, 8, 128, 128, G.weights_of(S), max_tokens=8)
+    S = mi.custom_layer(H=H, E=E, k=8, I=128, Is=128, seed=21)
+    L = MoeLayer(H, E, 8, 128, 128, G.weights_of(S), max_tokens=8)
     router_t = torch.from_numpy(np.ascontiguousarray(S.router().T)).cuda()   # [E, H] fp32
-    for call, T in enumerate((4, 1)):
+    for call, T in enumerate((4, 1, 8)):
         x_bits = mi.tokens(S.spec, T, stream=900 + call)
         lb_np = mi.logit_bias(S.spec, T, 0.5, stream=900 + call)
         x = torch.from_numpy(x_bits.view(np.int16)).cuda()
@@ -33,7 +37,7 @@ def test_noalloc_routing_matches_layer_forward_twice():
         ref_idx, ref_w = L.routing(T)
         idx = torch.full((T, 8), -1, dtype=torch.int32, device="cuda")
         w = torch.zeros((T, 8), dtype=torch.float32, device="cuda")
-        st = N.moe_route_topk_noalloc(x.data_ptr(), router_t.data_ptr(), None, lb.data_ptr(), T, 1024, 128, 8,
+        st = N.moe_route_topk_noalloc(x.data_ptr(), router_t.data_ptr(), None, lb.data_ptr(), T, H, E, 8,
                                       idx.data_ptr(), w.data_ptr(), torch.cuda.current_stream().cuda_stream)
         assert st == N.MOE_OK, N.moe_status_string(st)
         torch.cuda.synchronize()
@@ -46,6 +50,9 @@ def test_noalloc_routing_matches_layer_forward_twice():
         assert o.valid_topk(logits, a.astype(np.int64), G.NEAR_TIE).all()
         same = (a == b).all(axis=1)
         assert np.abs(w.cpu().numpy()[same] - ref_w.cpu().numpy()[same]).max() <= 1e-5
+        # weights against the oracle: the renormalised softmax of the selected fp64 logits
+        wref = o.routing_weights(logits, a.astype(np.int64))
+        assert np.abs(w.cpu().numpy() - wref).max() < 1e-5
         np.testing.assert_allclose(w.cpu().numpy().sum(1), 1.0, atol=1e-5)
     L.close()
 
