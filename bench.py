@@ -507,6 +507,96 @@ class StackedLayer:
         return self._sh
 
 
+class CachedLayer:
+    """Oracle accessor that draws each expert once (lazily) and keeps it, so the
+    timed calls exclude random draws; only the experts a sample touches are drawn."""
+
+    def __init__(self, S: mi.SynthLayer):
+        self.spec = S.spec
+        self._S = S
+        self._r = S.router()
+        self._b = S.router_bias()
+        self._sh = S.shared_raw()
+        self._e = {}
+
+    def router(self):
+        return self._r
+
+    def router_bias(self):
+        return self._b
+
+    def expert_raw(self, e):
+        if e not in self._e:
+            self._e[e] = self._S.expert_raw(e)
+        return self._e[e]
+
+    def shared_raw(self):
+        return self._sh
+
+
+# CPU-oracle legs: (name, workload, rows of one call or None for the workload's T, calls in the sample)
+CPU_LEGS = [("t1", "qwen_decode", None, 8), ("t4", "qwen_verify", None, 4), ("t4096_256rows", "qwen_prefill", 256, 1)]
+
+
+def _oracle_leg(wname: str, rows, ncalls: int, seconds: float) -> dict:
+    """Per-call seconds of the oracle on a bounded sample of one workload."""
+    from oracle import moe_oracle as o
+    w = mi.WORKLOADS[wname]
+    SL = CachedLayer(mi.SynthLayer(w.layer))
+    calls = []
+    for c in range(ncalls):
+        x = mi.workload_tokens(w, c)
+        lb = mi.workload_logit_bias(w, c) if w.logit_bias_sigma else None
+        if rows is not None:   # a seeded subset of the chunk's rows (the layer is row-independent)
+            sel = np.sort(np.random.default_rng(c).choice(x.shape[0], size=rows, replace=False))
+            x = x[sel]
+            lb = None if lb is None else lb[sel]
+        calls.append((x, lb))
+    for x, lb in calls:   # draws every touched expert once, outside the timing
+        o.moe_forward(SL, x, logit_bias=lb)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        x, lb = calls[n % len(calls)]
+        o.moe_forward(SL, x, logit_bias=lb)
+        n += 1
+        if time.perf_counter() - t0 >= seconds and n >= 2:
+            break
+    el = time.perf_counter() - t0
+    return {"s_per_call": el / n, "calls": n, "rows_per_call": int(calls[0][0].shape[0]), "elapsed_s": el}
+
+
+def _single_thread_legs(seconds: float) -> dict:
+    """The same legs in a child process with one BLAS/OpenMP thread."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-legs-child", str(seconds)],
+                       capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout)[-300:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_legs(seconds: float) -> list:
+    """Oracle timings at T=1, T=4 and on a 256-row subset of the T=4096 prefill chunk,
+    on all host cores (numpy/BLAS threads) and on one thread."""
+    allc = {name: _oracle_leg(wn, rows, nc, seconds) for name, wn, rows, nc in CPU_LEGS}
+    one = _single_thread_legs(seconds)
+    out = []
+    for name, wn, rows, nc in CPU_LEGS:
+        for cores, r in ((os.cpu_count(), allc.get(name)), (1, one.get(name))):
+            if not r or "s_per_call" not in r:
+                out.append({"leg": name, "workload": wn, "cores": cores, "error": str(one.get("error", "missing"))})
+                continue
+            T_full = mi.WORKLOADS[wn].T
+            leg = {"leg": name, "workload": wn, "cores": cores, "us_per_call": round(r["s_per_call"] * 1e6, 1),
+                   "rows_per_call": r["rows_per_call"], "calls_timed": r["calls"]}
+            if rows is not None:
+                leg["sample"] = f"{rows} seeded rows of each T={T_full} chunk (the layer is row-independent)"
+                leg["us_per_full_chunk_scaled"] = round(r["s_per_call"] * 1e6 * T_full / rows, 1)
+                leg["tokens_per_s"] = round(rows / r["s_per_call"], 1)
+            out.append(leg)
+    return out
+
+
 def cpu_baseline(seconds: float, wname: str = HEADLINE):
     from oracle import moe_oracle as o
     w = mi.WORKLOADS[wname]
@@ -520,8 +610,13 @@ def cpu_baseline(seconds: float, wname: str = HEADLINE):
         if time.perf_counter() - t0 >= seconds and n >= 2:
             break
     el = time.perf_counter() - t0
-    return {"value": round(el / n * 1e6, 1), "unit": "us", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n} T=1 calls of the {wname} layer (fp64 numpy oracle, {el:.1f} s)"}
+    res = {"value": round(el / n * 1e6, 1), "unit": "us", "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"{n} T=1 calls of the {wname} layer (fp64 numpy oracle, {el:.1f} s)"}
+    try:
+        res["legs"] = cpu_legs(max(2.0, seconds / 3))
+    except Exception as ex:  # report, never hide
+        res["legs"] = [{"error": repr(ex)}]
+    return res
 
 
 def run_reference(args):
@@ -598,7 +693,11 @@ def main():
     ap.add_argument("--profile", default=None, choices=sorted(mi.WORKLOADS) + ["lmhead_fp8"],
                     help="untimed calls of one workload, for ncu captures")
     ap.add_argument("--profile-calls", type=int, default=6)
+    ap.add_argument("--cpu-legs-child", type=float, default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_legs_child is not None:   # one-thread oracle legs (run by cpu_legs in a child process)
+        print(json.dumps({name: _oracle_leg(wn, rows, nc, args.cpu_legs_child) for name, wn, rows, nc in CPU_LEGS}))
+        return
     if args.profile:
         run_profile_driver(args)
         return

@@ -7,8 +7,8 @@ shares no code with the CUDA path.
 What it computes: "Three ways to speed up MoE inference on DGX Spark", section
 "Optimization 2": the bf16 output projection (hidden 2,560 -> vocabulary
 157,184) is quantized to FP8 when the head is built, which halves the bytes the
-per-token GEMV reads. Readings where the page is silent (listed in the design
-notes): FP8 is OCP E4M3 (bias 7, no infinities, 0x7F / 0xFF NaN, largest finite
+per-token GEMV reads. Readings where the page is silent (the plainest reading
+of a "dynamic FP8" head that halves the bf16 bytes): FP8 is OCP E4M3 (bias 7, no infinities, 0x7F / 0xFF NaN, largest finite
 448); one fp32 scale per output row, s = amax(|row|) / 448 in fp32 (1 for an
 all-zero row); codes q = RNE_E4M3(w / s) with the fp32 quotient and saturation
 to +-448; activations stay bf16; logits[t, v] = s_v * sum_h e4m3(q[v, h]) * x[t, h].

@@ -17,8 +17,9 @@ What it computes (a plain restatement of the layer the two pages describe):
   was slow in the first place" and "Optimization 1": 512 routed experts, 8
   selected plus one always-on shared expert; routed expert weights in MXFP4.
 
-Readings where the pages are silent (each is listed in the design notes):
-router scores are softmax probabilities renormalised over the selected k
+Readings where the pages are silent, taken here as the plainest reading the
+rest of the pages supports: router scores are softmax probabilities
+renormalised over the selected k
 (equal to a softmax over the k selected logits); the gated activation is
 SwiGLU, silu(gate) * up with silu(z) = z / (1 + exp(-z)); the shared expert
 has no gate of its own; exact logit ties go to the lower expert index;
