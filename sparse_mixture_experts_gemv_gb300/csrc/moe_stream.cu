@@ -92,9 +92,12 @@ struct StreamArgs {
   int group_records;           // records per ring group (8, or 4 when x is large)
   int ring_groups;             // slot groups in the ring
   int x_bytes_al;              // bytes of the x region (T rows of H + 8 bf16, 128-aligned)
+  int router_off;              // dynamic shared-memory offset for this CTA's router rows, or -1
+                               // (the rows are then loaded from global memory by the consumers)
   unsigned long long* words;   // [kMaxDecodeT][E] tagged logits
-  unsigned long long* partial; // [G][H][T] per-CTA partial outputs, tagged words
+  float* partial;              // [G][H][TP] per-CTA fp32 partial outputs
   unsigned long long* ctr;     // calls completed x G (each CTA adds 1 when it leaves)
+  unsigned long long* arrivals;  // partial outputs stored x G (each CTA adds 1 per call)
   int* idx;                    // [T][k]  diagnostics (CTA 0)
   float* weights;              // [T][k]
   DecodeMeta* meta;
@@ -106,7 +109,6 @@ struct StreamArgs {
 
 using stream::ld_relaxed_u64;
 using stream::mma_16816;
-using stream::st_relaxed_v2u64;
 using stream::tagged;
 using stream::consumers_sync;
 using stream::Ranges;
@@ -214,11 +216,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
     __syncwarp();
   };
   const int npre = min(NG, nfull_sh + (gmix >= 0 ? 1 : 0));   // groups whose shared records go out before routing
+  const int nr_rows = (E - b + G - 1) / G;             // router rows b, b + G, ... of this CTA
+  const float* router_smem = a.router_off >= 0 ? reinterpret_cast<const float*>(smem + a.router_off) : nullptr;
   if (producer) {
     if (lane == 0) {
-      sm100::mbar_arrive_expect_tx(&x_bar, (uint32_t)(T * H * 2));
+      const uint32_t rbytes = router_smem ? (uint32_t)(nr_rows * H * 4) : 0u;
+      sm100::mbar_arrive_expect_tx(&x_bar, (uint32_t)(T * H * 2) + rbytes);
       for (int t = 0; t < T; ++t)
         sm100::bulk_copy_g2s(xs + (size_t)t * XP, a.x + (size_t)t * H, (uint32_t)(H * 2), &x_bar);
+      for (int m = 0; router_smem && m < nr_rows; ++m)
+        sm100::bulk_copy_g2s(smem + a.router_off + (size_t)m * H * 4, a.router_t + (size_t)(b + m * G) * H,
+                             (uint32_t)(H * 4), &x_bar);
     }
     // The shared-expert records go out once x has landed: issued at kernel
     // start, their copies would queue ahead of x, the router rows and the
@@ -236,7 +244,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
     if (threadIdx.x == 0 && a.force_timeout && b == 0 && !bounded_wait_flag(a.never_set, 2000000LL))
       set_error(a.err, kDevTimeout);
     stream::router_publish<TMAX>(xs, XP, T, H, E, a.router_t, a.router_bias, a.logit_bias, a.words, tag, &x_bar,
-                                 a.err, &s_abort, s_rpart);
+                                 a.err, &s_abort, s_rpart, router_smem);
     stream::route_window(a.words, T, E, k, tag, rs, a.err, &s_abort);
   }
   __syncthreads();   // routing known to every warp, producer included
@@ -250,6 +258,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
         if (g2 == gmix) sm100::mbar_arrive(&full_bar[g2]);
         sm100::mbar_wait(&full_bar[g2], 0, a.err, &never, 20000000LL, false);
       }
+      stream::exchange_arrive(a.arrivals);
       leave();
     }
     return;
@@ -359,6 +368,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
       volatile int never = 0;
       for (int g2 = grp; g2 < ngroups && g2 < grp + NG; ++g2)
         sm100::mbar_wait(&full_bar[g2 % NG], (uint32_t)(g2 / NG) & 1u, a.err, &never, 20000000LL, false);
+      stream::exchange_arrive(a.arrivals);
       leave();
     }
     return;
@@ -367,9 +377,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) moe_decode_stream_kernel(co
   // ---------------------------------------------------------------- exchange of partial outputs
 #pragma unroll
   for (int j = 0; j < kMaxTiles; ++j)
-    if (j < ntile) stream::publish_tile(a.partial, b, H, T, 16 * (warp + kConsumerWarps * j), acc[j], tag);
-  consumers_sync();
-  stream::collect_outputs<true>(a.partial, reinterpret_cast<unsigned long long*>(ring), (size_t)NG * RG * stride, tag, T, H, a.out, a.err, &s_abort);
+    if (j < ntile) stream::publish_tile_f32(a.partial, b, H, T, 16 * (warp + kConsumerWarps * j), acc[j]);
+  stream::collect_outputs_f32(a.partial, reinterpret_cast<float*>(ring), a.arrivals, tag * (unsigned long long)G, T, H,
+                              a.out, a.err, &s_abort);
   if (threadIdx.x == 0) leave();
 }
 
@@ -402,7 +412,8 @@ bool stream_supported(const moe_layer* L, int T) {
   const int ng = stream_ring_groups(L, T);
   if (ng < 2) return false;
   // the final exchange stages G x (rows of this CTA) x TP fp32 values in the ring
-  return stream::collect_fits(L->num_sms, c.hidden, T, (size_t)ng * stream_group_records(T, c.hidden) * stream_record_stride(c.hidden));
+  return stream::collect_f32_fits(L->num_sms, c.hidden, T,
+                                  (size_t)ng * stream_group_records(T, c.hidden) * stream_record_stride(c.hidden));
 }
 
 template <int TMAX>
@@ -417,7 +428,18 @@ static cudaError_t launch_stream_t(moe_layer* L, const uint16_t* x, uint16_t* ou
   a.group_records = stream_group_records(T, c.hidden);
   a.ring_groups = stream_ring_groups(L, T);
   a.x_bytes_al = stream_x_bytes(T, c.hidden);
-  a.words = L->dec.logit_words; a.partial = L->dec.partial; a.ctr = L->dec.sync_ctr + 2;
+  {
+    // This CTA's router rows go by bulk copy into the shared memory behind the
+    // ring when it has room, else the consumers load them from global memory.
+    // (Copying them into a ring slot that no shared-expert record uses before
+    // routing was measured too: slower at T = 4 on GB300, 54.4 vs 53.7 us.)
+    const int G = L->num_sms;
+    const size_t rbytes = (size_t)((c.num_experts + G - 1) / G) * c.hidden * 4;
+    const size_t ring_end = (size_t)a.x_bytes_al + (size_t)a.ring_groups * a.group_records * a.rec_stride;
+    a.router_off = ring_end + rbytes <= (size_t)kStreamSmemMax ? (int)ring_end : -1;
+  }
+  a.words = L->dec.logit_words; a.partial = reinterpret_cast<float*>(L->dec.partial);
+  a.ctr = L->dec.sync_ctr + 2; a.arrivals = L->dec.sync_ctr + 3;
   a.idx = L->dec.idx; a.weights = L->dec.weights; a.meta = L->dec.meta;
   a.out = out; a.err = L->err; a.never_set = L->never_set;
   a.force_timeout = (c.flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? 1 : 0;
@@ -426,6 +448,10 @@ static cudaError_t launch_stream_t(moe_layer* L, const uint16_t* x, uint16_t* ou
   cfg.gridDim = dim3(L->num_sms);
   cfg.blockDim = dim3(kStreamThreads);
   cfg.dynamicSmemBytes = (size_t)a.x_bytes_al + (size_t)a.ring_groups * a.group_records * a.rec_stride;
+  if (a.router_off >= 0)
+    cfg.dynamicSmemBytes = std::max(cfg.dynamicSmemBytes,
+                                    (size_t)a.router_off + (size_t)((c.num_experts + L->num_sms - 1) / L->num_sms) *
+                                                               c.hidden * 4);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs co-resident: they wait on one another

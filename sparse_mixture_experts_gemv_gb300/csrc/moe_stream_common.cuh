@@ -47,12 +47,6 @@ MOE_DEV unsigned long long ld_relaxed_u64_nc(const unsigned long long* p) {
 MOE_DEV void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
-MOE_DEV void st_relaxed_v2u64(unsigned long long* p, unsigned long long v0, unsigned long long v1) {
-  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" :: "l"(p), "l"(v0), "l"(v1) : "memory");
-}
-MOE_DEV void ld_relaxed_v2u64(const unsigned long long* p, unsigned long long& v0, unsigned long long& v1) {
-  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(v0), "=l"(v1) : "l"(p));
-}
 MOE_DEV unsigned long long tagged(unsigned long long tag, float v) {
   return (tag << 32) | (unsigned long long)__float_as_uint(v);
 }
@@ -372,11 +366,15 @@ MOE_DEV bool poll_topk(const unsigned long long* words, int E, int k, unsigned l
 // router columns get bitwise equal logits, and the exact-tie rule (lower index
 // first) then decides between them. The row loads are issued before waiting
 // for x (x_bar). Every consumer thread has waited on x_bar when this returns.
+// When `rows_smem` is not null, the producer has bulk-copied this CTA's router
+// rows there (row m at rows_smem + m * H, completing on x_bar with x): a bulk
+// copy lands as soon as x does, while per-thread global loads of the rows
+// arrived about a microsecond later on GB300.
 template <int TMAX>
 MOE_DEV void router_publish(const uint16_t* xs, int XP, int T, int H, int E, const float* router_t,
                             const float* router_bias, const float* logit_bias, unsigned long long* words,
                             unsigned long long tag, uint64_t* x_bar, int* err, int* s_abort,
-                            float (*s_rpart)[TMAX]) {
+                            float (*s_rpart)[TMAX], const float* rows_smem = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, b = blockIdx.x;
   const int nr_rows = (E - b + G - 1) / G;
@@ -385,9 +383,13 @@ MOE_DEV void router_publish(const uint16_t* xs, int XP, int T, int H, int E, con
   const int H4 = H / 4;
   // the bias terms are loaded now, so that they do not add a memory round trip
   // after the dot products
+  // The logits are stored by the last four consumer warps, never by the warps
+  // that poll them in route_window (warps 0 .. T-1): a warp's first poll right
+  // after its own store took 1.2-1.7 us on GB300, against ~0.2 us otherwise.
+  const int pt = (int)threadIdx.x - (kConsumers - 128);   // nr_rows * T <= 128
   float rbias = 0.f, lbias = 0.f;
-  if ((int)threadIdx.x < nr_rows * T) {
-    const int m = threadIdx.x / T, t = threadIdx.x - m * T;
+  if (pt >= 0 && pt < nr_rows * T) {
+    const int m = pt / T, t = pt - m * T;
     const int e = b + m * G;
     rbias = router_bias[e];
     if (logit_bias) lbias = logit_bias[(size_t)t * E + e];
@@ -395,17 +397,22 @@ MOE_DEV void router_publish(const uint16_t* xs, int XP, int T, int H, int E, con
   bool x_ready = false;
   if (warp < items) {
     const int m = warp / P, p = warp - m * P;
-    const float* row = router_t + (size_t)(b + m * G) * H;
+    const float* row = rows_smem ? rows_smem + (size_t)m * H : router_t + (size_t)(b + m * G) * H;
     const int c0 = p * H4 / P, c1 = (p + 1) * H4 / P;
     float acc[TMAX];
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
     for (int cb = c0; cb < c1; cb += 32 * 8) {
       uint4 v[8];
+      if (rows_smem && !x_ready) {   // the rows arrive with x
+        volatile int never = 0;
+        if (!sm100::mbar_wait(x_bar, 0, err, &never, kSpinBudget, false)) *s_abort = 1;
+        x_ready = true;
+      }
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const int c = cb + lane + 32 * q;
-        if (c < c1) v[q] = ldg_stream(row + 4 * c);
+        if (c < c1) v[q] = rows_smem ? *reinterpret_cast<const uint4*>(row + 4 * c) : ldg_stream(row + 4 * c);
       }
       if (!x_ready) {
         volatile int never = 0;
@@ -444,8 +451,8 @@ MOE_DEV void router_publish(const uint16_t* xs, int XP, int T, int H, int E, con
     if (!sm100::mbar_wait(x_bar, 0, err, &never, kSpinBudget, false)) *s_abort = 1;
   }
   consumers_sync();
-  if ((int)threadIdx.x < nr_rows * T) {   // logit = partial sums in warp order + biases
-    const int m = threadIdx.x / T, t = threadIdx.x - m * T;
+  if (pt >= 0 && pt < nr_rows * T) {   // logit = partial sums in warp order + biases
+    const int m = pt / T, t = pt - m * T;
     const int e = b + m * G;
     float sl = 0.f;
     for (int p = 0; p < P; ++p) sl += s_rpart[m * P + p][t];
@@ -541,12 +548,11 @@ MOE_DEV void route_window(const unsigned long long* words, int T, int E, int k, 
 // ---------------------------------------------------------------------------
 // Exchange of partial outputs. Every CTA holds fp32 partial sums of all H
 // output rows over the records it streamed; the output is their sum over the
-// G CTAs. Each CTA publishes its partials as tagged words, word (b, n, t) at
-// (b * H + n) * TP + t, TP = exchange_pitch(T); CTA b then reduces the rows
-// [8 u0, 8 u1) of the 8-row units split evenly over the grid, for every token.
+// G CTAs. CTA b reduces the rows [8 u0, 8 u1) of the 8-row units split evenly
+// over the grid, for every token.
 // ---------------------------------------------------------------------------
-// Words per output row: T itself for one token, else T rounded up to even so
-// that a token pair is one 16-byte store.
+// Floats per output row in the partial buffer: T itself for one token, else T
+// rounded up to even so that a token pair is one 8-byte store.
 MOE_DEV int exchange_pitch(int T) { return T == 1 ? 1 : T + (T & 1); }
 
 struct RowSlice {
@@ -558,162 +564,134 @@ MOE_DEV RowSlice exchange_rows(int b, int G, int H) {
   return {8 * u0, 8 * (u1 - u0)};
 }
 
-// One output tile of this CTA's partials, straight from an mma accumulator
-// fragment: acc rows n0 + gq (regs 0, 1) and n0 + gq + 8 (regs 2, 3), tokens
-// 2 cq and 2 cq + 1. For odd T >= 3 the pad token's word is written too.
-MOE_DEV void publish_tile(unsigned long long* partial, int b, int H, int T, int n0, const float (&acc)[4],
-                          unsigned long long tag) {
+// ---------------------------------------------------------------------------
+// Exchange with plain fp32 partials and one arrival counter. Each CTA stores
+// its partial outputs as fp32, float (b, n, t) at (b * H + n) * TP + t, then
+// makes them visible GPU-wide (fence) before it adds 1 to the arrival counter;
+// one thread per CTA waits (acquire) until the counter shows every CTA of this
+// call, and the CTA then pulls the rows [8 u0, 8 u1) of all G sources into
+// shared memory in one pass of 16-byte L2 copies. (Publishing tagged 8-byte
+// words and re-copying stale blocks until every tag was current moved twice
+// the bytes and was ~1 us slower on GB300.) The counter only grows: this
+// call's CTAs wait for `target` arrivals (calls before it included), and every
+// CTA adds exactly 1 per call on every exit path.
+// ---------------------------------------------------------------------------
+MOE_DEV void publish_tile_f32(float* partial, int b, int H, int T, int n0, const float (&acc)[4]) {
   const int lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
   const int TP = exchange_pitch(T);
   if (T == 1) {
     if (cq == 0) {
-      st_relaxed_u64(partial + (size_t)b * H + n0 + gq, tagged(tag, acc[0]));
-      st_relaxed_u64(partial + (size_t)b * H + n0 + gq + 8, tagged(tag, acc[2]));
+      partial[(size_t)b * H + n0 + gq] = acc[0];
+      partial[(size_t)b * H + n0 + gq + 8] = acc[2];
     }
   } else if (2 * cq < T) {
 #pragma unroll
     for (int h = 0; h < 2; ++h)
-      st_relaxed_v2u64(partial + ((size_t)b * H + n0 + gq + 8 * h) * TP + 2 * cq, tagged(tag, acc[2 * h]),
-                       tagged(tag, acc[2 * h + 1]));
+      *reinterpret_cast<float2*>(partial + ((size_t)b * H + n0 + gq + 8 * h) * TP + 2 * cq) =
+          make_float2(acc[2 * h], acc[2 * h + 1]);
   }
 }
 
-// Consumer warps, after every warp of this CTA has published its tiles: 16-byte
-// asynchronous copies (cp.async, no registers held) bring the published blocks
-// of this CTA's rows from all G CTAs into shared memory (`stage`, `stage_bytes`
-// of it; as many sources per pass as fit); a copy that still carries an older
-// tag is made again. Two ways to retry: PER_WARP -- warp w owns the sources
-// p = w mod 16 of a pass and copies again the ones that are not current, on its
-// own, so that a late CTA's block is picked up one round trip after it lands;
-// otherwise the whole pass is copied again after a consumer barrier (fewer
-// registers; faster in the MXFP4 kernel, measured). (One bulk copy per source
-// block was tried: the copy engine works through the G small copies one after
-// another, several microseconds in all.) Each output (row, token) is then added
-// by four threads, thread i over the sources [iG/4, (i+1)G/4) in order, and the
-// four sums are combined as (s0 + s1) + (s2 + s3): a fixed order, so the
-// result does not depend on timing. Ends with a consumer barrier.
-template <bool PER_WARP>
-MOE_DEV void collect_outputs(const unsigned long long* partial, unsigned long long* stage, size_t stage_bytes,
-                             unsigned long long tag, int T, int H, uint16_t* out, int* err, int* s_abort) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+MOE_DEV unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// This CTA's arrival after its partials are stored (consumer threads, after a
+// consumer barrier; thread 0 only). Also used on the exit paths of a CTA that
+// aborts, so that the others do not wait for it.
+MOE_DEV void exchange_arrive(unsigned long long* arrivals) {
+  __threadfence();
+  atomicAdd(arrivals, 1ull);
+}
+
+// Consumer warps, after every warp of this CTA has stored its tiles with
+// publish_tile_f32: arrive, wait for all G CTAs of this call, pull this CTA's
+// rows of all G partials into `stage` (one pass; collect_f32_fits checks that
+// it holds them), add the G values of each output in a fixed order (four
+// threads per output, thread i over the sources [iG/4, (i+1)G/4), combined as
+// (s0 + s1) + (s2 + s3)) and write bf16. Ends with a consumer barrier.
+MOE_DEV void collect_outputs_f32(const float* partial, float* stage, unsigned long long* arrivals,
+                                 unsigned long long target, int T, int H, uint16_t* out, int* err, int* s_abort) {
   const int G = gridDim.x, b = blockIdx.x;
   const int TP = exchange_pitch(T);
   const RowSlice rs = exchange_rows(b, G, H);
-  const int blk_words = rs.nrow * TP;
-  const uint32_t blk_bytes = (uint32_t)blk_words * 8u;
+  const int blk = rs.nrow * TP;                       // floats of one source's block
+  const unsigned bu = (unsigned)blk / 4u;             // 16-byte units of one block
   const int nout = rs.nrow * T;
-  const unsigned long long want = tag & 0xFFFFFFFFull;
-  const int per_pass = (int)min((size_t)G, stage_bytes / (blk_bytes ? blk_bytes : 1u));
-  const unsigned bu = (unsigned)blk_words / 2u;   // 16-byte units per source block
-  constexpr int kOut = 2;   // outputs per thread: 4 * nout <= kOut * kConsumers
-  float sum[kOut] = {0.f, 0.f};
-  bool aborted = *s_abort != 0;   // read after the caller's consumer barrier: the same in every thread
-  if (nout > 0) {
+  __threadfence();                                    // this thread's partials are visible GPU-wide
+  consumers_sync();                                   // every warp's partials are stored
+  if (threadIdx.x == 0) exchange_arrive(arrivals);
+  // the arrivals are polled from another warp than the one that just added to
+  // the counter (see router_publish: a warp's first poll after its own store is slow)
+  if (threadIdx.x == 32) {
     const long long t0 = clock64();
-    for (int c0 = 0; c0 < G && !aborted; c0 += per_pass) {
-      const int pc = min(per_pass, G - c0);
-      bool timed_out = false;
-      if constexpr (PER_WARP) {
-        // this warp's sources q = warp, warp + 16, ... of the pass: copy until every word is current
-        const int nq = (pc - warp + kConsumerWarps - 1) / kConsumerWarps;
-        uint32_t todo = nq > 0 ? (nq >= 32 ? 0xFFFFFFFFu : (1u << nq) - 1u) : 0u;   // bit j: source warp + 16 j
-        while (todo) {
-          for (unsigned u = (unsigned)lane; u < (unsigned)nq * bu; u += 32u) {
-            const int jq = (int)(u / bu), w = (int)(u - (unsigned)jq * bu);
-            if ((todo >> jq) & 1u) {
-              const int q = warp + kConsumerWarps * jq;
-              sm100::cp_async_16(stage + (size_t)q * blk_words + 2 * w,
-                                 partial + ((size_t)(c0 + q) * H + rs.n0) * TP + 2 * w, 16u);
-            }
-          }
-          sm100::cp_async_commit();
-          sm100::cp_async_wait<0>();
-          __syncwarp();   // the warp's copies have landed
-          uint32_t stale = 0u;
-          for (unsigned u = (unsigned)lane; u < (unsigned)nq * (unsigned)blk_words; u += 32u) {
-            const int jq = (int)(u / (unsigned)blk_words), w = (int)(u - (unsigned)jq * (unsigned)blk_words);
-            if ((todo >> jq) & 1u) {
-              const int q = warp + kConsumerWarps * jq;
-              if ((stage[(size_t)q * blk_words + w] >> 32) != want) stale |= 1u << jq;
-            }
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) stale |= __shfl_xor_sync(0xFFFFFFFFu, stale, o);
-          todo = stale;
-          if (todo && clock64() - t0 > kSpinBudget) {
-            timed_out = true;
-            break;
-          }
-        }
-      } else {
-        while (true) {
-          for (int u = threadIdx.x; u < pc * (int)bu; u += kConsumers) {
-            const int q = (int)((unsigned)u / bu), w = u - q * (int)bu;
-            sm100::cp_async_16(stage + (size_t)q * blk_words + 2 * w,
-                               partial + ((size_t)(c0 + q) * H + rs.n0) * TP + 2 * w, 16u);
-          }
-          sm100::cp_async_commit();
-          sm100::cp_async_wait<0>();
-          consumers_sync();   // every thread's copies have landed
-          bool stale = false;
-          for (int u = threadIdx.x; u < pc * blk_words; u += kConsumers) stale |= (stage[u] >> 32) != want;
-          // a barrier: every thread is done reading the stage before it is copied into again
-          if (!consumers_sync_or(stale)) break;
-          if (consumers_sync_or(threadIdx.x == 0 && clock64() - t0 > kSpinBudget)) {   // one decision for all
-            timed_out = true;
-            break;
-          }
-        }
-      }
-      // the pass is complete in every warp; the stage is read, then copied into again
-      if (consumers_sync_or(timed_out)) {
-        if (threadIdx.x == 0) set_error(err, kDevTimeout);
-        aborted = true;
+    while (ld_acquire_u64(arrivals) < target) {
+      if (clock64() - t0 > kSpinBudget) {
+        set_error(err, kDevTimeout);
+        *s_abort = 1;
         break;
       }
-#pragma unroll
-      for (int r = 0; r < kOut; ++r) {
-        const int o4 = (int)threadIdx.x + r * kConsumers;
-        if (o4 < 4 * nout) {
-          const int o = o4 >> 2, i = o4 & 3;
-          const int nl = o / T, t = o - nl * T;
-          const int p0 = max(c0, (int)((unsigned)i * (unsigned)G / 4u));
-          const int p1 = min(c0 + pc, (int)((unsigned)(i + 1) * (unsigned)G / 4u));
-          const unsigned long long* src = stage + nl * TP + t;
-          float acc = sum[r];
-          for (int p = p0; p < p1; ++p) acc += __uint_as_float((uint32_t)src[(size_t)(p - c0) * blk_words]);
-          sum[r] = acc;
-        }
-      }
-      if (c0 + pc < G) consumers_sync();
     }
-    if (aborted && threadIdx.x == 0) *s_abort = 1;
+    __threadfence();
   }
   consumers_sync();
-  if (!aborted) {
+  const bool aborted = *s_abort != 0;
+  if (!aborted && nout > 0) {
+    for (unsigned u = threadIdx.x; u < (unsigned)G * bu; u += kConsumers) {
+      const unsigned q = u / bu, w = u - q * bu;
+      sm100::cp_async_16(stage + (size_t)q * blk + 4 * w, partial + ((size_t)q * H + rs.n0) * TP + 4 * w, 16u);
+    }
+    sm100::cp_async_commit();
+    sm100::cp_async_wait<0>();
+    consumers_sync();
+    // Four threads per output: thread i adds the sources [iG/4, (i+1)G/4) in
+    // order (the loop is unrolled so that the loads overlap; consecutive
+    // threads read neighbouring words of a source block, without bank
+    // conflicts), then the four sums are combined as (s0 + s1) + (s2 + s3): the
+    // same association on every call, so the result does not depend on timing.
+    // (32 threads per output with a butterfly was slower: 16-way bank
+    // conflicts on the staged blocks.)
+    constexpr int kOut = 2;   // outputs per thread: 4 * nout <= kOut * kConsumers
+    float sum[kOut] = {0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < kOut; ++r) {
+      const int o4 = (int)threadIdx.x + r * kConsumers;
+      if (o4 < 4 * nout) {
+        const int o = o4 >> 2, i = o4 & 3;
+        const int nl = o / T, t = o - nl * T;
+        const int p0 = (int)((unsigned)i * (unsigned)G / 4u), p1 = (int)((unsigned)(i + 1) * (unsigned)G / 4u);
+        const float* src = stage + nl * TP + t;
+        float acc = 0.f;
+#pragma unroll 8
+        for (int p = p0; p < p1; ++p) acc += src[(size_t)p * blk];
+        sum[r] = acc;
+      }
+    }
 #pragma unroll
     for (int r = 0; r < kOut; ++r) {
       const int o4 = (int)threadIdx.x + r * kConsumers;   // lanes 4o .. 4o + 3 share one output
-      float v = sum[r];
-      v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-      v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+      const float s0 = sum[r], s1 = __shfl_xor_sync(0xFFFFFFFFu, s0, 1);
+      const float lo = s0 + s1;                           // (s0 + s1) on lanes 4o, 4o + 1; (s2 + s3) on the others
+      const float hi = __shfl_xor_sync(0xFFFFFFFFu, lo, 2);
       if (o4 < 4 * nout && (o4 & 3) == 0) {
         const int o = o4 >> 2, nl = o / T, t = o - nl * T;
-        out[(size_t)t * H + rs.n0 + nl] = f32_to_bf16_rne(v);
+        out[(size_t)t * H + rs.n0 + nl] = f32_to_bf16_rne(lo + hi);
       }
     }
   }
   consumers_sync();
 }
 
-// Whether the exchange can run: one source's block of this CTA's rows fits in
-// the `stage_bytes` it is given, and four threads per output (row, token)
-// need at most two outputs per consumer thread.
-inline bool collect_fits(int G, int H, int T, size_t stage_bytes) {
+// Whether the fp32 exchange can run: all G sources' blocks of this CTA's rows
+// fit in one pass of `stage_bytes`, and four threads per output need at most
+// two outputs per consumer thread.
+inline bool collect_f32_fits(int G, int H, int T, size_t stage_bytes) {
   const int U = H / 8;
   const int nrow = 8 * ((U + G - 1) / G);
   const int TP = T == 1 ? 1 : T + (T & 1);
-  return (size_t)nrow * TP * 8 <= stage_bytes && 4 * nrow * T <= 2 * kConsumers;
+  return (size_t)G * nrow * TP * 4 <= stage_bytes && 4 * nrow * T <= 2 * kConsumers;
 }
 
 }  // namespace stream

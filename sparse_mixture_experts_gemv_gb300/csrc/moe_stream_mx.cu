@@ -88,9 +88,12 @@ struct MxArgs {
   int slot_bytes;              // bytes of one ring slot group
   int ring_groups;             // slot groups in the ring
   int x_bytes_al;              // bytes of one x copy (T rows of H + 8 halves, 128-aligned)
+  int router_off;              // dynamic shared-memory offset for this CTA's router rows, or -1
+                               // (the rows are then loaded from global memory by the consumers)
   unsigned long long* words;   // [kMaxDecodeT][E] tagged logits
-  unsigned long long* partial; // [G][H][TP] tagged partial outputs
+  float* partial;              // [G][H][TP] per-CTA fp32 partial outputs
   unsigned long long* ctr;     // calls completed x G (each CTA adds 1 when it leaves)
+  unsigned long long* arrivals;  // partial outputs stored x G (each CTA adds 1 per call)
   int* idx;                    // [T][k]  diagnostics (CTA 0)
   float* weights;              // [T][k]
   DecodeMeta* meta;
@@ -201,11 +204,17 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
     __syncwarp();
   };
   int issued = 0;
+  const int nr_rows = (E - b + G - 1) / G;             // router rows b, b + G, ... of this CTA
+  const float* router_smem = a.router_off >= 0 ? reinterpret_cast<const float*>(smem + a.router_off) : nullptr;
   if (producer) {
     if (lane == 0) {
-      sm100::mbar_arrive_expect_tx(&x_bar, (uint32_t)(T * H * 2));
+      const uint32_t rbytes = router_smem ? (uint32_t)(nr_rows * H * 4) : 0u;
+      sm100::mbar_arrive_expect_tx(&x_bar, (uint32_t)(T * H * 2) + rbytes);
       for (int t = 0; t < T; ++t)
         sm100::bulk_copy_g2s(xs + (size_t)t * XP, a.x + (size_t)t * H, (uint32_t)(H * 2), &x_bar);
+      for (int m = 0; router_smem && m < nr_rows; ++m)
+        sm100::bulk_copy_g2s(smem + a.router_off + (size_t)m * H * 4, a.router_t + (size_t)(b + m * G) * H,
+                             (uint32_t)(H * 4), &x_bar);
       volatile int never = 0;   // shared records only after x (see moe_stream.cu)
       sm100::mbar_wait(&x_bar, 0, a.err, &never, kSpinBudget, false);
     }
@@ -218,7 +227,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
     if (threadIdx.x == 0 && a.force_timeout && b == 0 && !bounded_wait_flag(a.never_set, 2000000LL))
       set_error(a.err, kDevTimeout);
     stream::router_publish<TMAX>(xs, XP, T, H, E, a.router_t, a.router_bias, a.logit_bias, a.words, tag, &x_bar,
-                                 a.err, &s_abort, s_rpart);
+                                 a.err, &s_abort, s_rpart, router_smem);
     bool x_range = false;   // an |x| above the f16 range: reported, never rounded to infinity silently
     for (int q = threadIdx.x; q < T * H / 2; q += kConsumers) {   // bf16 pairs -> f16 pairs
       const int t = q / (H / 2), c = q - t * (H / 2);
@@ -237,6 +246,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
       sm100::mbar_wait(&x_bar, 0, a.err, &never, 20000000LL, false);
       for (int g2 = 0; g2 < nsg && g2 < NG; ++g2)
         sm100::mbar_wait(&full_bar[g2], 0, a.err, &never, 20000000LL, false);
+      stream::exchange_arrive(a.arrivals);
       leave();
     }
     return;
@@ -392,6 +402,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
       volatile int never = 0;
       for (int g2 = grp; g2 < ngroups && g2 < grp + NG; ++g2)
         sm100::mbar_wait(&full_bar[g2 % NG], (uint32_t)(g2 / NG) & 1u, a.err, &never, 20000000LL, false);
+      stream::exchange_arrive(a.arrivals);
       leave();
     }
     return;
@@ -399,10 +410,9 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
 
   // ---------------------------------------------------------------- exchange of partial outputs
 #pragma unroll
-  for (int j = 0; j < NT; ++j)
-    stream::publish_tile(a.partial, b, H, T, 16 * (warp + kConsumerWarps * j), acc[j], tag);
-  consumers_sync();
-  stream::collect_outputs<false>(a.partial, reinterpret_cast<unsigned long long*>(ring), (size_t)NG * a.slot_bytes, tag, T, H, a.out, a.err, &s_abort);
+  for (int j = 0; j < NT; ++j) stream::publish_tile_f32(a.partial, b, H, T, 16 * (warp + kConsumerWarps * j), acc[j]);
+  stream::collect_outputs_f32(a.partial, reinterpret_cast<float*>(ring), a.arrivals, tag * (unsigned long long)G, T, H,
+                              a.out, a.err, &s_abort);
   if (threadIdx.x == 0) leave();
 }
 
@@ -439,7 +449,8 @@ bool stream_mx_supported(const moe_layer* L, int T) {
   if ((c.num_experts + L->num_sms - 1) / L->num_sms > stream::kMaxRouterRows) return false;
   const int ng = mx_ring_groups(L, T);
   if (ng < 2) return false;
-  return stream::collect_fits(L->num_sms, c.hidden, T, (size_t)ng * mx_slot_bytes(c.hidden, mx_group_records(T, c.hidden)));
+  return stream::collect_f32_fits(L->num_sms, c.hidden, T,
+                                  (size_t)ng * mx_slot_bytes(c.hidden, mx_group_records(T, c.hidden)));
 }
 
 template <int TMAX, int NT>
@@ -458,7 +469,15 @@ static cudaError_t launch_stream_mx_t(moe_layer* L, const uint16_t* x, uint16_t*
   a.slot_bytes = mx_slot_bytes(c.hidden, a.mx_group);
   a.ring_groups = mx_ring_groups(L, T);
   a.x_bytes_al = mx_x_bytes(T, c.hidden);
-  a.words = L->dec.logit_words; a.partial = L->dec.partial; a.ctr = L->dec.sync_ctr + 2;
+  {
+    // This CTA's router rows go by bulk copy into the shared memory behind the
+    // ring when it has room, else the consumers load them from global memory.
+    const size_t rbytes = (size_t)((c.num_experts + L->num_sms - 1) / L->num_sms) * c.hidden * 4;
+    const size_t ring_end = 2 * (size_t)a.x_bytes_al + (size_t)a.ring_groups * a.slot_bytes;
+    a.router_off = ring_end + rbytes <= (size_t)kMxSmemMax ? (int)ring_end : -1;
+  }
+  a.words = L->dec.logit_words; a.partial = reinterpret_cast<float*>(L->dec.partial);
+  a.ctr = L->dec.sync_ctr + 2; a.arrivals = L->dec.sync_ctr + 3;
   a.idx = L->dec.idx; a.weights = L->dec.weights; a.meta = L->dec.meta;
   a.out = out; a.err = L->err; a.never_set = L->never_set;
   a.force_timeout = (c.flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? 1 : 0;
@@ -467,6 +486,9 @@ static cudaError_t launch_stream_mx_t(moe_layer* L, const uint16_t* x, uint16_t*
   cfg.gridDim = dim3(L->num_sms);
   cfg.blockDim = dim3(stream::kThreads);
   cfg.dynamicSmemBytes = 2 * (size_t)a.x_bytes_al + (size_t)a.ring_groups * a.slot_bytes;
+  if (a.router_off >= 0)
+    cfg.dynamicSmemBytes = (size_t)a.router_off +
+                           (size_t)((c.num_experts + L->num_sms - 1) / L->num_sms) * c.hidden * 4;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs co-resident: they wait on one another
