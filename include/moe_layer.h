@@ -252,19 +252,21 @@ moe_status_t moe_layer_get_dispatch(moe_layer_t* layer, int32_t* hist_dev, int32
 
 /*
  * Copy the block map of the last grouped-path forward (MOE_ERR_INVALID_ARG after a
- * decode-path forward): the list of 128-row blocks of grouped routed rows that the
- * grouped GEMMs take as their M tiles ("Optimizing on-device inference for Apple
- * Silicon", section "Keep expert routing on the GPU": the dispatch writes the block
- * list on the GPU). Block b covers grouped rows [row0, min(row0 + 128, offsets[e+1]))
- * of expert e; blocks are in increasing expert order, then increasing row0.
+ * decode-path forward): the list of MOE_GROUPED_BLOCK_ROWS-row blocks of grouped
+ * routed rows that the grouped GEMMs take as their M tiles ("Optimizing on-device
+ * inference for Apple Silicon", section "Keep expert routing on the GPU": the dispatch
+ * writes the block list on the GPU). Block b covers grouped rows
+ * [row0, min(row0 + MOE_GROUPED_BLOCK_ROWS, offsets[e+1])) of expert e; blocks are in
+ * increasing expert order, then increasing row0.
  *   blocks_dev      int32 [max_blocks][2] device: (e, row0) of each block; the first
  *                   min(max_blocks, capacity) entries are copied, where capacity is
- *                   ceil(max_tokens * k / 128) + E + 1; entries at or after the
- *                   block count are unspecified
+ *                   ceil(max_tokens * k / MOE_GROUPED_BLOCK_ROWS) + E + 1; entries at or
+ *                   after the block count are unspecified
  *   num_blocks_dev  int32 [1] device: the block count written by the dispatch
  * Either pointer may be NULL. max_blocks < 0 is MOE_ERR_INVALID_ARG. Enqueued on
  * `stream`.
  */
+#define MOE_GROUPED_BLOCK_ROWS 128
 moe_status_t moe_layer_get_block_map(moe_layer_t* layer, int32_t* blocks_dev, int32_t max_blocks,
                                      int32_t* num_blocks_dev, void* stream);
 

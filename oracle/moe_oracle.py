@@ -269,6 +269,28 @@ def valid_topk(logits: np.ndarray, idx: np.ndarray, slack: float) -> np.ndarray:
 # ----------------------------------------------------------------------------
 
 
+def tile_plan(hist: np.ndarray, block_rows: int = 128, half_rows: int = 128) -> np.ndarray:
+    """Tiles by expert load ("Optimizing on-device inference for Apple Silicon",
+    section "Match tile size to expert load"): each expert's grouped rows are cut
+    into blocks of block_rows rows (the last block of an expert holds the rest),
+    and a block is computed as as many half_rows-row parts as it holds rows for.
+    The grouped GEMMs use block_rows = half_rows = 128: one 128-row tile per block,
+    so tiles follow each expert's own row count.
+
+    Returns int64 [n, 4]: (expert, first grouped row, rows in the block, halves),
+    in increasing expert order, then increasing first row.
+    """
+    hist = np.asarray(hist, dtype=np.int64)
+    plan = []
+    row = 0
+    for e, n in enumerate(hist):
+        for r0 in range(0, int(n), block_rows):
+            rows = min(block_rows, int(n) - r0)
+            plan.append((e, row + r0, rows, -(-rows // half_rows)))
+        row += int(n)
+    return np.array(plan, dtype=np.int64).reshape(-1, 4)
+
+
 def dispatch(idx: np.ndarray, E: int, block_rows: int) -> dict:
     """Group the (token, slot) assignments by expert.
 

@@ -28,6 +28,7 @@ MOE_WEIGHTS_INT4 = 2
 MOE_FLAG_FORCE_GROUPED = 0x1
 MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT = 0x100
 MOE_DECODE_MAX_T = 8
+MOE_GROUPED_BLOCK_ROWS = 128
 
 MOE_PATH_NONE = 0
 MOE_PATH_DECODE_GEMV = 1

@@ -55,6 +55,7 @@ namespace {
 using namespace sm100;
 
 constexpr int BM = 128;                  // rows (tokens) per tile = TMEM lanes
+static_assert(BM == MOE_GROUPED_BLOCK_ROWS, "block map rows of the C ABI");
 constexpr int BK = 64;                   // bf16 per 128-byte swizzle row
 constexpr int kStages = 4;
 constexpr int kStageA = BM * BK * 2;     // 16 KB

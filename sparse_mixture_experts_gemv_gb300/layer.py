@@ -130,7 +130,8 @@ class MoeLayer:
 
     def block_map(self, T: int, stream=None):
         """(blocks int32 [n, 2] of (expert, first grouped row), n) of the last grouped forward."""
-        cap = (self.max_tokens * self.k + 127) // 128 + self.E + 1
+        rows = N.MOE_GROUPED_BLOCK_ROWS
+        cap = (self.max_tokens * self.k + rows - 1) // rows + self.E + 1
         blocks = torch.full((cap, 2), -1, dtype=torch.int32, device=self.device)
         n = torch.zeros(1, dtype=torch.int32, device=self.device)
         s = (stream or torch.cuda.current_stream(self.device)).cuda_stream

@@ -16,15 +16,19 @@ FORCE = 0x1  # MOE_FLAG_FORCE_GROUPED
 
 def _check_dispatch(L, T, k, E, idx):
     hist, offs, perm, pos = (a.cpu().numpy().astype(np.int64) for a in L.dispatch(T))
-    ref = o.dispatch(idx, E, 128)
+    from sparse_mixture_experts_gemv_gb300 import _native as N
+    ref = o.dispatch(idx, E, N.MOE_GROUPED_BLOCK_ROWS)
     assert (hist == ref["hist"]).all()
     assert (offs == ref["offsets"]).all()
     assert (perm == ref["perm"]).all()           # bit-exact: token order within each expert
     assert (pos == ref["pos"].reshape(-1)).all()
-    # the block map the grouped GEMMs take as M tiles: (expert, first grouped row), bit-exact
+    # the block map the grouped GEMMs take as M tiles: (expert, first grouped row), bit-exact,
+    # and the oracle's tile plan by expert load gives the same blocks
     blocks, nb = L.block_map(T)
     assert nb == len(ref["blocks"]), (nb, len(ref["blocks"]))
     assert (blocks.cpu().numpy().astype(np.int64) == ref["blocks"]).all()
+    plan = o.tile_plan(hist, N.MOE_GROUPED_BLOCK_ROWS, N.MOE_GROUPED_BLOCK_ROWS)
+    assert (plan[:, :2] == blocks.cpu().numpy().astype(np.int64)).all()
 
 
 def test_tiny_forced_grouped_t8():
@@ -38,7 +42,7 @@ def test_tiny_forced_grouped_t8():
     _check_dispatch(L, 8, 2, 16, idx)
 
 
-@pytest.mark.parametrize("T", [1, 9, 100, 127, 128, 129, 300, 512])
+@pytest.mark.parametrize("T", [1, 9, 100, 127, 128, 129, 255, 256, 257, 300, 512])
 def test_tiny_grouped_ragged(T):
     spec = mi.WORKLOADS["tiny"].layer
     L = G.cuda_layer(spec, max_tokens=512, flags=FORCE)

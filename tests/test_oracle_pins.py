@@ -397,3 +397,30 @@ def test_worked_example_int4():
     for i, s in ex["out_nonzero"].items():
         want[0, int(i)] = _expr(s)
     np.testing.assert_allclose(r["out"], want, rtol=1e-14, atol=1e-15)
+
+
+def test_tile_plan_covers_every_row_once_and_follows_the_load():
+    """The tile plan by expert load: every grouped row in exactly one block, blocks
+    of at most block_rows rows in expert then row order, one part per half_rows
+    rows; equal to the dispatch's block list (256-row blocks of 128-row parts here,
+    128-row blocks of one part as the grouped GEMMs use them)."""
+    rng = np.random.default_rng(3)
+    E, T, k = 40, 700, 4
+    idx = np.stack([rng.choice(E, size=k, replace=False, p=np.arange(1, E + 1)[::-1] / (E * (E + 1) / 2))
+                    for _ in range(T)])
+    d = o.dispatch(idx, E, 256)
+    plan = o.tile_plan(d["hist"], 256, 128)
+    assert (plan[:, :2] == d["blocks"]).all()
+    covered = np.zeros(T * k, dtype=np.int64)
+    for e, r0, rows, halves in plan:
+        assert 1 <= rows <= 256 and halves == (1 if rows <= 128 else 2)
+        assert d["offsets"][e] <= r0 and r0 + rows <= d["offsets"][e + 1]
+        covered[r0:r0 + rows] += 1
+    assert (covered == 1).all()
+    # hand-made histogram: 0, 1, 128, 129, 256, 257 rows
+    plan = o.tile_plan(np.array([0, 1, 128, 129, 256, 257]), 256, 128)
+    assert plan.tolist() == [[1, 0, 1, 1], [2, 1, 128, 1], [3, 129, 129, 2], [4, 258, 256, 2],
+                             [5, 514, 256, 2], [5, 770, 1, 1]]
+    d128 = o.dispatch(idx, E, 128)
+    plan = o.tile_plan(d128["hist"])
+    assert (plan[:, :2] == d128["blocks"]).all() and (plan[:, 3] == 1).all()
