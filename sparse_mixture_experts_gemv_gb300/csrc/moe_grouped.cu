@@ -432,32 +432,43 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
     }
   } else if (GATHER && warp < 10) {
     // ------------------------------------------------------------ A gather (gate/up)
-    const int r = threadIdx.x - 192;   // tile row this thread copies
+    // Eight threads copy one 128-byte row of a stage (thread j of the eight takes
+    // 16-byte chunk j), so one cp.async instruction of a warp covers four whole
+    // rows (four cache lines) instead of one chunk of 32 different rows: the
+    // gather is bound by L1TEX requests. Thread t copies chunk t % 8 of rows
+    // t / 8 + 16 i, i = 0..7.
+    const int tid = threadIdx.x - 192;
+    const int jc = tid & 7, rb = tid >> 3;
     uint32_t it = 0;
     int pending = -1;
     for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
       const TileInfo ti = decode_tile(p, R, tile);
-      const int gr = ti.row0 + r;
-      int token = -1;
-      if (gr < ti.row_end) {
-        if (ti.shared) {
-          token = gr;
-        } else {
-          const int a = p.perm[gr];
-          if (a >= 0 && a < p.T * p.k) token = a / p.k;
-          else set_error(p.err, kDevCheck);
-        }
-      }
       const uint16_t* xa = (MXB && !ti.shared) ? p.x16 : p.x;  // routed 4-bit tiles take f16 rows
-      const uint16_t* src = xa + (size_t)(token < 0 ? 0 : token) * p.H;
-      const uint32_t nbytes = token < 0 ? 0u : 16u;
+      const uint16_t* src[8];
+      uint32_t nbytes[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int gr = ti.row0 + rb + 16 * i;
+        int token = -1;
+        if (gr < ti.row_end) {
+          if (ti.shared) {
+            token = gr;
+          } else {
+            const int a = p.perm[gr];
+            if (a >= 0 && a < p.T * p.k) token = a / p.k;
+            else set_error(p.err, kDevCheck);
+          }
+        }
+        src[i] = xa + (size_t)(token < 0 ? 0 : token) * p.H + 8 * jc;
+        nbytes[i] = token < 0 ? 0u : 16u;   // rows past the group's end are written as zeros
+      }
       bool ok = true;
       for (int kb = 0; kb < ti.ks; ++kb, ++it) {
         const int s = it % kStages;
         if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, p.err, abort_flag)) { ok = false; break; }
-        uint8_t* dst = sA + s * kStageA + r * 128;
+        uint8_t* dst = sA + s * kStageA + ((jc ^ (rb & 7)) << 4);   // (rb + 16 i) % 8 == rb % 8
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cp_async_16(dst + ((j ^ (r & 7)) << 4), src + kb * BK + j * 8, nbytes);
+        for (int i = 0; i < 8; ++i) cp_async_16(dst + (rb + 16 * i) * 128, src[i] + kb * BK, nbytes[i]);
         cp_async_commit();
         if (pending >= 0) {
           cp_async_wait<1>();
