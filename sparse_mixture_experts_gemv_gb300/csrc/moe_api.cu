@@ -182,6 +182,18 @@ __global__ void mx_down_scales_kernel(const uint8_t* __restrict__ ds, uint8_t* _
   }
 }
 
+// Groupwise affine int4 down (scale, bias) pairs [E][H][I/64] -> one vector of H
+// pairs per (expert, 64 features): out[e][blk][n] = scale | bias << 16.
+__global__ void i4_down_vectors_kernel(const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
+                                       uint32_t* __restrict__ out, int E, int H, int nblk) {
+  const size_t total = (size_t)E * nblk * H;
+  for (size_t o = blockIdx.x * (size_t)blockDim.x + threadIdx.x; o < total; o += (size_t)gridDim.x * blockDim.x) {
+    const size_t n = o % H, eb = o / H, blk = eb % nblk, e = eb / nblk;
+    const size_t q = (e * H + n) * nblk + blk;
+    out[o] = (uint32_t)scales[q] | ((uint32_t)biases[q] << 16);
+  }
+}
+
 // Groupwise affine int4: the (scale, bias) bf16 pair of group g of each row goes
 // to bytes [off + 4g, off + 4g + 4) of the row's record (scale first).
 __global__ void i4_group_params_kernel(const uint16_t* __restrict__ scales, const uint16_t* __restrict__ biases,
@@ -342,7 +354,9 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
   // the gate row, the up row and the down column, contiguous (6H bytes).
   const bool bf16_stream = c.weight_format == MOE_WEIGHTS_BF16 && H <= moe::kStreamMaxHidden;
   const bool mx_stream = c.weight_format == MOE_WEIGHTS_MXFP4 && H <= moe::kStreamMxMaxHidden && H % 512 == 0;
-  if (bf16_stream || mx_stream) {
+  const bool i4_stream = c.weight_format == MOE_WEIGHTS_INT4 && H <= moe::kStreamMxMaxHidden && H % 512 == 0 &&
+                         I % 64 == 0;
+  if (bf16_stream || mx_stream || i4_stream) {
     const size_t row = (size_t)H * 2, rec = (size_t)moe::stream_record_stride((int)H);
     dim3 block(32, 8);
     if (bf16_stream) {
@@ -352,6 +366,33 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
       MOE_CUDA(cudaMemcpy2D(L.w_rec + row, rec, w->up_dev, row, row, (size_t)E * I, cudaMemcpyDeviceToDevice));
       dim3 grid((unsigned)((I + 31) / 32), (unsigned)((H + 31) / 32), (unsigned)E);
       down_to_columns_kernel<<<grid, block>>>((const uint16_t*)w->down_dev, L.w_rec, (int)H, (int)I, (int)rec);
+      MOE_CUDA(cudaGetLastError());
+    } else if (i4_stream) {
+      // int4 records: gate codes | up codes (block-shuffled as for MXFP4) | gate
+      // (s, b) pairs | up (s, b) pairs (one 4-byte pair per 64 elements, padded
+      // to 16) | down column codes; down pairs apart, one vector per (e, 64 features)
+      const size_t i4s = (size_t)moe::stream_i4_record_stride((int)H);
+      const size_t so = (size_t)((H / 16 + 15) / 16 * 16), nblk = (size_t)I / 64;
+      const size_t rows = (size_t)E * I;
+      GET(L.w_mx, rows * i4s);
+      GET(L.mx_dsc, (size_t)E * nblk * H * 4);
+      MOE_CUDA(cudaMemset(L.w_mx, 0, rows * i4s));
+      mx_shuffle_codes_kernel<<<1024, 256>>>((const uint8_t*)w->gate_dev, L.w_mx, rows, (int)H, (int)i4s, 0);
+      MOE_CUDA(cudaGetLastError());
+      mx_shuffle_codes_kernel<<<1024, 256>>>((const uint8_t*)w->up_dev, L.w_mx, rows, (int)H, (int)i4s, (int)(H / 2));
+      MOE_CUDA(cudaGetLastError());
+      i4_group_params_kernel<<<1024, 256>>>((const uint16_t*)w->gate_scales_dev, (const uint16_t*)w->gate_biases_dev,
+                                            L.w_mx, rows, (int)(H / 64), (int64_t)i4s, H);
+      MOE_CUDA(cudaGetLastError());
+      i4_group_params_kernel<<<1024, 256>>>((const uint16_t*)w->up_scales_dev, (const uint16_t*)w->up_biases_dev,
+                                            L.w_mx, rows, (int)(H / 64), (int64_t)i4s, (int64_t)(H + so));
+      MOE_CUDA(cudaGetLastError());
+      dim3 g2((unsigned)(I / 64), (unsigned)(H / 64), (unsigned)E);
+      mx_down_to_columns_kernel<<<g2, 256>>>((const uint8_t*)w->down_dev, L.w_mx, (int)H, (int)I, (int)i4s,
+                                             (int)(H + 2 * so));
+      MOE_CUDA(cudaGetLastError());
+      i4_down_vectors_kernel<<<1024, 256>>>((const uint16_t*)w->down_scales_dev, (const uint16_t*)w->down_biases_dev,
+                                            reinterpret_cast<uint32_t*>(L.mx_dsc), (int)E, (int)H, (int)nblk);
       MOE_CUDA(cudaGetLastError());
     } else {
       // MXFP4 records: gate codes | up codes | gate scales | up scales | down column codes
@@ -465,9 +506,13 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
                  "[gate|up|down column] records of the shared and routed experts with the down projection fused, "
                  "partial-output exchange)"
                : moe::stream_mx_supported(&L, 1)
-               ? "moe_decode_stream_mx_kernel (cooperative: router with tagged logits, per-CTA top-k, bulk-copied "
-                 "MXFP4 [gate|up|down column] records decoded in registers, bf16 shared-expert records, "
-                 "partial-output exchange)"
+               ? (cfg->weight_format == MOE_WEIGHTS_INT4
+                      ? "moe_decode_stream_mx_kernel<int4> (cooperative: router with tagged logits, per-CTA top-k, "
+                        "bulk-copied int4 [gate|up|down column] records as exact f16 integers on the tensor cores, "
+                        "s * sum(q x) + b * sum(x) per group, bf16 shared-expert records, partial-output exchange)"
+                      : "moe_decode_stream_mx_kernel (cooperative: router with tagged logits, per-CTA top-k, "
+                        "bulk-copied MXFP4 [gate|up|down column] records decoded in registers, bf16 shared-expert "
+                        "records, partial-output exchange)")
                : (cfg->weight_format == MOE_WEIGHTS_MXFP4
                       ? "moe_decode_fused_kernel<mxfp4> (cooperative: router+shared, routed gate/up, down+combine)"
                       : cfg->weight_format == MOE_WEIGHTS_INT4

@@ -87,10 +87,12 @@ struct moe_layer {
                          // H each) + zero padding: stream_record_stride(H) bytes
                          // (bf16 layers with H <= kStreamMaxHidden; nullptr otherwise)
   uint8_t* ws_rec;       // shared-expert records [Is], same record format (also for MXFP4 layers)
-  uint8_t* w_mx;         // MXFP4 routed records [E][I], stream_mx_record_stride(H) bytes each:
+  uint8_t* w_mx;         // 4-bit routed records [E][I] of the MXFP4 / int4 streaming kernel:
                          // gate codes | up codes | gate scales | up scales | down column codes
-                         // (code orders for the tensor-core fragments, moe_stream_common.cuh)
-  uint8_t* mx_dsc;       // MXFP4 down scales [E][I / 32][H] (one H-byte vector per 32 features)
+                         // (code orders for the tensor-core fragments, moe_stream_common.cuh);
+                         // MXFP4 stream_mx_record_stride(H) bytes each, int4 stream_i4_record_stride(H)
+  uint8_t* mx_dsc;       // down scales: MXFP4 [E][I / 32][H] bytes (one H-byte vector per 32 features),
+                         // int4 [E][I / 64][H] (scale, bias) bf16 pairs
   moe::RowBytes row_bytes;
 
   moe::DecodeWorkspace dec;
@@ -135,6 +137,7 @@ int stream_record_stride(int H);          // bytes per routed/shared record (6H 
 // Record-streaming decode kernel for MXFP4 routed experts (moe_stream_mx.cu).
 bool stream_mx_supported(const moe_layer* L, int T);
 int stream_mx_record_stride(int H);       // bytes per routed MXFP4 record
+int stream_i4_record_stride(int H);       // bytes per routed groupwise affine int4 record (same kernel)
 cudaError_t stream_mx_prepare(moe_layer* L);
 cudaError_t launch_stream_mx(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* logit_bias,
                              cudaStream_t s);

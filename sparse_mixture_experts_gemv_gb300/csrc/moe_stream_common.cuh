@@ -279,6 +279,132 @@ MOE_DEV void mx_down_tiles(const uint8_t* gbase, int stride, int nvalid, const M
   }
 }
 
+// ---------------------------------------------------------------------------
+// Groupwise affine int4 records on the tensor cores ("Optimizing on-device
+// inference for Apple Silicon", section "Decode weights during matrix
+// multiplication": 4-bit weights with a bf16 scale and bias per group of 64,
+// value q * s + b, q unsigned). The record layout is the MXFP4 one (codes
+// block-shuffled the same way, down columns in the same paired 16-row tiles);
+// the scale segments hold one 4-byte (s, b) pair (s in the low half) per 64
+// elements, and the down columns' pairs live in vectors of H pairs per
+// (expert, 64 features). A dot product over a 32-element block is
+// s * sum(q x) + b * sum(x): the tensor cores take q exactly as f16 integers,
+// and sum(x) of every block and token is staged once per call.
+// ---------------------------------------------------------------------------
+// Two unsigned 4-bit codes of one byte (element 2i in the low nibble) -> f16x2,
+// exact: 0x6400 | q is the f16 1024 + q, and 1024 is subtracted in f16.
+MOE_DEV uint32_t u4x2_to_f16x2(uint32_t byte) {
+  const uint32_t w = 0x64006400u | (byte & 0x0Fu) | ((byte & 0xF0u) << 12);
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0x64006400u));
+  return r;
+}
+
+// One warp's part of the gate/up tiles of up to 16 int4 records, as
+// mx_gu_tiles: each block's two k-steps go to a fresh accumulator d, then
+// out += s * d + b * sum(x of the block) per (row, token). xsum: fp32
+// [token][block], tokens XSP floats apart.
+template <int MAXMT, int NBLK>
+MOE_DEV void i4_gu_tiles(const uint8_t* gbase, int stride, int nvalid, int nmt, const MxLayout& ly, int T, int XP,
+                         const uint16_t* x16, const float* xsum, int XSP, int blk0, float (&out)[MAXMT][4]) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
+#pragma unroll
+  for (int m = 0; m < MAXMT; ++m) out[m][0] = out[m][1] = out[m][2] = out[m][3] = 0.f;
+#pragma unroll
+  for (int bi = 0; bi < NBLK; ++bi) {
+    const int blk = blk0 + bi;
+    uint32_t b[2][2] = {{0u, 0u}, {0u, 0u}};
+    if (gq < T) {
+      const uint16_t* xr = x16 + gq * XP + 32 * blk + 2 * cq;
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        b[ks][0] = *reinterpret_cast<const uint32_t*>(xr + 16 * ks);
+        b[ks][1] = *reinterpret_cast<const uint32_t*>(xr + 16 * ks + 8);
+      }
+    }
+    const float xs0 = 2 * cq < T ? xsum[(2 * cq) * XSP + blk] : 0.f;
+    const float xs1 = 2 * cq + 1 < T ? xsum[(2 * cq + 1) * XSP + blk] : 0.f;
+#pragma unroll
+    for (int m = 0; m < MAXMT; ++m) {
+      if (m < nmt) {
+        const int r = 8 * m + gq;
+        uint32_t gw = 0u, uw = 0u, gp = 0u, up = 0u;
+        if (r < nvalid) {
+          const uint8_t* rec = gbase + (size_t)r * stride;
+          gw = *reinterpret_cast<const uint32_t*>(rec + 16 * blk + 4 * cq);
+          uw = *reinterpret_cast<const uint32_t*>(rec + ly.up_codes + 16 * blk + 4 * cq);
+          gp = *reinterpret_cast<const uint32_t*>(rec + ly.gate_scales + 4 * (blk >> 1));
+          up = *reinterpret_cast<const uint32_t*>(rec + ly.up_scales + 4 * (blk >> 1));
+        }
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          mma_16816_f16(d, u4x2_to_f16x2(gw >> (16 * ks)), u4x2_to_f16x2(uw >> (16 * ks)),
+                        u4x2_to_f16x2(gw >> (16 * ks + 8)), u4x2_to_f16x2(uw >> (16 * ks + 8)), b[ks][0], b[ks][1]);
+        const float gs = bf16_lo(gp), gb = bf16_hi(gp), us = bf16_lo(up), ub = bf16_hi(up);
+        out[m][0] = fmaf(gs, d[0], fmaf(gb, xs0, out[m][0]));
+        out[m][1] = fmaf(gs, d[1], fmaf(gb, xs1, out[m][1]));
+        out[m][2] = fmaf(us, d[2], fmaf(ub, xs0, out[m][2]));
+        out[m][3] = fmaf(us, d[3], fmaf(ub, xs1, out[m][3]));
+      }
+    }
+  }
+}
+
+// Sums over the records of c' (the same B fragments as the down tiles): an mma
+// against an all-ones A fragment, so each lane gets sum_r c'[r][2cq] and
+// sum_r c'[r][2cq + 1].
+MOE_DEV void colsum_f16(const uint32_t (&bh)[2], const uint32_t (&bl)[2], float& s0, float& s1) {
+  float d[4] = {0.f, 0.f, 0.f, 0.f};
+  constexpr uint32_t one2 = 0x3C003C00u;   // f16 pair (1, 1)
+  mma_16816_f16(d, one2, one2, one2, one2, bh[0], bh[1]);
+  mma_16816_f16(d, one2, one2, one2, one2, bl[0], bl[1]);
+  s0 = d[0];
+  s1 = d[1];
+}
+
+// One warp's output tiles of the down projection of up to 16 int4 records, as
+// mx_down_tiles: d = sum_r q[n][r] c'[r][t], then per row n of vector v,
+// acc += s_n * 2^cexp * d + b_n * csum[v][t] (csum: the unscaled sums of c
+// over the vector's records for tokens 2cq, 2cq + 1).
+template <int NTILE>
+MOE_DEV void i4_down_tiles(const uint8_t* gbase, int stride, int nvalid, const MxLayout& ly, int nv,
+                           const uint32_t* pv0, const uint32_t* pv1, float cexp2, const uint32_t (&bh)[2][2],
+                           const uint32_t (&bl)[2][2], const float (&csum)[2][2], float (&acc)[NTILE][4]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, gq = lane >> 2, cq = lane & 3;
+  const uint8_t* pa = gbase + (size_t)(2 * cq) * stride + ly.down_tiles + 2 * gq;
+  const uint8_t* pb = pa + (size_t)8 * stride;
+  const bool va = 2 * cq < nvalid, vb = 2 * cq + 8 < nvalid;
+#pragma unroll
+  for (int j = 0; j < NTILE; ++j) {
+    const int tt = warp + kConsumerWarps * j, n0 = 16 * tt;
+    constexpr int kHalf = NTILE / 2;
+    const int sel = j >= kHalf ? 1 : 0;
+    const int off = sel * stride + 16 * (warp + kConsumerWarps * (j - sel * kHalf));
+    const uint32_t ua = va ? *reinterpret_cast<const uint16_t*>(pa + off) : 0u;
+    const uint32_t ub = vb ? *reinterpret_cast<const uint16_t*>(pb + off) : 0u;
+    const uint32_t a0 = u4x2_to_f16x2(ua);        // row n0+g
+    const uint32_t a1 = u4x2_to_f16x2(ua >> 8);   // row n0+g+8
+    const uint32_t a2 = u4x2_to_f16x2(ub);
+    const uint32_t a3 = u4x2_to_f16x2(ub >> 8);
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+      if (v < nv) {
+        const uint32_t* pv = v ? pv1 : pv0;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816_f16(d, a0, a1, a2, a3, bh[v][0], bh[v][1]);
+        mma_16816_f16(d, a0, a1, a2, a3, bl[v][0], bl[v][1]);
+        const uint32_t p0 = pv[n0 + gq], p1 = pv[n0 + gq + 8];
+        const float s0 = bf16_lo(p0) * cexp2, b0 = bf16_hi(p0), s1 = bf16_lo(p1) * cexp2, b1 = bf16_hi(p1);
+        acc[j][0] = fmaf(s0, d[0], fmaf(b0, csum[v][0], acc[j][0]));
+        acc[j][1] = fmaf(s0, d[1], fmaf(b0, csum[v][1], acc[j][1]));
+        acc[j][2] = fmaf(s1, d[2], fmaf(b1, csum[v][0], acc[j][2]));
+        acc[j][3] = fmaf(s1, d[3], fmaf(b1, csum[v][1], acc[j][3]));
+      }
+    }
+  }
+}
+
 // c as an f16 hi + lo pair (packed with its neighbour) after scaling by s.
 MOE_DEV void f16_hilo2(float c0, float c1, float s, uint32_t& hi, uint32_t& lo) {
   const __half2 h = __floats2half2_rn(c0 * s, c1 * s);

@@ -72,6 +72,14 @@ constexpr int kMxMaxH = kStreamMxMaxHidden;   // output tiles per warp kept in r
 // tokens at H = 2560.
 constexpr int kMxSmemMax = 207 * 1024;
 static_assert(kMxSmemMax + 19584 <= 232448, "static + dynamic shared memory of one block");
+// Routed record formats of this kernel: MXFP4 (e2m1 codes, one e8m0 scale per
+// 32 elements) and groupwise affine int4 (q * s + b, one bf16 (s, b) pair per
+// 64 elements). The int4 instantiations also stage sum(x) per 32-element block
+// (2,560 bytes of static shared memory), so their dynamic budget is 3 KB lower.
+enum StreamQ { Q_MXFP4 = 0, Q_INT4 = 1 };
+constexpr int kI4SmemMax = kMxSmemMax - 3 * 1024;
+constexpr int kMaxXBlocks = kStreamMxMaxHidden / 32;
+template <int Q> constexpr int smem_budget() { return Q == Q_INT4 ? kI4SmemMax : kMxSmemMax; }
 
 struct MxArgs {
   const uint16_t* x;           // bf16 [T][H]
@@ -80,7 +88,7 @@ struct MxArgs {
   const float* router_bias;    // fp32 [E]
   const float* logit_bias;     // fp32 [T][E] or nullptr
   const uint8_t* rec;          // routed MXFP4 records [E][I] x mx_stride bytes
-  const uint8_t* dsc;          // down scales [E][I / 32][H] bytes
+  const uint8_t* dsc;          // down scale vectors: MXFP4 [E][I / 32][H] bytes, int4 [E][I / 64][H] (s, b) pairs
   const uint8_t* rec_sh;       // shared-expert bf16 records [Is] x sh_stride bytes
   int mx_stride, sh_stride;    // bytes per record
   int sc_off;                  // padded bytes of one scale segment (pad16(H / 32))
@@ -106,8 +114,11 @@ struct MxArgs {
 // NT = H / 256: output tiles per warp, bf16 gate/up k-steps per warp (shared
 // records) and twice the MXFP4 blocks per warp, fixed at compile time so that
 // the tile loops are straight-line code.
-template <int TMAX, int NT>
+template <int TMAX, int NT, int Q>
 __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kernel(const MxArgs a) {
+  constexpr bool kI4 = Q == Q_INT4;
+  constexpr int kVecFeat = kI4 ? 64 : 32;             // features sharing one down-scale vector
+  const int vbytes = kI4 ? 4 * a.H : a.H;             // bytes of one down-scale vector
   extern __shared__ __align__(128) uint8_t smem[];
   // An error word left set by an earlier call means the layer's cross-CTA
   // counters and tagged words may be mid-generation: do nothing (outputs stay
@@ -125,6 +136,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
   __shared__ __align__(16) float s_part[kConsumerWarps][kMaxMt][16][8];   // gate/up partial tiles
   __shared__ float s_cf[8][kMaxMx];                                 // c = w * silu(g) * u, [token][record]
   __shared__ unsigned s_cmax[2];                                    // largest |c| of a group (bits), by parity
+  __shared__ float s_xsum[kI4 ? kMaxDecodeT * kMaxXBlocks : 1];     // int4: sum of x per (token, 32-block)
   __shared__ __align__(16) uint16_t s_zero[8];                      // a zero row for missing bf16 records
   __shared__ stream::RouteSmem rs;
   __shared__ unsigned long long s_tag;
@@ -139,7 +151,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
   const int mxs = a.mx_stride, shs = a.sh_stride;
   const int RGM = a.mx_group;
   const int sv_off = RGM * mxs;                      // scale vectors of a routed group, in its slot
-  const int nblk = I / 32;
+  const int nblk = I / kVecFeat;                      // down-scale vectors per expert
   const bool producer = (warp == kConsumerWarps);
 
   if (threadIdx.x == 0) {
@@ -164,7 +176,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
   // (slot, block) of routed unit u: which down-scale vector it needs
   auto unit_blk = [&](int u, int& d, int& blk) {
     d = (int)((unsigned)u / (unsigned)I);
-    blk = (u - d * I) / 32;
+    blk = (u - d * I) / kVecFeat;
   };
   // Whole producer warp: lane 0 posts the group's byte count and issues its copies.
   auto issue_group = [&](int grp, int u0, int nr) {
@@ -181,7 +193,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
         unit_blk(u0 + first, d0, b0);
         unit_blk(u0 + first + n - 1, dl, bl);
         const bool two = (dl != d0 || bl != b0);
-        sm100::mbar_arrive_expect_tx(&full_bar[sg], (uint32_t)(n * mxs + (two ? 2 : 1) * H));
+        sm100::mbar_arrive_expect_tx(&full_bar[sg], (uint32_t)(n * mxs + (two ? 2 : 1) * vbytes));
         uint8_t* dst = base;
         unsigned u = (unsigned)(u0 + first);
         int left = n;
@@ -194,11 +206,11 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
           u += run;
           left -= run;
         }
-        sm100::bulk_copy_g2s(base + sv_off, a.dsc + ((size_t)rs.meta.slot_expert[d0] * nblk + b0) * H, (uint32_t)H,
-                             &full_bar[sg]);
+        sm100::bulk_copy_g2s(base + sv_off, a.dsc + ((size_t)rs.meta.slot_expert[d0] * nblk + b0) * vbytes,
+                             (uint32_t)vbytes, &full_bar[sg]);
         if (two)
-          sm100::bulk_copy_g2s(base + sv_off + H, a.dsc + ((size_t)rs.meta.slot_expert[dl] * nblk + bl) * H,
-                               (uint32_t)H, &full_bar[sg]);
+          sm100::bulk_copy_g2s(base + sv_off + vbytes, a.dsc + ((size_t)rs.meta.slot_expert[dl] * nblk + bl) * vbytes,
+                               (uint32_t)vbytes, &full_bar[sg]);
       }
     }
     __syncwarp();
@@ -237,6 +249,16 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
       *reinterpret_cast<__half2*>(x16 + t * XP + 2 * c) = h;
     }
     if (x_range) set_error(a.err, kDevCheck);
+    if constexpr (kI4) {   // sum(x) of every 32-element block and token, fp32 in a fixed order
+      for (int q = threadIdx.x; q < T * (H / 32); q += kConsumers) {
+        const int t = q / (H / 32), blk = q - t * (H / 32);
+        const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs + t * XP + 32 * blk);
+        float sm = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sm += bf16_lo(xw[i]) + bf16_hi(xw[i]);
+        s_xsum[t * kMaxXBlocks + blk] = sm;
+      }
+    }
     stream::route_window(a.words, T, E, k, tag, rs, a.err, &s_abort);
   }
   __syncthreads();   // routing and the f16 x known to every warp
@@ -313,7 +335,11 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
         stream::bf16_gu_tile<NT>(sm100::smem_u32(base), shs, nvalid, H, T, XP, xs_u32, zero_u32,
                                  warp * (H / kConsumerWarps), NT, d[0]);
       } else {
-        stream::mx_gu_tiles<kMaxMt, nbw>(base, mxs, nvalid, (nvalid + 7) / 8, ly, T, XP, x16, warp * nbw, d);
+        if constexpr (kI4)
+          stream::i4_gu_tiles<kMaxMt, nbw>(base, mxs, nvalid, (nvalid + 7) / 8, ly, T, XP, x16, s_xsum, kMaxXBlocks,
+                                           warp * nbw, d);
+        else
+          stream::mx_gu_tiles<kMaxMt, nbw>(base, mxs, nvalid, (nvalid + 7) / 8, ly, T, XP, x16, warp * nbw, d);
       }
       const int nmt = shared ? 1 : (nvalid + 7) / 8;
 #pragma unroll
@@ -372,7 +398,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
       // records [0, r1) use the group's first down-scale vector, [r1, nvalid)
       // the second: a new vector starts at the next multiple of 32 features
       const int i0 = (rg.u0 + first) - (int)((unsigned)(rg.u0 + first) / (unsigned)I) * I;
-      const int r1 = min(nvalid, 32 - (i0 & 31));
+      const int r1 = min(nvalid, kVecFeat - (i0 & (kVecFeat - 1)));
       const float* cr = s_cf[gq];
       const int nv = r1 < nvalid ? 2 : 1;
       uint32_t bh[2][2], bl[2][2];
@@ -383,8 +409,22 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
         stream::f16_hilo2(cv(2 * cq), cv(2 * cq + 1), down, bh[v][0], bl[v][0]);
         stream::f16_hilo2(cv(2 * cq + 8), cv(2 * cq + 9), down, bh[v][1], bl[v][1]);
       }
-      stream::mx_down_tiles<NT>(base, mxs, nvalid, ly, nv, base + sv_off, base + sv_off + H, up, bh,
-                                         bl, acc);
+      if constexpr (kI4) {
+        float csum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};   // sum of c over each vector's records, tokens 2cq, 2cq + 1
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          if (v < nv) {
+            float s0, s1;
+            stream::colsum_f16(bh[v], bl[v], s0, s1);
+            csum[v][0] = s0 * up;
+            csum[v][1] = s1 * up;
+          }
+        }
+        stream::i4_down_tiles<NT>(base, mxs, nvalid, ly, nv, reinterpret_cast<const uint32_t*>(base + sv_off),
+                                  reinterpret_cast<const uint32_t*>(base + sv_off + vbytes), up, bh, bl, csum, acc);
+      } else {
+        stream::mx_down_tiles<NT>(base, mxs, nvalid, ly, nv, base + sv_off, base + sv_off + H, up, bh, bl, acc);
+      }
     }
     __syncwarp();
     if (lane == 0) sm100::mbar_arrive(&empty_bar[sg]);
@@ -421,39 +461,49 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
 // ===========================================================================
 // Host side
 // ===========================================================================
-static int mx_sc_off(int H) { return (H / 32 + 15) / 16 * 16; }
-int stream_mx_record_stride(int H) { return 3 * H / 2 + 2 * mx_sc_off(H) + 16; }
+// Bytes of one scale segment of a record: MXFP4 one e8m0 byte per 32 elements,
+// int4 one 4-byte (s, b) pair per 64 elements; padded to 16.
+static int q_sc_off(int Q, int H) { return (Q == Q_INT4 ? H / 16 : H / 32 + 15) / 16 * 16; }
+static int q_record_stride(int Q, int H) { return 3 * H / 2 + 2 * q_sc_off(Q, H) + 16; }
+int stream_mx_record_stride(int H) { return q_record_stride(Q_MXFP4, H); }
+int stream_i4_record_stride(int H) { return q_record_stride(Q_INT4, H); }
+static int q_vec_bytes(int Q, int H) { return Q == Q_INT4 ? 4 * H : H; }
+static int q_budget(int Q) { return Q == Q_INT4 ? kI4SmemMax : kMxSmemMax; }
 static int mx_x_bytes(int T, int H) { return (int)(((size_t)T * (H + 8) * 2 + 127) / 128 * 128); }
-static int mx_slot_bytes(int H, int rgm) {
-  const size_t routed = (size_t)rgm * stream_mx_record_stride(H) + 2 * (size_t)H;
+static int mx_slot_bytes(int Q, int H, int rgm) {
+  const size_t routed = (size_t)rgm * q_record_stride(Q, H) + 2 * (size_t)q_vec_bytes(Q, H);
   const size_t shared = (size_t)kShGroup * stream_record_stride(H);
   return (int)((std::max(routed, shared) + 127) / 128 * 128);
 }
-// 16 MXFP4 records per routed group when two such slots fit beside the two x copies, else 8.
-static int mx_group_records(int T, int H) {
-  const size_t room = (size_t)kMxSmemMax - 2 * (size_t)mx_x_bytes(T, H);
-  return room >= 2 * (size_t)mx_slot_bytes(H, kMaxMx) ? kMaxMx : kMaxMx / 2;
+// 16 records per routed group when two such slots fit beside the two x copies, else 8.
+static int mx_group_records(int Q, int T, int H) {
+  const size_t room = (size_t)q_budget(Q) - 2 * (size_t)mx_x_bytes(T, H);
+  return room >= 2 * (size_t)mx_slot_bytes(Q, H, kMaxMx) ? kMaxMx : kMaxMx / 2;
 }
-static int mx_ring_groups(const moe_layer* L, int T) {
+static int mx_ring_groups(const moe_layer* L, int Q, int T) {
   const int H = L->cfg.hidden;
   const size_t xb = 2 * (size_t)mx_x_bytes(T, H);
-  if (xb >= (size_t)kMxSmemMax) return 0;
-  return (int)std::min<size_t>((kMxSmemMax - xb) / mx_slot_bytes(H, mx_group_records(T, H)), kMaxRingGroups);
+  if (xb >= (size_t)q_budget(Q)) return 0;
+  return (int)std::min<size_t>((q_budget(Q) - xb) / mx_slot_bytes(Q, H, mx_group_records(Q, T, H)), kMaxRingGroups);
 }
+static int layer_q(const moe_layer* L) { return L->cfg.weight_format == MOE_WEIGHTS_INT4 ? Q_INT4 : Q_MXFP4; }
 
 bool stream_mx_supported(const moe_layer* L, int T) {
   const auto& c = L->cfg;
-  if (c.weight_format != MOE_WEIGHTS_MXFP4 || !L->w_mx || !L->mx_dsc || !L->ws_rec) return false;
+  if (c.weight_format != MOE_WEIGHTS_MXFP4 && c.weight_format != MOE_WEIGHTS_INT4) return false;
+  if (!L->w_mx || !L->mx_dsc || !L->ws_rec) return false;
+  const int Q = layer_q(L);
   // 16 warps x whole 32-element blocks of H in the gate/up tiles
   if (c.hidden > kMxMaxH || c.hidden % 512 != 0 || T < 1 || T > kMaxDecodeT) return false;
+  if (Q == Q_INT4 && c.intermediate % 64 != 0) return false;
   if ((c.num_experts + L->num_sms - 1) / L->num_sms > stream::kMaxRouterRows) return false;
-  const int ng = mx_ring_groups(L, T);
+  const int ng = mx_ring_groups(L, Q, T);
   if (ng < 2) return false;
   return stream::collect_f32_fits(L->num_sms, c.hidden, T,
-                                  (size_t)ng * mx_slot_bytes(c.hidden, mx_group_records(T, c.hidden)));
+                                  (size_t)ng * mx_slot_bytes(Q, c.hidden, mx_group_records(Q, T, c.hidden)));
 }
 
-template <int TMAX, int NT>
+template <int TMAX, int NT, int Q>
 static cudaError_t launch_stream_mx_t(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* lb,
                                       cudaStream_t s) {
   const auto& c = L->cfg;
@@ -462,19 +512,19 @@ static cudaError_t launch_stream_mx_t(moe_layer* L, const uint16_t* x, uint16_t*
   a.Is = c.shared_intermediate;
   a.router_t = L->router_t; a.router_bias = L->router_bias; a.logit_bias = lb;
   a.rec = L->w_mx; a.dsc = L->mx_dsc; a.rec_sh = L->ws_rec;
-  a.mx_stride = stream_mx_record_stride(c.hidden);
+  a.mx_stride = q_record_stride(Q, c.hidden);
   a.sh_stride = stream_record_stride(c.hidden);
-  a.sc_off = mx_sc_off(c.hidden);
-  a.mx_group = mx_group_records(T, c.hidden);
-  a.slot_bytes = mx_slot_bytes(c.hidden, a.mx_group);
-  a.ring_groups = mx_ring_groups(L, T);
+  a.sc_off = q_sc_off(Q, c.hidden);
+  a.mx_group = mx_group_records(Q, T, c.hidden);
+  a.slot_bytes = mx_slot_bytes(Q, c.hidden, a.mx_group);
+  a.ring_groups = mx_ring_groups(L, Q, T);
   a.x_bytes_al = mx_x_bytes(T, c.hidden);
   {
     // This CTA's router rows go by bulk copy into the shared memory behind the
     // ring when it has room, else the consumers load them from global memory.
     const size_t rbytes = (size_t)((c.num_experts + L->num_sms - 1) / L->num_sms) * c.hidden * 4;
     const size_t ring_end = 2 * (size_t)a.x_bytes_al + (size_t)a.ring_groups * a.slot_bytes;
-    a.router_off = ring_end + rbytes <= (size_t)kMxSmemMax ? (int)ring_end : -1;
+    a.router_off = ring_end + rbytes <= (size_t)q_budget(Q) ? (int)ring_end : -1;
   }
   a.words = L->dec.logit_words; a.partial = reinterpret_cast<float*>(L->dec.partial);
   a.ctr = L->dec.sync_ctr + 2; a.arrivals = L->dec.sync_ctr + 3;
@@ -496,51 +546,61 @@ static cudaError_t launch_stream_mx_t(moe_layer* L, const uint16_t* x, uint16_t*
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   prof_mark(L, s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_decode_stream_mx_kernel<TMAX, NT>, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, moe_decode_stream_mx_kernel<TMAX, NT, Q>, a);
   prof_mark(L, s);
   return e;
 }
 
-template <int NT, typename F>
+template <int NT, int Q, typename F>
 static void set_all(F& set) {
-  set((const void*)moe_decode_stream_mx_kernel<1, NT>);
-  set((const void*)moe_decode_stream_mx_kernel<2, NT>);
-  set((const void*)moe_decode_stream_mx_kernel<4, NT>);
-  set((const void*)moe_decode_stream_mx_kernel<8, NT>);
+  set((const void*)moe_decode_stream_mx_kernel<1, NT, Q>, q_budget(Q));
+  set((const void*)moe_decode_stream_mx_kernel<2, NT, Q>, q_budget(Q));
+  set((const void*)moe_decode_stream_mx_kernel<4, NT, Q>, q_budget(Q));
+  set((const void*)moe_decode_stream_mx_kernel<8, NT, Q>, q_budget(Q));
 }
 
 cudaError_t stream_mx_prepare(moe_layer* L) {
   (void)L;
   cudaError_t e = cudaSuccess;
-  auto set = [&](const void* f) {
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmemMax);
+  auto set = [&](const void* f, int bytes) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   };
-  set_all<2>(set);
-  set_all<4>(set);
-  set_all<6>(set);
-  set_all<8>(set);
-  set_all<10>(set);
+  set_all<2, Q_MXFP4>(set);
+  set_all<4, Q_MXFP4>(set);
+  set_all<6, Q_MXFP4>(set);
+  set_all<8, Q_MXFP4>(set);
+  set_all<10, Q_MXFP4>(set);
+  set_all<2, Q_INT4>(set);
+  set_all<4, Q_INT4>(set);
+  set_all<6, Q_INT4>(set);
+  set_all<8, Q_INT4>(set);
+  set_all<10, Q_INT4>(set);
   return e;
 }
 
-template <int NT>
+template <int NT, int Q>
 static cudaError_t launch_stream_mx_nt(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* lb,
                                        cudaStream_t s) {
-  if (T <= 1) return launch_stream_mx_t<1, NT>(L, x, out, T, lb, s);
-  if (T <= 2) return launch_stream_mx_t<2, NT>(L, x, out, T, lb, s);
-  if (T <= 4) return launch_stream_mx_t<4, NT>(L, x, out, T, lb, s);
-  return launch_stream_mx_t<8, NT>(L, x, out, T, lb, s);
+  if (T <= 1) return launch_stream_mx_t<1, NT, Q>(L, x, out, T, lb, s);
+  if (T <= 2) return launch_stream_mx_t<2, NT, Q>(L, x, out, T, lb, s);
+  if (T <= 4) return launch_stream_mx_t<4, NT, Q>(L, x, out, T, lb, s);
+  return launch_stream_mx_t<8, NT, Q>(L, x, out, T, lb, s);
+}
+
+template <int Q>
+static cudaError_t launch_stream_q(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* lb,
+                                   cudaStream_t s) {
+  switch (L->cfg.hidden / 256) {   // H % 512 == 0, H <= 2560 (stream_mx_supported)
+    case 2: return launch_stream_mx_nt<2, Q>(L, x, out, T, lb, s);
+    case 4: return launch_stream_mx_nt<4, Q>(L, x, out, T, lb, s);
+    case 6: return launch_stream_mx_nt<6, Q>(L, x, out, T, lb, s);
+    case 8: return launch_stream_mx_nt<8, Q>(L, x, out, T, lb, s);
+    default: return launch_stream_mx_nt<10, Q>(L, x, out, T, lb, s);
+  }
 }
 
 cudaError_t launch_stream_mx(moe_layer* L, const uint16_t* x, uint16_t* out, int T, const float* lb, cudaStream_t s) {
-  switch (L->cfg.hidden / 256) {   // H % 512 == 0, H <= 2560 (stream_mx_supported)
-    case 2: return launch_stream_mx_nt<2>(L, x, out, T, lb, s);
-    case 4: return launch_stream_mx_nt<4>(L, x, out, T, lb, s);
-    case 6: return launch_stream_mx_nt<6>(L, x, out, T, lb, s);
-    case 8: return launch_stream_mx_nt<8>(L, x, out, T, lb, s);
-    case 10: return launch_stream_mx_nt<10>(L, x, out, T, lb, s);
-    default: return cudaErrorInvalidValue;
-  }
+  return layer_q(L) == Q_INT4 ? launch_stream_q<Q_INT4>(L, x, out, T, lb, s) : launch_stream_q<Q_MXFP4>(L, x, out, T, lb, s);
 }
 
 }  // namespace moe

@@ -260,23 +260,53 @@ def test_describe_names_the_active_path():
 # ---------------------------------------------------------------- int4 routed experts
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8])
 def test_small_int4_every_window_size(T):
-    """Groupwise affine int4 routed experts on the three-phase decode kernel
-    (per group s * sum(q x) + b * sum(x)), against the oracle."""
+    """Groupwise affine int4 routed experts on the record-streaming kernel
+    (codes as exact f16 integers on the tensor cores, s * sum(q x) + b * sum(x)
+    per block), against the oracle."""
     S = mi.custom_layer(H=512, E=16, k=4, I=256, Is=128, fmt="int4", seed=5)
     L = G.cuda_layer(S.spec, max_tokens=64)
     x = mi.tokens(S.spec, T, stream=7000 + T)
     out, idx, wt = G.run_cuda(L, x)
     assert L.stats().path == 1
     G.compare(G.synth(S.spec), x, out, idx, wt)
-    assert "int4" in L.describe()
+    assert "moe_decode_stream_mx_kernel<int4>" in L.describe()
+
+
+@pytest.mark.parametrize("H,I,T", [(1024, 384, 1), (1024, 384, 7), (2560, 128, 4)])
+def test_int4_stream_shapes(H, I, T):
+    """int4 records at other hidden sizes (other per-H instantiations), with
+    intermediate sizes whose 16-record groups straddle the 64-feature boundaries
+    of the down (scale, bias) vectors."""
+    S = mi.custom_layer(H=H, E=24, k=6, I=I, Is=128, fmt="int4", seed=H + I)
+    L = G.cuda_layer(S.spec, max_tokens=8)
+    assert "moe_decode_stream_mx_kernel<int4>" in L.describe()
+    x = mi.tokens(S.spec, T, stream=7100 + T)
+    out, idx, wt = G.run_cuda(L, x)
+    G.compare(G.synth(S.spec), x, out, idx, wt)
+
+
+def test_int4_three_phase_kernel_outside_stream_limits():
+    """H not a multiple of 512: int4 decode runs on the three-phase kernel."""
+    S = mi.custom_layer(H=768, E=16, k=4, I=256, Is=128, fmt="int4", seed=6)
+    L = G.cuda_layer(S.spec, max_tokens=8)
+    assert "moe_decode_fused_kernel<int4>" in L.describe()
+    for T in (1, 5):
+        x = mi.tokens(S.spec, T, stream=7200 + T)
+        out, idx, wt = G.run_cuda(L, x)
+        G.compare(G.synth(S.spec), x, out, idx, wt)
 
 
 def test_qwen_int4_decode():
     w = mi.WORKLOADS["qwen_int4_decode"]
     L = G.cuda_layer(w.layer, max_tokens=8)
     S = G.synth(w.layer)
+    assert "moe_decode_stream_mx_kernel<int4>" in L.describe()
     for call in range(3):
         x = mi.workload_tokens(w, call)
         out, idx, wt = G.run_cuda(L, x)
         r = G.compare(S, x, out, idx, wt)
     print("qwen int4 decode", r)
+    # a verify window on the same layer
+    x = mi.tokens(w.layer, 4, stream=7300)
+    out, idx, wt = G.run_cuda(L, x)
+    G.compare(S, x, out, idx, wt)

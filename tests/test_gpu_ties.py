@@ -132,15 +132,31 @@ def test_ties_mxfp4_stream_kernel():
 
 
 def test_ties_three_phase_kernel():
-    base = mi.custom_layer(H=512, E=320, k=8, I=128, Is=128, fmt="int4", seed=63)
+    """MXFP4 with H = 768 (not a multiple of 512) runs on the three-phase kernel."""
+    base = mi.custom_layer(H=768, E=320, k=8, I=128, Is=128, fmt="mxfp4", seed=63)
     S = TiedRouter(base, U=107)
-    L = _layer(S, "int4", max_tokens=8)
+    L = _layer(S, "mxfp4", max_tokens=8)
     try:
         assert "moe_decode_fused_kernel" in L.describe()
         nb = 0
         for T in (1, 3):
             for c in range(4):
-                nb += _check(S, L, mi.tokens(base.spec, T, stream=7200 + 10 * T + c), "bf16")
+                nb += _check(S, L, mi.tokens(base.spec, T, stream=7200 + 10 * T + c), "mxfp4")
+        assert nb > 0
+    finally:
+        L.close()
+
+
+def test_ties_int4_stream_kernel():
+    base = mi.custom_layer(H=512, E=320, k=8, I=128, Is=128, fmt="int4", seed=65)
+    S = TiedRouter(base, U=107)
+    L = _layer(S, "int4", max_tokens=8)
+    try:
+        assert "moe_decode_stream_mx_kernel<int4>" in L.describe()
+        nb = 0
+        for T in (1, 4):
+            for c in range(4):
+                nb += _check(S, L, mi.tokens(base.spec, T, stream=7500 + 10 * T + c), "bf16")
         assert nb > 0
     finally:
         L.close()
