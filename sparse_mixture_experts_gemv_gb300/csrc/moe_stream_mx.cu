@@ -406,8 +406,16 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
       for (int v = 0; v < 2; ++v) {
         const int lo_r = v ? r1 : 0, hi_r = v ? nvalid : r1;
         auto cv = [&](int r) { return (r >= lo_r && r < hi_r) ? cr[r] : 0.f; };
-        stream::f16_hilo2(cv(2 * cq), cv(2 * cq + 1), down, bh[v][0], bl[v][0]);
-        stream::f16_hilo2(cv(2 * cq + 8), cv(2 * cq + 9), down, bh[v][1], bl[v][1]);
+        if constexpr (kI4) {   // int4: c as f16 hi + lo (the bf16 output bounds)
+          stream::f16_hilo2(cv(2 * cq), cv(2 * cq + 1), down, bh[v][0], bl[v][0]);
+          stream::f16_hilo2(cv(2 * cq + 8), cv(2 * cq + 9), down, bh[v][1], bl[v][1]);
+        } else {               // MXFP4: c as one f16 (relative error 2^-12, inside the MXFP4 bounds)
+          const __half2 h0 = __floats2half2_rn(cv(2 * cq) * down, cv(2 * cq + 1) * down);
+          const __half2 h1 = __floats2half2_rn(cv(2 * cq + 8) * down, cv(2 * cq + 9) * down);
+          bh[v][0] = *reinterpret_cast<const uint32_t*>(&h0);
+          bh[v][1] = *reinterpret_cast<const uint32_t*>(&h1);
+          bl[v][0] = bl[v][1] = 0u;
+        }
       }
       if constexpr (kI4) {
         float csum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};   // sum of c over each vector's records, tokens 2cq, 2cq + 1
@@ -423,7 +431,7 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
         stream::i4_down_tiles<NT>(base, mxs, nvalid, ly, nv, reinterpret_cast<const uint32_t*>(base + sv_off),
                                   reinterpret_cast<const uint32_t*>(base + sv_off + vbytes), up, bh, bl, csum, acc);
       } else {
-        stream::mx_down_tiles<NT>(base, mxs, nvalid, ly, nv, base + sv_off, base + sv_off + H, up, bh, bl, acc);
+        stream::mx_down_tiles<NT>(base, mxs, nvalid, ly, nv, base + sv_off, base + sv_off + H, up, bh, acc);
       }
     }
     __syncwarp();
