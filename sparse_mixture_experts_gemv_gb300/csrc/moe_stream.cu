@@ -25,9 +25,13 @@
 //              shared memory (full/empty mbarriers). Consecutive features of one
 //              expert are adjacent in HBM, so a group of records is one or two
 //              contiguous copies.
-//   router     each CTA computes its 1-4 fp32 router logits and publishes each
-//              as a 64-bit word {call tag, value}; readers poll until every
-//              word carries the current call's tag (no separate barrier).
+//   router     the router rows are split evenly over the CTAs (1-2 rows each at
+//              E = 256), copied into shared memory with x, and every logit is
+//              computed by the same fp32 sequence, so equal rows give bitwise
+//              equal logits wherever they land. Each is published as a 64-bit
+//              word {call tag, value} by warps that never poll; readers poll
+//              until every word carries the current call's tag (no separate
+//              barrier).
 //   top-k      every CTA derives the routing from the published logits
 //              (identical inputs and arithmetic on every CTA).
 //   groups     up to 8 records per group. The gate/up dot products of the group
@@ -43,11 +47,11 @@
 //              here only because they do these small products in far fewer
 //              instructions than scalar FMAs, which keeps the consumers ahead of
 //              the copies.
-//   exchange   each CTA publishes its partial outputs [H][T] as 64-bit words
-//              {call tag, fp32 value}; each CTA polls the words of its slice of
-//              outputs from every CTA until all carry this call's tag (no grid
-//              barrier, no separate read), adds them in a fixed order
-//              (deterministic) and writes bf16.
+//   exchange   each CTA stores its fp32 partial outputs [H][T], fences, and adds
+//              one to an arrival counter; one thread per CTA waits (bounded)
+//              until the counter reaches this call's target, the CTA pulls its
+//              slice of outputs from every CTA into shared memory, adds the
+//              parts in a fixed CTA order (deterministic) and writes bf16.
 #include <cuda_runtime.h>
 #include <stdint.h>
 

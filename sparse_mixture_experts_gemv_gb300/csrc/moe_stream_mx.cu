@@ -2,9 +2,10 @@
 // (T <= MOE_DECODE_MAX_T): the same structure as the bf16 kernel in
 // moe_stream.cu -- a producer warp bulk-copies per-feature records of the
 // selected experts into a shared-memory ring, 16 consumer warps turn each
-// record into its contribution to the output, one tagged exchange adds the
-// CTAs' partial outputs -- with the expert weights decoded inside the dot
-// products.
+// record into its contribution to the output, one exchange behind an arrival
+// counter adds the CTAs' fp32 partial outputs -- with the expert weights
+// decoded inside the dot products. The same kernel serves groupwise affine
+// int4 routed experts (Q = INT4, below).
 //
 // "Three ways to speed up MoE inference on DGX Spark", section "Optimization
 // 1": the routed experts are MXFP4 (e2m1 codes, one e8m0 scale per 32
@@ -29,15 +30,24 @@
 //              the row's block scale; the 16 warp parts are added in order and
 //              c = w * silu(g) * u is formed per (record, token).
 //   down       K = the group's records: A = code[n][r] (f16), B = c[r][t] as
-//              f16 hi + lo after a power-of-two shift that keeps the group's
-//              largest |c| near 2^14; each 16-row tile's result is scaled by
+//              one f16 after a power-of-two shift that keeps the group's
+//              largest |c| near 2^14 (relative error 2^-12, far inside the
+//              MXFP4 output bounds); each 16-row tile's result is scaled by
 //              the rows' down scales and added to the fp32 output tile.
+// int4 (q * s + b, one bf16 (s, b) pair per 64 elements, "Optimizing on-device
+// inference for Apple Silicon", section "Decode weights during matrix
+// multiplication"): codes 0..15 become exact f16 integers (0x6400 | q is
+// 1024 + q), each 64-element group's dot product is s * sum(q x) + b * sum(x)
+// with sum(x) taken once per call, and c enters the down tiles as f16 hi + lo
+// (~22 bits) to keep the bf16 output bounds; the down bias term uses the sum of
+// c over a group's records, taken by the same MMA against an all-ones A.
 // At batch 1 the layer is bound by HBM; decoding e2m1 on the CUDA cores costs
 // several instructions per code byte, more than an SM's share of HBM leaves
 // time for, while a tensor-core fragment needs one cvt per two codes.
-// Readings: x is rounded to f16 for the MXFP4 products (exact for the normal
-// f16 range |x| in [2^-14, 65504]; smaller values lose bits, larger overflow);
-// every sum is fp32.
+// Readings: x is rounded to f16 for the 4-bit products (exact for the normal
+// f16 range |x| in [2^-14, 65504]; smaller values lose bits; a larger one is
+// reported as a device check failure, never rounded to infinity); every sum is
+// fp32.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
