@@ -166,6 +166,29 @@ class Bench:
             N.moe_layer_profile_enable(L.handle, False)
         return [a.elapsed_time(b) for a, b in ev], stages
 
+    def launch_floor(self, n=64):
+        """Event-to-event time (ms) of the same loop as time_calls (L2 flush, queued ahead behind a
+        sleep, no host sync between calls) with nothing between the events, and with one one-thread
+        kernel between them: the part of a single-launch call's time that is not the kernel's work."""
+        torch = self.torch
+        tiny = torch.zeros(1, device=self.dev)
+        res = {}
+        for name, body in (("events_only", None), ("one_tiny_kernel", lambda: tiny.add_(1.0))):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            if body is not None:   # the first launch loads the kernel's module: keep it out of the timing
+                body()
+                torch.cuda.synchronize()
+            torch.cuda._sleep(20_000_000)
+            for i in range(n):
+                self.flush_l2()
+                ev[i][0].record()
+                if body is not None:
+                    body()
+                ev[i][1].record()
+            torch.cuda.synchronize()
+            res[name] = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+        return res
+
     def warm_back_to_back(self, L, xs, lbs, outs, reps=4):
         torch = self.torch
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -307,6 +330,7 @@ def run_ours(args):
     achieved = alg_bytes / (k_us * 1e-6) / 1e9
     warm_us = B.warm_back_to_back(L, xs, lbs, outs) * 1e3
     e2e_us, h2d, d2h = B.e2e(L, w, min(w.calls, 32))
+    floor = B.launch_floor()
 
     result = {
         "metric": METRIC, "value": round(us, 3), "unit": "us", "n_gpus": world, "steps": args.steps,
@@ -320,7 +344,8 @@ def run_ours(args):
                   "frac_of_measured_hbm": alg_bytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
                   "warm_us_per_call": warm_us, "us_p50": float(np.median(times) * 1e3),
                   "us_p90": float(np.percentile(times, 90) * 1e3),
-                  "distinct_experts_mean": distinct},
+                  "distinct_experts_mean": distinct,
+                  "launch_floor_us": {k: round(v * 1e3, 3) for k, v in floor.items()}},
         "roofline": {"kernel": "moe_decode_stream_kernel<1>", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": None, "peak_source": peaks["source"],

@@ -76,6 +76,13 @@ typedef enum {
 /* Create-time flags (moe_layer_config_t.flags). */
 #define MOE_FLAG_FORCE_GROUPED 0x1u        /* run every T through the grouped (prefill)
                                               path, also T <= MOE_DECODE_MAX_T; for tests */
+#define MOE_FLAG_ONE_WEIGHT_COPY 0x2u      /* bf16 layers with hidden <= 2048: keep only the
+                                              decode kernel's per-feature [gate | up | down
+                                              column] records and have the grouped GEMMs read
+                                              them too (resident weights ~1.0x instead of ~2x;
+                                              the grouped down GEMM reads MN-major tiles and a
+                                              T=4096 Qwen-shaped prefill call measured ~10%
+                                              slower on GB300). Ignored for other layers.  */
 #define MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT 0x100u  /* test only: the router kernel waits on a
                                               device flag that nothing sets; the bounded wait
                                               runs out (~2 ms) and the next status check
@@ -269,6 +276,20 @@ moe_status_t moe_layer_get_dispatch(moe_layer_t* layer, int32_t* hist_dev, int32
 #define MOE_GROUPED_BLOCK_ROWS 128
 moe_status_t moe_layer_get_block_map(moe_layer_t* layer, int32_t* blocks_dev, int32_t max_blocks,
                                      int32_t* num_blocks_dev, void* stream);
+
+/*
+ * Device memory the layer holds (host outputs; either pointer may be NULL):
+ *   weight_bytes     its copies of the weights and the tables derived from them
+ *                    (router, routed experts, shared expert, scale tables). By
+ *                    default a layer keeps the decode kernels' feature records and
+ *                    the grouped GEMMs' row layouts (~2x the expert bytes); with
+ *                    MOE_FLAG_ONE_WEIGHT_COPY a bf16 layer with hidden <= 2048 keeps
+ *                    the records alone (~1.0x).
+ *   workspace_bytes  staging buffers and per-call scratch sized by max_tokens.
+ * The caller's weight buffers passed to moe_layer_create are not counted (the layer
+ * copies them and does not keep the pointers). NULL layer is MOE_ERR_INVALID_ARG.
+ */
+moe_status_t moe_layer_get_memory(const moe_layer_t* layer, int64_t* weight_bytes, int64_t* workspace_bytes);
 
 /*
  * Synchronise `stream`, then read and clear the device error word: MOE_OK,

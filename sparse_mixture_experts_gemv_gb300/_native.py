@@ -26,6 +26,7 @@ MOE_WEIGHTS_MXFP4 = 1
 MOE_WEIGHTS_INT4 = 2
 
 MOE_FLAG_FORCE_GROUPED = 0x1
+MOE_FLAG_ONE_WEIGHT_COPY = 0x2
 MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT = 0x100
 MOE_DECODE_MAX_T = 8
 MOE_GROUPED_BLOCK_ROWS = 128
@@ -83,6 +84,8 @@ _SIGNATURES = {
     "moe_layer_get_dispatch": (ctypes.c_int, [ctypes.c_void_p] + [ctypes.c_void_p] * 4 + [ctypes.c_void_p]),
     "moe_layer_get_block_map": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                ctypes.c_void_p]),
+    "moe_layer_get_memory": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64),
+                                            ctypes.POINTER(ctypes.c_int64)]),
     "moe_layer_sync_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "moe_layer_describe": (ctypes.c_char_p, [ctypes.c_void_p]),
     "moe_layer_profile_enable": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
@@ -188,6 +191,13 @@ def moe_layer_get_dispatch(layer: int, hist_dev, offsets_dev, perm_dev, pos_dev,
 
 def moe_layer_get_block_map(layer: int, blocks_dev, max_blocks: int, num_blocks_dev, stream: int = 0) -> int:
     return load().moe_layer_get_block_map(layer, blocks_dev, max_blocks, num_blocks_dev, stream)
+
+
+def moe_layer_get_memory(layer: int):
+    """(status, weight bytes, workspace bytes) the layer holds on the device."""
+    wb, ws = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = load().moe_layer_get_memory(layer, ctypes.byref(wb), ctypes.byref(ws))
+    return st, wb.value, ws.value
 
 
 def moe_layer_sync_status(layer: int, stream: int = 0) -> int:

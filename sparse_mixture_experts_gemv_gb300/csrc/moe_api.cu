@@ -35,12 +35,13 @@ namespace {
     if (e_ != cudaSuccess) return cuda_fail(e_, #call);          \
   } while (0)
 
-int64_t pad16(int64_t v) { return (v + 15) / 16 * 16; }
+int64_t pad32(int64_t v) { return (v + 31) / 32 * 32; }
 
 // Every device allocation of a layer goes through here so that a failed create
 // frees exactly what it got.
 struct Allocs {
   std::vector<void*> ptrs;
+  int64_t bytes_total = 0;   // every byte this layer allocated on the device
   moe_status_t get(void** p, size_t bytes) {
     if (bytes == 0) bytes = 16;
     cudaError_t e = cudaMalloc(p, bytes);
@@ -50,6 +51,7 @@ struct Allocs {
       return MOE_ERR_OOM;
     }
     ptrs.push_back(*p);
+    bytes_total += (int64_t)bytes;
     return MOE_OK;
   }
   void free_all() {
@@ -214,7 +216,8 @@ moe_status_t validate(const moe_layer_config_t* c, const moe_layer_weights_t* w)
   if (c->weight_format != MOE_WEIGHTS_BF16 && c->weight_format != MOE_WEIGHTS_MXFP4 &&
       c->weight_format != MOE_WEIGHTS_INT4)
     return MOE_ERR_INVALID_ARG;
-  if (c->flags & ~(uint32_t)(MOE_FLAG_FORCE_GROUPED | MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT)) return MOE_ERR_INVALID_ARG;
+  if (c->flags & ~(uint32_t)(MOE_FLAG_FORCE_GROUPED | MOE_FLAG_ONE_WEIGHT_COPY | MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT))
+    return MOE_ERR_INVALID_ARG;
   if (c->hidden % 256 != 0 || c->hidden > 8192) return MOE_ERR_UNSUPPORTED;
   if (c->intermediate % 128 != 0 || c->intermediate > 4096) return MOE_ERR_UNSUPPORTED;
   if (c->shared_intermediate % 128 != 0 || c->shared_intermediate > 4096) return MOE_ERR_UNSUPPORTED;
@@ -260,6 +263,7 @@ moe_status_t alloc_workspace(LayerOwner* o) {
   cudaMemset(L.err, 0, sizeof(int) * 4);
   cudaMemset(L.never_set, 0, sizeof(int));
   cudaMemset(L.dec.meta, 0, sizeof(moe::DecodeMeta));
+  L.mem_workspace_bytes += o->allocs.bytes_total;   // the layer's first allocations
   return MOE_OK;
 }
 
@@ -267,6 +271,7 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
   moe_layer& L = o->L;
   const auto& c = L.cfg;
   const int64_t H = c.hidden, E = c.num_experts, I = c.intermediate, Is = c.shared_intermediate;
+  const int64_t mem0 = o->allocs.bytes_total;
   moe_status_t st;
 #define GET(ptr, bytes) \
   if ((st = o->allocs.get((void**)&(ptr), (bytes))) != MOE_OK) return st
@@ -288,8 +293,20 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
   else
     MOE_CUDA(cudaMemset(L.router_bias, 0, sizeof(float) * E));
 
+  // With MOE_FLAG_ONE_WEIGHT_COPY, bf16 layers the record-streaming kernel
+  // serves keep one copy of the expert weights: the feature records below,
+  // which the grouped GEMMs then read too (gate/up rows K-major, down columns
+  // MN-major). Otherwise the row layouts of the three-phase decode kernel and
+  // the grouped GEMMs are kept as well (the grouped down GEMM is faster on them).
+  const bool records_only = (c.flags & MOE_FLAG_ONE_WEIGHT_COPY) && c.weight_format == MOE_WEIGHTS_BF16 &&
+                            H <= moe::kStreamMaxHidden;
+  L.row_bytes.gu = c.weight_format == MOE_WEIGHTS_BF16 ? H * 2 : 0;
+  L.row_bytes.down = c.weight_format == MOE_WEIGHTS_BF16 ? I * 2 : 0;
+
   // Routed experts: gate row i and up row i adjacent ([E][I][2][row]).
-  if (c.weight_format == MOE_WEIGHTS_BF16) {
+  if (records_only) {
+    // no row layouts
+  } else if (c.weight_format == MOE_WEIGHTS_BF16) {
     L.row_bytes.gu = H * 2;
     L.row_bytes.down = I * 2;
     GET(L.w_gu, (size_t)E * I * 2 * L.row_bytes.gu);
@@ -300,9 +317,10 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
     MOE_CUDA(cudaMemcpy(L.w_down, w->down_dev, (size_t)E * H * I * 2, cudaMemcpyDeviceToDevice));
   } else if (c.weight_format == MOE_WEIGHTS_INT4) {
     // One record per row: codes (K/2 bytes) then (scale, bias) bf16 pairs of the
-    // K/64 groups (4 bytes each, padded to 16).
-    L.row_bytes.gu = H / 2 + pad16(H / 16);
-    L.row_bytes.down = I / 2 + pad16(I / 16);
+    // K/64 groups (4 bytes each); rows padded to 32 bytes so that every row, and
+    // every 32-byte code chunk the grouped GEMMs load, starts on a DRAM sector.
+    L.row_bytes.gu = pad32(H / 2 + H / 16);
+    L.row_bytes.down = pad32(I / 2 + I / 16);
     GET(L.w_gu, (size_t)E * I * 2 * L.row_bytes.gu);
     GET(L.w_down, (size_t)E * H * L.row_bytes.down);
     MOE_CUDA(cudaMemset(L.w_gu, 0, (size_t)E * I * 2 * L.row_bytes.gu));
@@ -323,9 +341,10 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
                                           L.w_down, rows_d, (int)(I / 64), (int64_t)rd, I / 2);
     MOE_CUDA(cudaGetLastError());
   } else {
-    // One record per row: codes (K/2 bytes) then scales (K/32 bytes, padded to 16).
-    L.row_bytes.gu = H / 2 + pad16(H / 32);
-    L.row_bytes.down = I / 2 + pad16(I / 32);
+    // One record per row: codes (K/2 bytes) then scales (K/32 bytes); rows padded
+    // to 32 bytes (sector-aligned code chunks, as for int4).
+    L.row_bytes.gu = pad32(H / 2 + H / 32);
+    L.row_bytes.down = pad32(I / 2 + I / 32);
     GET(L.w_gu, (size_t)E * I * 2 * L.row_bytes.gu);
     GET(L.w_down, (size_t)E * H * L.row_bytes.down);
     MOE_CUDA(cudaMemset(L.w_gu, 0, (size_t)E * I * 2 * L.row_bytes.gu));
@@ -341,9 +360,11 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
   }
 
   // Shared expert (bf16): [Is][2][H] and [H][Is].
-  GET(L.ws_gu, sizeof(uint16_t) * std::max<int64_t>(Is, 1) * 2 * H);
-  GET(L.ws_down, sizeof(uint16_t) * std::max<int64_t>(Is, 1) * H);
-  if (Is > 0) {
+  if (!records_only) {
+    GET(L.ws_gu, sizeof(uint16_t) * std::max<int64_t>(Is, 1) * 2 * H);
+    GET(L.ws_down, sizeof(uint16_t) * std::max<int64_t>(Is, 1) * H);
+  }
+  if (Is > 0 && !records_only) {
     const size_t row = (size_t)H * 2;
     MOE_CUDA(cudaMemcpy2D(L.ws_gu, 2 * row, w->shared_gate_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
     MOE_CUDA(cudaMemcpy2D((uint8_t*)L.ws_gu + row, 2 * row, w->shared_up_dev, row, row, (size_t)Is, cudaMemcpyDeviceToDevice));
@@ -426,6 +447,7 @@ moe_status_t repack(LayerOwner* o, const moe_layer_weights_t* w) {
     }
   }
 #undef GET
+  L.mem_weight_bytes += o->allocs.bytes_total - mem0;
   return MOE_OK;
 }
 
@@ -504,15 +526,15 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
            moe::stream_supported(&L, 1)
                ? "moe_decode_stream_kernel (cooperative: router with tagged logits, per-CTA top-k, bulk-copied "
                  "[gate|up|down column] records of the shared and routed experts with the down projection fused, "
-                 "partial-output exchange)"
+                 "fp32 partial-output exchange)"
                : moe::stream_mx_supported(&L, 1)
                ? (cfg->weight_format == MOE_WEIGHTS_INT4
                       ? "moe_decode_stream_mx_kernel<int4> (cooperative: router with tagged logits, per-CTA top-k, "
                         "bulk-copied int4 [gate|up|down column] records as exact f16 integers on the tensor cores, "
-                        "s * sum(q x) + b * sum(x) per group, bf16 shared-expert records, partial-output exchange)"
+                        "s * sum(q x) + b * sum(x) per group, bf16 shared-expert records, fp32 partial-output exchange)"
                       : "moe_decode_stream_mx_kernel (cooperative: router with tagged logits, per-CTA top-k, "
                         "bulk-copied MXFP4 [gate|up|down column] records decoded in registers, bf16 shared-expert "
-                        "records, partial-output exchange)")
+                        "records, fp32 partial-output exchange)")
                : (cfg->weight_format == MOE_WEIGHTS_MXFP4
                       ? "moe_decode_fused_kernel<mxfp4> (cooperative: router+shared, routed gate/up, down+combine)"
                       : cfg->weight_format == MOE_WEIGHTS_INT4
@@ -525,6 +547,10 @@ moe_status_t moe_layer_create(const moe_layer_config_t* cfg, const moe_layer_wei
            cfg->weight_format == MOE_WEIGHTS_MXFP4 ? ", MXFP4 B rows decoded to f16 in the kernel"
            : cfg->weight_format == MOE_WEIGHTS_INT4 ? ", int4 B rows decoded to f16 in the kernel" : "",
            (cfg->flags & MOE_FLAG_TEST_FORCE_WAIT_TIMEOUT) ? " [test: forced wait timeout]" : "");
+  if (!L.w_gu && L.w_rec) {   // one copy of the weights: say so
+    const size_t n = strlen(L.describe);
+    snprintf(L.describe + n, sizeof(L.describe) - n, " [one weight copy: grouped GEMMs read the feature records]");
+  }
   *out = &o->L;
   return MOE_OK;
 }
@@ -642,6 +668,13 @@ moe_status_t moe_layer_get_block_map(moe_layer_t* L, int32_t* blocks, int32_t ma
   return MOE_OK;
 }
 
+moe_status_t moe_layer_get_memory(const moe_layer_t* L, int64_t* weight_bytes, int64_t* workspace_bytes) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  if (weight_bytes) *weight_bytes = L->mem_weight_bytes;
+  if (workspace_bytes) *workspace_bytes = L->mem_workspace_bytes;
+  return MOE_OK;
+}
+
 moe_status_t moe_layer_get_stats(moe_layer_t* L, void* stream, moe_stats_t* st) {
   if (!L || !st) return MOE_ERR_INVALID_ARG;
   memset(st, 0, sizeof(*st));
@@ -686,6 +719,7 @@ moe_status_t moe_layer_sync_status(moe_layer_t* L, void* stream) {
   MOE_CUDA(cudaMemset(L->err, 0, sizeof(int)));
   if (code != 0) {  // an aborted call can leave the grid-sync counters mid-generation
     MOE_CUDA(cudaMemset(L->dec.sync_ctr, 0, sizeof(unsigned long long) * 4));
+    if (L->grp.dispatch_ctr) MOE_CUDA(cudaMemset(L->grp.dispatch_ctr, 0, sizeof(unsigned long long)));
     MOE_CUDA(cudaMemset(L->dec.logit_words, 0, sizeof(unsigned long long) * moe::kMaxDecodeT * L->cfg.num_experts));
     MOE_CUDA(cudaMemset(L->dec.partial, 0,
                         sizeof(unsigned long long) * (size_t)L->num_sms * moe::kMaxDecodeT * L->cfg.hidden));

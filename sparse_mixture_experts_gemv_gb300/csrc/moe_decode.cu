@@ -898,6 +898,9 @@ cudaError_t launch_decode(moe_layer* L, const uint16_t* x, uint16_t* out, int T,
                           cudaStream_t s) {
   if (stream_supported(L, T)) return launch_stream(L, x, out, T, logit_bias, s);
   if (stream_mx_supported(L, T)) return launch_stream_mx(L, x, out, T, logit_bias, s);
+  // a layer that keeps only the feature records has no rows for this kernel:
+  // the grouped path serves any T
+  if (!L->w_gu || !L->ws_gu) return launch_grouped(L, x, out, T, logit_bias, s);
   if (L->cfg.weight_format == MOE_WEIGHTS_MXFP4) return launch_decode_fmt<FmtMXFP4>(L, x, out, T, logit_bias, s);
   if (L->cfg.weight_format == MOE_WEIGHTS_INT4) return launch_decode_fmt<FmtInt4>(L, x, out, T, logit_bias, s);
   return launch_decode_fmt<FmtBF16>(L, x, out, T, logit_bias, s);

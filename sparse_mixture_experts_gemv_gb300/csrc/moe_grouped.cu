@@ -62,6 +62,8 @@ constexpr int kStageA = BM * BK * 2;     // 16 KB
 constexpr int kStageB = 256 * BK * 2;    // 32 KB (N up to 256)
 constexpr int kTmemCols = 512;           // two 256-column fp32 accumulators
 constexpr int kChunk = 32;               // tokens per dispatch chunk (one per warp of the top-k CTA)
+constexpr size_t kDispatchMaskSmem = 128 * 1024;  // largest dynamic shared memory of the fused dispatch
+constexpr size_t kDispatchRedSmem = 2 * 4096 * sizeof(int);   // its per-part count table
 constexpr size_t kGemmSmem = (size_t)kStages * (kStageA + kStageB) + 1024 /*align*/ + 256 /*barriers*/;
 // MXFP4 B operands: a separate ring of raw stages (e2m1 codes of 256 B rows x 64
 // K, 32 bytes a row, then the rows' scale pairs) that converter warps decode into
@@ -99,6 +101,11 @@ struct GemmParams {
   const int* perm;          // [T*k] assignment t*k+j at each grouped row
   // B rows of expert e start at e * b_rows_per_expert (routed map)
   int b_rows_per_expert;
+  // bf16 B from the decode kernels' feature records (0: row layouts): the number
+  // of features per routed expert. Gate/up tiles then come from a 3-D map
+  // {H, gate/up, feature} (K-major, as the row layout), down tiles from the
+  // records' down columns as four 64 x 64 MN-major boxes per stage.
+  int b_rec;
   // epilogue outputs
   uint16_t* out_routed; int ld_routed;
   uint16_t* out_shared; int ld_shared;
@@ -303,8 +310,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
             for (int part = 0; part < 3; ++part)
               tma_load_2d(sB + s * kStageB + part * p.BN * BK * 2, &mapB_r, kcol, part * p.E + ti.nt * p.BN, &full[s]);
           } else if (!mxt) {
-            const int brow = (ti.shared ? 0 : ti.e * p.b_rows_per_expert) + ti.nt * p.BN;
-            tma_load_2d(sB + s * kStageB, ti.shared ? &mapB_s : &mapB_r, kcol, brow, &full[s]);
+            const CUtensorMap* mb = ti.shared ? &mapB_s : &mapB_r;
+            if (BQ == B_BF16 && p.b_rec && EPI == EPI_SWIGLU) {   // features nt*128 .. +127, {gate, up} rows
+              tma_load_3d(sB + s * kStageB, mb, kcol, 0, (ti.shared ? 0 : ti.e * p.b_rec) + ti.nt * (p.BN / 2),
+                          &full[s]);
+            } else if (BQ == B_BF16 && p.b_rec) {   // down columns: K rows = features, 64 n a box
+              const int krow = (ti.shared ? 0 : ti.e * p.b_rec) + kcol;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                tma_load_2d(sB + s * kStageB + j * (64 * BK * 2), mb, ti.nt * p.BN + 64 * j, krow, &full[s]);
+            } else {
+              const int brow = (ti.shared ? 0 : ti.e * p.b_rows_per_expert) + ti.nt * p.BN;
+              tma_load_2d(sB + s * kStageB, mb, kcol, brow, &full[s]);
+            }
           }
           if (!GATHER) tma_load_2d(sA + s * kStageA, ti.shared ? &mapA_s : &mapA_r, kcol, ti.row0, &full[s]);
         }
@@ -321,10 +339,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_bf = idesc_bf16_f32(BM, p.BN), idesc_h = idesc_f16_f32(BM, p.BN);
+      // down tiles from records: B is MN-major (transpose-B bit of the instruction descriptor)
+      const bool b_mn = BQ == B_BF16 && EPI == EPI_STORE && p.b_rec != 0;
+      const uint32_t idesc_bmn = idesc_bf | kIdescTransposeB;
       uint32_t it = 0, tc = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++tc) {
         const TileInfo ti = decode_tile(p, R, tile);
-        const uint32_t idesc = (MXB && !ti.shared) ? idesc_h : idesc_bf;
+        const uint32_t idesc = (MXB && !ti.shared) ? idesc_h : b_mn ? idesc_bmn : idesc_bf;
         const int ab = tc & 1;
         if (!mbar_wait(&acc_empty[ab], ((tc >> 1) & 1) ^ 1, p.err, abort_flag)) break;
         tc_fence_after();
@@ -340,9 +361,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
           for (int part = 0; part < kTerms; ++part) {
             const uint32_t bp = b0 + part * p.BN * BK * 2;
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              mma_bf16(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(bp + kk * 32), idesc,
-                       (kb | kk | part) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              // K-major B: the next 16 K columns are 32 bytes on; MN-major B: 16 K rows
+              // of 128 bytes on (two 8-row groups), the 64-column boxes 8 KB apart
+              const uint64_t bdesc = b_mn ? smem_desc_sw128_mn(bp + kk * 2048, 64 * BK * 2)
+                                          : smem_desc_sw128(bp + kk * 32);
+              mma_bf16(d, smem_desc_sw128(a0 + kk * 32), bdesc, idesc, (kb | kk | part) != 0 ? 1u : 0u);
+            }
           }
           mma_commit(&empty[s]);
         }
@@ -709,6 +734,188 @@ dispatch_scatter_kernel(const int* __restrict__ idx, const int* __restrict__ chu
   }
 }
 
+// Routing and dispatch in one cooperative launch of G CTAs (all co-resident; G
+// is fixed per layer, so that the arrival counter grows by G every call and a
+// call's generation is the counter / G), CTA b owning the S consecutive 32-token
+// chunks [b*S, (b+1)*S) (none for the last CTAs when T is small):
+//   1. top-k of each owned token (one warp per token), and per owned chunk a
+//      32-bit token mask per expert in shared memory (bit t: the chunk's token t
+//      chose e); the chunk's per-expert counts go to counts[c][e] as bytes.
+//   2. one bounded grid barrier (arrival counter, every CTA adds 1 per call).
+//   3. every CTA reads all counts and forms, per expert, the total and the rows
+//      of the chunks before its own; an exclusive scan over experts gives the
+//      grouped-row offsets. CTA 0 writes hist, offsets and the 128-row block map.
+//   4. the grouped row of assignment (t, j) with expert e is offsets[e] + the
+//      rows of e in earlier chunks + the tokens of its own chunk before t that
+//      chose e (a population count of the mask): all assignments at once.
+// The result is the same as that of the three kernels above (grouped rows in
+// increasing token order within each expert); only the launch count differs.
+__global__ void __launch_bounds__(1024, 1)
+route_dispatch_kernel(const float* __restrict__ logits, int T, int E, int k, int S, int* __restrict__ idx,
+                      float* __restrict__ weights, uint8_t* __restrict__ counts /* [chunks][E] */,
+                      unsigned long long* __restrict__ ctr, int* __restrict__ hist, int* __restrict__ offsets,
+                      int2* __restrict__ mtiles, int* __restrict__ num_routed, int max_mtiles,
+                      int* __restrict__ perm, int* __restrict__ pos, int* __restrict__ err) {
+  extern __shared__ uint32_t s_dyn[];
+  uint32_t* s_mask = s_dyn;                        // [S][E]
+  int* s_red = reinterpret_cast<int*>(s_dyn + S * E);   // [2][4096]: per-part totals, rows before
+  __shared__ int s_pre[kMaxExperts];               // rows of e before the current chunk
+  __shared__ int s_tot[kMaxExperts];               // rows of e in all chunks, then exclusive offsets
+  __shared__ int s_tiles[kMaxExperts];
+  __shared__ int s_wsum[2][32];
+  __shared__ int s_ok;
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int chunks = (T + kChunk - 1) / kChunk;
+  const int c0 = blockIdx.x * S, c1 = min(chunks, c0 + S);
+  for (int q = tid; q < S * E; q += blockDim.x) s_mask[q] = 0u;
+  for (int e = tid; e < E; e += blockDim.x) { s_pre[e] = 0; s_tot[e] = 0; }
+  // after an earlier error (outputs undefined until the status is read) a CTA
+  // only takes part in the barrier, so that the arrival counter stays whole
+  if (tid == 0) s_ok = *reinterpret_cast<volatile int*>(err) == 0;
+  __syncthreads();
+  const bool live = s_ok != 0;
+  // 1. top-k and the owned chunks' masks
+  for (int c = live ? c0 : c1; c < c1; ++c) {
+    const int t = c * kChunk + warp;
+    if (t < T) {
+      if (E <= 256) warp_topk<1>(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, weights + (size_t)t * k);
+      else warp_topk<2>(logits + (size_t)t * E, E, k, lane, idx + (size_t)t * k, weights + (size_t)t * k);
+      __syncwarp();
+      if (lane < k) {
+        const int e = idx[(size_t)t * k + lane];
+        if (e >= 0 && e < E) atomicOr(&s_mask[(c - c0) * E + e], 1u << warp);
+        else set_error(err, kDevCheck);
+      }
+    }
+  }
+  __syncthreads();
+  if (live)
+    for (int q = tid; q < (c1 - c0) * E; q += blockDim.x) counts[(size_t)c0 * E + q] = (uint8_t)__popc(s_mask[q]);
+  // 2. grid barrier
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned long long gen = atomicAdd(ctr, 1ull) / gridDim.x;
+    const unsigned long long target = (gen + 1) * gridDim.x;
+    const long long t0 = clock64();
+    int ok = 1;
+    unsigned long long v;
+    do {
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+      if (v >= target) break;
+      if (clock64() - t0 > 4000000000LL) {  // ~2 s: something is wrong, do not hang the GPU
+        set_error(err, kDevTimeout);
+        ok = 0;
+        break;
+      }
+    } while (true);
+    __threadfence();
+    s_ok = ok && live && *reinterpret_cast<volatile int*>(err) == 0;
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  if (!s_ok || (c0 >= c1 && blockIdx.x != 0)) return;
+  // 3. per-expert totals and rows before this CTA's chunks; counts are read as
+  //    4-expert words, P parts of the chunk range per word column, and the parts
+  //    are added in part order (plain stores, no contended atomics)
+  const int W = E / 4;                   // words per chunk row (E % 16 == 0)
+  const int P = (int)blockDim.x / W;     // >= 2 for E <= 512; P * E <= 4096
+  {
+    const int part = tid / W, wcol = tid - part * W;
+    if (part < P) {
+      int pre[4] = {0, 0, 0, 0}, tot[4] = {0, 0, 0, 0};
+      const uint32_t* cw = reinterpret_cast<const uint32_t*>(counts);
+#pragma unroll 8
+      for (int c = part; c < chunks; c += P) {
+        const uint32_t v = __ldcg(cw + (size_t)c * W + wcol);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int n = (int)((v >> (8 * b)) & 0xFFu);
+          tot[b] += n;
+          if (c < c0) pre[b] += n;
+        }
+      }
+      *reinterpret_cast<int4*>(s_red + part * E + 4 * wcol) = make_int4(tot[0], tot[1], tot[2], tot[3]);
+      *reinterpret_cast<int4*>(s_red + 4096 + part * E + 4 * wcol) = make_int4(pre[0], pre[1], pre[2], pre[3]);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int tot = 0, pre = 0;
+    for (int q = 0; q < P; ++q) {
+      tot += s_red[q * E + e];
+      pre += s_red[4096 + q * E + e];
+    }
+    s_tot[e] = tot;
+    s_pre[e] = pre;
+  }
+  __syncthreads();
+  // exclusive scans over experts of the rows and of the 128-row blocks
+  {
+    const int e = tid;
+    const int n = e < E ? s_tot[e] : 0;
+    const int nb = (n + BM - 1) / BM;
+    int a = n, b = nb;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xFFFFFFFFu, a, o), y = __shfl_up_sync(0xFFFFFFFFu, b, o);
+      if (lane >= o) { a += x; b += y; }
+    }
+    if (lane == 31) { s_wsum[0][warp] = a; s_wsum[1][warp] = b; }
+    __syncthreads();
+    if (warp == 0) {
+      int x = s_wsum[0][lane], y = s_wsum[1][lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int xs = __shfl_up_sync(0xFFFFFFFFu, x, o), ys = __shfl_up_sync(0xFFFFFFFFu, y, o);
+        if (lane >= o) { x += xs; y += ys; }
+      }
+      s_wsum[0][lane] = x - s_wsum[0][lane];   // exclusive over warps
+      s_wsum[1][lane] = y - s_wsum[1][lane];
+    }
+    __syncthreads();
+    const int off = s_wsum[0][warp] + a - n, tile0 = s_wsum[1][warp] + b - nb;
+    if (e < E) {
+      s_tot[e] = off;
+      if (blockIdx.x == 0) {
+        hist[e] = n;
+        offsets[e] = off;
+        for (int m = 0; m < nb; ++m) {
+          if (tile0 + m < max_mtiles) mtiles[tile0 + m] = make_int2(e, off + m * BM);
+          else set_error(err, kDevCheck);
+        }
+        if (e == E - 1) {
+          offsets[E] = off + n;   // == T * k
+          *num_routed = tile0 + nb;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // 4. grouped rows of the owned chunks' assignments
+  for (int c = c0; c < c1; ++c) {
+    const uint32_t* mask = s_mask + (c - c0) * E;
+    const int t = c * kChunk + (tid >> 5), j = lane;   // warp = token of the chunk, lane = slot
+    if (t < T && j < k) {
+      const size_t a = (size_t)t * k + j;
+      const int e = idx[a];
+      if (e >= 0 && e < E) {
+        const int g = s_tot[e] + s_pre[e] + __popc(mask[e] & ((1u << (tid >> 5)) - 1u));
+        if (g >= 0 && g < T * k) {
+          perm[g] = (int)a;
+          pos[a] = g;
+        } else {
+          set_error(err, kDevCheck);
+        }
+      }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) s_pre[e] += __popc(mask[e]);
+    __syncthreads();
+  }
+}
+
 // out[t, :] = sum_j w[t, j] * y[pos[t, j], :] + y_shared[t, :], fp32 sum, bf16 out.
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint16_t* __restrict__ y, const uint16_t* __restrict__ ys, const int* __restrict__ pos,
@@ -830,7 +1037,9 @@ struct GroupedMaps {
   CUtensorMap w_down;        // B down routed: [E*H][I], box {64, 256}
                              // (MXFP4: code bytes [E*H][row], box {32, 256})
   CUtensorMap ws_down;       // B down shared: [H][Is], box {64, 256}
+                             // (record layout: see encode_rec_gu / encode_rec_down)
   int router_bn;
+  bool b_rec;                // B of the bf16 GEMMs from the feature records
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -854,6 +1063,34 @@ cudaError_t encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// 3-D map over bf16 feature records ([rows][rec_bytes], gate row then up row of H
+// elements at the start of each): dims {H, 2, rows}, box {64, 2, 128}, so one
+// stage lands as 256 rows of 128 bytes -- feature f's gate row, then its up row --
+// with the 128-byte swizzle, exactly as the row layout's box {64, 256}.
+cudaError_t encode_rec_gu(CUtensorMap* m, const void* base, uint64_t rows, uint64_t H, uint64_t rec_bytes) {
+  cuuint64_t dims[3] = {H, 2, rows};
+  cuuint64_t strides[2] = {H * 2, rec_bytes};
+  cuuint32_t box[3] = {(cuuint32_t)BK, 2, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+// 2-D map over the records' down columns (H bf16 at byte 4H of each record):
+// dims {H, rows}, box {64 outputs, 64 features}: a 64 x 64 MN-major block of B
+// (64 K rows of 128 bytes, 128-byte swizzle).
+cudaError_t encode_rec_down(CUtensorMap* m, const uint8_t* rec, uint64_t rows, uint64_t H, uint64_t rec_bytes) {
+  cuuint64_t dims[2] = {H, rows};
+  cuuint64_t strides[1] = {rec_bytes};
+  cuuint32_t box[2] = {64, (cuuint32_t)BK};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint8_t*>(rec + 4 * H), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -886,6 +1123,24 @@ cudaError_t launch_pdl(K kernel, int grid, int block, size_t smem, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The same with all CTAs co-resident (they wait on one another).
+template <class K, class... A>
+cudaError_t launch_coop_pdl(K kernel, int grid, int block, size_t smem, cudaStream_t s, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace
 
 cudaError_t grouped_prepare(moe_layer* L) {
@@ -903,6 +1158,7 @@ cudaError_t grouped_prepare(moe_layer* L) {
   do {                                                                        \
     e = cudaMalloc((void**)&(ptr), (bytes) ? (bytes) : 16);                   \
     if (e != cudaSuccess) return e;                                           \
+    L->mem_workspace_bytes += (int64_t)((bytes) ? (bytes) : 16);              \
   } while (0)
   GALLOC(g.logits, sizeof(float) * (size_t)Tm * E);
   GALLOC(g.idx, sizeof(int) * TK);
@@ -910,6 +1166,9 @@ cudaError_t grouped_prepare(moe_layer* L) {
   GALLOC(g.hist, sizeof(int) * (E + 1));
   GALLOC(g.offsets, sizeof(int) * (E + 2));
   GALLOC(g.chunk_counts, sizeof(int) * (size_t)chunks * E);
+  GALLOC(g.dispatch_ctr, sizeof(unsigned long long));
+  g.dispatch_grid = chunks < L->num_sms ? chunks : L->num_sms;
+  if ((e = cudaMemset(g.dispatch_ctr, 0, sizeof(unsigned long long))) != cudaSuccess) return e;
   GALLOC(g.perm, sizeof(int) * TK);
   GALLOC(g.pos, sizeof(int) * TK);
   GALLOC(g.tiles, sizeof(int2) * g.max_tiles);
@@ -943,6 +1202,12 @@ cudaError_t grouped_prepare(moe_layer* L) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
 #undef GALLOC
+  {  // the per-stage scale / (s, b) tables are weights, not workspace
+    const int64_t blocks = (int64_t)E * (H / 64) * 2 * I + (int64_t)E * (I / 64) * H;
+    const int64_t tables = i4 ? 4 * blocks : mx ? 2 * blocks + (int64_t)E * 2 * I + (int64_t)E * H : 0;
+    L->mem_workspace_bytes -= tables;
+    L->mem_weight_bytes += tables;
+  }
 
   if ((e = get_encoder()) != cudaSuccess) return e;
   GroupedMaps* m = new GroupedMaps();
@@ -950,7 +1215,13 @@ cudaError_t grouped_prepare(moe_layer* L) {
   m->router_bn = (E % 64 == 0) ? 64 : (E % 32 == 0 ? 32 : 16);  // N tile dividing E (E % 16 == 0)
   if ((e = encode_2d(&m->router_split, L->router_split, 3ull * E, H, m->router_bn)) != cudaSuccess) return e;
   if ((e = encode_2d(&m->h, g.h, TK, I, BM)) != cudaSuccess) return e;
-  if (!mx && !i4) {
+  m->b_rec = !mx && !i4 && L->w_gu == nullptr;   // bf16 layers that keep only the feature records
+  const uint64_t rec_bytes = (uint64_t)stream_record_stride(H);
+  if (m->b_rec) {
+    if (!L->w_rec || (Is > 0 && !L->ws_rec)) return cudaErrorInvalidValue;
+    if ((e = encode_rec_gu(&m->w_gu, L->w_rec, (uint64_t)E * I, H, rec_bytes)) != cudaSuccess) return e;
+    if ((e = encode_rec_down(&m->w_down, L->w_rec, (uint64_t)E * I, H, rec_bytes)) != cudaSuccess) return e;
+  } else if (!mx && !i4) {
     if ((e = encode_2d(&m->w_gu, L->w_gu, (uint64_t)E * 2 * I, H, 256)) != cudaSuccess) return e;
     if ((e = encode_2d(&m->w_down, L->w_down, (uint64_t)E * H, I, 256)) != cudaSuccess) return e;
   } else {
@@ -958,7 +1229,11 @@ cudaError_t grouped_prepare(moe_layer* L) {
     if ((e = encode_codes(&m->w_down, L->w_down, (uint64_t)E * H, (uint64_t)L->row_bytes.down)) != cudaSuccess)
       return e;
   }
-  if (Is > 0) {
+  if (Is > 0 && m->b_rec) {
+    if ((e = encode_rec_gu(&m->ws_gu, L->ws_rec, (uint64_t)Is, H, rec_bytes)) != cudaSuccess) return e;
+    if ((e = encode_2d(&m->hs, g.hs, (uint64_t)Tm, Is, BM)) != cudaSuccess) return e;
+    if ((e = encode_rec_down(&m->ws_down, L->ws_rec, (uint64_t)Is, H, rec_bytes)) != cudaSuccess) return e;
+  } else if (Is > 0) {
     if ((e = encode_2d(&m->ws_gu, L->ws_gu, 2ull * Is, H, 256)) != cudaSuccess) return e;
     if ((e = encode_2d(&m->hs, g.hs, (uint64_t)Tm, Is, BM)) != cudaSuccess) return e;
     if ((e = encode_2d(&m->ws_down, L->ws_down, (uint64_t)H, Is, 256)) != cudaSuccess) return e;
@@ -968,7 +1243,8 @@ cudaError_t grouped_prepare(moe_layer* L) {
     m->ws_down = m->w_down;
   }
   constexpr auto kSmemAttr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_ROUTER, false, B_BF16>, kSmemAttr, (int)kGemmSmem);
+  e = cudaFuncSetAttribute(route_dispatch_kernel, kSmemAttr, (int)kDispatchMaskSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_ROUTER, false, B_BF16>, kSmemAttr, (int)kGemmSmem);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_SWIGLU, true, B_BF16>, kSmemAttr, (int)kGemmSmem);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI_STORE, false, B_BF16>, kSmemAttr, (int)kGemmSmem);
   if (e == cudaSuccess && mx)
@@ -984,7 +1260,7 @@ cudaError_t grouped_prepare(moe_layer* L) {
 
 void grouped_release(moe_layer* L) {
   auto& g = L->grp;
-  void* ptrs[] = {g.logits, g.idx, g.weights, g.hist, g.offsets, g.chunk_counts, g.perm, g.pos,
+  void* ptrs[] = {g.logits, g.idx, g.weights, g.hist, g.offsets, g.chunk_counts, g.dispatch_ctr, g.perm, g.pos,
                   g.tiles, g.num_tiles, g.h, g.hs, g.y, g.ys, g.x16, g.mx_gu_sc, g.mx_dn_sc, g.i4_gu_par, g.i4_dn_par,
                   g.mx_gu_sref, g.mx_dn_sref};
   for (void* p : ptrs)
@@ -1036,16 +1312,26 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
     if (e != cudaSuccess) return e;
   }
   prof_mark(L, s);
-  // 2-4. top-k, histogram, scan, block map, scatter
-  e = launch_pdl(topk_hist_kernel, chunks, 1024, 0, s, (const float*)g.logits, T, E, k, g.idx, g.weights,
-                 g.chunk_counts);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(dispatch_scan_kernel, 1, 1024, 0, s, g.chunk_counts, chunks, E, T, k, g.hist, g.offsets,
-                 (int2*)g.tiles, g.num_tiles, g.max_tiles, L->err);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(dispatch_scatter_kernel, chunks, 256, 0, s, (const int*)g.idx, (const int*)g.chunk_counts,
-                 (const int*)g.offsets, T, E, k, g.perm, g.pos, L->err);
-  if (e != cudaSuccess) return e;
+  // 2-4. top-k, histogram, scan, block map, scatter: one cooperative launch
+  //      while the owned chunks' masks fit in shared memory, else three kernels
+  const int G = g.dispatch_grid, S = (chunks + G - 1) / G;
+  const size_t mask_smem = sizeof(uint32_t) * (size_t)S * E + kDispatchRedSmem;
+  if (T > 0 && mask_smem <= kDispatchMaskSmem) {
+    e = launch_coop_pdl(route_dispatch_kernel, G, 1024, mask_smem, s, (const float*)g.logits, T, E, k, S, g.idx,
+                        g.weights, reinterpret_cast<uint8_t*>(g.chunk_counts), g.dispatch_ctr, g.hist, g.offsets,
+                        (int2*)g.tiles, g.num_tiles, g.max_tiles, g.perm, g.pos, L->err);
+    if (e != cudaSuccess) return e;
+  } else {
+    e = launch_pdl(topk_hist_kernel, chunks, 1024, 0, s, (const float*)g.logits, T, E, k, g.idx, g.weights,
+                   g.chunk_counts);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dispatch_scan_kernel, 1, 1024, 0, s, g.chunk_counts, chunks, E, T, k, g.hist, g.offsets,
+                   (int2*)g.tiles, g.num_tiles, g.max_tiles, L->err);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dispatch_scatter_kernel, chunks, 256, 0, s, (const int*)g.idx, (const int*)g.chunk_counts,
+                   (const int*)g.offsets, T, E, k, g.perm, g.pos, L->err);
+    if (e != cudaSuccess) return e;
+  }
   prof_mark(L, s);
   // 5. gate/up + SwiGLU (routed groups, then the shared expert over all tokens)
   {
@@ -1054,7 +1340,7 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
     p.BN = 256;
     p.nt_routed = 2 * I / 256; p.ks_routed = H / BK;
     p.n_shared_mtiles = Is > 0 ? mt_tokens : 0; p.nt_shared = Is > 0 ? 2 * Is / 256 : 1; p.ks_shared = H / BK;
-    p.x = x; p.perm = g.perm; p.b_rows_per_expert = 2 * I;
+    p.x = x; p.perm = g.perm; p.b_rows_per_expert = 2 * I; p.b_rec = m->b_rec ? I : 0;
     p.out_routed = g.h; p.ld_routed = I; p.out_shared = g.hs; p.ld_shared = Is;
     if (mx) {
       p.x16 = g.x16; p.q_par = g.mx_gu_sc; p.mx_sref = g.mx_gu_sref;
@@ -1078,7 +1364,7 @@ cudaError_t launch_grouped(moe_layer* L, const uint16_t* x, uint16_t* out, int T
     p.BN = 256;
     p.nt_routed = H / 256; p.ks_routed = I / BK;
     p.n_shared_mtiles = Is > 0 ? mt_tokens : 0; p.nt_shared = H / 256; p.ks_shared = Is > 0 ? Is / BK : 1;
-    p.b_rows_per_expert = H;
+    p.b_rows_per_expert = H; p.b_rec = m->b_rec ? I : 0;
     p.out_routed = g.y; p.ld_routed = H; p.out_shared = g.ys; p.ld_shared = H;
     if (mx) {
       p.q_par = g.mx_dn_sc; p.mx_sref = g.mx_dn_sref;

@@ -34,9 +34,11 @@ struct DecodeWorkspace {
   float* h;              // [kMaxDecodeT * k][I]   SwiGLU outputs of routed assignments (t*k+j)
   float* h_shared;       // [kMaxDecodeT][Is]
   unsigned long long* sync_ctr;   // [4] monotonic counters: [0], [1] grid syncs of the
-                                  // three-phase kernel, [2] CTA exits of the record-streaming kernel
+                                  // three-phase kernel; record-streaming kernels: [2] CTA exits
+                                  // (the call tag), [3] partial-output arrivals (1 per CTA per call)
   unsigned long long* logit_words;  // [kMaxDecodeT][E] router logits tagged with the call
-  unsigned long long* partial;  // [num_sms][H][kMaxDecodeT] per-CTA partial outputs, tagged words
+  unsigned long long* partial;  // [num_sms][H][kMaxDecodeT] 8-byte slots; the record-streaming
+                                // kernels store fp32 partial outputs [num_sms][H][T] in it
 };
 
 struct GroupedWorkspace {
@@ -47,7 +49,10 @@ struct GroupedWorkspace {
   float* weights;        // [T][k]
   int* hist;             // [E]
   int* offsets;          // [E + 1] grouped-row offsets (offsets[E] = T*k)
-  int* chunk_counts;     // [chunks][E] per 32-token chunk counts, then chunk bases
+  int* chunk_counts;     // per 32-token chunk counts: uint8 [chunks][E] (fused dispatch) or
+                         // int [E][chunks], then chunk bases (three-kernel dispatch)
+  unsigned long long* dispatch_ctr;  // arrivals of the fused dispatch kernel (each CTA adds 1 per call)
+  int dispatch_grid;     // CTAs of the fused dispatch kernel: min(SMs, chunks of max_tokens), fixed
   int* perm;             // [T*k]  assignment t*k+j at each grouped row
   int* pos;              // [T*k]  grouped row of each assignment
   int* tiles;            // int2 [max_tiles] (expert, first grouped row) of each 128-row block
@@ -74,6 +79,8 @@ struct moe_layer {
   int device;
   int num_sms;
   int decode_max_t;      // largest T the weight-streaming path serves for this shape
+  int64_t mem_weight_bytes;     // device bytes of the layer's resident weight copies and tables
+  int64_t mem_workspace_bytes;  // device bytes of its workspaces
 
   // Repacked weights (owned).
   float* router_t;       // fp32 [E][H]   (W_r transposed: one row per expert)

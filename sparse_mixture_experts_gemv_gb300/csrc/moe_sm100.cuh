@@ -80,6 +80,11 @@ MOE_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, int c0, int c1,
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       :: "r"(smem_u32(smem_dst)), "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)) : "memory");
 }
+MOE_DEV void tma_load_3d(void* smem_dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      :: "r"(smem_u32(smem_dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)) : "memory");
+}
 MOE_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
 }
@@ -125,6 +130,20 @@ MOE_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Descriptor of an MN-major, 128-byte-swizzled operand tile (rows of 128 bytes =
+// 64 consecutive M/N elements, one row per K index): leading byte offset = the
+// distance between 64-element column blocks along M/N (bits 16-29), stride byte
+// offset 1024 = one 8-row K group (bits 32-45); version and swizzle as above.
+MOE_DEV uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t mn_block_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulation, both
 // operands K-major, shape M x N: D format F32 (bits 4-5 = 1), A format BF16
 // (bits 7-9 = 1), B format BF16 (bits 10-12 = 1), N >> 3 in bits 17-22,
@@ -132,6 +151,8 @@ MOE_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Bit 16 of the instruction descriptor: B is MN-major (N contiguous) instead of K-major.
+constexpr uint32_t kIdescTransposeB = 1u << 16;
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 MOE_DEV void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {

@@ -326,7 +326,7 @@ MOE_DEV void i4_gu_tiles(const uint8_t* gbase, int stride, int nvalid, int nmt, 
   const int lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
 #pragma unroll
   for (int m = 0; m < MAXMT; ++m) out[m][0] = out[m][1] = out[m][2] = out[m][3] = 0.f;
-#pragma unroll
+#pragma unroll 1   // rolled: keeps the int4 loop body in the instruction cache (measured faster)
   for (int bi = 0; bi < NBLK; ++bi) {
     const int blk = blk0 + bi;
     uint32_t b[2][2] = {{0u, 0u}, {0u, 0u}};

@@ -141,6 +141,13 @@ class MoeLayer:
         nb = int(n.item())
         return blocks[:nb], nb
 
+    def memory(self):
+        """(weight bytes, workspace bytes) the layer holds on the device."""
+        st, wb, ws = N.moe_layer_get_memory(self.handle)
+        if st != N.MOE_OK:
+            raise N.MoeError(st, "moe_layer_get_memory")
+        return wb, ws
+
     def stats(self, stream=None) -> N.moe_stats_t:
         s = (stream or torch.cuda.current_stream(self.device)).cuda_stream
         return N.moe_layer_get_stats(self.handle, s)
