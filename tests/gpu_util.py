@@ -70,8 +70,16 @@ def compare(S, x_bits, out_bits, gpu_idx, gpu_w=None, logit_bias=None, fmt="bf16
     Token rows whose k-th/(k+1)-th oracle logit gap is below NEAR_TIE may pick either
     side of the tie: the CUDA selection must then be a valid top-k within NEAR_TIE,
     and those rows are compared with the oracle evaluated on the CUDA selection.
+    rows: compare only these token rows (the layer treats rows independently), so
+    that large calls are checked on a sample the oracle computes quickly.
     """
     k = S.spec.k
+    if rows is not None:
+        assert ref is None
+        rows = np.asarray(rows)
+        x_bits, out_bits, gpu_idx = x_bits[rows], out_bits[rows], gpu_idx[rows]
+        gpu_w = None if gpu_w is None else gpu_w[rows]
+        logit_bias = None if logit_bias is None else logit_bias[rows]
     if ref is None:
         ref = o.moe_forward(S, x_bits, logit_bias=logit_bias)
     logits = ref["logits"]

@@ -226,3 +226,33 @@ def test_qwen_int4_prefill_sampled_rows():
     rows = np.sort(np.random.default_rng(2).choice(4096, size=128, replace=False))
     r = G.compare(S, x[rows], out[rows], idx[rows], wt[rows], ref=o.moe_forward(S, x[rows]))
     print("qwen int4 prefill sampled rows", r)
+
+
+@pytest.mark.parametrize("max_tokens,T", [(10000, 9000), (10000, 4865), (10000, 33)])
+def test_dispatch_several_chunks_per_cta(max_tokens, T):
+    """The cooperative dispatch kernel runs a fixed grid of min(SMs, chunks of
+    max_tokens) CTAs; with 10000 tokens of capacity each CTA owns two 32-token
+    chunks (9000 tokens), a CTA boundary falls inside a chunk pair (4865), or most
+    CTAs own none (33). hist/offsets/perm/pos and the block map stay bit-exact."""
+    spec = mi.custom_layer(H=256, E=64, k=4, I=128, Is=128, seed=31).spec
+    L = G.cuda_layer(spec, max_tokens=max_tokens, flags=FORCE)
+    x = mi.tokens(spec, T, stream=3100 + T)
+    out, idx, wt = G.run_cuda(L, x)
+    _check_dispatch(L, T, spec.k, spec.E, idx)
+    rows = np.random.default_rng(T).choice(T, size=min(T, 64), replace=False)
+    G.compare(G.synth(spec), x, out, idx, wt, rows=np.sort(rows))
+
+
+def test_dispatch_three_kernel_form_for_huge_capacity():
+    """With 240000 tokens in one call and 512 experts, 50 chunks per CTA: the per-CTA
+    mask table of the cooperative dispatch (50 x 512 words + its count table) would
+    not fit in its shared memory, so the three-kernel form runs (top-k + histogram,
+    scan, scatter) and gives the same bit-exact dispatch."""
+    spec = mi.custom_layer(H=256, E=512, k=2, I=128, Is=128, seed=32).spec
+    L = G.cuda_layer(spec, max_tokens=240000, flags=FORCE)
+    T = 240000
+    x = mi.tokens(spec, T, stream=3200)
+    out, idx, wt = G.run_cuda(L, x)
+    _check_dispatch(L, T, spec.k, spec.E, idx)
+    rows = np.random.default_rng(5).choice(T, size=48, replace=False)
+    G.compare(G.synth(spec), x, out, idx, wt, rows=np.sort(rows))
