@@ -148,64 +148,42 @@ MOE_DEV bool bounded_wait_flag(const volatile int* flag, long long max_ns) {
 // ===========================================================================
 // Top-k of one token's logits by one warp.
 // ===========================================================================
-// Lane l holds the logits of experts l, l + 32, ... as order-preserving keys in
-// groups of 8, each group sorted descending (ties: lower expert first) by a
-// 19-comparator network; each round then takes the warp maximum of the lane
-// heads (redux), breaks exact ties by the lowest expert index (second redux)
-// and pops the winner's head. Writes the k experts in descending order and
-// their softmax weights renormalised over the k.
-template <int G>
-MOE_DEV void ce(uint32_t (&key)[G][8], int (&jj)[G][8], int g, int a, int b) {
-  const bool sw = key[g][b] > key[g][a] || (key[g][b] == key[g][a] && jj[g][b] < jj[g][a]);
-  const uint32_t ka = key[g][a], kb = key[g][b];
-  const int ja = jj[g][a], jb = jj[g][b];
-  key[g][a] = sw ? kb : ka; key[g][b] = sw ? ka : kb;
-  jj[g][a] = sw ? jb : ja; jj[g][b] = sw ? ja : jb;
-}
-
-// Top-k from keys already in registers: key[g][q] is the order key of expert
-// lane + 32 * (8 * g + q) (0 for experts >= E); jj is scratch.
+// Lane l holds the logits of experts l, l + 32, ... as order-preserving keys
+// (8 G of them, 0 for experts >= E). Each of k rounds (a rolled loop: this code
+// runs once per call and is mostly fetched cold, so it is kept small) takes
+// every lane's largest remaining key (the lower expert on equal keys), the
+// warp maximum of those (redux), the lowest expert index among equal maxima
+// (second redux), and removes the winner from its lane. Writes the k experts in
+// descending order (exact ties to the lower index) and their softmax weights
+// renormalised over the k.
 template <int G>
 MOE_DEV void warp_topk_keys(uint32_t (&key)[G][8], int (&jj)[G][8], int k, int lane, int* out_e, float* out_w) {
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int q = 0; q < 8; ++q) jj[g][q] = 8 * g + q;
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    ce<G>(key, jj, g, 0, 1); ce<G>(key, jj, g, 2, 3); ce<G>(key, jj, g, 4, 5); ce<G>(key, jj, g, 6, 7);
-    ce<G>(key, jj, g, 0, 2); ce<G>(key, jj, g, 1, 3); ce<G>(key, jj, g, 4, 6); ce<G>(key, jj, g, 5, 7);
-    ce<G>(key, jj, g, 1, 2); ce<G>(key, jj, g, 5, 6);
-    ce<G>(key, jj, g, 0, 4); ce<G>(key, jj, g, 1, 5); ce<G>(key, jj, g, 2, 6); ce<G>(key, jj, g, 3, 7);
-    ce<G>(key, jj, g, 2, 4); ce<G>(key, jj, g, 3, 5);
-    ce<G>(key, jj, g, 1, 2); ce<G>(key, jj, g, 3, 4); ce<G>(key, jj, g, 5, 6);
-  }
+  (void)jj;
   float v0 = 0.f, sum = 0.f, my_ex = 0.f;
   int my_e = 0;
 #pragma unroll 1
   for (int r = 0; r < k; ++r) {
-    uint32_t hk = key[0][0];
-    int hj = jj[0][0], hg = 0;
+    uint32_t bk = 0u;
+    int bq = 0;
 #pragma unroll
-    for (int g = 1; g < G; ++g)
-      if (key[g][0] > hk || (key[g][0] == hk && jj[g][0] < hj)) { hk = key[g][0]; hj = jj[g][0]; hg = g; }
-    const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, hk);
-    const uint32_t cand = (hk == gmax) ? (uint32_t)(lane + 32 * hj) : 0xFFFFFFFFu;
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (key[g][q] > bk) { bk = key[g][q]; bq = 8 * g + q; }   // strict: the lower local index wins a tie
+    const uint32_t gmax = __reduce_max_sync(0xFFFFFFFFu, bk);
+    const uint32_t cand = (bk == gmax) ? (uint32_t)(lane + 32 * bq) : 0xFFFFFFFFu;
     const uint32_t gidx = __reduce_min_sync(0xFFFFFFFFu, cand);
-    if (lane == (int)(gidx & 31u)) {  // pop the winner's head
+    if (lane == (int)(gidx & 31u)) {   // remove the winner
+      const int wq = (int)(gidx >> 5);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (g == hg) {
+      for (int g = 0; g < G; ++g)
 #pragma unroll
-          for (int q = 0; q < 7; ++q) { key[g][q] = key[g][q + 1]; jj[g][q] = jj[g][q + 1]; }
-          key[g][7] = 0u;
-          jj[g][7] = 1 << 20;
-        }
-      }
+        for (int q = 0; q < 8; ++q)
+          if (8 * g + q == wq) key[g][q] = 0u;
     }
     const float val = f32_from_order_key(gmax);
     if (r == 0) v0 = val;
-    const float ex = expf(val - v0);   // renormalised softmax over the k selected logits
+    const float ex = expf(val - v0);   // renormalised softmax over the k selected logits, summed in round order
     sum += ex;
     if (lane == r) { my_ex = ex; my_e = (int)gidx; }
   }
