@@ -544,15 +544,21 @@ MOE_DEV void router_publish(const uint16_t* xs, int XP, int T, int H, int E, con
     float acc[TMAX];
 #pragma unroll
     for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-    for (int cb = c0; cb < c1; cb += 32 * 8) {
-      uint4 v[8];
+    // Column blocks of 32 lanes x QV 16-byte loads. One-token kernels take
+    // QV = 2: this code runs once per call and is mostly fetched cold, so a short
+    // body wins (GB300: Qwen-shaped T=1 -0.5 us, Ling-shaped -1.3 us); windows of
+    // several tokens keep QV = 8, whose larger body holds more row loads in
+    // flight when the rows come from global memory (QV = 2 cost Ling T=4 1.1 us).
+    constexpr int QV = TMAX == 1 ? 2 : 8;
+    for (int cb = c0; cb < c1; cb += 32 * QV) {
+      uint4 v[QV];
       if (rows_smem && !x_ready) {   // the rows arrive with x
         volatile int never = 0;
         if (!sm100::mbar_wait(x_bar, 0, err, &never, kSpinBudget, false)) *s_abort = 1;
         x_ready = true;
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < QV; ++q) {
         const int c = cb + lane + 32 * q;
         if (c < c1) v[q] = rows_smem ? *reinterpret_cast<const uint4*>(row + 4 * c) : ldg_stream(row + 4 * c);
       }
@@ -562,7 +568,7 @@ MOE_DEV void router_publish(const uint16_t* xs, int XP, int T, int H, int E, con
         x_ready = true;
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < QV; ++q) {
         const int c = cb + lane + 32 * q;
         if (c < c1) {
 #pragma unroll
