@@ -198,14 +198,16 @@ MOE_DEV MxLayout mx_layout(int H, int so) { return MxLayout{H / 2, H, H + so, H 
 // rows 0-7 = gate rows of records 8m .. 8m+7, rows 8-15 = their up rows), over
 // 32-element blocks [blk0, blk0 + NBLK) of H. Each block's two k-steps go to a
 // fresh accumulator that is then scaled by the row's block scale and added.
-// x16: f16 x, rows XP halves apart. Records >= nvalid count as zero.
-template <int MAXMT, int NBLK>
+// x16: f16 x, rows XP halves apart. Records >= nvalid count as zero. UNROLL:
+// how far the block loop is unrolled (one-token kernels roll it: their group
+// code is fetched cold once per call and a short body wins there).
+template <int MAXMT, int NBLK, int UNROLL = NBLK>
 MOE_DEV void mx_gu_tiles(const uint8_t* gbase, int stride, int nvalid, int nmt, const MxLayout& ly, int T, int XP,
                          const uint16_t* x16, int blk0, float (&out)[MAXMT][4]) {
   const int lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
 #pragma unroll
   for (int m = 0; m < MAXMT; ++m) out[m][0] = out[m][1] = out[m][2] = out[m][3] = 0.f;
-#pragma unroll
+#pragma unroll UNROLL
   for (int bi = 0; bi < NBLK; ++bi) {
     const int blk = blk0 + bi;
     uint32_t b[2][2] = {{0u, 0u}, {0u, 0u}};   // x fragments of the block's two k-steps

@@ -349,7 +349,8 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
           stream::i4_gu_tiles<kMaxMt, nbw>(base, mxs, nvalid, (nvalid + 7) / 8, ly, T, XP, x16, s_xsum, kMaxXBlocks,
                                            warp * nbw, d);
         else
-          stream::mx_gu_tiles<kMaxMt, nbw>(base, mxs, nvalid, (nvalid + 7) / 8, ly, T, XP, x16, warp * nbw, d);
+          stream::mx_gu_tiles<kMaxMt, nbw, TMAX == 1 ? 1 : nbw>(base, mxs, nvalid, (nvalid + 7) / 8, ly, T, XP, x16,
+                                                                 warp * nbw, d);
       }
       const int nmt = shared ? 1 : (nvalid + 7) / 8;
 #pragma unroll
