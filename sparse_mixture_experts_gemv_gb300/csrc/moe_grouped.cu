@@ -61,6 +61,7 @@ constexpr int kStages = 4;
 constexpr int kStageA = BM * BK * 2;     // 16 KB
 constexpr int kStageB = 256 * BK * 2;    // 32 KB (N up to 256)
 constexpr int kTmemCols = 512;           // two 256-column fp32 accumulators
+constexpr int kGatherAhead = 2;          // stages between an A row's L2 prefetch and its copy
 constexpr int kChunk = 32;               // tokens per dispatch chunk (one per warp of the top-k CTA)
 constexpr size_t kDispatchMaskSmem = 128 * 1024;  // largest dynamic shared memory of the fused dispatch
 constexpr size_t kDispatchRedSmem = 2 * 4096 * sizeof(int);   // its per-part count table
@@ -461,7 +462,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
     // 16-byte chunk j), so one cp.async instruction of a warp covers four whole
     // rows (four cache lines) instead of one chunk of 32 different rows: the
     // gather is bound by L1TEX requests. Thread t copies chunk t % 8 of rows
-    // t / 8 + 16 i, i = 0..7.
+    // t / 8 + 16 i, i = 0..7. For bf16 layers the first thread of each row also
+    // requests the row's line kGatherAhead stages on into L2, so a copy usually
+    // waits for L2, not DRAM (gate/up at T = 4096 on GB300: 203 -> 182 us; the
+    // 4-bit kernels, whose converters share the issue slots, were 6-10 us slower
+    // with it, and prefetching 4-12 stages on gained less).
     const int tid = threadIdx.x - 192;
     const int jc = tid & 7, rb = tid >> 3;
     uint32_t it = 0;
@@ -495,6 +500,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA_r, const __grid_con
 #pragma unroll
         for (int i = 0; i < 8; ++i) cp_async_16(dst + (rb + 16 * i) * 128, src[i] + kb * BK, nbytes[i]);
         cp_async_commit();
+        if (!MXB && jc == 0 && kb + kGatherAhead < ti.ks) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (nbytes[i]) prefetch_l2(src[i] + (kb + kGatherAhead) * BK);
+        }
         if (pending >= 0) {
           cp_async_wait<1>();
           fence_proxy_async_smem();

@@ -85,6 +85,8 @@ MOE_DEV void tma_load_3d(void* smem_dst, const CUtensorMap* map, int c0, int c1,
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
       :: "r"(smem_u32(smem_dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)) : "memory");
 }
+// Requests the cache line holding ptr into L2 (no register result, no wait).
+MOE_DEV void prefetch_l2(const void* ptr) { asm volatile("prefetch.global.L2 [%0];" :: "l"(ptr) : "memory"); }
 MOE_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
 }
