@@ -771,7 +771,6 @@ route_dispatch_kernel(const float* __restrict__ logits, int T, int E, int k, int
   int* s_red = reinterpret_cast<int*>(s_dyn + S * E);   // [2][4096]: per-part totals, rows before
   __shared__ int s_pre[kMaxExperts];               // rows of e before the current chunk
   __shared__ int s_tot[kMaxExperts];               // rows of e in all chunks, then exclusive offsets
-  __shared__ int s_tiles[kMaxExperts];
   __shared__ int s_wsum[2][32];
   __shared__ int s_ok;
   pdl_wait();
