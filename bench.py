@@ -49,22 +49,34 @@ def _peaks():
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every PERIOD_MS with their own timestamps. Sampling is
+    running before the caller's region starts (__enter__ waits for the first
+    sample), and summary() keeps the samples stamped inside the region marked by
+    begin() / end(), widened by one period on each side."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, exe: str = "nvidia-smi", first_sample_timeout_s: float = 5.0):
         self.gpu = gpu_index
+        self.exe = exe
+        self.first_timeout = first_sample_timeout_s
         self.lines = []
         self.proc = None
+        self.t_begin = self.t_end = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                [self.exe, f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.th = threading.Thread(target=self._read, daemon=True)
             self.th.start()
+            t0 = time.time()
+            while not self.lines and self.proc.poll() is None and time.time() - t0 < self.first_timeout:
+                time.sleep(0.01)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -73,31 +85,54 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def begin(self):
+        self.t_begin = time.time()
+
+    def end(self):
+        self.t_end = time.time()
+
     def __exit__(self, *exc):
         if self.proc:
+            time.sleep(self.PERIOD_MS / 1000.0)   # the sample that closes the region
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            self.th.join(timeout=5)
+
+    @staticmethod
+    def _stamp(text: str):
+        from datetime import datetime
+        try:
+            return datetime.strptime(text, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def summary(self):
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        pad = self.PERIOD_MS / 1000.0
+        rows = []
         for ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
+                rows.append((self._stamp(f[0]), float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+        if self.t_begin is not None and self.t_end is not None:
+            inside = [r for r in rows if r[0] is not None and self.t_begin - pad <= r[0] <= self.t_end + pad]
+        else:
+            inside = rows
+        reasons = set()
+        for r in inside:
+            for n, v in zip(self.REASONS, r[3]):
                 if v.lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
+                "sm_max_mhz": inside[-1][2] if inside else (rows[-1][2] if rows else None),
+                "reasons": sorted(reasons), "samples": len(inside), "samples_total": len(rows),
+                "period_ms": self.PERIOD_MS}
 
 
 # ---------------------------------------------------------------------------
@@ -305,6 +340,7 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.begin()
         t0 = time.perf_counter()
         times = []
         for _ in range(args.steps):
@@ -312,6 +348,7 @@ def run_ours(args):
             times += t
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        clk.end()
     if world > 1:
         torch.distributed.barrier()
     us = float(np.mean(times) * 1e3)
