@@ -469,7 +469,8 @@ __global__ void __launch_bounds__(stream::kThreads, 1) moe_decode_stream_mx_kern
 
   // ---------------------------------------------------------------- exchange of partial outputs
 #pragma unroll
-  for (int j = 0; j < NT; ++j) stream::publish_tile_f32<TMAX == 1>(a.partial, b, H, T, 16 * (warp + kConsumerWarps * j), acc[j]);
+  for (int j = 0; j < NT; ++j)
+    stream::publish_tile_f32<TMAX == 1>(a.partial, b, H, T, 16 * (warp + kConsumerWarps * j), acc[j]);
   stream::collect_outputs_f32(a.partial, reinterpret_cast<float*>(ring), a.arrivals, tag * (unsigned long long)G, T, H,
                               a.out, a.err, &s_abort);
   if (threadIdx.x == 0) leave();
